@@ -1,0 +1,529 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+Workload (per GPU): the batched-decode batch -- 64 sequences with context lengths uniform in
+[512, 4096], 32 query / 8 KV heads, head_dim 128, 16-position pages shuffled over a pool
+with 10% free pages, bf16 K/V ~ N(0,1) (seeded, synthetic).
+
+One step = the whole decode hot path over that batch:
+    slot mapping of the 64 new tokens -> store of their K/V -> split-K paged decode -> merge.
+`value` is algorithmic bytes per step (K/V of every cached position read once, Q read, O
+written, new K/V read and written) over device time, inputs resident in HBM, L2 flushed
+between steps.  The line also carries the append-prefill leg (KV-rewind workload: 1,000
+documents x 50 new tokens over 300 cached, page sizes 16 and 64) with its TFLOP/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvc|reference]
+
+`--impl reference` times the CPU oracle (fp64) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged decode attention HBM GB/s (% of GB300 peak); append-prefill TFLOP/s"
+WORKLOAD = ("batched-decode: 64 seqs, ctx U[512,4096], 32 q / 8 kv heads, head_dim 128, "
+            "page 16, bf16, 10% free pages, pages shuffled")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
+    p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer (MB)")
+    p.add_argument("--append-steps", type=int, default=60)
+    p.add_argument("--no-append", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------------------
+
+def decode_bytes(case) -> int:
+    """K and V of every cached position read once, Q read, O written (bf16)."""
+    per_pos = 2 * case.kv_heads * case.head_dim * 2
+    qo = 2 * case.num_seqs * case.q_heads * case.head_dim * 2
+    return int(case.context_lens.astype(np.int64).sum()) * per_pos + qo
+
+
+def store_bytes(case) -> int:
+    """New K/V read and written, slots written and read."""
+    row = case.kv_heads * case.head_dim * 2
+    return case.num_tokens * (2 * row * 2 + 8)
+
+
+def append_work(case):
+    """(bytes, flops) of one append: K/V of each sequence's visible positions read once, Q
+    read, O written; 4*D flops per (query head, visible key) pair (QK and PV)."""
+    per_pos = 2 * case.kv_heads * case.head_dim * 2
+    q_lens = case.q_lens.astype(np.int64)
+    ctx = case.context_lens.astype(np.int64)
+    kv = int(ctx.sum()) * per_pos
+    qo = 2 * case.num_tokens * case.q_heads * case.head_dim * 2
+    # token i sees ctx - q_len + i + 1 keys
+    pairs = int((q_lens * (ctx - q_lens) + q_lens * (q_lens + 1) // 2).sum())
+    flops = 4 * case.head_dim * case.q_heads * pairs
+    return kv + qo, flops
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; timing only -- the path has no collective)
+# ---------------------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "kvc" else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_from_profile(kernel_tag: str, source_file: str):
+    """DRAM bytes per launch recorded by ncu for this kernel, if the kernel source has not
+    changed since (the summary records the source's sha256 prefix)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha256:\s*([0-9a-f]+)",
+                  text)
+    if not m:
+        return None
+    src = os.path.join(ROOT, "pagedattention_kvc_store_gb300", "csrc", source_file)
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m.group(1)) if digest.startswith(m.group(2)) else None
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------------------
+
+def run_kvc(args):
+    import torch
+
+    import pagedattention_kvc_store_gb300 as kvc
+    from workloads import config_case
+    from workloads.configs import SEED_BASE
+    from workloads.device import to_device
+
+    rank, world, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    # each rank decodes its own batch of 64 sequences (weak scaling, no collective)
+    case = config_case(2, seed=None if rank == 0 else SEED_BASE + 2 + 1000 * rank)
+    d = to_device(case, dev)
+    S, Hq, D = case.num_seqs, case.q_heads, case.head_dim
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device=dev)
+    pool = kvc.pool_desc(d.k_pool)
+    splits, chunk, ws = kvc.kvc_decode_plan(S, Hq, pool, case.max_ctx, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+
+    def store_part():
+        kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+        kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+
+    def decode_part():
+        kvc.kvc_decode(out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens,
+                       case.max_ctx, num_splits=0, workspace=work)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        store_part()
+        decode_part()
+        torch.cuda.synchronize()
+        g_store, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_store, stream=stream):
+            store_part()
+        with torch.cuda.graph(g_decode, stream=stream):
+            decode_part()
+        torch.cuda.synchronize()
+
+        K, W = args.steps, args.warmup
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for _ in range(W):
+            flush.zero_()
+            g_store.replay()
+            g_decode.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        t0 = time.perf_counter()
+        for e0, e1, e2 in evs:
+            flush.zero_()                       # L2 flush, outside the timed events
+            e0.record(stream)
+            g_store.replay()
+            e1.record(stream)
+            g_decode.replay()
+            e2.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier(world)
+        clk = clocks.stop()
+        step_ms = [a.elapsed_time(c) for a, _, c in evs]
+        dec_ms = [b.elapsed_time(c) for _, b, c in evs]
+        total_ms = max_over_ranks(sum(step_ms), world, dev)
+
+        step_b = decode_bytes(case) + store_bytes(case)
+        value = world * step_b * K / (total_ms / 1e3) / 1e9
+        dec_b = decode_bytes(case)
+        achieved = dec_b / (statistics.mean(dec_ms) / 1e3) / 1e9
+        launches_per_step = 2 + 1 + (1 if splits > 1 else 0)
+
+        e2e = None
+        if not args.no_e2e:
+            e2e = run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, max(20, K // 10))
+
+        append = None
+        if not args.no_append:
+            append = run_append(torch, kvc, args, dev, stream, flush, peaks, rank)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q; no dataset, no weights)",
+        "config": {"workload": WORKLOAD, "num_seqs": S, "q_heads": Hq,
+                   "kv_heads": case.kv_heads, "head_dim": D, "page_size": case.page_size,
+                   "sum_ctx": int(case.context_lens.sum()), "splits": splits,
+                   "chunk": chunk, "l2": f"flushed between steps ({args.flush_mb} MB write)",
+                   "timing": "CUDA events per step on the launching stream; graphs replayed",
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                     "peak_source": f"of {peaks['source']} (copy bandwidth)",
+                     "kernel": "paged_decode_kernel + merge_kernel (one kvc_decode call)",
+                     "bytes_per_launch": dec_b,
+                     "traffic": traffic_from_profile("decode_batched", "kvc_decode.cu")},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if append is not None:
+        line["append"] = append
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
+    """The same step through the public API with host buffers: pinned host -> device copies
+    of the step's inputs, the three calls, and the output read back, all timed."""
+    host = {name: getattr(d, name).cpu().pin_memory()
+            for name in ("q", "k_new", "v_new", "block_table", "context_lens")}
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    dev_in = {name: torch.empty_like(t, device=dev) for name, t in host.items()}
+
+    def step():
+        for name, t in host.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        kvc.kvc_slot_mapping(slots, dev_in["block_table"], dev_in["context_lens"], None,
+                             case.page_size)
+        kvc.kvc_store(d.k_pool, d.v_pool, dev_in["k_new"], dev_in["v_new"], slots)
+        kvc.kvc_decode(out, dev_in["q"], d.k_pool, d.v_pool, dev_in["block_table"],
+                       dev_in["context_lens"], case.max_ctx, num_splits=0, workspace=work)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    step_b = decode_bytes(case) + store_bytes(case)
+    return {"value": round(step_b / (statistics.mean(times) / 1e3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(statistics.mean(times), 5), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "path": "pinned H2D of q/k_new/v_new/block_table/context_lens, kvc_slot_mapping, "
+                    "kvc_store, kvc_decode (eager), D2H of out"}
+
+
+def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
+    """Append-prefill leg: KV-rewind workload, page sizes 16 and 64."""
+    from workloads import config_case
+    from workloads.configs import SEED_BASE
+    from workloads.device import to_device
+
+    result = {}
+    for P in (16, 64):
+        case = config_case(4, page_size=P, seed=None if rank == 0 else SEED_BASE + 4 + 1000 * rank)
+        d = to_device(case, dev)
+        slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+        out = torch.empty(case.num_tokens, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                          device=dev)
+
+        def store_part():
+            kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, d.q_indptr,
+                                 case.page_size, max_q_len=case.max_q_len)
+            kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+
+        def append_part():
+            kvc.kvc_append(out, d.q, d.k_pool, d.v_pool, d.block_table, d.q_indptr,
+                           d.context_lens, case.max_q_len, case.max_ctx)
+
+        store_part()
+        append_part()
+        torch.cuda.synchronize()
+        g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            store_part()
+        with torch.cuda.graph(g2, stream=stream):
+            append_part()
+        for _ in range(3):
+            g1.replay()
+            g2.replay()
+        torch.cuda.synchronize()
+        st_ms, ap_ms = [], []
+        for _ in range(args.append_steps):
+            flush.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            g1.replay()
+            e1.record(stream)
+            g2.replay()
+            e2.record(stream)
+            e2.synchronize()
+            st_ms.append(e0.elapsed_time(e1))
+            ap_ms.append(e1.elapsed_time(e2))
+        bytes_, flops = append_work(case)
+        t = statistics.mean(ap_ms) / 1e3
+        t_roof = max(flops / (peaks["bf16_sustained"] * 1e12), bytes_ / (peaks["hbm"] * 1e9))
+        bound = "tensor" if flops / (peaks["bf16_sustained"] * 1e12) > bytes_ / (peaks["hbm"] * 1e9) else "hbm"
+        result[f"p{P}"] = {
+            "tflops": round(flops / t / 1e12, 2), "gbs": round(bytes_ / t / 1e9, 1),
+            "ms": round(statistics.mean(ap_ms), 4),
+            "store_ms": round(statistics.mean(st_ms), 4),
+            "flops": flops, "bytes": bytes_, "roofline_bound": bound,
+            "roofline_frac": round(t_roof / t, 4),
+            "store_gbs": round(store_bytes(case) / (statistics.mean(st_ms) / 1e3) / 1e9, 1),
+            "gpu_launches": args.append_steps * 3,
+        }
+        del d, out, slots, g1, g2
+        torch.cuda.empty_cache()
+    result["workload"] = ("rewind-append: 1,000 docs x 50 new tokens over 300 cached, "
+                          "32 q / 8 kv heads, head_dim 128")
+    result["peaks"] = {"hbm_gbs": peaks["hbm"], "bf16_tflops": peaks["bf16_sustained"],
+                       "source": f"of {peaks['source']} (sustained bf16)"}
+    return result
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle (baseline only; never the product path)
+# ---------------------------------------------------------------------------------------
+
+def _oracle_step(oracle, case, seqs, threads, k_pool, v_pool):
+    bt = case.block_table[seqs]
+    ctx = case.context_lens[seqs]
+    q_lens = case.q_lens[seqs]
+    indptr = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    rows = np.concatenate([np.arange(case.q_indptr[s], case.q_indptr[s + 1]) for s in seqs])
+    slots = oracle.slot_mapping(bt, ctx, indptr, case.page_size)
+    oracle.store(k_pool, v_pool, case.k_new[rows], case.v_new[rows], slots)
+    oracle.attention(case.q[rows], k_pool, v_pool, bt, ctx, indptr, num_threads=threads)
+
+
+def _sub_bytes(case, seqs):
+    per_pos = 2 * case.kv_heads * case.head_dim * 2
+    row = case.kv_heads * case.head_dim * 2
+    n = len(seqs)
+    return (int(case.context_lens[seqs].astype(np.int64).sum()) * per_pos
+            + 2 * n * case.q_heads * case.head_dim * 2 + n * (2 * row * 2 + 8))
+
+
+def cpu_baseline(case, seconds):
+    from oracle import oracle
+    threads = len(os.sched_getaffinity(0))
+    seqs = np.arange(case.num_seqs)
+    kp, vp = case.k_pool.copy(), case.v_pool.copy()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _oracle_step(oracle, case, seqs, threads, kp, vp)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(_sub_bytes(case, seqs) / dt / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"the full 64-sequence batch, {reps} pass(es), {dt:.2f} s per pass "
+                      f"(fp64 C oracle: slot mapping, store, gathered attention)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_setup(args)
+    if rank != 0:
+        barrier(world)
+        return
+    from oracle import oracle
+    from workloads import config_case
+    oracle.build()
+    case = config_case(2)
+    threads = len(os.sched_getaffinity(0))
+    kp, vp = case.k_pool.copy(), case.v_pool.copy()
+    # size the sample so that warmup + steps take about two minutes
+    t0 = time.perf_counter()
+    _oracle_step(oracle, case, np.arange(1), threads, kp, vp)
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    n = int(np.clip(120.0 / ((args.steps + args.warmup) * t1), 1, case.num_seqs))
+    seqs = np.arange(n)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, case, seqs, threads, kp, vp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(oracle, case, seqs, threads, kp, vp)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = _sub_bytes(case, seqs) / dt / 1e9
+    sample = f"first {n} of the 64 sequences per step ({dt * 1e3:.2f} ms per step)"
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvc(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * kvc.h -- paged KV-cache store and paged attention for NVIDIA GB300 (sm_103a).
+ *
+ * A KV cache kept in fixed-size pages, addressed through per-sequence block tables:
+ *   TileInfer.jl "KV cache", sections "Pages and block tables" and "Growing, rolling back,
+ *   releasing"; "KV Cache Management and PagedAttention", sections "Connect token order to
+ *   storage locations", "Compute attention over scattered KV" and "Share common KV across
+ *   responses"; Quail "KV", sections "Paged KV", "KV rewind" and "Prefix sharing".
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Pools.  One K pool and one V pool per layer, each bf16 [num_pages][page_size][kv_heads]
+ *   [head_dim], row-major (the (position, kv head) vector is head_dim contiguous values).
+ *   Viewed by slot it is [num_pages * page_size][kv_heads][head_dim].
+ * Address rule.  Position p (0-based) of sequence s lives in page block_table[s][p /
+ *   page_size] at offset p % page_size; its slot is page * page_size + offset.
+ * Block table.  int32 [num_seqs][bt_stride], row-major.  Entries past a sequence's last
+ *   page are never read (the caller may zero-pad rows to a fixed width, e.g. a multiple of
+ *   16, so that a captured CUDA graph stays valid as sequences grow; page 0 in the padding
+ *   is harmless).  Several rows may list the same pages (a shared prefix).
+ * context_lens[s].  Number of positions of sequence s including the new token(s); the
+ *   newest token attends to its own key and value, so its K/V must be stored first.
+ * GQA.  q_heads = G * kv_heads; q head h reads kv head h / G.
+ * Scale.  Scores are q.k * scale; scale <= 0 selects 1/sqrt(head_dim).
+ * Memory.  Every pointer argument named *pool, q, k_new, v_new, out, block_table,
+ *   context_lens, q_indptr, slot_mapping, partial_*, workspace is a DEVICE pointer owned by
+ *   the caller.  The library allocates no memory, holds no pointer after a call returns,
+ *   and never synchronises: each call only enqueues kernels on `stream` (a cudaStream_t;
+ *   NULL is the legacy default stream).  Device arrays are not read on the host, so per-step
+ *   values may change between replays of a captured graph.
+ * Alignment.  bf16 tensors and pools must be 16-byte aligned (TMA and 16-byte vector
+ *   accesses); fp32 partials 16-byte aligned.
+ * Errors.  Scalars are checked on the host before anything is enqueued; a bad call returns
+ *   a status and enqueues nothing.  Device-side contents (page ids, slots, lengths) are
+ *   trusted: out-of-range values there are caller errors (page ids must be < num_pages,
+ *   context_lens[s] <= bt_stride * page_size).  kvc_last_error() gives a one-line reason
+ *   for the last failing call on the calling thread.
+ * Supported shapes.  head_dim 64 or 128; page_size 16, 32 or 64; G = q_heads / kv_heads
+ *   in {1, 2, 4, 8}; num_pages * page_size < 2^31.  Others return KVC_ERR_UNSUPPORTED.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvc_status {
+    KVC_OK = 0,
+    KVC_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer ...      */
+    KVC_ERR_UNSUPPORTED = 2,  /* shape outside the supported set above                   */
+    KVC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the plan requires      */
+    KVC_ERR_CUDA = 4,         /* a CUDA call failed (launch, tensor-map encode, ...)      */
+    KVC_ERR_DEVICE = 5        /* a kernel gave up a bounded wait (see kvc_device_errors)  */
+} kvc_status;
+
+typedef enum kvc_dtype {
+    KVC_BF16 = 0,             /* bf16, rounded to nearest even from the fp32 accumulator */
+    KVC_F32 = 1
+} kvc_dtype;
+
+typedef struct kvc_pool_desc {
+    int32_t num_pages;
+    int32_t page_size;        /* positions per page                                       */
+    int32_t kv_heads;
+    int32_t head_dim;
+} kvc_pool_desc;
+
+/* Human-readable name of a status, and the reason for the last failure on this thread. */
+const char *kvc_status_string(kvc_status status);
+const char *kvc_last_error(void);
+
+/*
+ * kvc_slot_mapping -- slot of every new token (TileInfer.jl "KV cache", "Pages and block
+ * tables": before a step, each new token's slot is computed from the block table).
+ *
+ * New token i of sequence s (0 <= i < q_len_s, q_len_s = q_indptr[s+1] - q_indptr[s]) is
+ * at position context_lens[s] - q_len_s + i; slot_mapping[q_indptr[s] + i] receives its
+ * slot.  q_indptr == NULL means one new token per sequence (decode): token s belongs to
+ * sequence s and num_tokens must equal num_seqs.  A position below zero (context_lens[s] <
+ * q_len_s) yields slot -1.  Integer arithmetic only: bit-exact.
+ *   slot_mapping  int32 [num_tokens]        (out)
+ *   block_table   int32 [num_seqs][bt_stride]
+ *   context_lens  int32 [num_seqs]
+ *   q_indptr      int32 [num_seqs + 1] or NULL
+ *   max_q_len     host upper bound on q_len_s (sizes the launch; 1 when q_indptr is NULL)
+ */
+kvc_status kvc_slot_mapping(int32_t *slot_mapping, const int32_t *block_table,
+                            int32_t bt_stride, const int32_t *context_lens,
+                            const int32_t *q_indptr, int32_t num_seqs, int32_t num_tokens,
+                            int32_t max_q_len, int32_t page_size, void *stream);
+
+/*
+ * kvc_store -- write each new token's key and value at its slot (TileInfer.jl "KV cache",
+ * "Pages and block tables": the step writes the new keys and values at their slots;
+ * "KV Cache Management and PagedAttention", "Grow the allocation as generation proceeds").
+ *
+ * k_pool[slot_mapping[t]][g][:] = k_new[t][g][:] and likewise for V, for every kv head g.
+ * A raw 16-bit copy: NaN payloads and signed zeros are kept.  slot_mapping[t] < 0 skips
+ * token t (padding).  Slots must be < num_pages * page_size and distinct within one call
+ * (two writers of one slot is the race copy-on-write exists to prevent).
+ *   k_new, v_new  bf16 [num_tokens][kv_heads][head_dim]
+ */
+kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void *k_new,
+                     const void *v_new, const int32_t *slot_mapping, int32_t num_tokens,
+                     void *stream);
+
+/*
+ * kvc_decode -- paged attention for one new token per sequence, GQA, reading K/V in place
+ * from scattered pages with no gather copy ("KV Cache Management and PagedAttention",
+ * "Compute attention over scattered KV"):
+ *   out[s][h] = softmax_p( q[s][h] . K_s[p][h/G] * scale ) . V_s[p][h/G],  p < ctx_s,
+ * where K_s[p] is the pool entry the address rule gives for position p of sequence s.
+ * ctx_s = 0 yields out = 0.
+ *
+ * Split-K ("flash decoding"): with more than one split, the positions of each sequence are
+ * cut into consecutive chunks of `chunk` positions (kvc_decode_plan); each chunk writes an
+ * fp32 partial, normalised over its own keys, and its log-sum-exp into the workspace, and
+ * kvc_merge (enqueued by this call) combines them.  The result does not depend on the
+ * split count beyond fp32 rounding.
+ *   out           [num_seqs][q_heads][head_dim], out_dtype KVC_BF16 or KVC_F32
+ *   q             bf16 [num_seqs][q_heads][head_dim]
+ *   max_ctx       host upper bound on every context_lens[s] (sizes the launch)
+ *   num_splits    0 = choose automatically, 1 = no split, n > 1 = at most n chunks
+ *   workspace     device scratch of at least kvc_decode_plan(...)'s workspace bytes when
+ *                 the plan has more than one split (may be NULL otherwise).  Layout:
+ *                 partial_o fp32 [num_seqs][q_heads][splits][head_dim] at offset 0, then
+ *                 partial_lse fp32 [num_seqs][q_heads][splits] at the 256-byte-aligned
+ *                 offset that follows.  Splits that hold no position get lse = -inf and
+ *                 an unwritten partial_o.
+ */
+kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k_pool,
+                      const void *v_pool, kvc_pool_desc pool, const int32_t *block_table,
+                      int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs,
+                      int32_t max_ctx, int32_t q_heads, float scale, int32_t num_splits,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kvc_decode_plan -- the split plan kvc_decode will use for these scalars: the number of
+ * splits (>= 1), the chunk length in positions (a multiple of 64 and of page_size; equal
+ * to the padded max_ctx when splits == 1) and the workspace bytes it needs (0 when
+ * splits == 1).  Any output pointer may be NULL.
+ */
+kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
+                           int32_t max_ctx, int32_t num_splits, int32_t *splits_out,
+                           int32_t *chunk_out, size_t *workspace_bytes_out);
+
+/*
+ * kvc_merge -- combine split partials by log-sum-exp.  For every row r:
+ *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M);
+ *   out[r] = sum_j w_j partial_o[r][j] / sum_j w_j;   lse_out[r] = M + log(sum_j w_j).
+ * Splits with lse = -inf hold no key: their partial_o is not read.  A row whose splits are
+ * all empty gets out = 0 and lse_out = -inf.  (The pages leave partitioning and combining
+ * inside the kernel open -- "KV Cache Management and PagedAttention", "Compute attention
+ * over scattered KV"; this is the plain combination of softmax-normalised pieces.)
+ *   partial_o    fp32 [rows][num_splits][head_dim]
+ *   partial_lse  fp32 [rows][num_splits]
+ *   out          [rows][head_dim], out_dtype KVC_BF16 or KVC_F32
+ *   lse_out      fp32 [rows] or NULL (natural log)
+ */
+kvc_status kvc_merge(void *out, int32_t out_dtype, const float *partial_o,
+                     const float *partial_lse, int32_t rows, int32_t num_splits,
+                     int32_t head_dim, float *lse_out, void *stream);
+
+/*
+ * kvc_append -- causal chunked prefill of new tokens over an already-cached prefix, the
+ * kernel behind KV rewind and shared-prefix reuse (Quail "KV", "KV rewind" and "Prefix
+ * sharing"; TileInfer.jl "KV cache", "Growing, rolling back, releasing" and "Prefix reuse
+ * in chat").  New token i of sequence s sits at position c_i = ctx_s - q_len_s + i and
+ *   out[t][h] = softmax_{p <= c_i}( q[t][h] . K_s[p][h/G] * scale ) . V_s[p][h/G]
+ * with t = q_indptr[s] + i.  The new tokens' K/V must already be in the pools (kvc_store).
+ *   q, out        [num_tokens][q_heads][head_dim]; q bf16, out per out_dtype
+ *   q_indptr      int32 [num_seqs + 1], q_indptr[0] = 0, q_indptr[num_seqs] = num_tokens
+ *   max_q_len     host upper bound on every q_len_s;  max_ctx likewise for context_lens
+ */
+kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k_pool,
+                      const void *v_pool, kvc_pool_desc pool, const int32_t *block_table,
+                      int32_t bt_stride, const int32_t *q_indptr,
+                      const int32_t *context_lens, int32_t num_seqs, int32_t num_tokens,
+                      int32_t max_q_len, int32_t max_ctx, int32_t q_heads, float scale,
+                      void *stream);
+
+/*
+ * kvc_device_errors -- read and clear the device-side error word.  Kernels bound every wait
+ * (about one second); a wait that runs out sets a bit here and the kernel returns early,
+ * leaving its outputs undefined.  Synchronises with the device.  *flags_out = 0 when no
+ * wait ever ran out.
+ */
+kvc_status kvc_device_errors(uint32_t *flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

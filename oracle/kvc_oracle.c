@@ -66,7 +66,8 @@ int64_t kvo_slot_of_position(const int32_t *block_table, int64_t bt_stride, int6
 /*
  * Slots of every new token of every sequence.  [TI] "Pages and block tables": before a
  * step, each new token gets its slot.  Sequence s owns tokens q_indptr[s] ..
- * q_indptr[s+1]-1; token i of s is at position context_lens[s] - q_len + i.
+ * q_indptr[s+1]-1; token i of s is at position context_lens[s] - q_len + i.  A token with
+ * no position (context_lens[s] < q_len) is padding and gets slot -1, which the store skips.
  */
 void kvo_slot_mapping(const int32_t *block_table, int64_t bt_stride,
                       const int32_t *context_lens, const int32_t *q_indptr, int64_t num_seqs,
@@ -78,7 +79,9 @@ void kvo_slot_mapping(const int32_t *block_table, int64_t bt_stride,
         for (int64_t i = 0; i < q_len; ++i) {
             int64_t position = (int64_t)context_lens[s] - q_len + i;
             slots_out[first + i] =
-                kvo_slot_of_position(block_table, bt_stride, s, position, page_size);
+                position < 0 ? -1
+                             : kvo_slot_of_position(block_table, bt_stride, s, position,
+                                                    page_size);
         }
     }
 }

@@ -1,0 +1,12 @@
+"""Paged KV-cache store and paged attention for NVIDIA GB300 (sm_103a).
+
+The product is the C-ABI library libkvc.so (include/kvc.h), built from ``csrc/`` by
+``build.build()``; ``kvc`` is its thin Python binding (same entry-point names).
+"""
+from .kvc import (EXPORTS, KVC_BF16, KVC_F32, KvcError, PoolDesc, kvc_append, kvc_decode,
+                  kvc_decode_plan, kvc_device_errors, kvc_merge, kvc_slot_mapping, kvc_store,
+                  lib, library_path, pool_desc)
+
+__all__ = ["EXPORTS", "KVC_BF16", "KVC_F32", "KvcError", "PoolDesc", "kvc_append",
+           "kvc_decode", "kvc_decode_plan", "kvc_device_errors", "kvc_merge",
+           "kvc_slot_mapping", "kvc_store", "lib", "library_path", "pool_desc"]

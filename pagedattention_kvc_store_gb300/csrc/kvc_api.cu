@@ -1,0 +1,448 @@
+// kvc_api.cu -- the C ABI declared in include/kvc.h: argument checks, split planning,
+// TMA tensor-map encoding and kernel dispatch.  No device memory is allocated here.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kvc.h"
+#include "kvc_launch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvc_status fail(kvc_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kvc_status ok()
+{
+    g_last_error.clear();
+    return KVC_OK;
+}
+
+kvc_status cuda_fail(cudaError_t err, const char *what)
+{
+    return fail(KVC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvc_status check_pool(const kvc_pool_desc &pool)
+{
+    if (pool.num_pages <= 0 || pool.page_size <= 0 || pool.kv_heads <= 0 || pool.head_dim <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "pool descriptor has a non-positive field");
+    if (pool.head_dim != 64 && pool.head_dim != 128)
+        return fail(KVC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", pool.head_dim);
+    if (pool.page_size != 16 && pool.page_size != 32 && pool.page_size != 64)
+        return fail(KVC_ERR_UNSUPPORTED, "page_size %d (supported: 16, 32, 64)",
+                    pool.page_size);
+    if (static_cast<int64_t>(pool.num_pages) * pool.page_size >= (int64_t(1) << 31))
+        return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
+    return KVC_OK;
+}
+
+kvc_status check_group(const kvc_pool_desc &pool, int32_t q_heads)
+{
+    if (q_heads <= 0 || q_heads % pool.kv_heads != 0)
+        return fail(KVC_ERR_INVALID_ARG, "q_heads %d is not a multiple of kv_heads %d", q_heads,
+                    pool.kv_heads);
+    const int g = q_heads / pool.kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(KVC_ERR_UNSUPPORTED, "GQA group %d (supported: 1, 2, 4, 8)", g);
+    return KVC_OK;
+}
+
+int device_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+        return n;
+    cudaGetLastError();   // a host without a GPU: plan for a GB300
+    return 152;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+struct Plan {
+    int splits;
+    int chunk;
+    size_t ws_bytes;
+    size_t lse_offset;
+};
+
+Plan make_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool, int32_t max_ctx,
+               int32_t requested)
+{
+    const int64_t ctx = max_ctx > 0 ? max_ctx : 1;
+    const int64_t unit = kvc::kStageKeys;   // a multiple of every supported page size
+    Plan p{};
+    if (requested == 1) {
+        p.splits = 1;
+        p.chunk = static_cast<int>(round_up(ctx, unit));
+    } else {
+        int64_t want = requested;
+        if (requested <= 0) {
+            // Enough CTAs for several per SM: (sequence, kv head) units times splits.
+            const int64_t units = static_cast<int64_t>(num_seqs > 0 ? num_seqs : 1) * pool.kv_heads;
+            want = ceil_div(4 * static_cast<int64_t>(device_sm_count()), units);
+        }
+        int64_t chunk = round_up(ceil_div(ctx, want), unit);
+        if (requested <= 0 && chunk < 256)
+            chunk = 256;
+        p.chunk = static_cast<int>(chunk);
+        p.splits = static_cast<int>(ceil_div(ctx, chunk));
+    }
+    if (p.splits > 1) {
+        const size_t rows = static_cast<size_t>(num_seqs) * q_heads;
+        const size_t o_bytes = rows * p.splits * pool.head_dim * sizeof(float);
+        p.lse_offset = static_cast<size_t>(round_up(static_cast<int64_t>(o_bytes), 256));
+        p.ws_bytes = p.lse_offset + rows * p.splits * sizeof(float);
+    }
+    return p;
+}
+
+// ------------------------------------------------------------------------------------------
+// TMA tensor maps over a pool viewed as [num_pages * page_size][kv_heads][head_dim] bf16,
+// boxes of [page_size][1][64] with 128-byte swizzle.  Encoding is host work; the last few
+// maps are memoised by (address, shape, device).
+// ------------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct MapEntry {
+    const void *ptr;
+    kvc_pool_desc pool;
+    int device;
+    CUtensorMap map;
+};
+
+std::mutex g_map_mutex;
+std::vector<MapEntry> g_maps;   // most recent last, at most 16
+
+kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
+{
+    int device = 0;
+    cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "cudaGetDevice");
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (size_t i = g_maps.size(); i-- > 0;) {
+            const MapEntry &e = g_maps[i];
+            if (e.ptr == base && e.device == device && e.pool.num_pages == pool.num_pages &&
+                e.pool.page_size == pool.page_size && e.pool.kv_heads == pool.kv_heads &&
+                e.pool.head_dim == pool.head_dim) {
+                *out = e.map;
+                return KVC_OK;
+            }
+        }
+    }
+    auto fn = encode_fn();
+    if (fn == nullptr)
+        return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(pool.head_dim),
+                                static_cast<cuuint64_t>(pool.kv_heads),
+                                static_cast<cuuint64_t>(pool.num_pages) * pool.page_size};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pool.head_dim) * 2,
+                                   static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(pool.page_size)};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUtensorMap map;
+    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)",
+                    static_cast<int>(r));
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    if (g_maps.size() >= 16)
+        g_maps.erase(g_maps.begin());
+    g_maps.push_back(MapEntry{base, pool, device, map});
+    *out = map;
+    return KVC_OK;
+}
+
+kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *q,
+                                const void *k_pool, const void *v_pool,
+                                const kvc_pool_desc &pool, const int32_t *block_table,
+                                int32_t bt_stride, const int32_t *context_lens,
+                                int32_t num_seqs, int32_t max_ctx, int32_t q_heads)
+{
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    if ((st = check_group(pool, q_heads)) != KVC_OK)
+        return st;
+    if (out_dtype != KVC_BF16 && out_dtype != KVC_F32)
+        return fail(KVC_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (num_seqs < 0 || num_seqs > 65535)
+        return fail(KVC_ERR_INVALID_ARG, "num_seqs %d (0 .. 65535)", num_seqs);
+    if (max_ctx < 0)
+        return fail(KVC_ERR_INVALID_ARG, "max_ctx %d", max_ctx);
+    if (bt_stride <= 0 || static_cast<int64_t>(bt_stride) * pool.page_size < max_ctx)
+        return fail(KVC_ERR_INVALID_ARG, "bt_stride %d cannot hold max_ctx %d", bt_stride,
+                    max_ctx);
+    if (num_seqs > 0 && (!out || !q || !k_pool || !v_pool || !block_table || !context_lens))
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return fail(KVC_ERR_INVALID_ARG, "q, out and pools must be 16-byte aligned");
+    return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvc_status_string(kvc_status status)
+{
+    switch (status) {
+    case KVC_OK: return "KVC_OK";
+    case KVC_ERR_INVALID_ARG: return "KVC_ERR_INVALID_ARG";
+    case KVC_ERR_UNSUPPORTED: return "KVC_ERR_UNSUPPORTED";
+    case KVC_ERR_WORKSPACE: return "KVC_ERR_WORKSPACE";
+    case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
+    case KVC_ERR_DEVICE: return "KVC_ERR_DEVICE";
+    }
+    return "KVC_ERR_UNKNOWN";
+}
+
+const char *kvc_last_error(void) { return g_last_error.c_str(); }
+
+kvc_status kvc_slot_mapping(int32_t *slot_mapping, const int32_t *block_table,
+                            int32_t bt_stride, const int32_t *context_lens,
+                            const int32_t *q_indptr, int32_t num_seqs, int32_t num_tokens,
+                            int32_t max_q_len, int32_t page_size, void *stream)
+{
+    if (num_seqs < 0 || num_tokens < 0 || max_q_len < 0 || bt_stride <= 0 || page_size <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "negative size or non-positive stride/page size");
+    if (q_indptr == nullptr && num_tokens != num_seqs)
+        return fail(KVC_ERR_INVALID_ARG,
+                    "without q_indptr every sequence has one token (num_tokens %d != %d)",
+                    num_tokens, num_seqs);
+    if (num_seqs > 0 && (!slot_mapping || !block_table || !context_lens))
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    if (num_seqs == 0 || num_tokens == 0)
+        return ok();
+    cudaError_t err = kvc::launch_slot_mapping(slot_mapping, block_table, bt_stride,
+                                               context_lens, q_indptr, num_seqs, num_tokens,
+                                               max_q_len, page_size,
+                                               static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "slot mapping launch");
+}
+
+kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void *k_new,
+                     const void *v_new, const int32_t *slot_mapping, int32_t num_tokens,
+                     void *stream)
+{
+    if (pool.num_pages <= 0 || pool.page_size <= 0 || pool.kv_heads <= 0 || pool.head_dim <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "pool descriptor has a non-positive field");
+    if (num_tokens < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if ((static_cast<int64_t>(pool.kv_heads) * pool.head_dim * 2) % 16 != 0)
+        return fail(KVC_ERR_UNSUPPORTED, "kv_heads * head_dim * 2 must be a multiple of 16");
+    if (num_tokens == 0)
+        return ok();
+    if (!k_pool || !v_pool || !k_new || !v_new || !slot_mapping)
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(KVC_ERR_INVALID_ARG, "pools and new K/V must be 16-byte aligned");
+    if (static_cast<int64_t>(pool.num_pages) * pool.page_size >= (int64_t(1) << 31))
+        return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
+    cudaError_t err = kvc::launch_store(k_pool, v_pool, pool.kv_heads, pool.head_dim,
+                                        pool.num_pages * pool.page_size, k_new,
+                                        v_new, slot_mapping, num_tokens,
+                                        static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "store launch");
+}
+
+kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
+                           int32_t max_ctx, int32_t num_splits, int32_t *splits_out,
+                           int32_t *chunk_out, size_t *workspace_bytes_out)
+{
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    if ((st = check_group(pool, q_heads)) != KVC_OK)
+        return st;
+    if (num_seqs < 0 || max_ctx < 0 || num_splits < 0)
+        return fail(KVC_ERR_INVALID_ARG, "negative num_seqs, max_ctx or num_splits");
+    const Plan p = make_plan(num_seqs, q_heads, pool, max_ctx, num_splits);
+    if (splits_out)
+        *splits_out = p.splits;
+    if (chunk_out)
+        *chunk_out = p.chunk;
+    if (workspace_bytes_out)
+        *workspace_bytes_out = p.ws_bytes;
+    return ok();
+}
+
+kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k_pool,
+                      const void *v_pool, kvc_pool_desc pool, const int32_t *block_table,
+                      int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs,
+                      int32_t max_ctx, int32_t q_heads, float scale, int32_t num_splits,
+                      void *workspace, size_t workspace_bytes, void *stream)
+{
+    kvc_status st = check_attention_args(out, out_dtype, q, k_pool, v_pool, pool, block_table,
+                                         bt_stride, context_lens, num_seqs, max_ctx, q_heads);
+    if (st != KVC_OK)
+        return st;
+    if (num_splits < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_splits %d", num_splits);
+    if (num_seqs == 0)
+        return ok();
+    const Plan p = make_plan(num_seqs, q_heads, pool, max_ctx, num_splits);
+    if (p.splits > 1) {
+        if (workspace == nullptr || workspace_bytes < p.ws_bytes)
+            return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given",
+                        p.ws_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+        if (!aligned16(workspace))
+            return fail(KVC_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    }
+    CUtensorMap tk, tv;
+    if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
+        return st;
+    if ((st = pool_tensor_map(v_pool, pool, &tv)) != KVC_OK)
+        return st;
+    kvc::DecodeLaunch l;
+    l.q = q;
+    l.out = out;
+    l.out_f32 = out_dtype == KVC_F32;
+    l.part_o = static_cast<float *>(workspace);
+    l.part_lse = p.splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                          p.lse_offset)
+                              : nullptr;
+    l.block_table = block_table;
+    l.bt_stride = bt_stride;
+    l.context_lens = context_lens;
+    l.num_seqs = num_seqs;
+    l.q_heads = q_heads;
+    l.kv_heads = pool.kv_heads;
+    l.head_dim = pool.head_dim;
+    l.page_size = pool.page_size;
+    l.chunk = p.chunk;
+    l.n_split = p.splits;
+    l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = kvc::launch_decode(l, tk, tv, s);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "decode launch");
+    if (p.splits > 1) {
+        err = kvc::launch_merge(out, l.out_f32, l.part_o, l.part_lse, num_seqs * q_heads,
+                                p.splits, pool.head_dim, nullptr, s);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "merge launch");
+    }
+    return ok();
+}
+
+kvc_status kvc_merge(void *out, int32_t out_dtype, const float *partial_o,
+                     const float *partial_lse, int32_t rows, int32_t num_splits,
+                     int32_t head_dim, float *lse_out, void *stream)
+{
+    if (out_dtype != KVC_BF16 && out_dtype != KVC_F32)
+        return fail(KVC_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (rows < 0 || num_splits <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "rows %d, num_splits %d", rows, num_splits);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(KVC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+    if (rows == 0)
+        return ok();
+    if (!out || !partial_o || !partial_lse)
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(partial_o) || !aligned16(out))
+        return fail(KVC_ERR_INVALID_ARG, "partial_o and out must be 16-byte aligned");
+    cudaError_t err = kvc::launch_merge(out, out_dtype == KVC_F32, partial_o, partial_lse, rows,
+                                        num_splits, head_dim, lse_out,
+                                        static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "merge launch");
+}
+
+kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k_pool,
+                      const void *v_pool, kvc_pool_desc pool, const int32_t *block_table,
+                      int32_t bt_stride, const int32_t *q_indptr,
+                      const int32_t *context_lens, int32_t num_seqs, int32_t num_tokens,
+                      int32_t max_q_len, int32_t max_ctx, int32_t q_heads, float scale,
+                      void *stream)
+{
+    kvc_status st = check_attention_args(out, out_dtype, q, k_pool, v_pool, pool, block_table,
+                                         bt_stride, context_lens, num_seqs, max_ctx, q_heads);
+    if (st != KVC_OK)
+        return st;
+    if (num_tokens < 0 || max_q_len < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_tokens %d, max_q_len %d", num_tokens, max_q_len);
+    if (num_seqs > 0 && q_indptr == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "q_indptr is required");
+    if (static_cast<int64_t>(max_q_len) * (q_heads / pool.kv_heads) > (int64_t(1) << 30))
+        return fail(KVC_ERR_INVALID_ARG, "max_q_len too large");
+    if (num_seqs == 0 || num_tokens == 0 || max_q_len == 0)
+        return ok();
+    CUtensorMap tk, tv;
+    if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
+        return st;
+    if ((st = pool_tensor_map(v_pool, pool, &tv)) != KVC_OK)
+        return st;
+    kvc::AppendLaunch l;
+    l.q = q;
+    l.out = out;
+    l.out_f32 = out_dtype == KVC_F32;
+    l.block_table = block_table;
+    l.bt_stride = bt_stride;
+    l.q_indptr = q_indptr;
+    l.context_lens = context_lens;
+    l.num_seqs = num_seqs;
+    l.num_tokens = num_tokens;
+    l.max_q_len = max_q_len;
+    l.q_heads = q_heads;
+    l.kv_heads = pool.kv_heads;
+    l.head_dim = pool.head_dim;
+    l.page_size = pool.page_size;
+    l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    cudaError_t err = kvc::launch_append(l, tk, tv, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");
+}
+
+kvc_status kvc_device_errors(uint32_t *flags_out)
+{
+    if (flags_out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "flags_out is null");
+    uint32_t a = 0, b = 0, c = 0;
+    cudaError_t err = kvc::read_and_clear_decode_errors(&a);
+    if (err == cudaSuccess)
+        err = kvc::read_and_clear_append_errors(&b);
+    if (err == cudaSuccess)
+        err = kvc::read_and_clear_store_errors(&c);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "reading the device error word");
+    *flags_out = a | b | c;
+    return *flags_out ? fail(KVC_ERR_DEVICE, "device error flags 0x%x", *flags_out) : ok();
+}
+
+}  // extern "C"

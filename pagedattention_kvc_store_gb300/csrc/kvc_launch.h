@@ -1,0 +1,61 @@
+// kvc_launch.h -- host-side launchers of the kvc kernels (internal; the C ABI is kvc.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvc {
+
+struct DecodeLaunch {
+    const void *q;
+    void *out;
+    int out_f32;
+    float *part_o;            // [S][Hq][n_split][D] when n_split > 1
+    float *part_lse;          // [S][Hq][n_split]
+    const int32_t *block_table;
+    int bt_stride;
+    const int32_t *context_lens;
+    int num_seqs, q_heads, kv_heads, head_dim, page_size;
+    int chunk, n_split;
+    float scale;
+};
+
+struct AppendLaunch {
+    const void *q;
+    void *out;
+    int out_f32;
+    const int32_t *block_table;
+    int bt_stride;
+    const int32_t *q_indptr;
+    const int32_t *context_lens;
+    int num_seqs, num_tokens, max_q_len, q_heads, kv_heads, head_dim, page_size;
+    float scale;
+};
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int bt_stride,
+                                const int32_t *context_lens, const int32_t *q_indptr,
+                                int num_seqs, int num_tokens, int max_q_len, int page_size,
+                                cudaStream_t stream);
+cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
+                         int num_slots, const void *k_new, const void *v_new,
+                         const int32_t *slots, int num_tokens, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeLaunch &a, const CUtensorMap &tmap_k,
+                          const CUtensorMap &tmap_v, cudaStream_t stream);
+cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const float *part_lse,
+                         int rows, int n_split, int head_dim, float *lse_out,
+                         cudaStream_t stream);
+cudaError_t launch_append(const AppendLaunch &a, const CUtensorMap &tmap_k,
+                          const CUtensorMap &tmap_v, cudaStream_t stream);
+
+// Device error words, one per translation unit that owns bounded waits.
+cudaError_t read_and_clear_decode_errors(uint32_t *flags);
+cudaError_t read_and_clear_append_errors(uint32_t *flags);
+cudaError_t read_and_clear_store_errors(uint32_t *flags);
+
+// Stage geometry shared by the decode and append pipelines.
+constexpr int kStageKeys = 64;   // positions per pipeline stage
+
+}  // namespace kvc

@@ -1,0 +1,169 @@
+// kvc_store.cu -- slot mapping and the paged KV store.
+//
+// Slot mapping: TileInfer.jl "KV cache", "Pages and block tables" (a token's slot is its
+// page from the block table times the page size, plus its offset in the page).
+// Store: same section (the new keys and values are written at their slots) and "KV Cache
+// Management and PagedAttention", "Grow the allocation as generation proceeds".
+//
+// Both are HBM-bound copies.  The store moves each token's (kv_heads * head_dim) bf16 row
+// -- contiguous in the NHD pool -- with 16-byte vector loads and stores, one thread per
+// 16-byte chunk, grid-stride over a grid sized in multiples of the SM count.
+#include "kvc_device.cuh"
+#include "kvc_launch.h"
+
+namespace kvc {
+
+namespace {
+
+__device__ uint32_t g_store_errors;
+
+// One thread per new token of a decode batch (one new token per sequence).
+__global__ void slot_mapping_decode_kernel(int32_t *__restrict__ slots,
+                                           const int32_t *__restrict__ block_table,
+                                           int bt_stride,
+                                           const int32_t *__restrict__ context_lens,
+                                           int num_seqs, int page_size)
+{
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= num_seqs)
+        return;
+    const int position = context_lens[s] - 1;
+    int slot = -1;
+    if (position >= bt_stride * page_size) {
+        atomicOr(&g_store_errors, kErrContextRange);
+    } else if (position >= 0) {
+        const int page = block_table[static_cast<size_t>(s) * bt_stride + position / page_size];
+        slot = page * page_size + position % page_size;
+    }
+    slots[s] = slot;
+}
+
+// One block per sequence, threads over its new tokens.
+__global__ void slot_mapping_ragged_kernel(int32_t *__restrict__ slots,
+                                           const int32_t *__restrict__ block_table,
+                                           int bt_stride,
+                                           const int32_t *__restrict__ context_lens,
+                                           const int32_t *__restrict__ q_indptr,
+                                           int page_size)
+{
+    const int s = blockIdx.x;
+    const int first = q_indptr[s];
+    const int q_len = q_indptr[s + 1] - first;
+    const int ctx = context_lens[s];
+    const int32_t *row = block_table + static_cast<size_t>(s) * bt_stride;
+    for (int i = threadIdx.x; i < q_len; i += blockDim.x) {
+        const int position = ctx - q_len + i;
+        int slot = -1;
+        if (position >= bt_stride * page_size)
+            atomicOr(&g_store_errors, kErrContextRange);
+        else if (position >= 0)
+            slot = row[position / page_size] * page_size + position % page_size;
+        slots[first + i] = slot;
+    }
+}
+
+__device__ __forceinline__ uint4 load_streaming(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// chunks = kv_heads * head_dim * 2 / 16 per token row.
+__global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
+                                                    uint4 *__restrict__ v_pool,
+                                                    const uint4 *__restrict__ k_new,
+                                                    const uint4 *__restrict__ v_new,
+                                                    const int32_t *__restrict__ slots,
+                                                    int num_tokens, int chunks, int num_slots)
+{
+    const size_t total = static_cast<size_t>(num_tokens) * chunks;
+    const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += step) {
+        const int t = static_cast<int>(i / chunks);
+        const int c = static_cast<int>(i - static_cast<size_t>(t) * chunks);
+        const int slot = __ldg(slots + t);
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {   // past the pool: skip the token, flag the call
+            if (c == 0)
+                atomicOr(&g_store_errors, kErrSlotRange);
+            continue;
+        }
+        const size_t dst = static_cast<size_t>(slot) * chunks + c;
+        const uint4 kv = load_streaming(k_new + i);
+        const uint4 vv = load_streaming(v_new + i);
+        k_pool[dst] = kv;
+        v_pool[dst] = vv;
+    }
+}
+
+int sm_count()
+{
+    static int count = 0;
+    if (count == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            count = n;
+        else
+            count = 152;
+    }
+    return count;
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int bt_stride,
+                                const int32_t *context_lens, const int32_t *q_indptr,
+                                int num_seqs, int num_tokens, int max_q_len, int page_size,
+                                cudaStream_t stream)
+{
+    (void)num_tokens;
+    if (num_seqs == 0)
+        return cudaSuccess;
+    if (q_indptr == nullptr) {
+        const int threads = 128;
+        slot_mapping_decode_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
+            slots, block_table, bt_stride, context_lens, num_seqs, page_size);
+    } else {
+        int threads = ((max_q_len + 31) / 32) * 32;
+        threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
+        slot_mapping_ragged_kernel<<<num_seqs, threads, 0, stream>>>(
+            slots, block_table, bt_stride, context_lens, q_indptr, page_size);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
+                         int num_slots, const void *k_new, const void *v_new,
+                         const int32_t *slots, int num_tokens, cudaStream_t stream)
+{
+    if (num_tokens == 0)
+        return cudaSuccess;
+    const int chunks = kv_heads * head_dim * 2 / 16;
+    const size_t total = static_cast<size_t>(num_tokens) * chunks;
+    const int threads = 256;
+    const size_t wanted = (total + threads - 1) / threads;
+    const size_t cap = static_cast<size_t>(sm_count()) * 8;
+    const int blocks = static_cast<int>(wanted < cap ? wanted : cap);
+    store_kernel<<<blocks, threads, 0, stream>>>(
+        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
+        num_tokens, chunks, num_slots);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_store_errors(uint32_t *flags)
+{
+    uint32_t zero = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(flags, g_store_errors, sizeof(uint32_t));
+    if (err != cudaSuccess)
+        return err;
+    return cudaMemcpyToSymbol(g_store_errors, &zero, sizeof(uint32_t));
+}
+
+}  // namespace kvc

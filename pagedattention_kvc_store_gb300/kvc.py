@@ -1,0 +1,223 @@
+"""Thin ctypes binding of libkvc (the C ABI in include/kvc.h).
+
+Argument marshalling only: every step of the store and of the attention runs in the CUDA
+kernels behind these calls.  Tensors are torch CUDA tensors; the functions pass their
+device pointers and the current CUDA stream.  There is no CPU path: without the compiled
+library or a GPU these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+KVC_BF16 = 0
+KVC_F32 = 1
+
+STATUS = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_UNSUPPORTED",
+          3: "KVC_ERR_WORKSPACE", 4: "KVC_ERR_CUDA", 5: "KVC_ERR_DEVICE"}
+
+# Every entry point declared in include/kvc.h.
+EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store",
+           "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors")
+
+
+class KvcError(RuntimeError):
+    def __init__(self, call: str, status: int, detail: str):
+        super().__init__(f"{call}: {STATUS.get(status, status)}: {detail}")
+        self.call = call
+        self.status = status
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvc.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libkvc.so not found at {path}")
+            L = ctypes.CDLL(path)
+            i32, p, sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+            f = ctypes.c_float
+            L.kvc_status_string.restype = ctypes.c_char_p
+            L.kvc_status_string.argtypes = [ctypes.c_int]
+            L.kvc_last_error.restype = ctypes.c_char_p
+            L.kvc_last_error.argtypes = []
+            L.kvc_slot_mapping.restype = ctypes.c_int
+            L.kvc_slot_mapping.argtypes = [p, p, i32, p, p, i32, i32, i32, i32, p]
+            L.kvc_store.restype = ctypes.c_int
+            L.kvc_store.argtypes = [p, p, PoolDesc, p, p, p, i32, p]
+            L.kvc_decode.restype = ctypes.c_int
+            L.kvc_decode.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, i32, i32, i32, f,
+                                     i32, p, sz, p]
+            L.kvc_decode_plan.restype = ctypes.c_int
+            L.kvc_decode_plan.argtypes = [i32, i32, PoolDesc, i32, i32,
+                                          ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                          ctypes.POINTER(sz)]
+            L.kvc_merge.restype = ctypes.c_int
+            L.kvc_merge.argtypes = [p, i32, p, p, i32, i32, i32, p, p]
+            L.kvc_append.restype = ctypes.c_int
+            L.kvc_append.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, p, i32, i32, i32,
+                                     i32, i32, f, p]
+            L.kvc_device_errors.restype = ctypes.c_int
+            L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            _lib = L
+    return _lib
+
+
+def _check(call: str, status: int) -> None:
+    if status != 0:
+        detail = lib().kvc_last_error().decode(errors="replace")
+        raise KvcError(call, status, detail)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(name: str, t: torch.Tensor, dtype=None, contiguous=True) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libkvc has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _out_dtype(out: torch.Tensor) -> int:
+    if out.dtype == torch.bfloat16:
+        return KVC_BF16
+    if out.dtype == torch.float32:
+        return KVC_F32
+    raise TypeError(f"out must be bfloat16 or float32, got {out.dtype}")
+
+
+def pool_desc(k_pool: torch.Tensor) -> PoolDesc:
+    """Descriptor of a [num_pages, page_size, kv_heads, head_dim] bf16 pool."""
+    if k_pool.dim() != 4:
+        raise ValueError("a pool is [num_pages, page_size, kv_heads, head_dim]")
+    n, P, h, d = (int(x) for x in k_pool.shape)
+    return PoolDesc(n, P, h, d)
+
+
+def kvc_slot_mapping(slot_mapping: torch.Tensor, block_table: torch.Tensor,
+                     context_lens: torch.Tensor, q_indptr: Optional[torch.Tensor],
+                     page_size: int, max_q_len: int = 1, stream=None) -> None:
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if q_indptr is not None:
+        _cuda("q_indptr", q_indptr, torch.int32)
+    S = int(context_lens.shape[0])
+    _check("kvc_slot_mapping", lib().kvc_slot_mapping(
+        _ptr(slot_mapping), _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
+        _ptr(q_indptr), S, int(slot_mapping.shape[0]), int(max_q_len), int(page_size),
+        _stream(stream)))
+
+
+def kvc_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
+              v_new: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_new", k_new),
+                    ("v_new", v_new)):
+        _cuda(name, t, torch.bfloat16)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    _check("kvc_store", lib().kvc_store(
+        _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool), _ptr(k_new), _ptr(v_new),
+        _ptr(slot_mapping), int(slot_mapping.shape[0]), _stream(stream)))
+
+
+def kvc_decode_plan(num_seqs: int, q_heads: int, pool: PoolDesc, max_ctx: int,
+                    num_splits: int = 0) -> Tuple[int, int, int]:
+    """(splits, chunk, workspace_bytes) that kvc_decode will use."""
+    splits, chunk, ws = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    _check("kvc_decode_plan", lib().kvc_decode_plan(
+        int(num_seqs), int(q_heads), pool, int(max_ctx), int(num_splits),
+        ctypes.byref(splits), ctypes.byref(chunk), ctypes.byref(ws)))
+    return splits.value, chunk.value, ws.value
+
+
+def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+               block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
+               scale: float = 0.0, num_splits: int = 0,
+               workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("kvc_decode", lib().kvc_decode(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
+        int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
+        int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def kvc_merge(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,
+              lse_out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """partial_o [rows, splits, D] fp32, partial_lse [rows, splits] fp32 -> out [rows, D]."""
+    _cuda("out", out)
+    _cuda("partial_o", partial_o, torch.float32)
+    _cuda("partial_lse", partial_lse, torch.float32)
+    if lse_out is not None:
+        _cuda("lse_out", lse_out, torch.float32)
+    rows, splits, d = (int(x) for x in partial_o.shape)
+    _check("kvc_merge", lib().kvc_merge(
+        _ptr(out), _out_dtype(out), _ptr(partial_o), _ptr(partial_lse), rows, splits, d,
+        _ptr(lse_out), _stream(stream)))
+
+
+def kvc_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+               block_table: torch.Tensor, q_indptr: torch.Tensor, context_lens: torch.Tensor,
+               max_q_len: int, max_ctx: int, scale: float = 0.0, stream=None) -> None:
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("q_indptr", q_indptr, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    _check("kvc_append", lib().kvc_append(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(block_table), int(block_table.shape[1]), _ptr(q_indptr), _ptr(context_lens),
+        int(context_lens.shape[0]), int(q.shape[0]), int(max_q_len), int(max_ctx),
+        int(q.shape[1]), float(scale), _stream(stream)))
+
+
+def kvc_device_errors() -> int:
+    flags = ctypes.c_uint32(0)
+    status = lib().kvc_device_errors(ctypes.byref(flags))
+    if status not in (0, 5):
+        _check("kvc_device_errors", status)
+    return int(flags.value)

@@ -1,0 +1,106 @@
+"""GPU parity of paged append (causal chunked prefill over a cached prefix) against the
+fp64 oracle, including the KV-rewind flow: append, truncate, append again over stale slots."""
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_kvc_store_gb300 as kvc
+from harness import GpuRun, OracleRun, assert_attention_close, out_to_f64, sample_seqs
+from workloads import build_case, config_case, normal_bf16
+from workloads.device import bf16_tensor, i32_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_rewind_append_full_size_sampled(page_size):
+    case = config_case(4, page_size=page_size)
+    g = GpuRun(case, decode=False)
+    g.store()
+    out = out_to_f64(g.attend(torch.bfloat16))
+    seqs = sample_seqs(case.num_seqs, 48, seed=page_size)
+    ref, _, rows = OracleRun(case).attention(seqs)
+    assert_attention_close(out[rows], ref, f"rewind append P={page_size}")
+
+
+@pytest.mark.parametrize("P,Hq,Hkv,D", [(16, 32, 8, 128), (32, 8, 8, 64), (64, 16, 2, 128),
+                                        (16, 16, 2, 64), (64, 8, 1, 128)])
+def test_append_ragged_shapes(P, Hq, Hkv, D):
+    case = build_case(P + Hq * 3 + D, name="ragged-append", page_size=P, q_heads=Hq,
+                      kv_heads=Hkv, head_dim=D,
+                      context_lens=lambda rng: rng.integers(1, 420, size=23),
+                      q_lens=lambda ctx: np.minimum(ctx, 1 + (ctx * 7) % 97))
+    g = GpuRun(case, decode=False)
+    g.store()
+    for dtype in (torch.float32, torch.bfloat16):
+        out = out_to_f64(g.attend(dtype))
+        ref, _ = OracleRun(case).attention()
+        assert_attention_close(out, ref, f"ragged append {P},{Hq},{Hkv},{D},{dtype}")
+
+
+def test_append_without_prefix_and_single_token():
+    # ctx == q_len: plain causal self-attention; q_len == 1: decode
+    ctx = np.array([1, 2, 17, 64, 65, 130, 5, 300])
+    qlen = np.array([1, 2, 17, 64, 1, 1, 5, 1])
+    case = build_case(77, name="edges", page_size=16, q_heads=8, kv_heads=2, head_dim=128,
+                      context_lens=lambda rng: ctx, q_lens=lambda c: qlen)
+    g = GpuRun(case, decode=False)
+    g.store()
+    out = out_to_f64(g.attend(torch.float32))
+    ref, _ = OracleRun(case).attention()
+    assert_attention_close(out, ref, "append edges")
+
+
+def test_append_of_one_token_matches_decode():
+    case = config_case(2, num_seqs=24)
+    g = GpuRun(case, decode=False)       # same case through the append path
+    g.store()
+    out_a = out_to_f64(g.attend(torch.float32))
+    gd = GpuRun(case, decode=True)
+    gd.store()
+    out_d = out_to_f64(gd.attend(torch.float32, 1))
+    assert np.abs(out_a - out_d).max() < 2e-3
+
+
+def test_kv_rewind_truncate_and_second_question():
+    # Quail "KV", "KV rewind": keep the document's KV, drop the question's, ask the next one.
+    n_docs = 64
+    case = config_case(4, page_size=16, num_seqs=n_docs)
+    g = GpuRun(case, decode=False)
+    g.store()
+    first = out_to_f64(g.attend(torch.bfloat16))
+    o = OracleRun(case)
+    ref1, _ = o.attention()
+    assert_attention_close(first, ref1, "first question")
+
+    # truncate every document back to its 300 cached positions: pages 22 -> 19
+    alloc = case.allocator
+    for s in case.seqs:
+        alloc.truncate(s, 300)
+        assert len(alloc.pages[s]) == 19
+    # the second question: 50 new tokens per document, pages reserved again
+    for s in case.seqs:
+        alloc.reserve(s, 50)
+    case.block_table = alloc.table(case.seqs, case.block_table.shape[1])
+    ss = np.random.SeedSequence(4242).spawn(2)
+    case.q = normal_bf16(ss[0], case.q.shape)
+    new = normal_bf16(ss[1], (2,) + case.k_new.shape)
+    case.k_new, case.v_new = np.ascontiguousarray(new[0]), np.ascontiguousarray(new[1])
+
+    # GPU: continue on the same device pools (stale slots 300.. still hold question 1)
+    g.d.block_table = i32_tensor(case.block_table, "cuda")
+    g.d.q = bf16_tensor(case.q, "cuda")
+    g.d.k_new = bf16_tensor(case.k_new, "cuda")
+    g.d.v_new = bf16_tensor(case.v_new, "cuda")
+    g.store()
+    second = out_to_f64(g.attend(torch.bfloat16))
+    # oracle: continue on its own pools after its own first store
+    case.k_pool, case.v_pool = o.k_pool, o.v_pool
+    ref2, _ = OracleRun(case).attention()
+    assert_attention_close(second, ref2, "second question after rewind")
+    assert np.abs(second - first).max() > 0.1   # a different question, a different answer
+
+
+def test_no_device_errors_were_raised():
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0

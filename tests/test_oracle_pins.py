@@ -404,3 +404,9 @@ def test_sharing_plan_last_token_cap():
     docs = [list(range(32)), list(range(32))]      # identical: cap at len - 1 = 31 -> 16
     order, parent, shared = sharing_plan(docs, P)
     assert shared == [0, 16] and parent == [None, 0]
+
+
+def test_slot_mapping_marks_tokens_without_a_position_as_padding():
+    bt = np.array([[3, 0, 5, 0]], dtype=np.int32)
+    slots = oracle.slot_mapping(bt, np.array([1]), np.array([0, 3]), 4)
+    assert slots.tolist() == [-1, -1, 12]

@@ -53,13 +53,14 @@ def _shared_prefix_groups(n_groups: int, members: int, prefix: int, vocab: int =
 
 
 def config_case(k: int, *, page_size: int = None, num_seqs: int = None,
-                poison: bool = True) -> Case:
+                poison: bool = True, seed: int = None) -> Case:
     """Build config k.  ``page_size`` overrides config 4's page size (16 or 64);
-    ``num_seqs`` shrinks configs 2-5 to their first sequences / groups / documents (for
-    quick checks; the full configs leave it None)."""
+    ``num_seqs`` shrinks configs 2-5 to fewer sequences / groups / documents (for quick
+    checks; the full configs leave it None); ``seed`` replaces the config's seed (another
+    batch drawn by the same recipe)."""
     cfg = dict(CONFIGS[k])
     name = cfg.pop("name")
-    seed = SEED_BASE + k
+    seed = SEED_BASE + k if seed is None else seed
     if k == 1:
         return build_case(seed, name=name, **cfg, num_pages=32, bt_width=32,
                           context_lens=lambda rng: np.array([1, 17, 33, 100]),
