@@ -149,6 +149,35 @@ kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool
                            int32_t *chunk_out, size_t *workspace_bytes_out);
 
 /*
+ * kvc_decode_noalloc -- kvc_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers of this library
+ * that are handed only their input and output buffers: an operator plugged into an
+ * inference engine that planned every byte of device memory when it started, or a serving
+ * loop that must not call cudaMalloc while it runs, because that call can synchronise the
+ * whole device and take an unbounded time.  Such a caller cannot provide kvc_decode's
+ * workspace.  Here the split partials go instead to scratch memory inside the library: one
+ * statically sized device array of KVC_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
+ * library holds until the process exits.  Nothing is allocated by the call.
+ *
+ * Arguments and result are those of kvc_decode without the workspace.  A split plan that
+ * needs more than KVC_NOALLOC_SCRATCH_BYTES of partials (see kvc_decode_plan) is rejected
+ * with KVC_ERR_WORKSPACE and nothing is enqueued: ask for fewer splits, or use kvc_decode
+ * with a workspace of your own.  The first call on each device (the current device) looks
+ * up where the scratch array lives on that device; make that first call before any stream
+ * capture.  Every call uses the same array, which keeps what the last call wrote; nothing
+ * in it has to start at zero, but two calls whose kernels overlap on the GPU (launched on
+ * different streams with no ordering between them) race on it, so the caller must order them.
+ */
+#define KVC_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+kvc_status kvc_decode_noalloc(void *out, int32_t out_dtype, const void *q,
+                              const void *k_pool, const void *v_pool, kvc_pool_desc pool,
+                              const int32_t *block_table, int32_t bt_stride,
+                              const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                              int32_t q_heads, float scale, int32_t num_splits, void *stream);
+
+/*
  * kvc_merge -- combine split partials by log-sum-exp.  For every row r:
  *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M);
  *   out[r] = sum_j w_j partial_o[r][j] / sum_j w_j;   lse_out[r] = M + log(sum_j w_j).

@@ -3,10 +3,12 @@
 The product is the C-ABI library libkvc.so (include/kvc.h), built from ``csrc/`` by
 ``build.build()``; ``kvc`` is its thin Python binding (same entry-point names).
 """
-from .kvc import (EXPORTS, KVC_BF16, KVC_F32, KvcError, PoolDesc, kvc_append, kvc_decode,
-                  kvc_decode_plan, kvc_device_errors, kvc_merge, kvc_slot_mapping, kvc_store,
-                  lib, library_path, pool_desc)
+from .kvc import (EXPORTS, KVC_BF16, KVC_F32, NOALLOC_SCRATCH_BYTES, KvcError, PoolDesc,
+                  kvc_append, kvc_decode, kvc_decode_noalloc, kvc_decode_plan,
+                  kvc_device_errors, kvc_merge, kvc_slot_mapping, kvc_store, lib,
+                  library_path, pool_desc)
 
-__all__ = ["EXPORTS", "KVC_BF16", "KVC_F32", "KvcError", "PoolDesc", "kvc_append",
-           "kvc_decode", "kvc_decode_plan", "kvc_device_errors", "kvc_merge",
-           "kvc_slot_mapping", "kvc_store", "lib", "library_path", "pool_desc"]
+__all__ = ["EXPORTS", "KVC_BF16", "KVC_F32", "NOALLOC_SCRATCH_BYTES", "KvcError", "PoolDesc",
+           "kvc_append", "kvc_decode", "kvc_decode_noalloc", "kvc_decode_plan",
+           "kvc_device_errors", "kvc_merge", "kvc_slot_mapping", "kvc_store", "lib",
+           "library_path", "pool_desc"]

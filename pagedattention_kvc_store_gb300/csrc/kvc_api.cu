@@ -219,6 +219,12 @@ kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *
 
 }  // namespace
 
+int kvc::set_last_error(int status, const char *message)
+{
+    g_last_error = message;
+    return status;
+}
+
 extern "C" {
 
 const char *kvc_status_string(kvc_status status)

@@ -55,6 +55,9 @@ cudaError_t read_and_clear_decode_errors(uint32_t *flags);
 cudaError_t read_and_clear_append_errors(uint32_t *flags);
 cudaError_t read_and_clear_store_errors(uint32_t *flags);
 
+// Record a failure reason for kvc_last_error() from another translation unit.
+int set_last_error(int status, const char *message);
+
 // Stage geometry shared by the decode and append pipelines.
 constexpr int kStageKeys = 64;   // positions per pipeline stage
 

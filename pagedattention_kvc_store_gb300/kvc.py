@@ -24,7 +24,11 @@ STATUS = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_UNSUPPORTED",
 
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store",
-           "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors")
+           "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
+           "kvc_decode_noalloc")
+
+# Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class KvcError(RuntimeError):
@@ -78,6 +82,9 @@ def lib() -> ctypes.CDLL:
             L.kvc_append.restype = ctypes.c_int
             L.kvc_append.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, p, i32, i32, i32,
                                      i32, i32, f, p]
+            L.kvc_decode_noalloc.restype = ctypes.c_int
+            L.kvc_decode_noalloc.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, i32, i32,
+                                             i32, f, i32, p]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -213,6 +220,29 @@ def kvc_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
         _ptr(block_table), int(block_table.shape[1]), _ptr(q_indptr), _ptr(context_lens),
         int(context_lens.shape[0]), int(q.shape[0]), int(max_q_len), int(max_ctx),
         int(q.shape[1]), float(scale), _stream(stream)))
+
+
+def kvc_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                       v_pool: torch.Tensor, block_table: torch.Tensor,
+                       context_lens: torch.Tensor, max_ctx: int, scale: float = 0.0,
+                       num_splits: int = 0, stream=None) -> None:
+    """kvc_decode without a workspace, for callers that may not allocate device memory:
+    the split partials go to scratch memory the library owns (NOALLOC_SCRATCH_BYTES on
+    every GPU that loads it).  Plans needing more scratch than that raise KvcError
+    (KVC_ERR_WORKSPACE).  Calls share that scratch, so calls whose kernels could overlap
+    on the GPU must be ordered by the caller; call it once on a device before any stream
+    capture."""
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    _check("kvc_decode_noalloc", lib().kvc_decode_noalloc(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
+        int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
+        int(num_splits), _stream(stream)))
 
 
 def kvc_device_errors() -> int:
