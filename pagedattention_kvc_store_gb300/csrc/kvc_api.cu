@@ -136,58 +136,105 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-struct MapEntry {
+// A tiled bf16 tensor map with 128-byte swizzle (boxes 64 elements wide), memoised by
+// (address, shape, box, device).
+struct MapKey {
     const void *ptr;
-    kvc_pool_desc pool;
     int device;
+    int rank;
+    cuuint64_t dims[4];
+    cuuint64_t strides[3];
+    cuuint32_t box[4];
+    bool operator==(const MapKey &o) const
+    {
+        if (ptr != o.ptr || device != o.device || rank != o.rank)
+            return false;
+        for (int i = 0; i < rank; ++i)
+            if (dims[i] != o.dims[i] || box[i] != o.box[i] ||
+                (i + 1 < rank && strides[i] != o.strides[i]))
+                return false;
+        return true;
+    }
+};
+
+struct MapEntry {
+    MapKey key;
     CUtensorMap map;
 };
 
 std::mutex g_map_mutex;
-std::vector<MapEntry> g_maps;   // most recent last, at most 16
+std::vector<MapEntry> g_maps;   // most recent last, at most 32
 
-kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
+kvc_status tensor_map(MapKey key, CUtensorMap *out)
 {
-    int device = 0;
-    cudaError_t err = cudaGetDevice(&device);
+    cudaError_t err = cudaGetDevice(&key.device);
     if (err != cudaSuccess)
         return cuda_fail(err, "cudaGetDevice");
     {
         std::lock_guard<std::mutex> lock(g_map_mutex);
-        for (size_t i = g_maps.size(); i-- > 0;) {
-            const MapEntry &e = g_maps[i];
-            if (e.ptr == base && e.device == device && e.pool.num_pages == pool.num_pages &&
-                e.pool.page_size == pool.page_size && e.pool.kv_heads == pool.kv_heads &&
-                e.pool.head_dim == pool.head_dim) {
-                *out = e.map;
+        for (size_t i = g_maps.size(); i-- > 0;)
+            if (g_maps[i].key == key) {
+                *out = g_maps[i].map;
                 return KVC_OK;
             }
-        }
     }
     auto fn = encode_fn();
     if (fn == nullptr)
         return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(pool.head_dim),
-                                static_cast<cuuint64_t>(pool.kv_heads),
-                                static_cast<cuuint64_t>(pool.num_pages) * pool.page_size};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pool.head_dim) * 2,
-                                   static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim * 2};
-    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(pool.page_size)};
-    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     CUtensorMap map;
-    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(key.rank),
+                    const_cast<void *>(key.ptr), key.dims, key.strides, key.box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)",
                     static_cast<int>(r));
     std::lock_guard<std::mutex> lock(g_map_mutex);
-    if (g_maps.size() >= 16)
+    if (g_maps.size() >= 32)
         g_maps.erase(g_maps.begin());
-    g_maps.push_back(MapEntry{base, pool, device, map});
+    g_maps.push_back(MapEntry{key, map});
     *out = map;
     return KVC_OK;
+}
+
+// Pool viewed as [num_pages * page_size][kv_heads][head_dim]; box [page_size][1][64].
+kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
+{
+    MapKey k{};
+    k.ptr = base;
+    k.rank = 3;
+    k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
+    k.dims[1] = static_cast<cuuint64_t>(pool.kv_heads);
+    k.dims[2] = static_cast<cuuint64_t>(pool.num_pages) * pool.page_size;
+    k.strides[0] = static_cast<cuuint64_t>(pool.head_dim) * 2;
+    k.strides[1] = static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim * 2;
+    k.box[0] = 64;
+    k.box[1] = 1;
+    k.box[2] = static_cast<cuuint32_t>(pool.page_size);
+    return tensor_map(k, out);
+}
+
+// Queries [T][q_heads][head_dim] viewed as [T][kv_heads][G][head_dim]; one box is the
+// 128 / G tokens x G heads of one kv head (128 rows of 64 columns).
+kvc_status query_tensor_map(const void *q, int32_t num_tokens, int32_t kv_heads, int32_t group,
+                            int32_t head_dim, CUtensorMap *out)
+{
+    MapKey k{};
+    k.ptr = q;
+    k.rank = 4;
+    k.dims[0] = static_cast<cuuint64_t>(head_dim);
+    k.dims[1] = static_cast<cuuint64_t>(group);
+    k.dims[2] = static_cast<cuuint64_t>(kv_heads);
+    k.dims[3] = static_cast<cuuint64_t>(num_tokens);
+    k.strides[0] = static_cast<cuuint64_t>(head_dim) * 2;
+    k.strides[1] = static_cast<cuuint64_t>(group) * head_dim * 2;
+    k.strides[2] = static_cast<cuuint64_t>(kv_heads) * group * head_dim * 2;
+    k.box[0] = 64;
+    k.box[1] = static_cast<cuuint32_t>(group);
+    k.box[2] = 1;
+    k.box[3] = static_cast<cuuint32_t>(128 / group);
+    return tensor_map(k, out);
 }
 
 kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *q,
@@ -410,10 +457,13 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
         return fail(KVC_ERR_INVALID_ARG, "max_q_len too large");
     if (num_seqs == 0 || num_tokens == 0 || max_q_len == 0)
         return ok();
-    CUtensorMap tk, tv;
+    CUtensorMap tq, tk, tv;
     if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
         return st;
     if ((st = pool_tensor_map(v_pool, pool, &tv)) != KVC_OK)
+        return st;
+    if ((st = query_tensor_map(q, num_tokens, pool.kv_heads, q_heads / pool.kv_heads,
+                               pool.head_dim, &tq)) != KVC_OK)
         return st;
     kvc::AppendLaunch l;
     l.q = q;
@@ -431,7 +481,7 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
     l.head_dim = pool.head_dim;
     l.page_size = pool.page_size;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
-    cudaError_t err = kvc::launch_append(l, tk, tv, static_cast<cudaStream_t>(stream));
+    cudaError_t err = kvc::launch_append_tc(l, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");
 }
 
@@ -439,15 +489,17 @@ kvc_status kvc_device_errors(uint32_t *flags_out)
 {
     if (flags_out == nullptr)
         return fail(KVC_ERR_INVALID_ARG, "flags_out is null");
-    uint32_t a = 0, b = 0, c = 0;
+    uint32_t a = 0, b = 0, c = 0, d = 0;
     cudaError_t err = kvc::read_and_clear_decode_errors(&a);
     if (err == cudaSuccess)
         err = kvc::read_and_clear_append_errors(&b);
     if (err == cudaSuccess)
         err = kvc::read_and_clear_store_errors(&c);
+    if (err == cudaSuccess)
+        err = kvc::read_and_clear_append_tc_errors(&d);
     if (err != cudaSuccess)
         return cuda_fail(err, "reading the device error word");
-    *flags_out = a | b | c;
+    *flags_out = a | b | c | d;
     return *flags_out ? fail(KVC_ERR_DEVICE, "device error flags 0x%x", *flags_out) : ok();
 }
 

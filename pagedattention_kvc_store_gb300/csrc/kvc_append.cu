@@ -270,12 +270,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t pa[8][2];
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-            const float p0 = fast_exp2(sc[n][0] - mu_a), p1 = fast_exp2(sc[n][1] - mu_a);
-            const float p2 = fast_exp2(sc[n][2] - mu_b), p3 = fast_exp2(sc[n][3] - mu_b);
-            l_a += p0 + p1;
-            l_b += p2 + p3;
-            pa[n][0] = pack_bf16x2(p0, p1);
-            pa[n][1] = pack_bf16x2(p2, p3);
+            pa[n][0] = pack_bf16x2(fast_exp2(sc[n][0] - mu_a), fast_exp2(sc[n][1] - mu_a));
+            pa[n][1] = pack_bf16x2(fast_exp2(sc[n][2] - mu_b), fast_exp2(sc[n][3] - mu_b));
+            l_a += bf16x2_sum(pa[n][0]);
+            l_b += bf16x2_sum(pa[n][1]);
         }
         // O += P V, 16 positions per k-step
 #pragma unroll

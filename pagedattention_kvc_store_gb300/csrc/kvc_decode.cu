@@ -263,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 p[i] = fast_exp2(x[i] - m_use);
-            l_run += (p[0] + p[1]) + (p[2] + p[3]);
             const uint32_t pa0 = pack_bf16x2(p[0], p[1]);   // row r, positions cq, cq+1
             const uint32_t pa2 = pack_bf16x2(p[2], p[3]);   // row r, positions 8+cq, 9+cq
+            l_run += bf16x2_sum(pa0) + bf16x2_sum(pa2);
 #pragma unroll
             for (int dt = 0; dt < D / 16; ++dt) {
                 uint32_t v0, v1, v2, v3;

@@ -49,11 +49,16 @@ cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const floa
                          cudaStream_t stream);
 cudaError_t launch_append(const AppendLaunch &a, const CUtensorMap &tmap_k,
                           const CUtensorMap &tmap_v, cudaStream_t stream);
+// tcgen05 version; tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes.
+cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
+                             const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                             cudaStream_t stream);
 
 // Device error words, one per translation unit that owns bounded waits.
 cudaError_t read_and_clear_decode_errors(uint32_t *flags);
 cudaError_t read_and_clear_append_errors(uint32_t *flags);
 cudaError_t read_and_clear_store_errors(uint32_t *flags);
+cudaError_t read_and_clear_append_tc_errors(uint32_t *flags);
 
 // Record a failure reason for kvc_last_error() from another translation unit.
 int set_last_error(int status, const char *message);

@@ -6,7 +6,7 @@ import torch
 
 import pagedattention_kvc_store_gb300 as kvc
 from harness import GpuRun, OracleRun, assert_attention_close, out_to_f64, sample_seqs
-from workloads import build_case, config_case, normal_bf16
+from workloads import bf16_bits, build_case, config_case, f32_from_bf16, normal_bf16
 from workloads.device import bf16_tensor, i32_tensor
 
 pytestmark = pytest.mark.gpu
@@ -99,6 +99,25 @@ def test_kv_rewind_truncate_and_second_question():
     ref2, _ = OracleRun(case).attention()
     assert_attention_close(second, ref2, "second question after rewind")
     assert np.abs(second - first).max() > 0.1   # a different question, a different answer
+
+
+def test_append_when_later_keys_dominate():
+    # Keys of later pages are scaled up so each row's running max jumps by far more than
+    # 2^8 mid-stream: the kernel must rescale what it has accumulated.
+    case = build_case(31, name="rising", page_size=16, q_heads=16, kv_heads=2, head_dim=128,
+                      context_lens=lambda rng: rng.integers(150, 400, size=9),
+                      q_lens=lambda ctx: np.minimum(ctx, 40))
+    for s in case.seqs:
+        for k, page in enumerate(case.allocator.pages[s]):
+            f = np.float32(1.0 + 6.0 * k)          # page k holds positions 16k .. 16k+15
+            vals = f32_from_bf16(case.k_pool[page]) * f
+            case.k_pool[page] = np.where(case.k_pool[page] == 0x7FC0, case.k_pool[page],
+                                         bf16_bits(vals))
+    g = GpuRun(case, decode=False)
+    g.store()
+    out = out_to_f64(g.attend(torch.float32))
+    ref, _ = OracleRun(case).attention()
+    assert_attention_close(out, ref, "rising keys")
 
 
 def test_no_device_errors_were_raised():
