@@ -427,6 +427,8 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "roofline_frac": round(t_roof / t, 4),
             "store_gbs": round(store_bytes(case) / (statistics.mean(st_ms) / 1e3) / 1e9, 1),
             "gpu_launches": args.append_steps * 3,
+            "traffic": (traffic_from_profile("append_rewind_p16", "kvc_append_tc.cu")
+                        if P == 16 else None),
         }
         del d, out, slots, g1, g2
         torch.cuda.empty_cache()
