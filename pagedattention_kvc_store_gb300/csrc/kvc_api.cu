@@ -198,8 +198,10 @@ kvc_status tensor_map(MapKey key, CUtensorMap *out)
     return KVC_OK;
 }
 
-// Pool viewed as [num_pages * page_size][kv_heads][head_dim]; box [page_size][1][64].
-kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
+// Pool [num_pages * page_size][kv_heads][head_dim] viewed as the 3-D tensor
+// {head_dim, kv head, slot}; one box {64, 1, page_size} is one 64-column half of one page of
+// one kv head (append: a 64-position stage is then [half][64 rows][64], one uniform operand).
+kvc_status pool_tensor_map_halves(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
 {
     MapKey k{};
     k.ptr = base;
@@ -212,6 +214,29 @@ kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensor
     k.box[0] = 64;
     k.box[1] = 1;
     k.box[2] = static_cast<cuuint32_t>(pool.page_size);
+    return tensor_map(k, out);
+}
+
+// Pool [num_pages * page_size][kv_heads][head_dim] viewed as the 4-D tensor
+// {64 columns, slot, column half, kv head}; one box {64, page_size, head_dim / 64, 1} is a whole
+// page of one kv head and lands in shared memory as [half][page_size rows][64 columns]
+// (decode: one TMA instruction per page).
+kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
+{
+    MapKey k{};
+    k.ptr = base;
+    k.rank = 4;
+    k.dims[0] = 64;
+    k.dims[1] = static_cast<cuuint64_t>(pool.num_pages) * pool.page_size;
+    k.dims[2] = static_cast<cuuint64_t>(pool.head_dim / 64);
+    k.dims[3] = static_cast<cuuint64_t>(pool.kv_heads);
+    k.strides[0] = static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim * 2;   // slot
+    k.strides[1] = 128;                                                           // half
+    k.strides[2] = static_cast<cuuint64_t>(pool.head_dim) * 2;                    // kv head
+    k.box[0] = 64;
+    k.box[1] = static_cast<cuuint32_t>(pool.page_size);
+    k.box[2] = static_cast<cuuint32_t>(pool.head_dim / 64);
+    k.box[3] = 1;
     return tensor_map(k, out);
 }
 
@@ -458,9 +483,9 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
     if (num_seqs == 0 || num_tokens == 0 || max_q_len == 0)
         return ok();
     CUtensorMap tq, tk, tv;
-    if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
+    if ((st = pool_tensor_map_halves(k_pool, pool, &tk)) != KVC_OK)
         return st;
-    if ((st = pool_tensor_map(v_pool, pool, &tv)) != KVC_OK)
+    if ((st = pool_tensor_map_halves(v_pool, pool, &tv)) != KVC_OK)
         return st;
     if ((st = query_tensor_map(q, num_tokens, pool.kv_heads, q_heads / pool.kv_heads,
                                pool.head_dim, &tq)) != KVC_OK)
@@ -489,17 +514,15 @@ kvc_status kvc_device_errors(uint32_t *flags_out)
 {
     if (flags_out == nullptr)
         return fail(KVC_ERR_INVALID_ARG, "flags_out is null");
-    uint32_t a = 0, b = 0, c = 0, d = 0;
+    uint32_t a = 0, c = 0, d = 0;
     cudaError_t err = kvc::read_and_clear_decode_errors(&a);
-    if (err == cudaSuccess)
-        err = kvc::read_and_clear_append_errors(&b);
     if (err == cudaSuccess)
         err = kvc::read_and_clear_store_errors(&c);
     if (err == cudaSuccess)
         err = kvc::read_and_clear_append_tc_errors(&d);
     if (err != cudaSuccess)
         return cuda_fail(err, "reading the device error word");
-    *flags_out = a | b | c | d;
+    *flags_out = a | c | d;
     return *flags_out ? fail(KVC_ERR_DEVICE, "device error flags 0x%x", *flags_out) : ok();
 }
 

@@ -13,13 +13,15 @@
 //               page and 64-column half, 128-byte swizzle) through a 2-deep ring;
 //   warp 1      allocates TMEM and issues the MMAs from one thread:
 //                 S = Q K^T   (M 128, N 64, K head_dim)   into TMEM columns [D, D+64)
-//                 O += P V    (M 128, N head_dim, K 64)   into TMEM columns [0, D)
+//                 O += P V    (M 128, N head_dim, K 64)   into TMEM columns [0, D), with P
+//                                                        read from TMEM (two buffers)
 //               and zeroes V rows past the last visible position, so that NaN or Inf left
 //               in unused slots never meets a zero probability inside the tensor core;
 //   warps 2-5   softmax: thread r owns row r (TMEM lane r): reads its S row, applies the
-//               scale and the causal limit, keeps a running max / sum, writes P (bf16,
-//               swizzled) to shared memory for the PV MMA, and at the end normalises its
-//               O row straight from TMEM to global memory.
+//               scale and the causal limit, keeps a running max / sum, writes P (bf16 pairs)
+//               into one of two TMEM buffers for the PV MMA -- so block b + 1's P can be
+//               written while block b's PV product still reads the other -- and at the end
+//               normalises its O row from TMEM through shared memory to global memory.
 // The running max is updated lazily: O is rescaled (in TMEM) only when a row's max grows by
 // more than 2^8, so a block's exponentials do not wait for the previous PV product.  The
 // result is exact either way; probabilities are then at most 2^8 before normalisation.
@@ -47,13 +49,14 @@ struct TcGeom {
     static constexpr int kQBytes = kHalves * kM * 128;
     static constexpr int kTileBytes = kHalves * kBN * 128;   // K or V of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kPBytes = kM * kBN * 2;
     static constexpr int kOffStages = kQBytes;
-    static constexpr int kOffP = kOffStages + kStages * kStageBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
+    static constexpr int kOffBar = kOffStages + kStages * kStageBytes;
     static constexpr size_t kSmemBytes = kOffBar + 128;   // base is 1024-aligned
-    static constexpr uint32_t kTmemCols = D == 64 ? 128 : 256;   // O [0, D), S [D, D + 64)
-    static_assert(D + kBN <= static_cast<int>(kTmemCols), "TMEM layout");
+    // TMEM: O [0, D), S [D, D + 64), P buffers [D + 64, D + 96) and [D + 96, D + 128)
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr uint32_t kColS = D;
+    static constexpr uint32_t kColP = D + kBN;
+    static_assert(D + kBN + kBN <= static_cast<int>(kTmemCols), "TMEM layout");
 };
 
 struct Args {
@@ -74,9 +77,9 @@ enum BarIndex : int {
     kBarQFull = kBarKvEmpty + kStages,
     kBarSFull,
     kBarSFree,
-    kBarPFull,
-    kBarPvDone,
-    kBarDrain,
+    kBarPFull,                      // [2]: one per P buffer
+    kBarPvDone = kBarPFull + 2,     // [2]
+    kBarDrain = kBarPvDone + 2,
     kBarCount
 };
 
@@ -100,7 +103,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     uint8_t *sQ = smem;
     uint8_t *sStages = smem + Geom::kOffStages;
-    uint8_t *sP = smem + Geom::kOffP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Geom::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBarCount);
 
@@ -129,10 +131,64 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     const int n_blocks = (n_keys + kBN - 1) / kBN;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kBarCount; ++i)
-            mbar_init(&bars[i], (i == kBarSFree || i == kBarPFull) ? 128u : 1u);
-        fence_mbar_init();
+    // Producer state (warp 0).  The query tile and the first stages are issued before the
+    // CTA-wide barrier below, so the loads overlap the TMEM allocation.
+    const int32_t *bt_row = a.block_table + static_cast<size_t>(s) * a.bt_stride;
+    const int n_pages = (n_keys + P - 1) / P;
+    int cached_base = -32;
+    int cached_page = 0;
+    int issued = 0;
+    uint64_t policy = 0;
+    // Load the K and V pages of stage b (all lanes of warp 0; lane 0 issues the copies).
+    auto produce_block = [&](int b) {
+        const int st = b % kStages;
+        const int key0 = b * kBN;
+        const int np = (min(kBN, n_keys - key0) + P - 1) / P;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&bars[kBarKvFull + st], static_cast<uint32_t>(np * P * D * 2 * 2));
+        uint8_t *kdst = sStages + st * Geom::kStageBytes;
+        uint8_t *vdst = kdst + Geom::kTileBytes;
+        for (int i = 0; i < np; ++i) {
+            const int lp = key0 / P + i;
+            if (lp >= cached_base + 32) {
+                cached_base = lp;
+                cached_page = (lp + lane < n_pages) ? bt_row[lp + lane] : 0;
+            }
+            const int page = __shfl_sync(0xffffffffu, cached_page, lp - cached_base);
+            if (lane == 0) {
+                const int slot0 = page * P;
+#pragma unroll
+                for (int h = 0; h < kHalves; ++h) {
+                    const int off = h * kBN * 128 + i * P * 128;
+                    tma_load_3d(kdst + off, &tmap_k, h * 64, kvh, slot0, &bars[kBarKvFull + st],
+                                policy);
+                    tma_load_3d(vdst + off, &tmap_v, h * 64, kvh, slot0, &bars[kBarKvFull + st],
+                                policy);
+                }
+            }
+        }
+        issued = b + 1;
+    };
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < kBarCount; ++i)
+                mbar_init(&bars[i],
+                          (i == kBarSFree || i == kBarPFull || i == kBarPFull + 1) ? 128u : 1u);
+            fence_mbar_init();
+            prefetch_tensormap(&tmap_q);
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+            // the tile's 128 / G tokens x G heads of this kv head, token-major
+            mbar_arrive_expect_tx(&bars[kBarQFull], Geom::kQBytes);
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h)
+                tma_load_4d(sQ + h * kM * 128, &tmap_q, h * 64, 0, kvh, tok0 + row_begin / G,
+                            &bars[kBarQFull]);
+        }
+        __syncwarp();
+        policy = l2_policy_evict_last();   // the sibling row tile re-reads these pages
+        for (int b = 0; b < min(kStages, n_blocks); ++b)
+            produce_block(b);
     }
     if (warp == 1)
         tmem_alloc(tmem_slot, Geom::kTmemCols);
@@ -141,64 +197,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_o = tmem;
-    const uint32_t tmem_s = tmem + D;
+    const uint32_t tmem_s = tmem + Geom::kColS;
+    const uint32_t tmem_p = tmem + Geom::kColP;   // buffer j at tmem_p + 32 j
     bool ok = true;
 
     if (warp == 0) {
         // ------------------------------ TMA producer -------------------------------------
-        const int32_t *bt_row = a.block_table + static_cast<size_t>(s) * a.bt_stride;
-        const int n_pages = (n_keys + P - 1) / P;
-        if (lane == 0) {
-            prefetch_tensormap(&tmap_q);
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
-            // the tile's 128 / G tokens x G heads of this kv head, token-major
-            mbar_arrive_expect_tx(&bars[kBarQFull], Geom::kQBytes);
-#pragma unroll
-            for (int h = 0; h < kHalves; ++h)
-                tma_load_4d(sQ + h * kM * 128, &tmap_q, h * 64, 0, kvh,
-                            tok0 + row_begin / G, &bars[kBarQFull]);
-        }
-        const uint64_t policy = l2_policy_evict_last();   // the sibling row tile re-reads
-        int cached_base = -32;
-        int cached_page = 0;
-        int issued = 0;
-        for (int b = 0; b < n_blocks; ++b) {
+        for (int b = kStages; b < n_blocks; ++b) {
             const int st = b % kStages;
-            if (b >= kStages) {
-                const bool waited = mbar_wait(&bars[kBarKvEmpty + st], ((b / kStages) - 1) & 1);
-                if (!__all_sync(0xffffffffu, waited)) {
-                    ok = false;
-                    break;
-                }
+            const bool waited = mbar_wait(&bars[kBarKvEmpty + st], ((b / kStages) - 1) & 1);
+            if (!__all_sync(0xffffffffu, waited)) {
+                ok = false;
+                break;
             }
-            const int key0 = b * kBN;
-            const int np = (min(kBN, n_keys - key0) + P - 1) / P;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&bars[kBarKvFull + st],
-                                      static_cast<uint32_t>(np * P * D * 2 * 2));
-            uint8_t *kdst = sStages + st * Geom::kStageBytes;
-            uint8_t *vdst = kdst + Geom::kTileBytes;
-            for (int i = 0; i < np; ++i) {
-                const int lp = key0 / P + i;
-                if (lp >= cached_base + 32) {
-                    cached_base = lp;
-                    cached_page = (lp + lane < n_pages) ? bt_row[lp + lane] : 0;
-                }
-                const int page = __shfl_sync(0xffffffffu, cached_page, lp - cached_base);
-                if (lane == 0) {
-                    const int slot0 = page * P;
-#pragma unroll
-                    for (int h = 0; h < kHalves; ++h) {
-                        const int off = h * kBN * 128 + i * P * 128;
-                        tma_load_3d(kdst + off, &tmap_k, h * 64, kvh, slot0,
-                                    &bars[kBarKvFull + st], policy);
-                        tma_load_3d(vdst + off, &tmap_v, h * 64, kvh, slot0,
-                                    &bars[kBarKvFull + st], policy);
-                    }
-                }
-            }
-            issued = b + 1;
+            produce_block(b);
         }
         if (!ok && lane == 0) {
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
@@ -213,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         constexpr uint32_t kIdescQK = umma_idesc_bf16(kM, kBN, 0);
         constexpr uint32_t kIdescPV = umma_idesc_bf16(kM, D, 1);
         const uint32_t q_addr = smem_addr(sQ);
-        const uint32_t p_addr = smem_addr(sP);
         const uint32_t stage_addr = smem_addr(sStages);
 
         auto wait_all = [&](uint64_t *bar, uint32_t parity) {
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             if (next_pv < next_qk) {
-                bool ready = mbar_test(&bars[kBarPFull], next_pv & 1);
+                bool ready = mbar_test(&bars[kBarPFull + (next_pv & 1)], (next_pv >> 1) & 1);
                 ready = __shfl_sync(0xffffffffu, ready, 0);
                 if (ready) {
                     const int st = next_pv % kStages;
@@ -284,15 +295,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (lane == 0) {
                         const uint32_t v_addr =
                             stage_addr + st * Geom::kStageBytes + Geom::kTileBytes;
+                        const uint32_t p_cols = tmem_p + (next_pv & 1) * 32;
 #pragma unroll
                         for (int k = 0; k < kBN / 16; ++k) {
-                            const uint64_t da = umma_desc_sw128(p_addr + k * 32, 16, 1024);
                             const uint64_t db =
                                 umma_desc_sw128(v_addr + k * 16 * 128, kBN * 128, 1024);
-                            umma_bf16_ss(tmem_o, da, db, kIdescPV,
+                            umma_bf16_ts(tmem_o, p_cols + k * 8, db, kIdescPV,
                                          (next_pv > 0 || k > 0) ? 1u : 0u);
                         }
-                        umma_commit(&bars[kBarPvDone]);
+                        umma_commit(&bars[kBarPvDone + (next_pv & 1)]);
                         umma_commit(&bars[kBarKvEmpty + st]);
                     }
                     __syncwarp();
@@ -328,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY;
         float l_sum = 0.0f;
-        uint8_t *prow = sP + row * 128;
 
         for (int b = 0; b < n_blocks; ++b) {
             if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarSFull], b & 1))) {
@@ -352,42 +362,62 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_arrive(&bars[kBarSFree]);
 
             const int key0 = b * kBN;
-            float mb = -INFINITY;
+            // causal limit (and positions past the loaded range) on the raw scores
+            if (key0 + kBN - 1 > lim) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float v = x[c] * sl2;
-                if (key0 + c > lim)
-                    v = -INFINITY;
-                x[c] = v;
-                mb = fmaxf(mb, v);
+                for (int c = 0; c < 64; ++c)
+                    if (key0 + c > lim)
+                        x[c] = -INFINITY;
             }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                mx = fmaxf(mx, x[c]);
+            const float mb = mx * sl2;   // base-2 scaled row max of this block (scale > 0)
             // lazy rescale: move the reference max only when it grows by more than 2^8
             float alpha = 1.0f;
             bool moved = false;
-            if (mb > m_used + kRescaleLog2 || (m_used == -INFINITY && mb != -INFINITY)) {
+            if (mb > m_used + kRescaleLog2) {
                 alpha = (m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - mb);
                 m_used = mb;
                 moved = true;
             }
-            const float mu = (m_used == -INFINITY) ? 0.0f : m_used;
+            const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
             uint32_t pk[32];
             float psum = 0.0f;
+            if (__any_sync(0xffffffffu, valid)) {
+                // p = 2^(s * scale * log2(e) - m); every fourth column on the FMA pipe
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                pk[c] = pack_bf16x2(fast_exp2(x[2 * c] - mu), fast_exp2(x[2 * c + 1] - mu));
-                psum += bf16x2_sum(pk[c]);
+                for (int c = 0; c < 32; ++c) {
+                    const float e0 = fast_exp2(fmaf(x[2 * c], sl2, neg_mu));
+                    const float y1 = fmaf(x[2 * c + 1], sl2, neg_mu);
+                    const float e1 = (c & 1) ? exp2_fma(y1) : fast_exp2(y1);
+                    pk[c] = pack_bf16x2(e0, e1);
+                    psum += bf16x2_sum(pk[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)   // a warp of padding rows: P = 0
+                    pk[c] = 0u;
             }
             l_sum = l_sum * alpha + psum;
 
-            if (b > 0) {
-                // the previous PV product must be done before P is overwritten and before O
-                // is rescaled
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone], (b - 1) & 1))) {
+            // P buffer b & 1 was last read by PV(b - 2); O may be rescaled only once PV(b - 1)
+            // is done.
+            const int pb = b & 1;
+            if (b >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + pb],
+                                                             ((b >> 1) - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            if (b > 0 && __any_sync(0xffffffffu, moved)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + ((b - 1) & 1)],
+                                                       ((b - 1) >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                if (__any_sync(0xffffffffu, moved)) {
+                {
                     const float f = moved ? alpha : 1.0f;
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -402,49 +432,77 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tmem_wait_st();
                 }
             }
-            // P row -> shared memory, K-major, 128-byte swizzle (chunk c at c ^ (row & 7))
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            fence_proxy_async_smem();
+            tc_fence_after_sync();
+            // P row -> TMEM buffer pb: column j holds positions 2j, 2j + 1
+            tmem_st32u(tmem_p + pb * 32 + lane_off, pk);
+            tmem_wait_st();
             tc_fence_before_sync();
-            mbar_arrive(&bars[kBarPFull]);
+            mbar_arrive(&bars[kBarPFull + pb]);
         }
 
-        // epilogue: O row / l -> global
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone], (n_blocks - 1) & 1)))
+        // epilogue: O row / l -> global, once the last PV product is done
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + ((n_blocks - 1) & 1)],
+                                                     ((n_blocks - 1) >> 1) & 1)))
             ok = false;
         tc_fence_after_sync();
         if (!ok)
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
         const float inv = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
-        const int g = gr - ti * G;
-        const size_t out_row =
-            (static_cast<size_t>(tok0 + ti) * a.q_heads + static_cast<size_t>(kvh) * G + g) * D;
+        if (a.out_f32) {
+            const int g = gr - ti * G;
+            const size_t out_row =
+                (static_cast<size_t>(tok0 + ti) * a.q_heads + static_cast<size_t>(kvh) * G + g) *
+                D;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float o[32];
-            tmem_ld32(tmem_o + lane_off + c0, o);
-            tmem_wait_ld();
-            if (valid && ok) {
-                if (a.out_f32) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tmem_ld32(tmem_o + lane_off + c0, o);
+                tmem_wait_ld();
+                if (valid && ok) {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) +
                                                              out_row + c0);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         dst[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv,
                                              o[4 * c + 2] * inv, o[4 * c + 3] * inv);
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        static_cast<__nv_bfloat16 *>(a.out) + out_row + c0);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                                            pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                            pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                                            pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
                 }
+            }
+        } else {
+            // Stage the bf16 tile in the query buffer (dead since the last QK product): row r
+            // holds D * 2 bytes, 16-byte chunk c at (c & ~7) | ((c & 7) ^ (r & 7)), so eight
+            // consecutive rows hit distinct banks.  Then store whole rows, coalesced.
+            constexpr int kChunks = D / 8;
+            uint8_t *stage_row = sQ + row * (D * 2);
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tmem_ld32(tmem_o + lane_off + c0, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = c0 / 8 + c;
+                    const int phys = (chunk & ~7) | ((chunk & 7) ^ (row & 7));
+                    *reinterpret_cast<uint4 *>(stage_row + phys * 16) =
+                        make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                   pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                   pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                   pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                }
+            }
+            named_barrier(1, 128);
+            const int n_rows = min(kM, rows - row_begin);
+            const int t = threadIdx.x - 64;   // 0 .. 127 over the softmax warps
+            for (int idx = t; ok && idx < n_rows * kChunks; idx += 128) {
+                const int r = idx / kChunks;
+                const int chunk = idx - r * kChunks;
+                const int phys = (chunk & ~7) | ((chunk & 7) ^ (r & 7));
+                const int grr = row_begin + r;
+                const int tok = grr / G;
+                const size_t dst_row = (static_cast<size_t>(tok0 + tok) * a.q_heads +
+                                        static_cast<size_t>(kvh) * G + (grr - tok * G)) * D;
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + dst_row +
+                                           chunk * 8) =
+                    *reinterpret_cast<const uint4 *>(sQ + r * (D * 2) + phys * 16);
             }
         }
     }

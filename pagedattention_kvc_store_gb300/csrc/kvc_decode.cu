@@ -10,7 +10,7 @@
 // Kernel design (GB300):
 //   * one CTA per (split, kv head, sequence); 4 consumer warps + 1 TMA producer warp;
 //   * the producer streams 64-position stages of K and V into a 3-deep shared-memory ring
-//     with cp.async.bulk.tensor (one box per page and 64-column half, 128-byte swizzle so
+//     with cp.async.bulk.tensor (one box per page, both 64-column halves, 128-byte swizzle so
 //     that ldmatrix reads are bank-conflict free), completion counted on mbarriers;
 //   * each consumer warp takes 16 of the 64 positions of every stage: S = Q K^T and O += P V
 //     on the tensor cores (mma.sync m16n8k16, the G query heads padded to 16 rows -- too thin
@@ -42,7 +42,7 @@ static_assert(kKeysPerWarp == 16, "each consumer warp covers one 16-position MMA
 
 template <int D>
 struct DecodeGeom {
-    static constexpr int kTileBytes = (D / 64) * kStageKeys * 128;   // K (or V) of one stage
+    static constexpr int kTileBytes = kStageKeys * D * 2;   // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
     // after the ring: full[kStages], empty[kStages] mbarriers
@@ -81,7 +81,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
     using Geom = DecodeGeom<D>;
-    constexpr int kHalves = D / 64;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -171,12 +170,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int page = __shfl_sync(0xffffffffu, cached_page, lp - cached_base);
                 if (lane == 0) {
                     const int slot0 = page * P;
-#pragma unroll
-                    for (int h = 0; h < kHalves; ++h) {
-                        const int off = h * kStageKeys * 128 + i * P * 128;
-                        tma_load_3d(kdst + off, &tmap_k, h * 64, kvh, slot0, &full[st], policy);
-                        tma_load_3d(vdst + off, &tmap_v, h * 64, kvh, slot0, &full[st], policy);
-                    }
+                    const int off = i * P * D * 2;
+                    tma_load_4d_hint(kdst + off, &tmap_k, 0, slot0, 0, kvh, &full[st], policy);
+                    tma_load_4d_hint(vdst + off, &tmap_v, 0, slot0, 0, kvh, &full[st], policy);
                 }
             }
             issued = b + 1;
@@ -216,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int k_col = ((lane >> 3) & 1) << 3;
     const int v_row = warp * kKeysPerWarp + (lane & 7) + (((lane >> 3) & 1) << 3);
     const int v_col = (lane >> 4) << 3;
+    const int log2p = __ffs(P) - 1;
     const float sl2 = a.scale_log2;
     bool ok = true;
 
@@ -233,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + swz_offset<kStageKeys>(k_row, kk * 16 + k_col), b0, b1, b2, b3);
+                ldsm_x4(kbase + page_tile_offset<D>(k_row, kk * 16 + k_col, log2p), b0, b1, b2,
+                        b3);
                 mma_bf16_16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
                 mma_bf16_16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
             }
@@ -269,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int dt = 0; dt < D / 16; ++dt) {
                 uint32_t v0, v1, v2, v3;
-                ldsm_x4_trans(vbase + swz_offset<kStageKeys>(v_row, dt * 16 + v_col), v0, v1,
-                              v2, v3);
+                ldsm_x4_trans(vbase + page_tile_offset<D>(v_row, dt * 16 + v_col, log2p), v0,
+                              v1, v2, v3);
                 if (n_valid < kKeysPerWarp) {
                     v0 = keep_keys(v0, cq, n_valid);
                     v1 = keep_keys(v1, 8 + cq, n_valid);

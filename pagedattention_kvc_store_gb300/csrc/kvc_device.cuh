@@ -210,6 +210,33 @@ __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]; A is M lanes x K columns of tensor memory, column j of a
+// 16-bit A holding elements 2j (low half) and 2j + 1 (high half) of the row.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane from raw words (warp-collective).
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
@@ -303,6 +330,18 @@ __device__ __forceinline__ void tmem_wait_st()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 4-D tiled tensor load with an L2 cache-policy hint (used for K/V pages).
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *map, int c0, int c1,
+                                                 int c2, int c3, uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // 4-D tiled tensor load (used for query tiles).
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, int c3, uint64_t *bar)
@@ -321,6 +360,26 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x on the FMA pipe, for the share of a softmax's exponentials that would otherwise queue on
+// the MUFU unit.  x is rounded to the nearest integer n by adding 1.5 * 2^23 (the low mantissa
+// bits of the sum then hold n), 2^(x - n) with x - n in [-1/2, 1/2] is a cubic, and n is added
+// to the exponent field.  The cubic is a relative-error least-squares fit of 2^f on [-1/2, 1/2]
+// (Lawson-reweighted), max relative error 7.5e-5 -- far below the bf16 rounding the
+// probabilities get next.  x = -inf (a masked position) gives exactly 0; x is clamped at -125 so
+// the result stays a normal number.
+__device__ __forceinline__ float exp2_fma(float x)
+{
+    const float xc = fmaxf(x, -125.0f);
+    const float t = xc + 12582912.0f;
+    const float n = t - 12582912.0f;
+    const float f = xc - n;
+    const float p = fmaf(fmaf(fmaf(5.517132143e-2f, f, 2.426105423e-1f), f, 6.932609856e-1f), f,
+                         9.999281094e-1f);
+    const int e = (__float_as_int(t) - 0x4B400000) << 23;
+    const float r = __int_as_float(__float_as_int(p) + e);
+    return x == -INFINITY ? 0.0f : r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -345,16 +404,20 @@ __device__ __forceinline__ uint32_t keep_keys(uint32_t v, int key_lo, int n_vali
     return v & (lo | hi);
 }
 
-// Byte offset, inside a stage tile written by TMA with 128-byte swizzling, of the 16-byte
-// chunk holding element column `col` (bf16 index in 0..head_dim-1) of row `row`.  The tile
-// is stored as head_dim/64 column halves of [rows][64] bf16 (128 bytes per row); inside a
-// 1024-byte block of 8 rows, chunk c of row r sits at chunk c ^ (r & 7).
-template <int ROWS>
-__device__ __forceinline__ uint32_t swz_offset(int row, int col)
+// Byte offset, inside a stage tile of whole pages, of the 16-byte chunk holding element
+// column `col` (bf16 index in 0..head_dim-1) of row `row` (position in the stage).  Each page
+// of `page_rows` rows is stored [half][page_rows][64] bf16 (128 bytes per row) by one TMA box
+// with 128-byte swizzling: inside each 1024-byte block of 8 rows, chunk c of row r sits at
+// chunk c ^ (r & 7).  page_rows is a multiple of 8.
+template <int D>
+__device__ __forceinline__ uint32_t page_tile_offset(int row, int col, int log2_page_rows)
 {
+    const int page = row >> log2_page_rows;
+    const int r = row & ((1 << log2_page_rows) - 1);
     const int half = col >> 6;
     const int chunk = (col & 63) >> 3;
-    return static_cast<uint32_t>(half * ROWS * 128 + row * 128 + ((chunk ^ (row & 7)) << 4));
+    return static_cast<uint32_t>((page * (D / 64) + half) << (log2_page_rows + 7)) +
+           static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
 }
 
 }  // namespace kvc

@@ -47,23 +47,22 @@ cudaError_t launch_decode(const DecodeLaunch &a, const CUtensorMap &tmap_k,
 cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const float *part_lse,
                          int rows, int n_split, int head_dim, float *lse_out,
                          cudaStream_t stream);
-cudaError_t launch_append(const AppendLaunch &a, const CUtensorMap &tmap_k,
-                          const CUtensorMap &tmap_v, cudaStream_t stream);
-// tcgen05 version; tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes.
+// tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes.
 cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
                              const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                              cudaStream_t stream);
 
 // Device error words, one per translation unit that owns bounded waits.
 cudaError_t read_and_clear_decode_errors(uint32_t *flags);
-cudaError_t read_and_clear_append_errors(uint32_t *flags);
 cudaError_t read_and_clear_store_errors(uint32_t *flags);
 cudaError_t read_and_clear_append_tc_errors(uint32_t *flags);
 
 // Record a failure reason for kvc_last_error() from another translation unit.
 int set_last_error(int status, const char *message);
 
-// Stage geometry shared by the decode and append pipelines.
+// Stage geometry shared by the decode and append pipelines: a stage holds kStageKeys
+// positions of one kv head as whole pages, each page stored [half][page_size rows][64 columns]
+// with 128-byte swizzle (one TMA box per page).
 constexpr int kStageKeys = 64;   // positions per pipeline stage
 
 }  // namespace kvc
