@@ -50,6 +50,9 @@ def parse_args():
     p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer (MB)")
     p.add_argument("--append-steps", type=int, default=60)
     p.add_argument("--no-append", action="store_true")
+    p.add_argument("--no-legs", action="store_true",
+                   help="skip the shared-prefix and long-context decode legs")
+    p.add_argument("--leg-steps", type=int, default=30)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -205,6 +208,107 @@ def traffic_from_profile(kernel_tag: str, source_file: str):
 # the CUDA path
 # ---------------------------------------------------------------------------------------
 
+def time_graph(torch, fn, stream, flush, steps):
+    """Capture fn in a CUDA graph; mean device time (ms) over `steps` replays, L2 flushed
+    between replays outside the timed events."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    del g
+    return statistics.mean(ts)
+
+
+def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
+    """Shared-prefix decode (grouped vs plain) and long-context split-K decode."""
+    from workloads import config_case
+    from workloads.configs import SEED_BASE
+    from workloads.device import i32_tensor, to_device
+
+    legs = {}
+    per_pos = lambda c: 2 * c.kv_heads * c.head_dim * 2
+    qo = lambda c: 2 * c.num_seqs * c.q_heads * c.head_dim * 2
+    # shared prefix: 32 groups x 8 sequences over 2,048 shared positions
+    case = config_case(3, seed=None if rank == 0 else SEED_BASE + 3 + 1000 * rank)
+    d = to_device(case, dev)
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+    kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    indptr = np.arange(0, case.num_seqs + 1, 8, dtype=np.int32)
+    prefix = np.full(len(case.groups), case.shared_positions, np.int32)
+    gi, gs, gp = (i32_tensor(indptr, dev), i32_tensor(np.concatenate(case.groups), dev),
+                  i32_tensor(prefix, dev))
+    pool = kvc.pool_desc(d.k_pool)
+    ws_g = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
+                                             len(case.groups), int(prefix.max()))
+    work_g = torch.empty(ws_g, dtype=torch.uint8, device=dev)
+    _, _, ws_p = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+    work_p = torch.empty(max(ws_p, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        t_g = time_graph(torch, lambda: kvc.kvc_decode_shared_prefix(
+            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx, gi, gs,
+            gp, 8, int(prefix.max()), work_g), stream, flush, args.leg_steps)
+        t_p = time_graph(torch, lambda: kvc.kvc_decode(
+            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+            num_splits=0, workspace=work_p), stream, flush, args.leg_steps)
+    unique_pos = int(case.context_lens.sum()) - 7 * len(case.groups) * int(prefix[0])
+    unique_b = unique_pos * per_pos(case) + qo(case)
+    logical_b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
+    legs["shared_prefix"] = {
+        "workload": "32 groups x 8 seqs, 2,048 shared positions + U[64,512] own, 32/8 heads, "
+                    "D 128, P 16",
+        "grouped_us": round(t_g * 1e3, 1), "plain_us": round(t_p * 1e3, 1),
+        "unique_bytes": unique_b, "logical_bytes": logical_b,
+        "grouped_unique_gbs": round(unique_b / (t_g / 1e3) / 1e9, 1),
+        "grouped_frac_of_hbm": round(unique_b / (t_g / 1e3) / 1e9 / peaks["hbm"], 4),
+        "plain_unique_gbs": round(unique_b / (t_p / 1e3) / 1e9, 1),
+        "plain_effective_gbs": round(logical_b / (t_p / 1e3) / 1e9, 1),
+        "gpu_launches_per_step": {"grouped": 5, "plain": 2},
+    }
+    del d, out, work_g, work_p, slots
+    torch.cuda.empty_cache()
+    # long context: 8 sequences of 32k..128k positions
+    case = config_case(5, seed=None if rank == 0 else SEED_BASE + 5 + 1000 * rank)
+    d = to_device(case, dev)
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+    kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    pool = kvc.pool_desc(d.k_pool)
+    splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        t = time_graph(torch, lambda: kvc.kvc_decode(
+            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+            num_splits=0, workspace=work), stream, flush, args.leg_steps)
+    b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
+    legs["long_decode"] = {
+        "workload": "8 seqs, ctx U[32768,131072], 64/8 heads, D 128, P 64, split-K + merge",
+        "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
+        "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
+        "chunk": chunk, "gpu_launches_per_step": 2,
+    }
+    del d, out, work, slots
+    torch.cuda.empty_cache()
+    return legs
+
+
 def run_kvc(args):
     import torch
 
@@ -290,6 +394,9 @@ def run_kvc(args):
         append = None
         if not args.no_append:
             append = run_append(torch, kvc, args, dev, stream, flush, peaks, rank)
+        legs = None
+        if not args.no_legs:
+            legs = run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -316,6 +423,8 @@ def run_kvc(args):
         line["e2e"] = e2e
     if append is not None:
         line["append"] = append
+    if legs is not None:
+        line["decode_legs"] = legs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
     if rank == 0:

@@ -149,6 +149,43 @@ kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool
                            int32_t *chunk_out, size_t *workspace_bytes_out);
 
 /*
+ * kvc_decode_shared_prefix -- kvc_decode for batches in which groups of sequences begin with
+ * the same physical pages ("KV Cache Management and PagedAttention", "Share common KV across
+ * responses": several block tables point at one copy of the common KV; each response still
+ * attends with its own query over its own context; Quail "KV", "Prefix sharing").
+ *
+ * The result is exactly kvc_decode's (up to fp32 rounding); the shared pages are read once
+ * per group instead of once per member.  Group g's members are the sequences
+ * group_seqs[group_indptr[g] .. group_indptr[g+1]); every member's block table lists the same
+ * first prefix_len[g] / page_size pages (the first member's row is the one read) and every
+ * member's context_lens is at least prefix_len[g] (rounded down to whole pages).  A sequence
+ * may belong to at most one group; sequences in no group are decoded over their whole context.
+ *   group_indptr    int32 [num_groups + 1] (device)
+ *   group_seqs      int32 [group_indptr[num_groups]] sequence indices (device)
+ *   prefix_len      int32 [num_groups] shared positions (device)
+ *   max_group_size  host bound on members per group; max_group_size * G must be <= 64
+ *   max_prefix_len  host bound on prefix_len
+ *   workspace       kvc_decode_shared_prefix_plan(...) bytes (required), 16-byte aligned
+ * The other arguments are kvc_decode's.  Five kernels are enqueued: a set-up pass, the prefix
+ * partials (one CTA per prefix chunk, kv head and group), the suffix partials (the decode
+ * kernel started at each member's prefix end) and the log-sum-exp merge.
+ */
+kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
+                                    const void *k_pool, const void *v_pool, kvc_pool_desc pool,
+                                    const int32_t *block_table, int32_t bt_stride,
+                                    const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t max_ctx, int32_t q_heads, float scale,
+                                    const int32_t *group_indptr, const int32_t *group_seqs,
+                                    const int32_t *prefix_len, int32_t num_groups,
+                                    int32_t max_group_size, int32_t max_prefix_len,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes kvc_decode_shared_prefix needs for these scalars. */
+kvc_status kvc_decode_shared_prefix_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
+                                         int32_t max_ctx, int32_t num_groups,
+                                         int32_t max_prefix_len, size_t *workspace_bytes_out);
+
+/*
  * kvc_decode_noalloc -- kvc_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for callers of this library

@@ -262,6 +262,39 @@ kvc_status query_tensor_map(const void *q, int32_t num_tokens, int32_t kv_heads,
     return tensor_map(k, out);
 }
 
+// Split plan of kvc_decode_shared_prefix: prefix chunks, then the suffix plan of kvc_decode.
+struct GroupPlan {
+    int prefix_chunk, n_prefix;
+    Plan suffix;
+    int stride;
+    size_t lse_offset, key_start_offset, ws_bytes;
+};
+
+GroupPlan make_group_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool,
+                          int32_t max_ctx, int32_t num_groups, int32_t max_prefix_len)
+{
+    GroupPlan g{};
+    const int64_t unit = kvc::kStageKeys;
+    if (max_prefix_len > 0 && num_groups > 0) {
+        const int64_t units = static_cast<int64_t>(num_groups) * pool.kv_heads;
+        const int64_t want = ceil_div(4 * static_cast<int64_t>(device_sm_count()), units);
+        int64_t chunk = round_up(ceil_div(max_prefix_len, want), unit);
+        if (chunk < 256)
+            chunk = 256;
+        g.prefix_chunk = static_cast<int>(chunk);
+        g.n_prefix = static_cast<int>(ceil_div(max_prefix_len, chunk));
+    }
+    g.suffix = make_plan(num_seqs, q_heads, pool, max_ctx, 0);
+    g.stride = g.n_prefix + g.suffix.splits;
+    const size_t rows = static_cast<size_t>(num_seqs) * q_heads;
+    const size_t o_bytes = rows * g.stride * pool.head_dim * sizeof(float);
+    g.lse_offset = static_cast<size_t>(round_up(static_cast<int64_t>(o_bytes), 256));
+    g.key_start_offset = static_cast<size_t>(
+        round_up(static_cast<int64_t>(g.lse_offset + rows * g.stride * sizeof(float)), 256));
+    g.ws_bytes = g.key_start_offset + static_cast<size_t>(num_seqs) * sizeof(int32_t);
+    return g;
+}
+
 kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *q,
                                 const void *k_pool, const void *v_pool,
                                 const kvc_pool_desc &pool, const int32_t *block_table,
@@ -441,6 +474,128 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
     return ok();
 }
 
+kvc_status kvc_decode_shared_prefix_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
+                                         int32_t max_ctx, int32_t num_groups,
+                                         int32_t max_prefix_len, size_t *workspace_bytes_out)
+{
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    if ((st = check_group(pool, q_heads)) != KVC_OK)
+        return st;
+    if (num_seqs < 0 || max_ctx < 0 || num_groups < 0 || max_prefix_len < 0)
+        return fail(KVC_ERR_INVALID_ARG, "negative size");
+    const GroupPlan g = make_group_plan(num_seqs, q_heads, pool, max_ctx, num_groups,
+                                        max_prefix_len);
+    if (workspace_bytes_out)
+        *workspace_bytes_out = g.ws_bytes;
+    return ok();
+}
+
+kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
+                                    const void *k_pool, const void *v_pool, kvc_pool_desc pool,
+                                    const int32_t *block_table, int32_t bt_stride,
+                                    const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t max_ctx, int32_t q_heads, float scale,
+                                    const int32_t *group_indptr, const int32_t *group_seqs,
+                                    const int32_t *prefix_len, int32_t num_groups,
+                                    int32_t max_group_size, int32_t max_prefix_len,
+                                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    kvc_status st = check_attention_args(out, out_dtype, q, k_pool, v_pool, pool, block_table,
+                                         bt_stride, context_lens, num_seqs, max_ctx, q_heads);
+    if (st != KVC_OK)
+        return st;
+    if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0 || max_prefix_len > max_ctx)
+        return fail(KVC_ERR_INVALID_ARG, "bad group sizes (0 <= max_prefix_len <= max_ctx)");
+    const int G = q_heads / pool.kv_heads;
+    if (static_cast<int64_t>(max_group_size) * G > 64)
+        return fail(KVC_ERR_UNSUPPORTED,
+                    "a group's query rows (members x q_heads / kv_heads = %d) exceed 64",
+                    max_group_size * G);
+    if (num_groups > 65535)
+        return fail(KVC_ERR_INVALID_ARG, "num_groups %d (at most 65535)", num_groups);
+    if (num_groups > 0 && (!group_indptr || !group_seqs || !prefix_len))
+        return fail(KVC_ERR_INVALID_ARG, "null group array");
+    if (num_seqs == 0)
+        return ok();
+    const GroupPlan g = make_group_plan(num_seqs, q_heads, pool, max_ctx, num_groups,
+                                        max_prefix_len);
+    if (workspace == nullptr || workspace_bytes < g.ws_bytes)
+        return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", g.ws_bytes,
+                    workspace == nullptr ? size_t(0) : workspace_bytes);
+    if (!aligned16(workspace))
+        return fail(KVC_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    CUtensorMap tk, tv;
+    if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
+        return st;
+    if ((st = pool_tensor_map(v_pool, pool, &tv)) != KVC_OK)
+        return st;
+    char *ws = static_cast<char *>(workspace);
+    float *part_o = reinterpret_cast<float *>(ws);
+    float *part_lse = reinterpret_cast<float *>(ws + g.lse_offset);
+    int32_t *key_start = reinterpret_cast<int32_t *>(ws + g.key_start_offset);
+    const float sc = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    cudaError_t err = kvc::launch_grouped_setup(part_lse, key_start, group_indptr, group_seqs,
+                                                prefix_len, num_groups, num_seqs, q_heads,
+                                                g.n_prefix, g.stride, pool.page_size, bt_stride,
+                                                s);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "grouped setup launch");
+    if (g.n_prefix > 0) {
+        kvc::GroupedPrefixLaunch p;
+        p.q = q;
+        p.part_o = part_o;
+        p.part_lse = part_lse;
+        p.block_table = block_table;
+        p.bt_stride = bt_stride;
+        p.group_indptr = group_indptr;
+        p.group_seqs = group_seqs;
+        p.prefix_len = prefix_len;
+        p.num_groups = num_groups;
+        p.max_rows = max_group_size * G;
+        p.num_seqs = num_seqs;
+        p.q_heads = q_heads;
+        p.kv_heads = pool.kv_heads;
+        p.head_dim = pool.head_dim;
+        p.page_size = pool.page_size;
+        p.chunk = g.prefix_chunk;
+        p.n_split = g.n_prefix;
+        p.split_stride = g.stride;
+        p.scale = sc;
+        if ((err = kvc::launch_grouped_prefix(p, tk, tv, s)) != cudaSuccess)
+            return cuda_fail(err, "grouped prefix launch");
+    }
+    kvc::DecodeLaunch l;
+    l.q = q;
+    l.out = out;
+    l.out_f32 = out_dtype == KVC_F32;
+    l.part_o = part_o;
+    l.part_lse = part_lse;
+    l.block_table = block_table;
+    l.bt_stride = bt_stride;
+    l.context_lens = context_lens;
+    l.num_seqs = num_seqs;
+    l.q_heads = q_heads;
+    l.kv_heads = pool.kv_heads;
+    l.head_dim = pool.head_dim;
+    l.page_size = pool.page_size;
+    l.chunk = g.suffix.chunk;
+    l.n_split = g.suffix.splits;
+    l.scale = sc;
+    l.key_start = key_start;
+    l.split_base = g.n_prefix;
+    l.split_stride = g.stride;
+    if ((err = kvc::launch_decode(l, tk, tv, s)) != cudaSuccess)
+        return cuda_fail(err, "suffix decode launch");
+    if ((err = kvc::launch_merge(out, l.out_f32, part_o, part_lse, num_seqs * q_heads, g.stride,
+                                 pool.head_dim, nullptr, s)) != cudaSuccess)
+        return cuda_fail(err, "merge launch");
+    return ok();
+}
+
 kvc_status kvc_merge(void *out, int32_t out_dtype, const float *partial_o,
                      const float *partial_lse, int32_t rows, int32_t num_splits,
                      int32_t head_dim, float *lse_out, void *stream)
@@ -518,11 +673,14 @@ kvc_status kvc_device_errors(uint32_t *flags_out)
     cudaError_t err = kvc::read_and_clear_decode_errors(&a);
     if (err == cudaSuccess)
         err = kvc::read_and_clear_store_errors(&c);
+    uint32_t e = 0;
     if (err == cudaSuccess)
         err = kvc::read_and_clear_append_tc_errors(&d);
+    if (err == cudaSuccess)
+        err = kvc::read_and_clear_grouped_errors(&e);
     if (err != cudaSuccess)
         return cuda_fail(err, "reading the device error word");
-    *flags_out = a | c | d;
+    *flags_out = a | c | d | e;
     return *flags_out ? fail(KVC_ERR_DEVICE, "device error flags 0x%x", *flags_out) : ok();
 }
 

@@ -62,8 +62,11 @@ struct Args {
     const int32_t *block_table;
     int bt_stride;
     const int32_t *context_lens;
+    const int32_t *key_start;   // optional [S]: positions below it are another kernel's
     int q_heads, group, page_size;
     int chunk, n_split;
+    int split_base, split_stride;   // partial j of this launch is split split_base + j of
+                                    // split_stride per row
     float scale_log2;
 };
 
@@ -101,7 +104,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             atomicOr(&g_decode_errors, kErrContextRange);
         ctx = a.bt_stride * a.page_size;
     }
-    const int k_begin = split * a.chunk;
+    const int k_first = a.key_start ? a.key_start[s] : 0;   // a multiple of page_size
+    const int k_begin = k_first + split * a.chunk;
     const int k_end = min(ctx, k_begin + a.chunk);
     const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
 
@@ -109,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // This chunk holds no position of the sequence.
         if (SPLIT) {
             if (threadIdx.x < G)
-                a.part_lse[(row0 + threadIdx.x) * a.n_split + split] = -INFINITY;
+                a.part_lse[(row0 + threadIdx.x) * a.split_stride + a.split_base + split] =
+                    -INFINITY;
         } else {
             for (int i = threadIdx.x; i < G * D; i += blockDim.x)
                 store_out(a.out, a.out_f32, row0 * D + i, 0.0f);
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const float val = O / L;
         if (SPLIT) {
-            const size_t prow = (row0 + row) * a.n_split + split;
+            const size_t prow = (row0 + row) * a.split_stride + a.split_base + split;
             a.part_o[prow * D + d] = val;
             if (d == 0)
                 a.part_lse[prow] = (M + log2f(L)) * kLn2;
@@ -405,11 +410,14 @@ cudaError_t launch_decode_t(const DecodeLaunch &l, const CUtensorMap &tk, const 
     a.block_table = l.block_table;
     a.bt_stride = l.bt_stride;
     a.context_lens = l.context_lens;
+    a.key_start = l.key_start;
     a.q_heads = l.q_heads;
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
     a.chunk = l.chunk;
     a.n_split = l.n_split;
+    a.split_base = l.split_base;
+    a.split_stride = l.split_stride > 0 ? l.split_stride : l.n_split;
     a.scale_log2 = l.scale * kLog2e;
     const size_t smem = DecodeGeom<D>::kSmemBytes;
     auto kernel = paged_decode_kernel<D, SPLIT>;
@@ -430,7 +438,7 @@ cudaError_t launch_decode(const DecodeLaunch &l, const CUtensorMap &tk, const CU
 {
     if (l.num_seqs == 0)
         return cudaSuccess;
-    const bool split = l.n_split > 1;
+    const bool split = l.n_split > 1 || l.split_stride > 1 || l.key_start != nullptr;
     if (l.head_dim == 128)
         return split ? launch_decode_t<128, true>(l, tk, tv, stream)
                      : launch_decode_t<128, false>(l, tk, tv, stream);

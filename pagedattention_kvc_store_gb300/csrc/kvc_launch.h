@@ -20,6 +20,28 @@ struct DecodeLaunch {
     int num_seqs, q_heads, kv_heads, head_dim, page_size;
     int chunk, n_split;
     float scale;
+    // Optional, for decode over a suffix: keys start at key_start[s] (a multiple of page
+    // size), and the partials of this launch are splits split_base .. of split_stride.
+    const int32_t *key_start = nullptr;
+    int split_base = 0;
+    int split_stride = 0;   // 0: n_split
+};
+
+// Grouped decode over a shared prefix: for each group, the first prefix_len[g] positions are
+// the same pages for every member (the leader's block-table row lists them).
+struct GroupedPrefixLaunch {
+    const void *q;
+    float *part_o;            // [S][Hq][split_stride][D]
+    float *part_lse;          // [S][Hq][split_stride]
+    const int32_t *block_table;
+    int bt_stride;
+    const int32_t *group_indptr;   // [num_groups + 1] into group_seqs
+    const int32_t *group_seqs;
+    const int32_t *prefix_len;     // [num_groups]
+    int num_groups, max_rows;      // max_rows = largest group size * G (<= 64)
+    int num_seqs, q_heads, kv_heads, head_dim, page_size;
+    int chunk, n_split, split_stride;
+    float scale;
 };
 
 struct AppendLaunch {
@@ -47,6 +69,15 @@ cudaError_t launch_decode(const DecodeLaunch &a, const CUtensorMap &tmap_k,
 cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const float *part_lse,
                          int rows, int n_split, int head_dim, float *lse_out,
                          cudaStream_t stream);
+// Grouped decode: sets every row's prefix partials to empty and key_start to 0, then each
+// group's members' key_start to the group's prefix length.
+cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int32_t *group_indptr,
+                                 const int32_t *group_seqs, const int32_t *prefix_len,
+                                 int num_groups, int num_seqs, int q_heads, int n_prefix_splits,
+                                 int split_stride, int page_size, int bt_stride,
+                                 cudaStream_t stream);
+cudaError_t launch_grouped_prefix(const GroupedPrefixLaunch &a, const CUtensorMap &tmap_k,
+                                  const CUtensorMap &tmap_v, cudaStream_t stream);
 // tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes.
 cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
                              const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
@@ -56,6 +87,7 @@ cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
 cudaError_t read_and_clear_decode_errors(uint32_t *flags);
 cudaError_t read_and_clear_store_errors(uint32_t *flags);
 cudaError_t read_and_clear_append_tc_errors(uint32_t *flags);
+cudaError_t read_and_clear_grouped_errors(uint32_t *flags);
 
 // Record a failure reason for kvc_last_error() from another translation unit.
 int set_last_error(int status, const char *message);

@@ -25,7 +25,7 @@ STATUS = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_UNSUPPORTED",
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store",
            "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
-           "kvc_decode_noalloc")
+           "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -85,6 +85,12 @@ def lib() -> ctypes.CDLL:
             L.kvc_decode_noalloc.restype = ctypes.c_int
             L.kvc_decode_noalloc.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, i32, i32,
                                              i32, f, i32, p]
+            L.kvc_decode_shared_prefix.restype = ctypes.c_int
+            L.kvc_decode_shared_prefix.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, i32,
+                                                   i32, i32, f, p, p, p, i32, i32, i32, p, sz, p]
+            L.kvc_decode_shared_prefix_plan.restype = ctypes.c_int
+            L.kvc_decode_shared_prefix_plan.argtypes = [i32, i32, PoolDesc, i32, i32, i32,
+                                                        ctypes.POINTER(sz)]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -243,6 +249,41 @@ def kvc_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
         _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         int(num_splits), _stream(stream)))
+
+
+def kvc_decode_shared_prefix_plan(num_seqs: int, q_heads: int, pool: PoolDesc, max_ctx: int,
+                                  num_groups: int, max_prefix_len: int) -> int:
+    """Workspace bytes kvc_decode_shared_prefix needs."""
+    ws = ctypes.c_size_t()
+    _check("kvc_decode_shared_prefix_plan", lib().kvc_decode_shared_prefix_plan(
+        int(num_seqs), int(q_heads), pool, int(max_ctx), int(num_groups), int(max_prefix_len),
+        ctypes.byref(ws)))
+    return ws.value
+
+
+def kvc_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                             v_pool: torch.Tensor, block_table: torch.Tensor,
+                             context_lens: torch.Tensor, max_ctx: int,
+                             group_indptr: torch.Tensor, group_seqs: torch.Tensor,
+                             prefix_len: torch.Tensor, max_group_size: int, max_prefix_len: int,
+                             workspace: torch.Tensor, scale: float = 0.0, stream=None) -> None:
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    for name, t in (("group_indptr", group_indptr), ("group_seqs", group_seqs),
+                    ("prefix_len", prefix_len)):
+        _cuda(name, t, torch.int32)
+    _cuda("workspace", workspace)
+    _check("kvc_decode_shared_prefix", lib().kvc_decode_shared_prefix(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
+        int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
+        _ptr(group_indptr), _ptr(group_seqs), _ptr(prefix_len), int(prefix_len.shape[0]),
+        int(max_group_size), int(max_prefix_len), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def kvc_device_errors() -> int:

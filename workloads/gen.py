@@ -171,7 +171,7 @@ class Case:
     seqs: List[int] = field(default_factory=list)
     docs: Optional[List[np.ndarray]] = None      # token ids, where the case has them
     groups: Optional[List[List[int]]] = None     # sequences that share a prefix
-    shared_positions: int = 0
+    shared_positions: object = 0                 # per group (or one value for all groups)
 
     @property
     def num_seqs(self) -> int:
@@ -236,22 +236,31 @@ def build_case(seed: int, *, name: str, page_size: int, q_heads: int, kv_heads: 
     P = page_size
     sharing = share_groups(np.random.default_rng(s_tok), ctx) if share_groups else None
     shared_pos = sharing["shared_positions"] if sharing else 0
+    group_shared = []
+    if sharing:
+        sp = sharing["shared_positions"]
+        group_shared = [int(sp[i]) if np.ndim(sp) else int(sp)
+                        for i in range(len(sharing["groups"]))]
     if num_pages is None:
         need = sum(-(-int(c) // P) for c in ctx)
         if sharing:
-            need -= sum(len(g) - 1 for g in sharing["groups"]) * (shared_pos // P)
+            need -= sum((len(g) - 1) * (sh // P) for g, sh in zip(sharing["groups"],
+                                                                   group_shared))
         num_pages = max(1, int(np.ceil(need * (1.0 + slack))))
     alloc = PageAllocator(num_pages, P, np.random.default_rng(s_perm).permutation(num_pages))
     seqs = list(range(S))
+    grouped = set()
     if sharing:
-        for group in sharing["groups"]:
+        for group, sh in zip(sharing["groups"], group_shared):
             leader = group[0]
             alloc.reserve(leader, int(ctx[leader]))
+            grouped.add(leader)
             for member in group[1:]:
-                alloc.share(member, leader, shared_pos)
-                alloc.reserve(member, int(ctx[member]) - shared_pos)
-    else:
-        for s in seqs:
+                alloc.share(member, leader, sh)
+                alloc.reserve(member, int(ctx[member]) - sh)
+                grouped.add(member)
+    for s in seqs:
+        if s not in grouped:
             alloc.reserve(s, int(ctx[s]))
     if bt_width is None:
         bt_width = round_up(max(1, max(len(alloc.pages[s]) for s in seqs) if S else 1), 16)
@@ -270,7 +279,7 @@ def build_case(seed: int, *, name: str, page_size: int, q_heads: int, kv_heads: 
                 block_table=bt, q=q, k_new=np.ascontiguousarray(new[0]),
                 v_new=np.ascontiguousarray(new[1]), k_pool=k_pool, v_pool=v_pool,
                 allocator=alloc, seqs=seqs,
-                docs=sharing["docs"] if sharing else None,
+                docs=sharing.get("docs") if sharing else None,
                 groups=sharing["groups"] if sharing else None,
                 shared_positions=shared_pos)
 
