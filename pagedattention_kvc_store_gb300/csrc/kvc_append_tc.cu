@@ -7,24 +7,32 @@
 // the pages its block table lists.
 //
 // Tiling: the rows of one (sequence, kv head) are its (new token, query head of the group)
-// pairs, token-major, 128 per tile (the tcgen05 M).  One CTA per (row tile, kv head,
-// sequence):
-//   warp 0      TMA: the 128-row query tile once, then 64-position K/V stages (one box per
-//               page and 64-column half, 128-byte swizzle) through a 2-deep ring;
-//   warp 1      allocates TMEM and issues the MMAs from one thread:
-//                 S = Q K^T   (M 128, N 64, K head_dim)   into TMEM columns [D, D+64)
-//                 O += P V    (M 128, N head_dim, K 64)   into TMEM columns [0, D), with P
-//                                                        read from TMEM (two buffers)
-//               and zeroes V rows past the last visible position, so that NaN or Inf left
-//               in unused slots never meets a zero probability inside the tensor core;
-//   warps 2-5   softmax: thread r owns row r (TMEM lane r): reads its S row, applies the
+// pairs, token-major, in tiles of 128 (the tcgen05 M).  A work item is a pair of consecutive
+// tiles of one (sequence, kv head); both tiles attend over the same pages, so every K or V
+// stage loaded for the item feeds two tiles.  The kernel is persistent: one CTA per SM walks
+// items c, c + grid, ... and its roles run ahead across item boundaries:
+//   warp 0      TMA, K and V: 128-position stages (one box per page and 64-column half,
+//               128-byte swizzle), K(b) and V(b) in separate slots of one ring, so a K slot is
+//               refilled as soon as both tiles' S = Q K^T products have read it;
+//   warp 1      allocates TMEM (512 columns) and issues, from one thread and in a fixed order,
+//               S_w = Q_w K(b)^T (M 128, N 128, K head_dim) and O_w += P_w V(b) (M 128,
+//               N head_dim, K 128, P read from TMEM) for the tiles w.  tcgen05.mma issue
+//               blocks while the tensor pipe is busy, so this warp does nothing else; products
+//               of one thread run in issue order, so S_w(b + 1) is issued right behind the PV
+//               product that reads P_w(b) from the same columns.  Before the last PV of an
+//               item it zeroes the V rows between the last visible position and the next
+//               multiple of 16, so NaN or Inf left in unused slots never meets a zero
+//               probability inside the tensor core;
+//   warp 2      TMA, the item's query tiles (one buffer, refilled once the item's last S
+//               products are done);
+//   warps 3-6   softmax of tile 0, warps 7-10 softmax of tile 1: thread r owns row r (TMEM
+//               lane r; warp w reaches lanes 32 (w % 4) ..): reads its S row, applies the
 //               scale and the causal limit, keeps a running max / sum, writes P (bf16 pairs)
-//               into one of two TMEM buffers for the PV MMA -- so block b + 1's P can be
-//               written while block b's PV product still reads the other -- and at the end
-//               normalises its O row from TMEM through shared memory to global memory.
+//               over the first half of the S columns, and at the end of the item writes O / l.
 // The running max is updated lazily: O is rescaled (in TMEM) only when a row's max grows by
-// more than 2^8, so a block's exponentials do not wait for the previous PV product.  The
-// result is exact either way; probabilities are then at most 2^8 before normalisation.
+// more than 2^8.  The result is exact either way; probabilities are then at most 2^8 before
+// normalisation.  Barrier phases follow counters kept identically by every role (items, ring
+// slots, and each tile's blocks and items), so they line up across items.
 #include <math.h>
 
 #include "kvc_device.cuh"
@@ -36,27 +44,30 @@ namespace {
 
 __device__ uint32_t g_append_tc_errors;
 
-constexpr int kM = 128;            // rows per tile
-constexpr int kBN = kStageKeys;    // positions per stage (64)
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kM = 128;           // rows per tile
+constexpr int kBN = 128;          // positions per K or V stage (the N of S = Q K^T)
+constexpr int kRoleWarps = 3;     // K/V loads, MMA issue, query loads
+constexpr int kSoftmaxWarps = 8;  // two groups of four
+constexpr int kThreads = (kRoleWarps + kSoftmaxWarps) * 32;
+constexpr int kMaxStages = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct TcGeom {
     static constexpr int kHalves = D / 64;
-    static constexpr int kQBytes = kHalves * kM * 128;
-    static constexpr int kTileBytes = kHalves * kBN * 128;   // K or V of one stage
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kOffStages = kQBytes;
+    static constexpr int kQBytes = kHalves * kM * 128;       // one query tile
+    static constexpr int kStageBytes = kHalves * kBN * 128;  // K or V of 128 positions
+    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kOffStages = 2 * kQBytes;           // Q: [tile]
     static constexpr int kOffBar = kOffStages + kStages * kStageBytes;
-    static constexpr size_t kSmemBytes = kOffBar + 128;   // base is 1024-aligned
-    // TMEM: O [0, D), S [D, D + 64), P buffers [D + 64, D + 96) and [D + 96, D + 128)
-    static constexpr uint32_t kTmemCols = 256;
+    static constexpr size_t kSmemBytes = kOffBar + 256;      // base is 1024-aligned
+    // TMEM, per tile w at w * 256: O [0, D), S [D, D + 128); P overwrites S [D, D + 64).
+    static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = D;
-    static constexpr uint32_t kColP = D + kBN;
-    static_assert(D + kBN + kBN <= static_cast<int>(kTmemCols), "TMEM layout");
+    static_assert(D + kBN <= 256, "TMEM layout");
+    static_assert(kStages <= kMaxStages, "ring barriers");
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct Args {
@@ -66,129 +77,112 @@ struct Args {
     int bt_stride;
     const int32_t *q_indptr;
     const int32_t *context_lens;
-    int q_heads, group, page_size;
+    int kv_heads, q_heads, group, page_size, pairs_per_seq, num_items;
     float scale_log2;
 };
 
-// Barrier slots after the P buffer.
 enum BarIndex : int {
-    kBarKvFull = 0,                 // [kStages]
-    kBarKvEmpty = kBarKvFull + kStages,
-    kBarQFull = kBarKvEmpty + kStages,
-    kBarSFull,
-    kBarSFree,
-    kBarPFull,                      // [2]: one per P buffer
-    kBarPvDone = kBarPFull + 2,     // [2]
+    kBarKvFull = 0,                         // [ring slot]
+    kBarKvEmpty = kBarKvFull + kMaxStages,  // [ring slot], one MMA commit
+    kBarQFull = kBarKvEmpty + kMaxStages,
+    kBarQEmpty = kBarQFull + 1,             // one MMA commit after the item's last S products
+    kBarSFull = kBarQEmpty + 1,             // [tile]
+    kBarPFull = kBarSFull + 2,              // [tile], 128 arrivals
+    kBarPvDone = kBarPFull + 2,             // [tile], once per item
     kBarDrain = kBarPvDone + 2,
     kBarCount
 };
 
+// One work item: tiles 2 tp and 2 tp + 1 of one (sequence, kv head).
+struct Item {
+    int s, kvh, tp;
+    int tok0, q_len, ctx, rows, row_begin;   // row_begin: first row of tile 2 tp
+    bool has_b;                              // tile 2 tp + 1 exists
+    int n_keys, n_blocks;                    // positions the item's later tile sees
+};
+
+__device__ __forceinline__ bool load_item(const Args &a, int it, Item &x)
+{
+    x.tp = it % a.pairs_per_seq;
+    const int rest = it / a.pairs_per_seq;
+    x.kvh = rest % a.kv_heads;
+    x.s = rest / a.kv_heads;
+    x.tok0 = a.q_indptr[x.s];
+    x.q_len = a.q_indptr[x.s + 1] - x.tok0;
+    x.ctx = a.context_lens[x.s];
+    if (x.ctx > a.bt_stride * a.page_size) {
+        if (threadIdx.x == 0)
+            atomicOr(&g_append_tc_errors, kErrContextRange);
+        x.ctx = a.bt_stride * a.page_size;
+    }
+    x.rows = x.q_len * a.group;
+    x.row_begin = x.tp * 2 * kM;
+    if (x.row_begin >= x.rows)
+        return false;
+    x.has_b = x.row_begin + kM < x.rows;
+    const int row_last = min(x.rows, x.row_begin + 2 * kM) - 1;
+    x.n_keys = min(x.ctx, x.ctx - x.q_len + row_last / a.group + 1);
+    if (x.n_keys <= 0)
+        return false;
+    x.n_blocks = (x.n_keys + kBN - 1) / kBN;
+    return true;
+}
+
+// Walks this CTA's items: it = blockIdx.x, blockIdx.x + gridDim.x, ..., skipping empty ones.
+struct Walker {
+    int it;
+    bool done;
+    Item x;
+    __device__ __forceinline__ void next(const Args &a)
+    {
+        do {
+            it += gridDim.x;
+            if (it >= a.num_items) {
+                done = true;
+                return;
+            }
+        } while (!load_item(a, it, x));
+    }
+    __device__ __forceinline__ void start(const Args &a)
+    {
+        it = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+        done = false;
+        next(a);
+    }
+};
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     paged_append_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                            const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
     using Geom = TcGeom<D>;
     constexpr int kHalves = D / 64;
+    constexpr int kStages = Geom::kStages;
 
     // The swizzled tiles need a 1024-byte-aligned base; the dynamic shared window of a kernel
-    // with no static shared memory starts there, which is checked rather than padded for (the
-    // padding would cost the second CTA per SM).
+    // with no static shared memory starts there, which is checked rather than padded for.
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_addr(smem) & 1023u) != 0) {
         if (threadIdx.x == 0)
             atomicOr(&g_append_tc_errors, kErrSmemAlign);
         return;
     }
-    uint8_t *sQ = smem;
     uint8_t *sStages = smem + Geom::kOffStages;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Geom::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBarCount);
+    auto q_tile = [&](int tile) { return smem + tile * Geom::kQBytes; };
 
-    const int tile = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int s = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.group;
     const int P = a.page_size;
-    const int tok0 = a.q_indptr[s];
-    const int q_len = a.q_indptr[s + 1] - tok0;
-    int ctx = a.context_lens[s];
-    if (ctx > a.bt_stride * P) {
-        if (threadIdx.x == 0 && tile == 0)
-            atomicOr(&g_append_tc_errors, kErrContextRange);
-        ctx = a.bt_stride * P;
-    }
-    const int rows = q_len * G;
-    const int row_begin = tile * kM;
-    if (row_begin >= rows)
-        return;
-    const int row_last = min(rows, row_begin + kM) - 1;
-    const int n_keys = min(ctx, ctx - q_len + row_last / G + 1);
-    if (n_keys <= 0)
-        return;
-    const int n_blocks = (n_keys + kBN - 1) / kBN;
 
-    // Producer state (warp 0).  The query tile and the first stages are issued before the
-    // CTA-wide barrier below, so the loads overlap the TMEM allocation.
-    const int32_t *bt_row = a.block_table + static_cast<size_t>(s) * a.bt_stride;
-    const int n_pages = (n_keys + P - 1) / P;
-    int cached_base = -32;
-    int cached_page = 0;
-    int issued = 0;
-    uint64_t policy = 0;
-    // Load the K and V pages of stage b (all lanes of warp 0; lane 0 issues the copies).
-    auto produce_block = [&](int b) {
-        const int st = b % kStages;
-        const int key0 = b * kBN;
-        const int np = (min(kBN, n_keys - key0) + P - 1) / P;
-        if (lane == 0)
-            mbar_arrive_expect_tx(&bars[kBarKvFull + st], static_cast<uint32_t>(np * P * D * 2 * 2));
-        uint8_t *kdst = sStages + st * Geom::kStageBytes;
-        uint8_t *vdst = kdst + Geom::kTileBytes;
-        for (int i = 0; i < np; ++i) {
-            const int lp = key0 / P + i;
-            if (lp >= cached_base + 32) {
-                cached_base = lp;
-                cached_page = (lp + lane < n_pages) ? bt_row[lp + lane] : 0;
-            }
-            const int page = __shfl_sync(0xffffffffu, cached_page, lp - cached_base);
-            if (lane == 0) {
-                const int slot0 = page * P;
-#pragma unroll
-                for (int h = 0; h < kHalves; ++h) {
-                    const int off = h * kBN * 128 + i * P * 128;
-                    tma_load_3d(kdst + off, &tmap_k, h * 64, kvh, slot0, &bars[kBarKvFull + st],
-                                policy);
-                    tma_load_3d(vdst + off, &tmap_v, h * 64, kvh, slot0, &bars[kBarKvFull + st],
-                                policy);
-                }
-            }
-        }
-        issued = b + 1;
-    };
-    if (warp == 0) {
-        if (lane == 0) {
-            for (int i = 0; i < kBarCount; ++i)
-                mbar_init(&bars[i],
-                          (i == kBarSFree || i == kBarPFull || i == kBarPFull + 1) ? 128u : 1u);
-            fence_mbar_init();
-            prefetch_tensormap(&tmap_q);
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
-            // the tile's 128 / G tokens x G heads of this kv head, token-major
-            mbar_arrive_expect_tx(&bars[kBarQFull], Geom::kQBytes);
-#pragma unroll
-            for (int h = 0; h < kHalves; ++h)
-                tma_load_4d(sQ + h * kM * 128, &tmap_q, h * 64, 0, kvh, tok0 + row_begin / G,
-                            &bars[kBarQFull]);
-        }
-        __syncwarp();
-        policy = l2_policy_evict_last();   // the sibling row tile re-reads these pages
-        for (int b = 0; b < min(kStages, n_blocks); ++b)
-            produce_block(b);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kBarCount; ++i)
+            mbar_init(&bars[i], (i == kBarPFull || i == kBarPFull + 1) ? 128u : 1u);
+        fence_mbar_init();
     }
     if (warp == 1)
         tmem_alloc(tmem_slot, Geom::kTmemCols);
@@ -196,127 +190,217 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem;
-    const uint32_t tmem_s = tmem + Geom::kColS;
-    const uint32_t tmem_p = tmem + Geom::kColP;   // buffer j at tmem_p + 32 j
     bool ok = true;
 
     if (warp == 0) {
-        // ------------------------------ TMA producer -------------------------------------
-        for (int b = kStages; b < n_blocks; ++b) {
-            const int st = b % kStages;
-            const bool waited = mbar_wait(&bars[kBarKvEmpty + st], ((b / kStages) - 1) & 1);
-            if (!__all_sync(0xffffffffu, waited)) {
-                ok = false;
-                break;
+        // ------------------------------ K / V loads --------------------------------------
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+        const uint64_t policy = l2_policy_evict_first();
+        Walker w;
+        w.start(a);
+        int n = 0;   // ring slots filled so far
+        while (ok && !w.done) {
+            const Item &x = w.x;
+            const int32_t *bt_row = a.block_table + static_cast<size_t>(x.s) * a.bt_stride;
+            const int n_pages = (x.n_keys + P - 1) / P;
+            int cached_base = -32;
+            int cached_page = 0;
+            for (int b = 0; b < x.n_blocks && ok; ++b) {
+                const int key0 = b * kBN;
+                const int np = (min(kBN, x.n_keys - key0) + P - 1) / P;
+                for (int kind = 0; kind < 2; ++kind, ++n) {   // K(b), then V(b)
+                    const int st = n % kStages;
+                    if (n >= kStages &&
+                        !__all_sync(0xffffffffu,
+                                    mbar_wait(&bars[kBarKvEmpty + st], ((n / kStages) - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&bars[kBarKvFull + st],
+                                              static_cast<uint32_t>(np * P * D * 2));
+                    uint8_t *dst = sStages + st * Geom::kStageBytes;
+                    const CUtensorMap *map = kind == 0 ? &tmap_k : &tmap_v;
+                    for (int i = 0; i < np; ++i) {
+                        const int lp = key0 / P + i;
+                        if (lp >= cached_base + 32 || lp < cached_base) {
+                            cached_base = lp;
+                            cached_page = (lp + lane < n_pages) ? bt_row[lp + lane] : 0;
+                        }
+                        const int page = __shfl_sync(0xffffffffu, cached_page, lp - cached_base);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int h = 0; h < kHalves; ++h)
+                                tma_load_3d(dst + h * kBN * 128 + i * P * 128, map, h * 64, x.kvh,
+                                            page * P, &bars[kBarKvFull + st], policy);
+                        }
+                    }
+                }
             }
-            produce_block(b);
+            if (!ok)
+                break;
+            w.next(a);
         }
         if (!ok && lane == 0) {
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
-            for (int b = max(0, issued - kStages); b < issued; ++b)
-                if (!mbar_wait(&bars[kBarKvFull + b % kStages], (b / kStages) & 1))
+            // let every copy in flight land before the CTA can exit
+            for (int m = max(0, n - kStages); m < n; ++m)
+                if (!mbar_wait(&bars[kBarKvFull + m % kStages], (m / kStages) & 1))
                     atomicOr(&g_append_tc_errors, kErrDrainWait);
-            if (!mbar_wait(&bars[kBarQFull], 0))
+        }
+    } else if (warp == 2) {
+        // ------------------------------ query loads --------------------------------------
+        if (lane == 0)
+            prefetch_tensormap(&tmap_q);
+        Walker w;
+        w.start(a);
+        int li = 0;   // items whose query tiles were requested
+        while (ok && !w.done) {
+            const Item &x = w.x;
+            if (li > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(&bars[kBarQEmpty], (li - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                // the tiles' 128 / G tokens x G heads of this kv head, token-major
+                mbar_arrive_expect_tx(&bars[kBarQFull],
+                                      (x.has_b ? 2 : 1) * static_cast<uint32_t>(Geom::kQBytes));
+                for (int t = 0; t < (x.has_b ? 2 : 1); ++t)
+#pragma unroll
+                    for (int h = 0; h < kHalves; ++h)
+                        tma_load_4d(q_tile(t) + h * kM * 128, &tmap_q, h * 64, 0, x.kvh,
+                                    x.tok0 + (x.row_begin + t * kM) / G, &bars[kBarQFull]);
+            }
+            ++li;
+            w.next(a);
+        }
+        if (!ok && lane == 0) {
+            atomicOr(&g_append_tc_errors, kErrAppendTcWait);
+            // the last request may still be in flight
+            if (!mbar_wait(&bars[kBarQFull], (li - 1) & 1))
                 atomicOr(&g_append_tc_errors, kErrDrainWait);
         }
     } else if (warp == 1) {
-        // ------------------------------ MMA issuer ---------------------------------------
-        constexpr uint32_t kIdescQK = umma_idesc_bf16(kM, kBN, 0);
+        // ------------------------------ MMA issue ----------------------------------------
         constexpr uint32_t kIdescPV = umma_idesc_bf16(kM, D, 1);
-        const uint32_t q_addr = smem_addr(sQ);
         const uint32_t stage_addr = smem_addr(sStages);
-
-        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
-            const bool w = mbar_wait(bar, parity);
-            return __all_sync(0xffffffffu, w);
+        auto stage_of = [&](int n) { return stage_addr + (n % kStages) * Geom::kStageBytes; };
+        auto wait_slot = [&](int n) {
+            return __all_sync(0xffffffffu,
+                              mbar_wait(&bars[kBarKvFull + n % kStages], (n / kStages) & 1));
         };
-        // Zero V rows n_valid .. kBN-1 of stage st (positions past the last visible one).
-        auto zero_v_tail = [&](int st, int n_valid) {
-            uint8_t *vt = sStages + st * Geom::kStageBytes + Geom::kTileBytes;
-            const int rows_to_zero = kBN - n_valid;
-            for (int idx = lane; idx < rows_to_zero * kHalves * 8; idx += 32) {
-                const int chunk = idx & 7;
-                const int rest = idx >> 3;
-                const int h = rest % kHalves;
-                const int r = n_valid + rest / kHalves;
-                *reinterpret_cast<uint4 *>(vt + h * kBN * 128 + r * 128 + chunk * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+        // S_t = Q_t K^T over n_cols positions (a multiple of 16)
+        auto issue_qk = [&](int t, uint32_t k_addr, int n_cols) {
+            const uint32_t idesc = umma_idesc_bf16(kM, n_cols, 0);
+            const uint32_t q_addr = smem_addr(q_tile(t));
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint64_t da =
+                    umma_desc_sw128(q_addr + (k >> 2) * kM * 128 + (k & 3) * 32, 16, 1024);
+                const uint64_t db =
+                    umma_desc_sw128(k_addr + (k >> 2) * kBN * 128 + (k & 3) * 32, 16, 1024);
+                umma_bf16_ss(tmem + t * 256 + Geom::kColS, da, db, idesc, k > 0 ? 1u : 0u);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
         };
-        auto issue_qk = [&](int st) {
+        // O_t (+)= P_t V over k_steps x 16 positions
+        auto issue_pv = [&](int t, uint32_t v_addr, int k_steps, bool first) {
+            for (int k = 0; k < k_steps; ++k) {
+                const uint64_t db = umma_desc_sw128(v_addr + k * 16 * 128, kBN * 128, 1024);
+                umma_bf16_ts(tmem + t * 256, tmem + t * 256 + Geom::kColS + k * 8, db, kIdescPV,
+                             (!first || k > 0) ? 1u : 0u);
+            }
+        };
+        Walker w;
+        w.start(a);
+        int n = 0;    // ring slots consumed so far
+        int li = 0;   // items
+        int tb0 = 0, tb1 = 0;   // blocks of tile 0 / tile 1
+        while (ok && !w.done) {
+            const Item &x = w.x;
+            const int nt = x.has_b ? 2 : 1;
+            const int nb = x.n_blocks;
+            const int last_valid = x.n_keys - (nb - 1) * kBN;   // positions in the last block
+            const int last_cols = (last_valid + 15) & ~15;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarQFull], li & 1)) || !wait_slot(n)) {
+                ok = false;
+                break;
+            }
             tc_fence_after_sync();
             if (lane == 0) {
-                const uint32_t k_addr = stage_addr + st * Geom::kStageBytes;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t da =
-                        umma_desc_sw128(q_addr + (k >> 2) * kM * 128 + (k & 3) * 32, 16, 1024);
-                    const uint64_t db =
-                        umma_desc_sw128(k_addr + (k >> 2) * kBN * 128 + (k & 3) * 32, 16, 1024);
-                    umma_bf16_ss(tmem_s, da, db, kIdescQK, k > 0 ? 1u : 0u);
+                for (int t = 0; t < nt; ++t) {
+                    issue_qk(t, stage_of(n), nb == 1 ? last_cols : kBN);
+                    umma_commit(&bars[kBarSFull + t]);
                 }
-                umma_commit(&bars[kBarSFull]);
+                if (nb == 1)
+                    umma_commit(&bars[kBarQEmpty]);
+                umma_commit(&bars[kBarKvEmpty + n % kStages]);
             }
             __syncwarp();
-        };
-
-        if (!wait_all(&bars[kBarQFull], 0))
-            ok = false;
-        // Event loop: issue whichever of QK_{next_qk} (needs its K/V stage and the softmax
-        // warps to have read the previous S) and PV_{next_pv} (needs P) is ready first, so
-        // the PV product of a block never waits for the next block's loads.
-        int next_qk = 0, next_pv = 0;
-        long long idle_since = clock64();
-        while (ok && next_pv < n_blocks) {
-            bool progressed = false;
-            if (next_qk < n_blocks) {
-                const int st = next_qk % kStages;
-                bool ready = mbar_test(&bars[kBarKvFull + st], (next_qk / kStages) & 1) &&
-                             (next_qk == 0 || mbar_test(&bars[kBarSFree], (next_qk - 1) & 1));
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    const int n_valid = n_keys - next_qk * kBN;
-                    if (n_valid < kBN)
-                        zero_v_tail(st, n_valid);
-                    issue_qk(st);
-                    ++next_qk;
-                    progressed = true;
+            ++n;
+            for (int b = 0; b < nb && ok; ++b) {
+                const bool last = b + 1 == nb;
+                const int vn = n++;   // V(b)
+                if (!wait_slot(vn)) {
+                    ok = false;
+                    break;
                 }
-            }
-            if (next_pv < next_qk) {
-                bool ready = mbar_test(&bars[kBarPFull + (next_pv & 1)], (next_pv >> 1) & 1);
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    const int st = next_pv % kStages;
+                if (last && last_valid < last_cols) {
+                    // V rows last_valid .. last_cols - 1 of every column half
+                    uint8_t *vt = sStages + (vn % kStages) * Geom::kStageBytes;
+                    const int rows_to_zero = last_cols - last_valid;
+                    for (int idx = lane; idx < rows_to_zero * kHalves * 8; idx += 32) {
+                        const int chunk = idx & 7;
+                        const int rest = idx >> 3;
+                        const int h = rest % kHalves;
+                        const int r = last_valid + rest / kHalves;
+                        *reinterpret_cast<uint4 *>(vt + h * kBN * 128 + r * 128 + chunk * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const int kn = n;   // K(b + 1)
+                for (int t = 0; t < nt; ++t) {
+                    const int tb = t == 0 ? tb0++ : tb1++;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPFull + t], tb & 1)) ||
+                        (!last && t == 0 && !wait_slot(kn))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after_sync();
                     if (lane == 0) {
-                        const uint32_t v_addr =
-                            stage_addr + st * Geom::kStageBytes + Geom::kTileBytes;
-                        const uint32_t p_cols = tmem_p + (next_pv & 1) * 32;
-#pragma unroll
-                        for (int k = 0; k < kBN / 16; ++k) {
-                            const uint64_t db =
-                                umma_desc_sw128(v_addr + k * 16 * 128, kBN * 128, 1024);
-                            umma_bf16_ts(tmem_o, p_cols + k * 8, db, kIdescPV,
-                                         (next_pv > 0 || k > 0) ? 1u : 0u);
+                        issue_pv(t, stage_of(vn), last ? last_cols / 16 : kBN / 16, b == 0);
+                        if (last) {
+                            umma_commit(&bars[kBarPvDone + t]);
+                        } else {
+                            issue_qk(t, stage_of(kn), b + 2 == nb ? last_cols : kBN);
+                            umma_commit(&bars[kBarSFull + t]);
                         }
-                        umma_commit(&bars[kBarPvDone + (next_pv & 1)]);
-                        umma_commit(&bars[kBarKvEmpty + st]);
                     }
                     __syncwarp();
-                    ++next_pv;
-                    progressed = true;
                 }
+                if (!ok)
+                    break;
+                if (lane == 0) {
+                    umma_commit(&bars[kBarKvEmpty + vn % kStages]);
+                    if (!last) {
+                        umma_commit(&bars[kBarKvEmpty + kn % kStages]);
+                        if (b + 2 == nb)
+                            umma_commit(&bars[kBarQEmpty]);
+                    }
+                }
+                __syncwarp();
+                if (!last)
+                    ++n;
             }
-            if (progressed) {
-                idle_since = clock64();
-            } else if (clock64() - idle_since > kWaitLimitCycles) {
-                ok = false;
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            ++li;
+            w.next(a);
         }
         if (!ok && lane == 0)
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
@@ -328,183 +412,148 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
     } else {
-        // ------------------------------ softmax warps ------------------------------------
-        const int quad = warp & 3;                  // TMEM lane quarter this warp may access
-        const int row = quad * 32 + lane;           // row of the tile = TMEM lane
+        // ------------------------------ softmax + epilogue -------------------------------
+        const int t = (warp - kRoleWarps) >> 2;      // tile
+        const int quad = warp & 3;                   // TMEM lanes 32 quad ..
+        const int row = quad * 32 + lane;            // row of the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const int gr = row_begin + row;
-        const bool valid = gr < rows;
-        const int ti = gr / G;
-        const int lim = valid ? ctx - q_len + ti : -1;   // last visible position
+        const uint32_t tmem_o = tmem + t * 256 + lane_off;
+        const uint32_t tmem_s = tmem + t * 256 + Geom::kColS + lane_off;
         const float sl2 = a.scale_log2;
-        float m_used = -INFINITY;
-        float l_sum = 0.0f;
-
-        for (int b = 0; b < n_blocks; ++b) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarSFull], b & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            float x[64];
-            {
-                float t0[32], t1[32];
-                tmem_ld32(tmem_s + lane_off, t0);
-                tmem_ld32(tmem_s + lane_off + 32, t1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = t0[c];
-                    x[32 + c] = t1[c];
-                }
-            }
-            tc_fence_before_sync();
-            mbar_arrive(&bars[kBarSFree]);
-
-            const int key0 = b * kBN;
-            // causal limit (and positions past the loaded range) on the raw scores
-            if (key0 + kBN - 1 > lim) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (key0 + c > lim)
-                        x[c] = -INFINITY;
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-                mx = fmaxf(mx, x[c]);
-            const float mb = mx * sl2;   // base-2 scaled row max of this block (scale > 0)
-            // lazy rescale: move the reference max only when it grows by more than 2^8
-            float alpha = 1.0f;
-            bool moved = false;
-            if (mb > m_used + kRescaleLog2) {
-                alpha = (m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - mb);
-                m_used = mb;
-                moved = true;
-            }
-            const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
-            uint32_t pk[32];
-            float psum = 0.0f;
-            if (__any_sync(0xffffffffu, valid)) {
-                // p = 2^(s * scale * log2(e) - m); every fourth column on the FMA pipe
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float e0 = fast_exp2(fmaf(x[2 * c], sl2, neg_mu));
-                    const float y1 = fmaf(x[2 * c + 1], sl2, neg_mu);
-                    const float e1 = (c & 1) ? exp2_fma(y1) : fast_exp2(y1);
-                    pk[c] = pack_bf16x2(e0, e1);
-                    psum += bf16x2_sum(pk[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c)   // a warp of padding rows: P = 0
-                    pk[c] = 0u;
-            }
-            l_sum = l_sum * alpha + psum;
-
-            // P buffer b & 1 was last read by PV(b - 2); O may be rescaled only once PV(b - 1)
-            // is done.
-            const int pb = b & 1;
-            if (b >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + pb],
-                                                             ((b >> 1) - 1) & 1))) {
-                ok = false;
-                break;
-            }
-            if (b > 0 && __any_sync(0xffffffffu, moved)) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + ((b - 1) & 1)],
-                                                       ((b - 1) >> 1) & 1))) {
+        Walker w;
+        w.start(a);
+        int tb = 0;   // blocks of this tile so far
+        int ti = 0;   // items of this tile so far
+        for (; ok && !w.done; w.next(a)) {
+            const Item &x = w.x;
+            if (t == 1 && !x.has_b)
+                continue;
+            const int row_begin = x.row_begin + t * kM;
+            const int gr = row_begin + row;
+            const bool valid = gr < x.rows;
+            const int tok = gr / G;
+            const int lim = valid ? x.ctx - x.q_len + tok : -1;   // last visible position
+            const bool warp_valid = __any_sync(0xffffffffu, valid);
+            float m_used = -INFINITY;
+            float l_sum = 0.0f;
+            for (int b = 0; b < x.n_blocks; ++b, ++tb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarSFull + t], tb & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                {
+                uint32_t pk[2][32];
+                float alpha = 1.0f;
+                bool moved = false;
+                if (warp_valid) {
+                    float xs[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tmem_ld32(tmem_s + 32 * c, xs[c]);
+                    tmem_wait_ld();
+                    const int key0 = b * kBN;
+                    if (key0 + kBN - 1 > lim) {   // causal limit / positions past the block
+#pragma unroll
+                        for (int j = 0; j < kBN; ++j)
+                            if (key0 + j > lim)
+                                xs[j >> 5][j & 31] = -INFINITY;
+                    }
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < kBN; ++j)
+                        mx = fmaxf(mx, xs[j >> 5][j & 31]);
+                    const float mb = mx * sl2;   // base-2 scaled row max of this block
+                    if (mb > m_used + kRescaleLog2) {
+                        alpha = (m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - mb);
+                        m_used = mb;
+                        moved = true;
+                    }
+                    const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
+                    float psum = 0.0f;
+                    // p = 2^(s * scale * log2(e) - m); every fourth column on the FMA pipe
+#pragma unroll
+                    for (int j = 0; j < kBN / 2; ++j) {
+                        const float x0 = xs[(2 * j) >> 5][(2 * j) & 31];
+                        const float x1 = xs[(2 * j + 1) >> 5][(2 * j + 1) & 31];
+                        const float e0 = fast_exp2(fmaf(x0, sl2, neg_mu));
+                        const float y1 = fmaf(x1, sl2, neg_mu);
+                        const float e1 = (j & 1) ? exp2_fma(y1) : fast_exp2(y1);
+                        pk[j >> 5][j & 31] = pack_bf16x2(e0, e1);
+                        psum += bf16x2_sum(pk[j >> 5][j & 31]);
+                    }
+                    l_sum = l_sum * alpha + psum;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {   // a warp of padding rows: P = 0
+                        pk[0][j] = 0u;
+                        pk[1][j] = 0u;
+                    }
+                }
+                // O holds every earlier PV product (S(b) was committed after them): rescale
+                // it in place when the max moved.
+                if (b > 0 && __any_sync(0xffffffffu, moved)) {
                     const float f = moved ? alpha : 1.0f;
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         float o[32];
-                        tmem_ld32(tmem_o + lane_off + c0, o);
+                        tmem_ld32(tmem_o + c0, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            o[c] *= f;
-                        tmem_st32(tmem_o + lane_off + c0, o);
+                        for (int j = 0; j < 32; ++j)
+                            o[j] *= f;
+                        tmem_st32(tmem_o + c0, o);
                     }
-                    tmem_wait_st();
                 }
+                tmem_st32u(tmem_s, pk[0]);
+                tmem_st32u(tmem_s + 32, pk[1]);
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(&bars[kBarPFull + t]);
             }
+            if (!ok)
+                break;
+            // epilogue: once this tile's last PV is done, O / l -> global
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + t], ti & 1))) {
+                ok = false;
+                break;
+            }
+            ++ti;
             tc_fence_after_sync();
-            // P row -> TMEM buffer pb: column j holds positions 2j, 2j + 1
-            tmem_st32u(tmem_p + pb * 32 + lane_off, pk);
-            tmem_wait_st();
+            const float inv = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
+            const int g = gr - tok * G;
+            const size_t out_row =
+                (static_cast<size_t>(x.tok0 + tok) * a.q_heads + static_cast<size_t>(x.kvh) * G +
+                 g) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tmem_ld32(tmem_o + c0, o);
+                tmem_wait_ld();
+                if (valid) {
+                    if (a.out_f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) +
+                                                                 out_row + c0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(o[4 * j] * inv, o[4 * j + 1] * inv,
+                                                 o[4 * j + 2] * inv, o[4 * j + 3] * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            static_cast<__nv_bfloat16 *>(a.out) + out_row + c0);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                                pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                                pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                                pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                    }
+                }
+                __syncwarp();
+            }
             tc_fence_before_sync();
-            mbar_arrive(&bars[kBarPFull + pb]);
         }
-
-        // epilogue: O row / l -> global, once the last PV product is done
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars[kBarPvDone + ((n_blocks - 1) & 1)],
-                                                     ((n_blocks - 1) >> 1) & 1)))
-            ok = false;
-        tc_fence_after_sync();
         if (!ok)
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
-        const float inv = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
-        if (a.out_f32) {
-            const int g = gr - ti * G;
-            const size_t out_row =
-                (static_cast<size_t>(tok0 + ti) * a.q_heads + static_cast<size_t>(kvh) * G + g) *
-                D;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem_o + lane_off + c0, o);
-                tmem_wait_ld();
-                if (valid && ok) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) +
-                                                             out_row + c0);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv,
-                                             o[4 * c + 2] * inv, o[4 * c + 3] * inv);
-                }
-            }
-        } else {
-            // Stage the bf16 tile in the query buffer (dead since the last QK product): row r
-            // holds D * 2 bytes, 16-byte chunk c at (c & ~7) | ((c & 7) ^ (r & 7)), so eight
-            // consecutive rows hit distinct banks.  Then store whole rows, coalesced.
-            constexpr int kChunks = D / 8;
-            uint8_t *stage_row = sQ + row * (D * 2);
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem_o + lane_off + c0, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = c0 / 8 + c;
-                    const int phys = (chunk & ~7) | ((chunk & 7) ^ (row & 7));
-                    *reinterpret_cast<uint4 *>(stage_row + phys * 16) =
-                        make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                                   pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                   pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                                   pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-                }
-            }
-            named_barrier(1, 128);
-            const int n_rows = min(kM, rows - row_begin);
-            const int t = threadIdx.x - 64;   // 0 .. 127 over the softmax warps
-            for (int idx = t; ok && idx < n_rows * kChunks; idx += 128) {
-                const int r = idx / kChunks;
-                const int chunk = idx - r * kChunks;
-                const int phys = (chunk & ~7) | ((chunk & 7) ^ (r & 7));
-                const int grr = row_begin + r;
-                const int tok = grr / G;
-                const size_t dst_row = (static_cast<size_t>(tok0 + tok) * a.q_heads +
-                                        static_cast<size_t>(kvh) * G + (grr - tok * G)) * D;
-                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + dst_row +
-                                           chunk * 8) =
-                    *reinterpret_cast<const uint4 *>(sQ + r * (D * 2) + phys * 16);
-            }
-        }
     }
 
     tc_fence_before_sync();
@@ -513,6 +562,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after_sync();
         tmem_dealloc(tmem, Geom::kTmemCols);
     }
+}
+
+int sm_count()
+{
+    static int count = 0;
+    if (count == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            count = n;
+        else
+            count = 152;
+    }
+    return count;
 }
 
 template <int D>
@@ -526,9 +589,16 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     a.bt_stride = l.bt_stride;
     a.q_indptr = l.q_indptr;
     a.context_lens = l.context_lens;
+    a.kv_heads = l.kv_heads;
     a.q_heads = l.q_heads;
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
+    const int tiles = (l.max_q_len * a.group + kM - 1) / kM;
+    a.pairs_per_seq = (tiles + 1) / 2;
+    const long long items = static_cast<long long>(a.pairs_per_seq) * l.kv_heads * l.num_seqs;
+    if (items > 0x7FFFFFFFLL)
+        return cudaErrorInvalidValue;
+    a.num_items = static_cast<int>(items);
     a.scale_log2 = l.scale * kLog2e;
     const size_t smem = TcGeom<D>::kSmemBytes;
     auto kernel = paged_append_tc_kernel<D>;
@@ -536,8 +606,7 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
                                            static_cast<int>(smem));
     if (err != cudaSuccess)
         return err;
-    const int tiles = (l.max_q_len * a.group + kM - 1) / kM;
-    dim3 grid(tiles, l.kv_heads, l.num_seqs);
+    const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
     kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
