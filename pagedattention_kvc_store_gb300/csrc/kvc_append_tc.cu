@@ -366,20 +366,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kn = n;   // K(b + 1)
                 for (int t = 0; t < nt; ++t) {
                     const int tb = t == 0 ? tb0++ : tb1++;
-                    if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPFull + t], tb & 1)) ||
-                        (!last && t == 0 && !wait_slot(kn))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPFull + t], tb & 1))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     if (lane == 0) {
                         issue_pv(t, stage_of(vn), last ? last_cols / 16 : kBN / 16, b == 0);
-                        if (last) {
+                        if (last)
                             umma_commit(&bars[kBarPvDone + t]);
-                        } else {
-                            issue_qk(t, stage_of(kn), b + 2 == nb ? last_cols : kBN);
-                            umma_commit(&bars[kBarSFull + t]);
-                        }
+                    }
+                    __syncwarp();
+                    if (last)
+                        continue;
+                    // K(b + 1) is waited for only once PV(b) of tile 0 is on its way
+                    if (t == 0 && !wait_slot(kn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    if (lane == 0) {
+                        issue_qk(t, stage_of(kn), b + 2 == nb ? last_cols : kBN);
+                        umma_commit(&bars[kBarSFull + t]);
                     }
                     __syncwarp();
                 }
@@ -442,51 +450,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                uint32_t pk[2][32];
+                const int key0 = b * kBN;
+                // positions of this block the row may see: columns 0 .. n_vis - 1
+                const int n_vis = min(max(lim - key0 + 1, 0), kBN);
                 float alpha = 1.0f;
                 bool moved = false;
                 if (warp_valid) {
+                    // pass 1: the row max; masked columns are set to -inf in TMEM as well, so
+                    // the exponent pass below needs no mask
                     float xs[4][32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         tmem_ld32(tmem_s + 32 * c, xs[c]);
                     tmem_wait_ld();
-                    const int key0 = b * kBN;
-                    if (key0 + kBN - 1 > lim) {   // causal limit / positions past the block
+                    float mx = -INFINITY;
+                    if (__all_sync(0xffffffffu, n_vis == kBN)) {
 #pragma unroll
                         for (int j = 0; j < kBN; ++j)
-                            if (key0 + j > lim)
-                                xs[j >> 5][j & 31] = -INFINITY;
-                    }
-                    float mx = -INFINITY;
+                            mx = fmaxf(mx, xs[j >> 5][j & 31]);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < kBN; ++j)
-                        mx = fmaxf(mx, xs[j >> 5][j & 31]);
+                        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                if (32 * c + j >= n_vis)
+                                    xs[c][j] = -INFINITY;
+                                mx = fmaxf(mx, xs[c][j]);
+                            }
+                            tmem_st32(tmem_s + 32 * c, xs[c]);
+                        }
+                        tmem_wait_st();
+                    }
                     const float mb = mx * sl2;   // base-2 scaled row max of this block
                     if (mb > m_used + kRescaleLog2) {
                         alpha = (m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - mb);
                         m_used = mb;
                         moved = true;
-                    }
-                    const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
-                    float psum = 0.0f;
-                    // p = 2^(s * scale * log2(e) - m); every fourth column on the FMA pipe
-#pragma unroll
-                    for (int j = 0; j < kBN / 2; ++j) {
-                        const float x0 = xs[(2 * j) >> 5][(2 * j) & 31];
-                        const float x1 = xs[(2 * j + 1) >> 5][(2 * j + 1) & 31];
-                        const float e0 = fast_exp2(fmaf(x0, sl2, neg_mu));
-                        const float y1 = fmaf(x1, sl2, neg_mu);
-                        const float e1 = (j & 1) ? exp2_fma(y1) : fast_exp2(y1);
-                        pk[j >> 5][j & 31] = pack_bf16x2(e0, e1);
-                        psum += bf16x2_sum(pk[j >> 5][j & 31]);
-                    }
-                    l_sum = l_sum * alpha + psum;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {   // a warp of padding rows: P = 0
-                        pk[0][j] = 0u;
-                        pk[1][j] = 0u;
                     }
                 }
                 // O holds every earlier PV product (S(b) was committed after them): rescale
@@ -504,8 +503,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(tmem_o + c0, o);
                     }
                 }
-                tmem_st32u(tmem_s, pk[0]);
-                tmem_st32u(tmem_s + 32, pk[1]);
+                // pass 2, 32 columns at a time (a short loop body keeps the instruction
+                // footprint small): p = 2^(s * scale * log2(e) - m), every fourth column on the
+                // FMA pipe; the bf16 pairs of chunk c go to S columns [16 c, 16 c + 16), which
+                // hold only chunks already read.
+                const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
+                float psum = 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+                    if (warp_valid) {
+                        float v[32];
+                        tmem_ld32(tmem_s + 32 * c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float e0 = fast_exp2(fmaf(v[2 * j], sl2, neg_mu));
+                            const float y1 = fmaf(v[2 * j + 1], sl2, neg_mu);
+                            const float e1 = (j & 1) ? exp2_fma(y1) : fast_exp2(y1);
+                            pk[j] = pack_bf16x2(e0, e1);
+                            psum += bf16x2_sum(pk[j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)   // a warp of padding rows: P = 0
+                            pk[j] = 0u;
+                    }
+                    tmem_st16u(tmem_s + 16 * c, pk);
+                }
+                l_sum = l_sum * alpha + psum;
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(&bars[kBarPFull + t]);
