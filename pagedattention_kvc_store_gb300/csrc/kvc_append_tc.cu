@@ -101,15 +101,17 @@ struct Item {
     int n_keys, n_blocks;                    // positions the item's later tile sees
 };
 
-__device__ __forceinline__ bool load_item(const Args &a, int it, Item &x)
+// The fields of item `it` from its sequence's query offsets and context length (no loads).
+__device__ __forceinline__ bool make_item(const Args &a, int it, int tok0, int tok1, int ctx,
+                                          Item &x)
 {
     x.tp = it % a.pairs_per_seq;
     const int rest = it / a.pairs_per_seq;
     x.kvh = rest % a.kv_heads;
     x.s = rest / a.kv_heads;
-    x.tok0 = a.q_indptr[x.s];
-    x.q_len = a.q_indptr[x.s + 1] - x.tok0;
-    x.ctx = a.context_lens[x.s];
+    x.tok0 = tok0;
+    x.q_len = tok1 - tok0;
+    x.ctx = ctx;
     if (x.ctx > a.bt_stride * a.page_size) {
         if (threadIdx.x == 0)
             atomicOr(&g_append_tc_errors, kErrContextRange);
@@ -128,25 +130,59 @@ __device__ __forceinline__ bool load_item(const Args &a, int it, Item &x)
     return true;
 }
 
+__device__ __forceinline__ int seq_of(const Args &a, int it)
+{
+    return it / a.pairs_per_seq / a.kv_heads;
+}
+
 // Walks this CTA's items: it = blockIdx.x, blockIdx.x + gridDim.x, ..., skipping empty ones.
+// A global load under a full memory pipe takes microseconds, so the metadata of the next
+// item index is requested one item ahead (its registers are read only at the next step).
 struct Walker {
     int it;
     bool done;
     Item x;
+    int pit;                  // index whose metadata is in flight in p_*
+    int p_tok0, p_tok1, p_ctx;
+    __device__ __forceinline__ void prefetch(const Args &a, int idx)
+    {
+        pit = idx;
+        if (idx < a.num_items) {
+            const int s = seq_of(a, idx);
+            p_tok0 = a.q_indptr[s];
+            p_tok1 = a.q_indptr[s + 1];
+            p_ctx = a.context_lens[s];
+        }
+    }
     __device__ __forceinline__ void next(const Args &a)
     {
-        do {
+        for (;;) {
             it += gridDim.x;
             if (it >= a.num_items) {
                 done = true;
                 return;
             }
-        } while (!load_item(a, it, x));
+            int tok0, tok1, ctx;
+            if (it == pit) {
+                tok0 = p_tok0;
+                tok1 = p_tok1;
+                ctx = p_ctx;
+            } else {
+                const int s = seq_of(a, it);
+                tok0 = a.q_indptr[s];
+                tok1 = a.q_indptr[s + 1];
+                ctx = a.context_lens[s];
+            }
+            if (make_item(a, it, tok0, tok1, ctx, x))
+                break;
+        }
+        prefetch(a, it + gridDim.x);
     }
     __device__ __forceinline__ void start(const Args &a)
     {
         it = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
         done = false;
+        pit = -1;
         next(a);
     }
 };
@@ -201,13 +237,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t policy = l2_policy_evict_first();
         Walker w;
         w.start(a);
+        // block-table entries 0 .. 31 of the current item's sequence, one per lane, requested
+        // one item ahead like the item metadata
+        auto bt_head = [&](int idx) {
+            return (idx < a.num_items && lane < a.bt_stride)
+                       ? a.block_table[static_cast<size_t>(seq_of(a, idx)) * a.bt_stride + lane]
+                       : 0;
+        };
+        int head_it = w.done ? -1 : w.it;
+        int head_page = w.done ? 0 : bt_head(w.it);
         int n = 0;   // ring slots filled so far
         while (ok && !w.done) {
             const Item &x = w.x;
             const int32_t *bt_row = a.block_table + static_cast<size_t>(x.s) * a.bt_stride;
             const int n_pages = (x.n_keys + P - 1) / P;
-            int cached_base = -32;
-            int cached_page = 0;
+            int cached_base = 0;
+            int cached_page = (head_it == w.it) ? head_page : bt_head(w.it);
+            head_it = w.it + static_cast<int>(gridDim.x);   // the next index, if not skipped
+            head_page = bt_head(head_it);
             for (int b = 0; b < x.n_blocks && ok; ++b) {
                 const int key0 = b * kBN;
                 const int np = (min(kBN, x.n_keys - key0) + P - 1) / P;
@@ -222,22 +269,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0)
                         mbar_arrive_expect_tx(&bars[kBarKvFull + st],
                                               static_cast<uint32_t>(np * P * D * 2));
+                    __syncwarp();
                     uint8_t *dst = sStages + st * Geom::kStageBytes;
                     const CUtensorMap *map = kind == 0 ? &tmap_k : &tmap_v;
-                    for (int i = 0; i < np; ++i) {
-                        const int lp = key0 / P + i;
-                        if (lp >= cached_base + 32 || lp < cached_base) {
-                            cached_base = lp;
-                            cached_page = (lp + lane < n_pages) ? bt_row[lp + lane] : 0;
-                        }
-                        const int page = __shfl_sync(0xffffffffu, cached_page, lp - cached_base);
-                        if (lane == 0) {
-#pragma unroll
-                            for (int h = 0; h < kHalves; ++h)
-                                tma_load_3d(dst + h * kBN * 128 + i * P * 128, map, h * 64, x.kvh,
-                                            page * P, &bars[kBarKvFull + st], policy);
-                        }
+                    const int lp0 = key0 / P;   // first page of the block
+                    if (lp0 < cached_base || lp0 + np > cached_base + 32) {
+                        cached_base = lp0;
+                        cached_page = (lp0 + lane < n_pages) ? bt_row[lp0 + lane] : 0;
                     }
+                    // Lane i * kHalves + h issues the box of page i, column half h: boxes issued
+                    // by one thread one after another run at a fraction of the TMA rate that
+                    // lanes issuing together reach for these small boxes.
+                    const int i = lane / kHalves;
+                    const int h = lane % kHalves;
+                    const int page =
+                        __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
+                    if (i < np)
+                        tma_load_3d(dst + h * kBN * 128 + i * P * 128, map, h * 64, x.kvh,
+                                    page * P, &bars[kBarKvFull + st], policy);
                 }
             }
             if (!ok)
@@ -265,15 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            if (lane == 0) {
-                // the tiles' 128 / G tokens x G heads of this kv head, token-major
+            // the tiles' 128 / G tokens x G heads of this kv head, token-major; lane
+            // t * kHalves + h loads column half h of tile t
+            if (lane == 0)
                 mbar_arrive_expect_tx(&bars[kBarQFull],
                                       (x.has_b ? 2 : 1) * static_cast<uint32_t>(Geom::kQBytes));
-                for (int t = 0; t < (x.has_b ? 2 : 1); ++t)
-#pragma unroll
-                    for (int h = 0; h < kHalves; ++h)
-                        tma_load_4d(q_tile(t) + h * kM * 128, &tmap_q, h * 64, 0, x.kvh,
-                                    x.tok0 + (x.row_begin + t * kM) / G, &bars[kBarQFull]);
+            __syncwarp();
+            if (lane < (x.has_b ? 2 : 1) * kHalves) {
+                const int t = lane / kHalves;
+                const int h = lane % kHalves;
+                tma_load_4d(q_tile(t) + h * kM * 128, &tmap_q, h * 64, 0, x.kvh,
+                            x.tok0 + (x.row_begin + t * kM) / G, &bars[kBarQFull]);
             }
             ++li;
             w.next(a);
