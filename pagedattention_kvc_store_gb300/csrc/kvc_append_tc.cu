@@ -12,7 +12,9 @@
 // stage loaded for the item feeds two tiles.  The kernel is persistent: one CTA per SM walks
 // items c, c + grid, ... and its roles run ahead across item boundaries:
 //   warp 0      TMA, K and V: 128-position stages (one box per page and 64-column half,
-//               128-byte swizzle), K(b) and V(b) in separate slots of one ring, so a K slot is
+//               128-byte swizzle, the boxes of a stage issued by parallel lanes), K(b) and V(b)
+//               in separate slots of one ring filled in the order K(0), K(1), V(0), K(2), V(1),
+//               ..., so V(b) lands next to K(b + 1), about when PV(b) needs it, and a K slot is
 //               refilled as soon as both tiles' S = Q K^T products have read it;
 //   warp 1      allocates TMEM (512 columns) and issues, from one thread and in a fixed order,
 //               S_w = Q_w K(b)^T (M 128, N 128, K head_dim) and O_w += P_w V(b) (M 128,
@@ -23,8 +25,8 @@
 //               item it zeroes the V rows between the last visible position and the next
 //               multiple of 16, so NaN or Inf left in unused slots never meets a zero
 //               probability inside the tensor core;
-//   warp 2      TMA, the item's query tiles (one buffer, refilled once the item's last S
-//               products are done);
+//   warp 2      TMA, the item's query tiles (one buffer per tile, refilled once that tile's
+//               last S product of the item is done);
 //   warps 3-6   softmax of tile 0, warps 7-10 softmax of tile 1: thread r owns row r (TMEM
 //               lane r; warp w reaches lanes 32 (w % 4) ..): reads its S row, applies the
 //               scale and the causal limit, keeps a running max / sum, writes P (bf16 pairs)
@@ -84,9 +86,9 @@ struct Args {
 enum BarIndex : int {
     kBarKvFull = 0,                         // [ring slot]
     kBarKvEmpty = kBarKvFull + kMaxStages,  // [ring slot], one MMA commit
-    kBarQFull = kBarKvEmpty + kMaxStages,
-    kBarQEmpty = kBarQFull + 1,             // one MMA commit after the item's last S products
-    kBarSFull = kBarQEmpty + 1,             // [tile]
+    kBarQFull = kBarKvEmpty + kMaxStages,   // [tile]
+    kBarQEmpty = kBarQFull + 2,             // [tile], one MMA commit after its last S product
+    kBarSFull = kBarQEmpty + 2,             // [tile]
     kBarPFull = kBarSFull + 2,              // [tile], 128 arrivals
     kBarPvDone = kBarPFull + 2,             // [tile], once per item
     kBarDrain = kBarPvDone + 2,
@@ -255,10 +257,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int cached_page = (head_it == w.it) ? head_page : bt_head(w.it);
             head_it = w.it + static_cast<int>(gridDim.x);   // the next index, if not skipped
             head_page = bt_head(head_it);
-            for (int b = 0; b < x.n_blocks && ok; ++b) {
+            const int nb = x.n_blocks;
+            for (int j = 0; j < 2 * nb; ++j, ++n) {
+                // Fill order K(0), K(1), V(0), K(2), V(1), ..., V(nb - 1): K runs one block
+                // ahead, so V(b) lands about when PV(b) needs it, next to K(b + 1).
+                const bool is_k = j == 0 || (j < 2 * nb - 1 && (j & 1));
+                const int b = is_k ? (j + 1) / 2 : (j == 2 * nb - 1 ? nb - 1 : j / 2 - 1);
                 const int key0 = b * kBN;
                 const int np = (min(kBN, x.n_keys - key0) + P - 1) / P;
-                for (int kind = 0; kind < 2; ++kind, ++n) {   // K(b), then V(b)
+                {
                     const int st = n % kStages;
                     if (n >= kStages &&
                         !__all_sync(0xffffffffu,
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               static_cast<uint32_t>(np * P * D * 2));
                     __syncwarp();
                     uint8_t *dst = sStages + st * Geom::kStageBytes;
-                    const CUtensorMap *map = kind == 0 ? &tmap_k : &tmap_v;
+                    const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
                     const int lp0 = key0 / P;   // first page of the block
                     if (lp0 < cached_base || lp0 + np > cached_base + 32) {
                         cached_base = lp0;
@@ -306,34 +313,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tmap_q);
         Walker w;
         w.start(a);
-        int li = 0;   // items whose query tiles were requested
+        int qi[2] = {0, 0};   // items whose query tile t was requested
         while (ok && !w.done) {
             const Item &x = w.x;
-            if (li > 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(&bars[kBarQEmpty], (li - 1) & 1))) {
-                ok = false;
+            // Tile t of the next item loads as soon as tile t of this one has had its last S
+            // product, so tile 0 can start before tile 1 is free.  Lane h loads column half h
+            // of the tile's 128 / G tokens x G heads of this kv head, token-major.
+            for (int t = 0; t < (x.has_b ? 2 : 1); ++t) {
+                if (qi[t] > 0 &&
+                    !__all_sync(0xffffffffu,
+                                mbar_wait(&bars[kBarQEmpty + t], (qi[t] - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bars[kBarQFull + t],
+                                          static_cast<uint32_t>(Geom::kQBytes));
+                __syncwarp();
+                if (lane < kHalves)
+                    tma_load_4d(q_tile(t) + lane * kM * 128, &tmap_q, lane * 64, 0, x.kvh,
+                                x.tok0 + (x.row_begin + t * kM) / G, &bars[kBarQFull + t]);
+                ++qi[t];
+            }
+            if (!ok)
                 break;
-            }
-            // the tiles' 128 / G tokens x G heads of this kv head, token-major; lane
-            // t * kHalves + h loads column half h of tile t
-            if (lane == 0)
-                mbar_arrive_expect_tx(&bars[kBarQFull],
-                                      (x.has_b ? 2 : 1) * static_cast<uint32_t>(Geom::kQBytes));
-            __syncwarp();
-            if (lane < (x.has_b ? 2 : 1) * kHalves) {
-                const int t = lane / kHalves;
-                const int h = lane % kHalves;
-                tma_load_4d(q_tile(t) + h * kM * 128, &tmap_q, h * 64, 0, x.kvh,
-                            x.tok0 + (x.row_begin + t * kM) / G, &bars[kBarQFull]);
-            }
-            ++li;
             w.next(a);
         }
         if (!ok && lane == 0) {
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
-            // the last request may still be in flight
-            if (!mbar_wait(&bars[kBarQFull], (li - 1) & 1))
-                atomicOr(&g_append_tc_errors, kErrDrainWait);
+            // the last requests may still be in flight
+            for (int t = 0; t < 2; ++t)
+                if (qi[t] > 0 && !mbar_wait(&bars[kBarQFull + t], (qi[t] - 1) & 1))
+                    atomicOr(&g_append_tc_errors, kErrDrainWait);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issue ----------------------------------------
@@ -367,34 +378,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         Walker w;
         w.start(a);
-        int n = 0;    // ring slots consumed so far
-        int li = 0;   // items
-        int tb0 = 0, tb1 = 0;   // blocks of tile 0 / tile 1
+        int n0 = 0;             // ring index of the item's first slot
+        int qi[2] = {0, 0};     // items of tile 0 / tile 1
+        int tb[2] = {0, 0};     // blocks of tile 0 / tile 1
         while (ok && !w.done) {
             const Item &x = w.x;
             const int nt = x.has_b ? 2 : 1;
             const int nb = x.n_blocks;
             const int last_valid = x.n_keys - (nb - 1) * kBN;   // positions in the last block
             const int last_cols = (last_valid + 15) & ~15;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarQFull], li & 1)) || !wait_slot(n)) {
+            // ring indices in the producer's fill order K(0), K(1), V(0), K(2), V(1), ...
+            auto k_slot = [&](int b) { return n0 + (b == 0 ? 0 : 2 * b - 1); };
+            auto v_slot = [&](int b) { return n0 + (b == nb - 1 ? 2 * nb - 1 : 2 * b + 2); };
+            if (!wait_slot(k_slot(0))) {
                 ok = false;
                 break;
             }
-            tc_fence_after_sync();
-            if (lane == 0) {
-                for (int t = 0; t < nt; ++t) {
-                    issue_qk(t, stage_of(n), nb == 1 ? last_cols : kBN);
-                    umma_commit(&bars[kBarSFull + t]);
+            for (int t = 0; t < nt && ok; ++t) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarQFull + t], qi[t] & 1))) {
+                    ok = false;
+                    break;
                 }
-                if (nb == 1)
-                    umma_commit(&bars[kBarQEmpty]);
-                umma_commit(&bars[kBarKvEmpty + n % kStages]);
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    issue_qk(t, stage_of(k_slot(0)), nb == 1 ? last_cols : kBN);
+                    umma_commit(&bars[kBarSFull + t]);
+                    if (nb == 1)
+                        umma_commit(&bars[kBarQEmpty + t]);
+                }
+                __syncwarp();
             }
+            if (!ok)
+                break;
+            if (lane == 0)
+                umma_commit(&bars[kBarKvEmpty + k_slot(0) % kStages]);
             __syncwarp();
-            ++n;
             for (int b = 0; b < nb && ok; ++b) {
                 const bool last = b + 1 == nb;
-                const int vn = n++;   // V(b)
+                const int vn = v_slot(b);
                 if (!wait_slot(vn)) {
                     ok = false;
                     break;
@@ -414,13 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                const int kn = n;   // K(b + 1)
+                const int kn = last ? 0 : k_slot(b + 1);
                 for (int t = 0; t < nt; ++t) {
-                    const int tb = t == 0 ? tb0++ : tb1++;
-                    if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPFull + t], tb & 1))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarPFull + t], tb[t] & 1))) {
                         ok = false;
                         break;
                     }
+                    ++tb[t];
                     tc_fence_after_sync();
                     if (lane == 0) {
                         issue_pv(t, stage_of(vn), last ? last_cols / 16 : kBN / 16, b == 0);
@@ -439,6 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         issue_qk(t, stage_of(kn), b + 2 == nb ? last_cols : kBN);
                         umma_commit(&bars[kBarSFull + t]);
+                        if (b + 2 == nb)
+                            umma_commit(&bars[kBarQEmpty + t]);
                     }
                     __syncwarp();
                 }
@@ -446,19 +469,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 if (lane == 0) {
                     umma_commit(&bars[kBarKvEmpty + vn % kStages]);
-                    if (!last) {
+                    if (!last)
                         umma_commit(&bars[kBarKvEmpty + kn % kStages]);
-                        if (b + 2 == nb)
-                            umma_commit(&bars[kBarQEmpty]);
-                    }
                 }
                 __syncwarp();
-                if (!last)
-                    ++n;
             }
             if (!ok)
                 break;
-            ++li;
+            for (int t = 0; t < nt; ++t)
+                ++qi[t];
+            n0 += 2 * nb;
             w.next(a);
         }
         if (!ok && lane == 0)
