@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
     p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer (MB)")
     p.add_argument("--append-steps", type=int, default=60)
+    p.add_argument("--append-docs", type=int, default=1000,
+                   help="documents in the rewind-append leg (smaller for profiler captures)")
     p.add_argument("--no-append", action="store_true")
     p.add_argument("--no-legs", action="store_true",
                    help="skip the shared-prefix and long-context decode legs")
@@ -485,7 +487,8 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
 
     result = {}
     for P in (16, 64):
-        case = config_case(4, page_size=P, seed=None if rank == 0 else SEED_BASE + 4 + 1000 * rank)
+        case = config_case(4, page_size=P, num_seqs=args.append_docs,
+                           seed=None if rank == 0 else SEED_BASE + 4 + 1000 * rank)
         d = to_device(case, dev)
         slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
         out = torch.empty(case.num_tokens, case.q_heads, case.head_dim, dtype=torch.bfloat16,
@@ -537,12 +540,12 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "store_gbs": round(store_bytes(case) / (statistics.mean(st_ms) / 1e3) / 1e9, 1),
             "gpu_launches": args.append_steps * 3,
             "traffic": (traffic_from_profile("append_rewind_p16", "kvc_append_tc.cu")
-                        if P == 16 else None),
+                        if P == 16 and args.append_docs == 1000 else None),
         }
         del d, out, slots, g1, g2
         torch.cuda.empty_cache()
-    result["workload"] = ("rewind-append: 1,000 docs x 50 new tokens over 300 cached, "
-                          "32 q / 8 kv heads, head_dim 128")
+    result["workload"] = (f"rewind-append: {args.append_docs:,} docs x 50 new tokens over 300 "
+                          "cached, 32 q / 8 kv heads, head_dim 128")
     result["peaks"] = {"hbm_gbs": peaks["hbm"], "bf16_tflops": peaks["bf16_sustained"],
                        "source": f"of {peaks['source']} (sustained bf16)"}
     return result
