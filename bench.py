@@ -179,6 +179,19 @@ def barrier(world):
         dist.barrier()
 
 
+def rank_seed(config: int, rank: int):
+    """Workload seed of a rank: rank 0 runs the named configuration's own inputs, every other
+    rank a different seeded batch of the same shape (replicas process distinct work)."""
+    from workloads.configs import SEED_BASE
+    return None if rank == 0 else SEED_BASE + config + 1000 * rank
+
+
+def whole_job_value(world: int, bytes_per_step: int, steps: int, max_total_ms: float) -> float:
+    """GB/s over all ranks: every rank moved bytes_per_step per step; time is the slowest
+    rank's total over the timed steps."""
+    return world * bytes_per_step * steps / (max_total_ms / 1e3) / 1e9
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     if world == 1:
         return x
@@ -237,14 +250,13 @@ def time_graph(torch, fn, stream, flush, steps):
 def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     """Shared-prefix decode (grouped vs plain) and long-context split-K decode."""
     from workloads import config_case
-    from workloads.configs import SEED_BASE
     from workloads.device import i32_tensor, to_device
 
     legs = {}
     per_pos = lambda c: 2 * c.kv_heads * c.head_dim * 2
     qo = lambda c: 2 * c.num_seqs * c.q_heads * c.head_dim * 2
     # shared prefix: 32 groups x 8 sequences over 2,048 shared positions
-    case = config_case(3, seed=None if rank == 0 else SEED_BASE + 3 + 1000 * rank)
+    case = config_case(3, seed=rank_seed(3, rank))
     d = to_device(case, dev)
     slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
     kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
@@ -285,7 +297,7 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     del d, out, work_g, work_p, slots
     torch.cuda.empty_cache()
     # long context: 8 sequences of 32k..128k positions
-    case = config_case(5, seed=None if rank == 0 else SEED_BASE + 5 + 1000 * rank)
+    case = config_case(5, seed=rank_seed(5, rank))
     d = to_device(case, dev)
     slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
     kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
@@ -316,7 +328,6 @@ def run_kvc(args):
 
     import pagedattention_kvc_store_gb300 as kvc
     from workloads import config_case
-    from workloads.configs import SEED_BASE
     from workloads.device import to_device
 
     rank, world, local = dist_setup(args)
@@ -325,7 +336,7 @@ def run_kvc(args):
     peaks = load_peaks()
 
     # each rank decodes its own batch of 64 sequences (weak scaling, no collective)
-    case = config_case(2, seed=None if rank == 0 else SEED_BASE + 2 + 1000 * rank)
+    case = config_case(2, seed=rank_seed(2, rank))
     d = to_device(case, dev)
     S, Hq, D = case.num_seqs, case.q_heads, case.head_dim
     slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
@@ -384,7 +395,7 @@ def run_kvc(args):
         total_ms = max_over_ranks(sum(step_ms), world, dev)
 
         step_b = decode_bytes(case) + store_bytes(case)
-        value = world * step_b * K / (total_ms / 1e3) / 1e9
+        value = whole_job_value(world, step_b, K, total_ms)
         dec_b = decode_bytes(case)
         achieved = dec_b / (statistics.mean(dec_ms) / 1e3) / 1e9
         launches_per_step = 2 + 1 + (1 if splits > 1 else 0)
@@ -482,13 +493,12 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
 def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
     """Append-prefill leg: KV-rewind workload, page sizes 16 and 64."""
     from workloads import config_case
-    from workloads.configs import SEED_BASE
     from workloads.device import to_device
 
     result = {}
     for P in (16, 64):
         case = config_case(4, page_size=P, num_seqs=args.append_docs,
-                           seed=None if rank == 0 else SEED_BASE + 4 + 1000 * rank)
+                           seed=rank_seed(4, rank))
         d = to_device(case, dev)
         slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
         out = torch.empty(case.num_tokens, case.q_heads, case.head_dim, dtype=torch.bfloat16,
@@ -595,8 +605,10 @@ def cpu_baseline(case, seconds):
 
 def run_reference(args):
     rank, world, _ = dist_setup(args)
-    if rank != 0:
+    if rank != 0:   # rank 0 alone times the oracle; the others wait for it and exit
         barrier(world)
+        import torch.distributed as dist
+        dist.destroy_process_group()
         return
     from oracle import oracle
     from workloads import config_case
@@ -629,6 +641,9 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 def main():
