@@ -54,7 +54,8 @@ typedef enum kvc_status {
     KVC_ERR_UNSUPPORTED = 2,  /* shape outside the supported set above                   */
     KVC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the plan requires      */
     KVC_ERR_CUDA = 4,         /* a CUDA call failed (launch, tensor-map encode, ...)      */
-    KVC_ERR_DEVICE = 5        /* a kernel gave up a bounded wait (see kvc_device_errors)  */
+    KVC_ERR_DEVICE = 5,       /* a kernel gave up a bounded wait (see kvc_device_errors)  */
+    KVC_ERR_OUT_OF_RANGE = 6  /* kvc_validate found a bad table entry, slot or length       */
 } kvc_status;
 
 typedef enum kvc_dtype {
@@ -256,6 +257,35 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
  * wait ever ran out.
  */
 kvc_status kvc_device_errors(uint32_t *flags_out);
+
+/*
+ * kvc_validate -- opt-in deep check of the device-side tables of a step, for debugging
+ * (no counterpart on the pages; every other call trusts these contents).  Checks, in order:
+ *   1. 0 <= context_lens[s] <= bt_stride * page_size for every sequence s;
+ *   2. every page id a sequence reaches, block_table[s][i] for i < ceil(context_lens[s] /
+ *      page_size), lies in [0, num_pages)  (TileInfer.jl "KV cache", "Pages and block tables":
+ *      a row lists the pages that hold the sequence's positions);
+ *   3. every slot_mapping[t] is negative (padding, skipped by kvc_store) or below
+ *      num_pages * page_size;
+ *   4. no two tokens have the same non-negative slot (two writers of one slot in one store:
+ *      "KV Cache Management and PagedAttention", "Split shared blocks when a write is needed",
+ *      names that as the bug copy-on-write prevents).
+ * block_table / context_lens may be NULL (num_seqs 0) to check slots only, and slot_mapping
+ * NULL (num_tokens 0) to check tables only.  Unlike every other call it synchronises `stream`
+ * and reads the verdict on the host.
+ *   workspace      device bytes, at least *bytes_out of kvc_validate_workspace_size(pool)
+ *                  (two bitmaps over the pool's slots and a verdict record); overwritten
+ *   bad_index_out  host; on KVC_ERR_OUT_OF_RANGE the smallest offending index of the first
+ *                  failing check (a sequence for checks 1-2, a token for 3-4; for 4 the
+ *                  smallest token whose slot another token also writes), else -1
+ * Returns KVC_OK when every check passes, KVC_ERR_OUT_OF_RANGE (kvc_last_error names the
+ * check) when one fails, or an argument / CUDA error.
+ */
+kvc_status kvc_validate_workspace_size(kvc_pool_desc pool, size_t *bytes_out);
+kvc_status kvc_validate(kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                        const int32_t *context_lens, int32_t num_seqs,
+                        const int32_t *slot_mapping, int32_t num_tokens, void *workspace,
+                        size_t workspace_bytes, int64_t *bad_index_out, void *stream);
 
 #ifdef __cplusplus
 }

@@ -341,6 +341,7 @@ const char *kvc_status_string(kvc_status status)
     case KVC_ERR_WORKSPACE: return "KVC_ERR_WORKSPACE";
     case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
     case KVC_ERR_DEVICE: return "KVC_ERR_DEVICE";
+    case KVC_ERR_OUT_OF_RANGE: return "KVC_ERR_OUT_OF_RANGE";
     }
     return "KVC_ERR_UNKNOWN";
 }
@@ -682,6 +683,65 @@ kvc_status kvc_device_errors(uint32_t *flags_out)
         return cuda_fail(err, "reading the device error word");
     *flags_out = a | c | d | e;
     return *flags_out ? fail(KVC_ERR_DEVICE, "device error flags 0x%x", *flags_out) : ok();
+}
+
+kvc_status kvc_validate_workspace_size(kvc_pool_desc pool, size_t *bytes_out)
+{
+    if (bytes_out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "bytes_out is null");
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    *bytes_out = kvc::validate_workspace_bytes(static_cast<long long>(pool.num_pages) *
+                                               pool.page_size);
+    return ok();
+}
+
+kvc_status kvc_validate(kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                        const int32_t *context_lens, int32_t num_seqs,
+                        const int32_t *slot_mapping, int32_t num_tokens, void *workspace,
+                        size_t workspace_bytes, int64_t *bad_index_out, void *stream)
+{
+    if (bad_index_out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "bad_index_out is null");
+    *bad_index_out = -1;
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    if (num_seqs < 0 || num_tokens < 0)
+        return fail(KVC_ERR_INVALID_ARG, "negative num_seqs %d or num_tokens %d", num_seqs,
+                    num_tokens);
+    if (num_seqs > 0 && (block_table == nullptr || context_lens == nullptr || bt_stride <= 0))
+        return fail(KVC_ERR_INVALID_ARG, "tables missing or bt_stride %d", bt_stride);
+    if (num_tokens > 0 && slot_mapping == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "slot_mapping is null");
+    const size_t need =
+        kvc::validate_workspace_bytes(static_cast<long long>(pool.num_pages) * pool.page_size);
+    if (workspace == nullptr || workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+        return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes (4-byte aligned) needed", need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = kvc::launch_validate(block_table, bt_stride, context_lens, num_seqs,
+                                           slot_mapping, num_tokens, pool.page_size,
+                                           pool.num_pages, workspace, s);
+    kvc::ValidateRecord rec;
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(&rec, workspace, sizeof(rec), cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess)
+        err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "validate");
+    static const char *const kWhat[kvc::kValidateChecks] = {
+        "context_lens[s] outside [0, bt_stride * page_size]",
+        "page id outside [0, num_pages)",
+        "slot past the pool",
+        "slot written by two tokens"};
+    for (int c = 0; c < kvc::kValidateChecks; ++c)
+        if (rec.first_bad[c] != 0x7FFFFFFF) {
+            *bad_index_out = rec.first_bad[c];
+            return fail(KVC_ERR_OUT_OF_RANGE, "%s (index %d)", kWhat[c], rec.first_bad[c]);
+        }
+    return ok();
 }
 
 }  // extern "C"

@@ -56,6 +56,17 @@ struct AppendLaunch {
     float scale;
 };
 
+// kvc_validate: the smallest offending index of each check (INT32_MAX when it passed), then two
+// bitmaps over the pool's slots.
+constexpr int kValidateChecks = 4;
+struct ValidateRecord {
+    int first_bad[kValidateChecks];
+};
+size_t validate_workspace_bytes(long long num_slots);
+cudaError_t launch_validate(const int32_t *block_table, int bt_stride, const int32_t *context_lens,
+                            int num_seqs, const int32_t *slots, int num_tokens, int page_size,
+                            int num_pages, void *workspace, cudaStream_t stream);
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int bt_stride,
                                 const int32_t *context_lens, const int32_t *q_indptr,

@@ -20,12 +20,15 @@ KVC_BF16 = 0
 KVC_F32 = 1
 
 STATUS = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_UNSUPPORTED",
-          3: "KVC_ERR_WORKSPACE", 4: "KVC_ERR_CUDA", 5: "KVC_ERR_DEVICE"}
+          3: "KVC_ERR_WORKSPACE", 4: "KVC_ERR_CUDA", 5: "KVC_ERR_DEVICE",
+          6: "KVC_ERR_OUT_OF_RANGE"}
+KVC_ERR_OUT_OF_RANGE = 6
 
 # Every entry point declared in include/kvc.h.
 EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store",
            "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
-           "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan")
+           "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
+           "kvc_validate_workspace_size", "kvc_validate")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -93,6 +96,11 @@ def lib() -> ctypes.CDLL:
                                                         ctypes.POINTER(sz)]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.kvc_validate_workspace_size.restype = ctypes.c_int
+            L.kvc_validate_workspace_size.argtypes = [PoolDesc, ctypes.POINTER(sz)]
+            L.kvc_validate.restype = ctypes.c_int
+            L.kvc_validate.argtypes = [PoolDesc, p, i32, p, i32, p, i32, p, sz,
+                                       ctypes.POINTER(ctypes.c_int64), p]
             _lib = L
     return _lib
 
@@ -292,3 +300,41 @@ def kvc_device_errors() -> int:
     if status not in (0, 5):
         _check("kvc_device_errors", status)
     return int(flags.value)
+
+
+def kvc_validate_workspace_size(pool: PoolDesc) -> int:
+    """Device bytes kvc_validate needs for this pool."""
+    n = ctypes.c_size_t()
+    _check("kvc_validate_workspace_size", lib().kvc_validate_workspace_size(pool, ctypes.byref(n)))
+    return n.value
+
+
+def kvc_validate(pool: PoolDesc, block_table: Optional[torch.Tensor] = None,
+                 context_lens: Optional[torch.Tensor] = None,
+                 slot_mapping: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None) -> Tuple[int, str]:
+    """Deep check of a step's tables (synchronises).  Returns (-1, "") when every check passes,
+    else (smallest offending index of the first failing check, reason)."""
+    num_seqs = 0
+    bt_stride = 1
+    if block_table is not None:
+        _cuda("block_table", block_table, torch.int32)
+        _cuda("context_lens", context_lens, torch.int32)
+        num_seqs, bt_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    num_tokens = 0
+    if slot_mapping is not None:
+        _cuda("slot_mapping", slot_mapping, torch.int32)
+        num_tokens = int(slot_mapping.numel())
+    if workspace is None:
+        workspace = torch.empty(kvc_validate_workspace_size(pool), dtype=torch.uint8,
+                                device="cuda")
+    _cuda("workspace", workspace)
+    bad = ctypes.c_int64(-1)
+    status = lib().kvc_validate(
+        pool, _ptr(block_table), bt_stride, _ptr(context_lens), num_seqs, _ptr(slot_mapping),
+        num_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(bad), _stream(stream))
+    if status == KVC_ERR_OUT_OF_RANGE:
+        return int(bad.value), lib().kvc_last_error().decode(errors="replace")
+    _check("kvc_validate", status)
+    return -1, ""
