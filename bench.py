@@ -320,6 +320,25 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     }
     del d, out, work, slots
     torch.cuda.empty_cache()
+    # copy-on-write page copies: 4,096 pages of P 16 x 8 kv heads x D 128 (32 KB per pool)
+    # from one half of a 16,384-page pool to shuffled pages of the other half
+    n_pages, n_copy = 16384, 4096
+    rng = np.random.default_rng(rank_seed(6, rank) or 6)
+    kp = torch.empty(n_pages, 16, 8, 128, dtype=torch.bfloat16, device=dev).normal_()
+    vp = torch.empty_like(kp).normal_()
+    perm = rng.permutation(n_pages).astype(np.int32)
+    src, dst = i32_tensor(perm[:n_copy], dev), i32_tensor(perm[n_copy:2 * n_copy], dev)
+    with torch.cuda.stream(stream):
+        t = time_graph(torch, lambda: kvc.kvc_copy_pages(kp, vp, src, dst), stream, flush,
+                       args.leg_steps)
+    b = 2 * 2 * n_copy * 16 * 8 * 128 * 2          # K and V, read and written
+    legs["page_copy"] = {
+        "workload": "copy-on-write of 4,096 pages (P 16, 8 kv heads, D 128) in a 16,384-page pool",
+        "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
+        "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "gpu_launches_per_step": 1,
+    }
+    del kp, vp
+    torch.cuda.empty_cache()
     return legs
 
 

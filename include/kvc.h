@@ -259,6 +259,23 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
 kvc_status kvc_device_errors(uint32_t *flags_out);
 
 /*
+ * kvc_copy_pages -- copy-on-write page copy ("KV Cache Management and PagedAttention", "Split
+ * shared blocks when a write is needed": before a sequence writes into a page that other
+ * sequences still reference, the page is copied to a new one and the writer's block-table
+ * entry is pointed at the copy; Quail "KV", "Prefix sharing").  For every i < num_copies,
+ * page dst_pages[i] of both pools receives the bytes of page src_pages[i] (all page_size
+ * positions, all kv heads; a raw 16-bit copy, NaN payloads kept).  Deciding what to copy and
+ * repointing the tables is host work (the caller's allocator and reference counts).
+ *   src_pages, dst_pages  int32 [num_copies], device; ids in [0, num_pages)
+ * Every copy reads the pools as they were before the call: a page that is both a source and a
+ * destination in one call, or two copies to one destination, is a caller error (the result is
+ * undefined).  Page ids outside the pool are skipped and set kvc_device_errors' range bit.
+ */
+kvc_status kvc_copy_pages(void *k_pool, void *v_pool, kvc_pool_desc pool,
+                          const int32_t *src_pages, const int32_t *dst_pages,
+                          int32_t num_copies, void *stream);
+
+/*
  * kvc_validate -- opt-in deep check of the device-side tables of a step, for debugging
  * (no counterpart on the pages; every other call trusts these contents).  Checks, in order:
  *   1. 0 <= context_lens[s] <= bt_stride * page_size for every sequence s;

@@ -106,6 +106,28 @@ void kvo_store(uint16_t *k_pool, uint16_t *v_pool, int64_t kv_heads, int64_t hea
     }
 }
 
+/*
+ * Copy-on-write page copy ([PA] "Split shared blocks when a write is needed": the shared
+ * block is copied to a new block, keeping the KV already in it, before the writer's table
+ * entry is pointed at the copy).  Every copy reads the pools as they were before the call:
+ * the sources are copied aside first, then written to their destinations.
+ */
+void kvo_copy_pages(uint16_t *k_pool, uint16_t *v_pool, int64_t page_elems,
+                    const int64_t *src_pages, const int64_t *dst_pages, int64_t num_copies,
+                    uint16_t *scratch_k, uint16_t *scratch_v)
+{
+    for (int64_t i = 0; i < num_copies; ++i)
+        for (int64_t e = 0; e < page_elems; ++e) {
+            scratch_k[i * page_elems + e] = k_pool[src_pages[i] * page_elems + e];
+            scratch_v[i * page_elems + e] = v_pool[src_pages[i] * page_elems + e];
+        }
+    for (int64_t i = 0; i < num_copies; ++i)
+        for (int64_t e = 0; e < page_elems; ++e) {
+            k_pool[dst_pages[i] * page_elems + e] = scratch_k[i * page_elems + e];
+            v_pool[dst_pages[i] * page_elems + e] = scratch_v[i * page_elems + e];
+        }
+}
+
 /* ---------------------------------------------------------------------------------- */
 /* Attention                                                                          */
 /* ---------------------------------------------------------------------------------- */

@@ -48,6 +48,8 @@ def _load():
             lib.kvo_slot_mapping.argtypes = [p, i64, p, p, i64, i64, p]
             lib.kvo_store.restype = None
             lib.kvo_store.argtypes = [p, p, i64, i64, p, p, p, i64]
+            lib.kvo_copy_pages.restype = None
+            lib.kvo_copy_pages.argtypes = [p, p, i64, p, p, i64, p, p]
             lib.kvo_attention.restype = None
             lib.kvo_attention.argtypes = [p, p, p, i64, i64, i64, p, i64, p, p, i64, i64,
                                           ctypes.c_double, p, p, p, p, i64]
@@ -90,6 +92,20 @@ def store(k_pool, v_pool, k_new, v_new, slots) -> None:
     hkv, d = k_pool.shape[2], k_pool.shape[3]
     _load().kvo_store(_ptr(k_pool), _ptr(v_pool), hkv, d, _ptr(kn), _ptr(vn), _ptr(sl),
                       sl.shape[0])
+
+
+def copy_pages(k_pool, v_pool, src_pages, dst_pages) -> None:
+    """In place: page dst[i] of both pools receives page src[i] (uint16 bit patterns)."""
+    assert k_pool.dtype == np.uint16 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.uint16 and v_pool.flags.c_contiguous
+    src = _c(src_pages, np.int64)
+    dst = _c(dst_pages, np.int64)
+    assert src.shape == dst.shape
+    page_elems = int(np.prod(k_pool.shape[1:]))
+    sk = np.empty(max(src.shape[0], 1) * page_elems, dtype=np.uint16)
+    sv = np.empty_like(sk)
+    _load().kvo_copy_pages(_ptr(k_pool), _ptr(v_pool), page_elems, _ptr(src), _ptr(dst),
+                           src.shape[0], _ptr(sk), _ptr(sv))
 
 
 def attention(q, k_pool, v_pool, block_table, context_lens, q_indptr, scale=None,

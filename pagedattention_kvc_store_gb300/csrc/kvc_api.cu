@@ -395,6 +395,28 @@ kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void 
     return err == cudaSuccess ? ok() : cuda_fail(err, "store launch");
 }
 
+kvc_status kvc_copy_pages(void *k_pool, void *v_pool, kvc_pool_desc pool,
+                          const int32_t *src_pages, const int32_t *dst_pages,
+                          int32_t num_copies, void *stream)
+{
+    if (pool.num_pages <= 0 || pool.page_size <= 0 || pool.kv_heads <= 0 || pool.head_dim <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "pool descriptor has a non-positive field");
+    if (num_copies < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_copies %d", num_copies);
+    if ((static_cast<int64_t>(pool.page_size) * pool.kv_heads * pool.head_dim * 2) % 16 != 0)
+        return fail(KVC_ERR_UNSUPPORTED, "a page must be a multiple of 16 bytes");
+    if (num_copies == 0)
+        return ok();
+    if (!k_pool || !v_pool || !src_pages || !dst_pages)
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(k_pool) || !aligned16(v_pool))
+        return fail(KVC_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    cudaError_t err = kvc::launch_copy_pages(k_pool, v_pool, pool.num_pages, pool.page_size,
+                                             pool.kv_heads, pool.head_dim, src_pages, dst_pages,
+                                             num_copies, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "copy_pages launch");
+}
+
 kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
                            int32_t max_ctx, int32_t num_splits, int32_t *splits_out,
                            int32_t *chunk_out, size_t *workspace_bytes_out)

@@ -26,6 +26,7 @@ enum DeviceErrorBits : uint32_t {
     kErrContextRange = 1u << 7,    // context_lens[s] > bt_stride * page_size: clamped
     kErrAppendTcWait = 1u << 8,    // the tcgen05 append gave up a wait
     kErrSmemAlign = 1u << 9,       // dynamic shared memory not 1024-byte aligned: no work done
+    kErrPageRange = 1u << 10,      // a page copy named a page outside the pool: skipped
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)

@@ -75,6 +75,9 @@ cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int 
 cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
                          int num_slots, const void *k_new, const void *v_new,
                          const int32_t *slots, int num_tokens, cudaStream_t stream);
+cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,
+                              int kv_heads, int head_dim, const int32_t *src_pages,
+                              const int32_t *dst_pages, int num_copies, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeLaunch &a, const CUtensorMap &tmap_k,
                           const CUtensorMap &tmap_v, cudaStream_t stream);
 cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const float *part_lse,

@@ -101,6 +101,37 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
     }
 }
 
+// Copy-on-write: whole pages of both pools, src_pages[i] -> dst_pages[i].  chunks = 16-byte
+// chunks per page (page_size * kv_heads * head_dim * 2 / 16); a grid-stride loop over
+// (copy, chunk), so consecutive threads stream consecutive bytes of one page.
+__global__ void __launch_bounds__(256) copy_pages_kernel(uint4 *__restrict__ k_pool,
+                                                         uint4 *__restrict__ v_pool,
+                                                         const int32_t *__restrict__ src_pages,
+                                                         const int32_t *__restrict__ dst_pages,
+                                                         int num_copies, int chunks, int num_pages)
+{
+    const size_t total = static_cast<size_t>(num_copies) * chunks;
+    const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += step) {
+        const int n = static_cast<int>(i / chunks);
+        const int c = static_cast<int>(i - static_cast<size_t>(n) * chunks);
+        const int src = __ldg(src_pages + n);
+        const int dst = __ldg(dst_pages + n);
+        if (src < 0 || src >= num_pages || dst < 0 || dst >= num_pages) {
+            if (c == 0)
+                atomicOr(&g_store_errors, kErrPageRange);
+            continue;
+        }
+        const size_t from = static_cast<size_t>(src) * chunks + c;
+        const size_t to = static_cast<size_t>(dst) * chunks + c;
+        const uint4 kv = load_streaming(k_pool + from);
+        const uint4 vv = load_streaming(v_pool + from);
+        k_pool[to] = kv;
+        v_pool[to] = vv;
+    }
+}
+
 int sm_count()
 {
     static int count = 0;
@@ -154,6 +185,24 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
         static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
         num_tokens, chunks, num_slots);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,
+                              int kv_heads, int head_dim, const int32_t *src_pages,
+                              const int32_t *dst_pages, int num_copies, cudaStream_t stream)
+{
+    if (num_copies == 0)
+        return cudaSuccess;
+    const int chunks = page_size * kv_heads * head_dim * 2 / 16;
+    const size_t total = static_cast<size_t>(num_copies) * chunks;
+    const int threads = 256;
+    const size_t wanted = (total + threads - 1) / threads;
+    const size_t cap = static_cast<size_t>(sm_count()) * 8;
+    const int blocks = static_cast<int>(wanted < cap ? wanted : cap);
+    copy_pages_kernel<<<blocks, threads, 0, stream>>>(
+        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), src_pages, dst_pages,
+        num_copies, chunks, num_pages);
     return cudaGetLastError();
 }
 

@@ -28,7 +28,7 @@ KVC_ERR_OUT_OF_RANGE = 6
 EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store",
            "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
-           "kvc_validate_workspace_size", "kvc_validate")
+           "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
                                                         ctypes.POINTER(sz)]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.kvc_copy_pages.restype = ctypes.c_int
+            L.kvc_copy_pages.argtypes = [p, p, PoolDesc, p, p, i32, p]
             L.kvc_validate_workspace_size.restype = ctypes.c_int
             L.kvc_validate_workspace_size.argtypes = [PoolDesc, ctypes.POINTER(sz)]
             L.kvc_validate.restype = ctypes.c_int
@@ -172,6 +174,20 @@ def kvc_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
     _check("kvc_store", lib().kvc_store(
         _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool), _ptr(k_new), _ptr(v_new),
         _ptr(slot_mapping), int(slot_mapping.shape[0]), _stream(stream)))
+
+
+def kvc_copy_pages(k_pool: torch.Tensor, v_pool: torch.Tensor, src_pages: torch.Tensor,
+                   dst_pages: torch.Tensor, stream=None) -> None:
+    """Copy-on-write: page dst_pages[i] of both pools receives page src_pages[i]."""
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _cuda("src_pages", src_pages, torch.int32)
+    _cuda("dst_pages", dst_pages, torch.int32)
+    if src_pages.numel() != dst_pages.numel():
+        raise ValueError("src_pages and dst_pages differ in length")
+    _check("kvc_copy_pages", lib().kvc_copy_pages(
+        _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool), _ptr(src_pages), _ptr(dst_pages),
+        int(src_pages.numel()), _stream(stream)))
 
 
 def kvc_decode_plan(num_seqs: int, q_heads: int, pool: PoolDesc, max_ctx: int,

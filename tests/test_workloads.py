@@ -93,3 +93,50 @@ def test_shared_prefix_config_matches_the_sharing_plan():
             assert not set(c.block_table[m, 128: -(-int(c.context_lens[m]) // 16)]) & set(
                 c.block_table[leader, : -(-int(c.context_lens[leader]) // 16)])
     assert computed_tokens(c.docs, shared) == int(c.context_lens.sum()) - 2048 * 7 * 4
+
+
+def test_copy_on_write_follows_the_worked_example():
+    """PageAllocator.fork / reserve against the copy-on-write example of "KV Cache Management
+    and PagedAttention" ("Split shared blocks when a write is needed", Figure 6)."""
+    from conftest import golden_lines
+
+    rows = [ln.split(" | ") for ln in golden_lines("copy_on_write.txt")]
+    for common, prefix in ((6, ""), (8, "full-")):
+        a = PageAllocator(8, 4, permutation=np.arange(8))
+        a.reserve(0, common)                      # the common input: P0, P1
+        a.fork(1, 0)                              # response 2 shares both blocks
+        p0, p1 = a.pages[0]
+        named = {p0: "P0", p1: "P1"}
+        steps = [r for r in rows if r[0].startswith(prefix) and
+                 (prefix or not r[0].startswith("full-"))]
+        for step, writer, copies, physical, rc0, rc1 in steps:
+            made = []
+            if writer != "-":
+                seq = int(writer) - 1
+                for src, dst in a.reserve(seq, 1):
+                    named.setdefault(dst, f"P{len(named)}")
+                    made.append(f"{named[src]}->{named[dst]}")
+            assert (",".join(made) or "-") == copies, step
+            assert a.physical_pages() == int(physical), step
+            assert a.refcount[p0] == int(rc0) and a.refcount[p1] == int(rc1), step
+        # P0 is still in both tables; each response ends with its own last block
+        assert a.pages[0][0] == a.pages[1][0] == p0
+        assert a.pages[0][-1] != a.pages[1][-1]
+
+
+def test_copy_on_write_oracle_copies_whole_pages():
+    """oracle.copy_pages: destinations receive the sources' bits (NaN payloads included),
+    every other page keeps its bits, and all copies read the pools as before the call."""
+    from oracle import oracle
+
+    rng = np.random.default_rng(5)
+    k = rng.integers(0, 1 << 16, size=(10, 4, 2, 8), dtype=np.uint16)
+    v = rng.integers(0, 1 << 16, size=(10, 4, 2, 8), dtype=np.uint16)
+    k[3, 1, 0, 0] = 0x7FC1                       # a NaN with a payload
+    k0, v0 = k.copy(), v.copy()
+    src, dst = np.array([3, 7, 2]), np.array([5, 2, 9])   # page 2 is read and written
+    oracle.copy_pages(k, v, src, dst)
+    for s_, d_ in zip(src, dst):
+        assert np.array_equal(k[d_], k0[s_]) and np.array_equal(v[d_], v0[s_])
+    for p in set(range(10)) - set(dst.tolist()):
+        assert np.array_equal(k[p], k0[p]) and np.array_equal(v[p], v0[p])

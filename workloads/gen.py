@@ -9,7 +9,7 @@ from __future__ import annotations
 import concurrent.futures as futures
 import os
 from dataclasses import dataclass, field
-from typing import Callable, Dict, List, Optional, Sequence
+from typing import Callable, Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -108,15 +108,43 @@ class PageAllocator:
     def pages_for(self, positions: int) -> int:
         return -(-int(positions) // self.page_size)
 
-    def reserve(self, seq: int, n: int) -> None:
+    def reserve(self, seq: int, n: int) -> List[Tuple[int, int]]:
+        """Room for the sequence's next n positions.  Returns the page copies (src, dst) the
+        caller must make before writing: when the first new position falls inside a partly
+        filled last page that other sequences still reference, that page is copied to a new
+        one and the sequence's entry points at the copy ("KV Cache Management and
+        PagedAttention", section "Split shared blocks when a write is needed"); a full shared
+        page stays shared, and the new positions go to new pages."""
         pages = self.pages.setdefault(seq, [])
         length = self.length.get(seq, 0)
         need = self.pages_for(length + n) - len(pages)
-        if need > len(self.free):
-            raise OutOfPages(f"sequence {seq} needs {need} pages, {len(self.free)} free")
+        cow = n > 0 and length % self.page_size != 0 and self.refcount[pages[-1]] > 1
+        if need + int(cow) > len(self.free):
+            raise OutOfPages(f"sequence {seq} needs {need + int(cow)} pages, "
+                             f"{len(self.free)} free")
+        copies: List[Tuple[int, int]] = []
+        if cow:
+            old = pages[-1]
+            pages[-1] = self._pop()
+            self._drop(old)
+            copies.append((old, pages[-1]))
         for _ in range(need):
             pages.append(self._pop())
         self.length[seq] = length + n
+        return copies
+
+    def fork(self, seq: int, donor: int) -> None:
+        """Start ``seq`` on every page of the donor, a partly filled last page included (two
+        responses continuing one common input)."""
+        assert seq not in self.pages
+        for page in self.pages[donor]:
+            self.refcount[page] += 1
+        self.pages[seq] = list(self.pages[donor])
+        self.length[seq] = self.length[donor]
+
+    def physical_pages(self) -> int:
+        """Pages referenced by at least one sequence."""
+        return int(np.count_nonzero(self.refcount))
 
     def share(self, seq: int, donor: int, positions: int) -> None:
         """Start ``seq`` on the donor's first ``positions`` (a whole number of pages)."""
