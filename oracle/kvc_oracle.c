@@ -6,13 +6,15 @@
  * shares no code, header or constant with the CUDA library; the two meet only through
  * the seeded input generators.
  *
- * Floating point is fp64 throughout.  bf16 inputs are widened exactly (a bf16 value is
- * the top 16 bits of an fp32 value) and never rounded again.
+ * Floating point is fp64 throughout, except the INT8 quantiser, whose integer codes are
+ * decided in fp32 (the precision the device decides them in; the pages fix none).  bf16
+ * inputs are widened exactly (a bf16 value is the top 16 bits of an fp32 value) and never
+ * rounded again.
  *
  * Sources (page title, section):
  *   [KV]   Quail "KV", sections "Paged KV", "KV rewind", "The sharing plan"
  *   [TI]   TileInfer.jl "KV cache", sections "Pages and block tables",
- *          "Growing, rolling back, releasing"
+ *          "Growing, rolling back, releasing", "INT8 cache"
  *   [PA]   "KV Cache Management and PagedAttention", sections "Connect token order to
  *          storage locations", "Grow the allocation as generation proceeds",
  *          "Compute attention over scattered KV"
@@ -128,6 +130,65 @@ void kvo_copy_pages(uint16_t *k_pool, uint16_t *v_pool, int64_t page_elems,
         }
 }
 
+/*
+ * INT8 quantisation of one (position, kv head) vector ([TI] "INT8 cache"): x ~ scale * code,
+ * symmetric, scale = max |x| / 127, codes rounded to nearest (ties to even) and kept in
+ * [-127, 127]; done once, when the position is written.  The pages fix no precision for the
+ * scale, so it is computed in fp32 (max and quotient both fp32, rounded to nearest), the
+ * precision the device takes the same integer decision in.  An all-zero vector gets scale 0
+ * and codes 0.
+ */
+void kvo_quantize_vector(const uint16_t *x, int64_t n, int8_t *codes, float *scale)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf((float)bf16_bits_to_double(x[i]));
+        if (a > m)
+            m = a;
+    }
+    float sc = m / 127.0f;
+    *scale = sc;
+    for (int64_t i = 0; i < n; ++i) {
+        if (sc == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        float r = rintf((float)bf16_bits_to_double(x[i]) / sc);
+        if (r > 127.0f)
+            r = 127.0f;
+        if (r < -127.0f)
+            r = -127.0f;
+        codes[i] = (int8_t)r;
+    }
+}
+
+/*
+ * Store into INT8 pages: token t's K and V vectors of every kv head are quantised and
+ * written at slot_mapping[t] (slot < 0: skipped).
+ *   k_codes/v_codes [num_pages][page_size][kv_heads][head_dim] int8
+ *   k_scales/v_scales [num_pages][kv_heads][page_size] fp32
+ *   k_new/v_new [num_tokens][kv_heads][head_dim] bf16 bits
+ */
+void kvo_store_int8(int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,
+                    int64_t page_size, int64_t kv_heads, int64_t head_dim,
+                    const uint16_t *k_new, const uint16_t *v_new, const int64_t *slots,
+                    int64_t num_tokens)
+{
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0)
+            continue;
+        int64_t page = slot / page_size, off = slot % page_size;
+        for (int64_t g = 0; g < kv_heads; ++g) {
+            int64_t src = (t * kv_heads + g) * head_dim;
+            int64_t dst = (slot * kv_heads + g) * head_dim;
+            int64_t sidx = (page * kv_heads + g) * page_size + off;
+            kvo_quantize_vector(k_new + src, head_dim, k_codes + dst, &k_scales[sidx]);
+            kvo_quantize_vector(v_new + src, head_dim, v_codes + dst, &v_scales[sidx]);
+        }
+    }
+}
+
 /* ---------------------------------------------------------------------------------- */
 /* Attention                                                                          */
 /* ---------------------------------------------------------------------------------- */
@@ -143,6 +204,9 @@ typedef struct {
     const int32_t *key_lo, *key_hi; /* optional per-sequence key window */
     double *out, *lse;
     int64_t thread_index, num_threads;
+    /* INT8 pages (NULL for bf16): codes [pages][P][Hkv][D], scales [pages][Hkv][P] */
+    const int8_t *k_codes, *v_codes;
+    const float *k_scales, *v_scales;
 } kvo_attention_job;
 
 /*
@@ -161,10 +225,23 @@ static void attention_one_group(const kvo_attention_job *job, int64_t s, int64_t
     const int64_t first = job->q_indptr[s];
     const int64_t q_len = job->q_indptr[s + 1] - first;
 
-    /* Gather: key position p of this head -> k_rows[p*D .. p*D+D-1]. */
+    /* Gather: key position p of this head -> k_rows[p*D .. p*D+D-1].  INT8 pages hold
+     * x = scale * code ([TI] "INT8 cache"); the oracle forms that value exactly in fp64. */
     for (int64_t p = 0; p < ctx; ++p) {
         int64_t slot = kvo_slot_of_position(job->block_table, job->bt_stride, s, p,
                                             job->page_size);
+        if (job->k_codes) {
+            int64_t page = slot / job->page_size, off = slot % job->page_size;
+            double ks = job->k_scales[(page * Hkv + g) * job->page_size + off];
+            double vs = job->v_scales[(page * Hkv + g) * job->page_size + off];
+            const int8_t *kc = job->k_codes + (slot * Hkv + g) * D;
+            const int8_t *vc = job->v_codes + (slot * Hkv + g) * D;
+            for (int64_t d = 0; d < D; ++d) {
+                k_rows[p * D + d] = ks * (double)kc[d];
+                v_rows[p * D + d] = vs * (double)vc[d];
+            }
+            continue;
+        }
         const uint16_t *kv = job->k_pool + (slot * Hkv + g) * D;
         const uint16_t *vv = job->v_pool + (slot * Hkv + g) * D;
         for (int64_t d = 0; d < D; ++d) {
@@ -257,12 +334,7 @@ static void *attention_worker(void *arg)
  *   num_threads  >= 1; threads take disjoint (sequence, kv head) items, so the result does
  *                not depend on it
  */
-void kvo_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
-                   int64_t page_size, int64_t kv_heads, int64_t head_dim,
-                   const int32_t *block_table, int64_t bt_stride,
-                   const int32_t *context_lens, const int32_t *q_indptr, int64_t num_seqs,
-                   int64_t q_heads, double scale, const int32_t *key_lo,
-                   const int32_t *key_hi, double *out, double *lse, int64_t num_threads)
+static void run_attention(kvo_attention_job base, int64_t num_threads)
 {
     if (num_threads < 1)
         num_threads = 1;
@@ -270,11 +342,9 @@ void kvo_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_
         (kvo_attention_job *)calloc((size_t)num_threads, sizeof(kvo_attention_job));
     pthread_t *threads = (pthread_t *)calloc((size_t)num_threads, sizeof(pthread_t));
     for (int64_t k = 0; k < num_threads; ++k) {
-        kvo_attention_job j = {q,         k_pool,       v_pool,   page_size, kv_heads,
-                               head_dim,  q_heads,      block_table, bt_stride,
-                               context_lens, q_indptr,  num_seqs, scale,     key_lo,
-                               key_hi,    out,          lse,      k,         num_threads};
-        jobs[k] = j;
+        jobs[k] = base;
+        jobs[k].thread_index = k;
+        jobs[k].num_threads = num_threads;
     }
     if (num_threads == 1) {
         attention_worker(&jobs[0]);
@@ -286,6 +356,45 @@ void kvo_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_
     }
     free(threads);
     free(jobs);
+}
+
+void kvo_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                   int64_t page_size, int64_t kv_heads, int64_t head_dim,
+                   const int32_t *block_table, int64_t bt_stride,
+                   const int32_t *context_lens, const int32_t *q_indptr, int64_t num_seqs,
+                   int64_t q_heads, double scale, const int32_t *key_lo,
+                   const int32_t *key_hi, double *out, double *lse, int64_t num_threads)
+{
+    kvo_attention_job j = {q,         k_pool,       v_pool,   page_size, kv_heads,
+                           head_dim,  q_heads,      block_table, bt_stride,
+                           context_lens, q_indptr,  num_seqs, scale,     key_lo,
+                           key_hi,    out,          lse,      0,         1,
+                           NULL,      NULL,         NULL,     NULL};
+    run_attention(j, num_threads);
+}
+
+/*
+ * The same attention over INT8 pages ([TI] "INT8 cache"): position p of kv head g holds
+ * codes c (int8) and one scale s, and stands for the vector s * c.  Attention in the pages'
+ * form (the key scale multiplying its score, the value scale its probability) equals the
+ * plain attention over those vectors, which is what the oracle computes.
+ *   k_codes/v_codes  [num_pages][page_size][kv_heads][head_dim] int8
+ *   k_scales/v_scales [num_pages][kv_heads][page_size] fp32
+ */
+void kvo_attention_int8(const uint16_t *q, const int8_t *k_codes, const int8_t *v_codes,
+                        const float *k_scales, const float *v_scales, int64_t page_size,
+                        int64_t kv_heads, int64_t head_dim, const int32_t *block_table,
+                        int64_t bt_stride, const int32_t *context_lens,
+                        const int32_t *q_indptr, int64_t num_seqs, int64_t q_heads,
+                        double scale, const int32_t *key_lo, const int32_t *key_hi,
+                        double *out, double *lse, int64_t num_threads)
+{
+    kvo_attention_job j = {q,         NULL,         NULL,     page_size, kv_heads,
+                           head_dim,  q_heads,      block_table, bt_stride,
+                           context_lens, q_indptr,  num_seqs, scale,     key_lo,
+                           key_hi,    out,          lse,      0,         1,
+                           k_codes,   v_codes,      k_scales, v_scales};
+    run_attention(j, num_threads);
 }
 
 /*

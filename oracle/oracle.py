@@ -48,6 +48,13 @@ def _load():
             lib.kvo_slot_mapping.argtypes = [p, i64, p, p, i64, i64, p]
             lib.kvo_store.restype = None
             lib.kvo_store.argtypes = [p, p, i64, i64, p, p, p, i64]
+            lib.kvo_quantize_vector.restype = None
+            lib.kvo_quantize_vector.argtypes = [p, i64, p, p]
+            lib.kvo_store_int8.restype = None
+            lib.kvo_store_int8.argtypes = [p, p, p, p, i64, i64, i64, p, p, p, i64]
+            lib.kvo_attention_int8.restype = None
+            lib.kvo_attention_int8.argtypes = [p, p, p, p, p, i64, i64, i64, p, i64, p, p,
+                                               i64, i64, ctypes.c_double, p, p, p, p, i64]
             lib.kvo_copy_pages.restype = None
             lib.kvo_copy_pages.argtypes = [p, p, i64, p, p, i64, p, p]
             lib.kvo_attention.restype = None
@@ -92,6 +99,55 @@ def store(k_pool, v_pool, k_new, v_new, slots) -> None:
     hkv, d = k_pool.shape[2], k_pool.shape[3]
     _load().kvo_store(_ptr(k_pool), _ptr(v_pool), hkv, d, _ptr(kn), _ptr(vn), _ptr(sl),
                       sl.shape[0])
+
+
+def quantize_vector(x_bits):
+    """INT8 codes and fp32 scale of one bf16 vector (uint16 bits): x ~ scale * code."""
+    x = _c(x_bits, np.uint16)
+    codes = np.empty(x.shape[0], dtype=np.int8)
+    scale = np.zeros(1, dtype=np.float32)
+    _load().kvo_quantize_vector(_ptr(x), x.shape[0], _ptr(codes), _ptr(scale))
+    return codes, float(scale[0])
+
+
+def store_int8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, slots) -> None:
+    """In place: quantise every new token's K/V vectors into INT8 pages at their slots.
+    codes int8 [pages, P, Hkv, D]; scales float32 [pages, Hkv, P]."""
+    for a, t in ((k_codes, np.int8), (v_codes, np.int8), (k_scales, np.float32),
+                 (v_scales, np.float32)):
+        assert a.dtype == t and a.flags.c_contiguous
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    sl = _c(slots, np.int64)
+    P, hkv, d = k_codes.shape[1], k_codes.shape[2], k_codes.shape[3]
+    _load().kvo_store_int8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), P,
+                           hkv, d, _ptr(kn), _ptr(vn), _ptr(sl), sl.shape[0])
+
+
+def attention_int8(q, k_codes, v_codes, k_scales, v_scales, block_table, context_lens,
+                   q_indptr, scale=None, key_lo=None, key_hi=None, num_threads: int = 1):
+    """fp64 paged attention over INT8 pages (x = scale * code); returns (out, lse)."""
+    q = _c(q, np.uint16)
+    kc = _c(k_codes, np.int8)
+    vc = _c(v_codes, np.int8)
+    ks = _c(k_scales, np.float32)
+    vs = _c(v_scales, np.float32)
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    ind = _c(q_indptr, np.int32)
+    lo = None if key_lo is None else _c(key_lo, np.int32)
+    hi = None if key_hi is None else _c(key_hi, np.int32)
+    t, hq, d = q.shape
+    page_size, hkv = kc.shape[1], kc.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = np.empty((t, hq, d), dtype=np.float64)
+    lse = np.empty((t, hq), dtype=np.float64)
+    _load().kvo_attention_int8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), page_size, hkv,
+                               d, _ptr(bt), bt.shape[1], _ptr(ctx), _ptr(ind), ctx.shape[0],
+                               hq, float(scale), _ptr(lo), _ptr(hi), _ptr(out), _ptr(lse),
+                               int(num_threads))
+    return out, lse
 
 
 def copy_pages(k_pool, v_pool, src_pages, dst_pages) -> None:
