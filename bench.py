@@ -320,6 +320,48 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     }
     del d, out, work, slots
     torch.cuda.empty_cache()
+    # INT8 pages: the batched-decode batch quantised by kvc_store_int8 (every slot of the bf16
+    # pools, as if each were a new token), decoded by kvc_decode_int8 beside kvc_decode
+    case = config_case(2, seed=rank_seed(2, rank))
+    d = to_device(case, dev)
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+    kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+    pages, P, H, D = (int(x) for x in d.k_pool.shape)
+    kc = torch.empty(pages, P, H, D, dtype=torch.int8, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.empty(pages, H, P, dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    all_slots = torch.arange(pages * P, dtype=torch.int32, device=dev)
+    kvc.kvc_store_int8(kc, vc, ks, vs, d.k_pool.view(pages * P, H, D),
+                       d.v_pool.view(pages * P, H, D), all_slots)
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    pool = kvc.pool_desc(d.k_pool)
+    splits, chunk, ws = kvc.kvc_decode_int8_plan(case.num_seqs, case.q_heads, pool,
+                                                 case.max_ctx, 0)
+    _, _, ws16 = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+    work = torch.empty(max(ws, ws16, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        t8 = time_graph(torch, lambda: kvc.kvc_decode_int8(
+            out, d.q, kc, vc, ks, vs, d.block_table, d.context_lens, case.max_ctx,
+            num_splits=0, workspace=work), stream, flush, args.leg_steps)
+        t16 = time_graph(torch, lambda: kvc.kvc_decode(
+            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+            num_splits=0, workspace=work), stream, flush, args.leg_steps)
+    b8 = int(case.context_lens.sum()) * 2 * H * (D + 4) + qo(case)
+    b16 = decode_bytes(case)
+    legs["int8_decode"] = {
+        "workload": "batched decode on INT8 pages: 64 seqs, ctx U[512,4096], 32/8 heads, D 128, "
+                    "P 16 (132 B per vector)",
+        "us": round(t8 * 1e3, 1), "bytes": b8, "gbs": round(b8 / (t8 / 1e3) / 1e9, 1),
+        "frac_of_hbm": round(b8 / (t8 / 1e3) / 1e9 / peaks["hbm"], 4),
+        "bf16_us": round(t16 * 1e3, 1), "bf16_bytes": b16,
+        "speedup_vs_bf16": round(t16 / t8, 3), "splits": splits,
+        "gpu_launches_per_step": 2 if splits > 1 else 1,
+    }
+    del d, out, work, slots, kc, vc, ks, vs, all_slots
+    torch.cuda.empty_cache()
     # copy-on-write page copies: 4,096 pages of P 16 x 8 kv heads x D 128 (32 KB per pool)
     # from one half of a 16,384-page pool to shuffled pages of the other half
     n_pages, n_copy = 16384, 4096

@@ -259,6 +259,44 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
 kvc_status kvc_device_errors(uint32_t *flags_out);
 
 /*
+ * INT8 pages (TileInfer.jl "KV cache", section "INT8 cache": the pools hold int8 codes with
+ * one fp32 scale per cached vector -- one kv head at one position -- x ~ scale * code,
+ * symmetric, scale = max|x| / 127, quantised once when the position is written; attention
+ * does not dequantise: a key's scale multiplies its score, a value's scale its probability
+ * before the PV product).  132 bytes per vector at head_dim 128 instead of 256.
+ *   k_codes, v_codes   int8 [num_pages][page_size][kv_heads][head_dim] (the bf16 pools'
+ *                      layout with one byte per value)
+ *   k_scales, v_scales fp32 [num_pages][kv_heads][page_size] (the scales of one page and kv
+ *                      head are contiguous)
+ * All four 16-byte aligned; `pool` describes them as it describes a bf16 pool.
+ *
+ * kvc_store_int8 -- quantise and store new K/V at their slots (kvc_store's contract
+ * otherwise: slot < 0 skipped, slots past the pool skipped and flagged).  Codes are
+ * rint(x / scale) (ties to even) clamped to [-127, 127], with scale = max|x| / 127 and both
+ * quotients computed in fp32 round-to-nearest; an all-zero vector stores scale 0 and codes 0.
+ * Integer codes and scales are bit-exact.  k_new, v_new: bf16 [num_tokens][kv_heads][head_dim].
+ */
+kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                          kvc_pool_desc pool, const void *k_new, const void *v_new,
+                          const int32_t *slot_mapping, int32_t num_tokens, void *stream);
+
+/*
+ * kvc_decode_int8 -- kvc_decode over INT8 pages (same arguments and outputs).  Its split-K
+ * plan and workspace come from kvc_decode_int8_plan (the automatic split count differs from
+ * kvc_decode's: the INT8 kernel keeps more CTAs resident per SM).  head_dim 128 only (others:
+ * KVC_ERR_UNSUPPORTED).
+ */
+kvc_status kvc_decode_int8_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
+                                int32_t max_ctx, int32_t num_splits, int32_t *splits_out,
+                                int32_t *chunk_out, size_t *workspace_bytes_out);
+kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
+                           const void *v_codes, const float *k_scales, const float *v_scales,
+                           kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                           int32_t q_heads, float scale, int32_t num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * kvc_copy_pages -- copy-on-write page copy ("KV Cache Management and PagedAttention", "Split
  * shared blocks when a write is needed": before a sequence writes into a page that other
  * sequences still reference, the page is copied to a new one and the writer's block-table

@@ -75,6 +75,8 @@ int device_sm_count()
     return 152;
 }
 
+constexpr int kInt8PlanTarget = 12;   // CTAs per SM the INT8 decode's automatic splits aim at
+
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
 
@@ -85,8 +87,12 @@ struct Plan {
     size_t lse_offset;
 };
 
+// Split-K plan.  Automatic splits aim at `ctas_per_sm_target` CTAs per SM over the whole
+// launch: several waves of the kernel's resident CTAs, enough to spread the ramp and the
+// uneven sequence lengths (bf16 decode: 2 resident CTAs per SM, target 4; INT8 decode: 3
+// resident, target 12, measured best on the batched-decode workload).
 Plan make_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool, int32_t max_ctx,
-               int32_t requested)
+               int32_t requested, int ctas_per_sm_target = 4)
 {
     const int64_t ctx = max_ctx > 0 ? max_ctx : 1;
     const int64_t unit = kvc::kStageKeys;   // a multiple of every supported page size
@@ -99,7 +105,8 @@ Plan make_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool, int
         if (requested <= 0) {
             // Enough CTAs for several per SM: (sequence, kv head) units times splits.
             const int64_t units = static_cast<int64_t>(num_seqs > 0 ? num_seqs : 1) * pool.kv_heads;
-            want = ceil_div(4 * static_cast<int64_t>(device_sm_count()), units);
+            want = ceil_div(ctas_per_sm_target * static_cast<int64_t>(device_sm_count()),
+                            units);
         }
         int64_t chunk = round_up(ceil_div(ctx, want), unit);
         if (requested <= 0 && chunk < 256)
@@ -142,12 +149,13 @@ struct MapKey {
     const void *ptr;
     int device;
     int rank;
+    bool int8 = false;   // uint8 elements (INT8 pages) instead of bf16
     cuuint64_t dims[4];
     cuuint64_t strides[3];
     cuuint32_t box[4];
     bool operator==(const MapKey &o) const
     {
-        if (ptr != o.ptr || device != o.device || rank != o.rank)
+        if (ptr != o.ptr || device != o.device || rank != o.rank || int8 != o.int8)
             return false;
         for (int i = 0; i < rank; ++i)
             if (dims[i] != o.dims[i] || box[i] != o.box[i] ||
@@ -183,7 +191,8 @@ kvc_status tensor_map(MapKey key, CUtensorMap *out)
         return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     CUtensorMap map;
-    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(key.rank),
+    CUresult r = fn(&map, key.int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    static_cast<cuuint32_t>(key.rank),
                     const_cast<void *>(key.ptr), key.dims, key.strides, key.box, elem_strides,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -212,6 +221,26 @@ kvc_status pool_tensor_map_halves(const void *base, const kvc_pool_desc &pool, C
     k.strides[0] = static_cast<cuuint64_t>(pool.head_dim) * 2;
     k.strides[1] = static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim * 2;
     k.box[0] = 64;
+    k.box[1] = 1;
+    k.box[2] = static_cast<cuuint32_t>(pool.page_size);
+    return tensor_map(k, out);
+}
+
+// INT8 codes [num_pages * page_size][kv_heads][head_dim] viewed as the 3-D tensor
+// {head_dim, kv head, slot} of bytes; one box {head_dim, 1, page_size} is one page of one kv
+// head, [page_size rows][head_dim bytes] (128 bytes at head_dim 128, one swizzle row).
+kvc_status pool_tensor_map_int8(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
+{
+    MapKey k{};
+    k.ptr = base;
+    k.rank = 3;
+    k.int8 = true;
+    k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
+    k.dims[1] = static_cast<cuuint64_t>(pool.kv_heads);
+    k.dims[2] = static_cast<cuuint64_t>(pool.num_pages) * pool.page_size;
+    k.strides[0] = static_cast<cuuint64_t>(pool.head_dim);
+    k.strides[1] = static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim;
+    k.box[0] = static_cast<cuuint32_t>(pool.head_dim);
     k.box[1] = 1;
     k.box[2] = static_cast<cuuint32_t>(pool.page_size);
     return tensor_map(k, out);
@@ -393,6 +422,115 @@ kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void 
                                         v_new, slot_mapping, num_tokens,
                                         static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? ok() : cuda_fail(err, "store launch");
+}
+
+kvc_status kvc_decode_int8_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
+                                int32_t max_ctx, int32_t num_splits, int32_t *splits_out,
+                                int32_t *chunk_out, size_t *workspace_bytes_out)
+{
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    if (num_seqs < 0 || q_heads <= 0 || max_ctx < 0 || num_splits < 0)
+        return fail(KVC_ERR_INVALID_ARG, "negative size or non-positive q_heads");
+    const Plan p = make_plan(num_seqs, q_heads, pool, max_ctx, num_splits, kInt8PlanTarget);
+    if (splits_out)
+        *splits_out = p.splits;
+    if (chunk_out)
+        *chunk_out = p.chunk;
+    if (workspace_bytes_out)
+        *workspace_bytes_out = p.ws_bytes;
+    return ok();
+}
+
+kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                          kvc_pool_desc pool, const void *k_new, const void *v_new,
+                          const int32_t *slot_mapping, int32_t num_tokens, void *stream)
+{
+    kvc_status st = check_pool(pool);
+    if (st != KVC_OK)
+        return st;
+    if (num_tokens < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if (num_tokens == 0)
+        return ok();
+    if (!k_codes || !v_codes || !k_scales || !v_scales || !k_new || !v_new || !slot_mapping)
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) ||
+        !aligned16(v_scales) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(KVC_ERR_INVALID_ARG, "codes, scales and new K/V must be 16-byte aligned");
+    cudaError_t err = kvc::launch_store_int8(k_codes, v_codes, k_scales, v_scales,
+                                             pool.kv_heads, pool.head_dim, pool.page_size,
+                                             pool.num_pages * pool.page_size, k_new, v_new,
+                                             slot_mapping, num_tokens,
+                                             static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "store_int8 launch");
+}
+
+kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
+                           const void *v_codes, const float *k_scales, const float *v_scales,
+                           kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                           int32_t q_heads, float scale, int32_t num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    kvc_status st = check_attention_args(out, out_dtype, q, k_codes, v_codes, pool, block_table,
+                                         bt_stride, context_lens, num_seqs, max_ctx, q_heads);
+    if (st != KVC_OK)
+        return st;
+    if (pool.head_dim != 128)
+        return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
+                    pool.head_dim);
+    if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
+        return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
+    if (num_splits < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_splits %d", num_splits);
+    if (num_seqs == 0)
+        return ok();
+    const Plan p = make_plan(num_seqs, q_heads, pool, max_ctx, num_splits, kInt8PlanTarget);
+    if (p.splits > 1) {
+        if (workspace == nullptr || workspace_bytes < p.ws_bytes)
+            return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given",
+                        p.ws_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+        if (!aligned16(workspace))
+            return fail(KVC_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    }
+    CUtensorMap tk, tv;
+    if ((st = pool_tensor_map_int8(k_codes, pool, &tk)) != KVC_OK)
+        return st;
+    if ((st = pool_tensor_map_int8(v_codes, pool, &tv)) != KVC_OK)
+        return st;
+    kvc::DecodeInt8Launch l;
+    l.q = q;
+    l.k_scales = k_scales;
+    l.v_scales = v_scales;
+    l.out = out;
+    l.out_f32 = out_dtype == KVC_F32;
+    l.part_o = static_cast<float *>(workspace);
+    l.part_lse = p.splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                          p.lse_offset)
+                              : nullptr;
+    l.block_table = block_table;
+    l.bt_stride = bt_stride;
+    l.context_lens = context_lens;
+    l.num_seqs = num_seqs;
+    l.q_heads = q_heads;
+    l.kv_heads = pool.kv_heads;
+    l.page_size = pool.page_size;
+    l.chunk = p.chunk;
+    l.n_split = p.splits;
+    l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = kvc::launch_decode_int8(l, tk, tv, s);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "decode_int8 launch");
+    if (p.splits > 1) {
+        err = kvc::launch_merge(out, l.out_f32, l.part_o, l.part_lse, num_seqs * q_heads,
+                                p.splits, pool.head_dim, nullptr, s);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "merge launch");
+    }
+    return ok();
 }
 
 kvc_status kvc_copy_pages(void *k_pool, void *v_pool, kvc_pool_desc pool,
@@ -701,6 +839,10 @@ kvc_status kvc_device_errors(uint32_t *flags_out)
         err = kvc::read_and_clear_append_tc_errors(&d);
     if (err == cudaSuccess)
         err = kvc::read_and_clear_grouped_errors(&e);
+    uint32_t f = 0;
+    if (err == cudaSuccess)
+        err = kvc::read_and_clear_decode_int8_errors(&f);
+    e |= f;
     if (err != cudaSuccess)
         return cuda_fail(err, "reading the device error word");
     *flags_out = a | c | d | e;

@@ -1,0 +1,477 @@
+// kvc_decode_int8.cu -- paged decode attention over INT8 pages.
+//
+// What it computes: the attention of kvc_decode ("KV Cache Management and PagedAttention",
+// "Compute attention over scattered KV") over pages that hold int8 codes with one fp32 scale
+// per (position, kv head) vector (TileInfer.jl "KV cache", "INT8 cache").  As that section
+// says, the cache is not dequantised: a key's scale multiplies its score, and a value's scale
+// its probability before the PV product.  Codes are converted to fp16 in registers (exact:
+// |code| <= 127) for the tensor cores; the scales stay outside the products.  fp16 rather than
+// bf16 because two codes become an exact fp16 pair in three integer/half operations: bytes
+// b placed under the exponent 0x64 read as 1024 + b, and the code is b - 128; the query is
+// converted to fp16 once (scaled by a power of two when it would overflow fp16), and the
+// probabilities (at most 1) times the value scales enter the PV product as fp16.
+//
+// Layout: codes [num_pages * P][Hkv][128] int8 like the bf16 pools (128 bytes per vector);
+// scales [num_pages][Hkv][P] fp32, so the P scales of one (page, kv head) are one contiguous
+// run that a single bulk copy brings in.
+//
+// Kernel design (head_dim 128): one CTA per (split, kv head, sequence), 4 consumer warps and a
+// producer warp, three CTAs per SM.  The producer streams 64-position stages -- per page one TMA
+// box of K codes, one of V codes (128-byte swizzle) and one bulk copy each of the K and V
+// scales, issued by parallel lanes -- through a 4-deep ring.  Consumer warp w takes positions 16 w .. 16 w + 15 of each stage:
+//   S = Q K^T on mma.sync m16n8k16 (fp16; the G query heads padded to 16 rows).  The order
+//   in which head_dim is contracted is free, so thread (., t) takes dims 32 t + 4 kk .. + 3
+//   for k-step kk: its K codes for a position are 32 contiguous bytes (two 16-byte loads) and
+//   its Q pairs two contiguous pairs;
+//   O^T += V^T (P * v_scale)^T with M = 16 dims and N = 8 query rows: the probabilities a
+//   thread holds from the S fragment are exactly its B fragment, half as many MMAs and
+//   accumulators as O = P V with rows padded to 16; the dims of tile dt are permuted so that
+//   thread row r reads dims 32 q + 4 r .. + 3 (q = 0..3), one 4-byte word per position and q,
+//   and the accumulators are put back in dim order when the warps combine.
+// Online softmax in base 2, masked positions excluded before the exponential and their
+// probabilities set to 0 by selection (a scale left in an unused slot may be NaN).
+#include <math.h>
+
+#include "kvc_device.cuh"
+#include "kvc_launch.h"
+
+namespace kvc {
+
+namespace {
+
+__device__ uint32_t g_decode_int8_errors;
+
+constexpr int D = 128;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 4;
+constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;   // 16
+constexpr int kMaxGroup = 8;
+constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int kCodeBytes = kStageKeys * D;                  // K (or V) codes of one stage
+constexpr int kScaleBytes = kStageKeys * 4;
+constexpr int kOffV = kCodeBytes;
+constexpr int kOffKs = 2 * kCodeBytes;
+constexpr int kOffVs = kOffKs + kScaleBytes;
+constexpr int kStageBytes = ((2 * kCodeBytes + 2 * kScaleBytes) + 1023) & ~1023;
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kCombineBytes = kConsumerWarps * kMaxGroup * (D + 2) * 4;
+static_assert(kCombineBytes <= kRingBytes, "combine area aliases the ring");
+constexpr size_t kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8;
+
+struct Args {
+    const __nv_bfloat16 *q;
+    const float *k_scales, *v_scales;
+    void *out;
+    int out_f32;
+    float *part_o;
+    float *part_lse;
+    const int32_t *block_table;
+    int bt_stride;
+    const int32_t *context_lens;
+    int q_heads, kv_heads, group, page_size;
+    int chunk, n_split;
+    float scale_log2;
+};
+
+__device__ __forceinline__ void store_out(void *out, int out_f32, size_t idx, float v)
+{
+    if (out_f32)
+        static_cast<float *>(out)[idx] = v;
+    else
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// fp16 pair (low: byte c of a, high: byte c of b) of two words of int8 codes, exact.  The
+// bytes are moved under exponent bits 0x64 (fp16 1024 + m for m in 0..255) with the sign bit
+// of the code flipped (m = code + 128), and 1152 is subtracted from both halves.
+template <int c>
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t a, uint32_t b)
+{
+    const uint32_t bytes = __byte_perm(a, b, c | ((4 + c) << 8));   // [a.c, a.0, b.c, a.0]
+    const uint32_t biased = (bytes & 0x00FF00FFu) ^ 0x64806480u;
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&biased),
+                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Both fp16 pairs of one word of int8 codes (codes 0, 1 and codes 2, 3), exact: the word's
+// sign bits flipped (m = code + 128), the bytes put under exponent 0x64 and 1152 subtracted.
+__device__ __forceinline__ void word_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t m = w ^ 0x80808080u;
+    const uint32_t e = 0x64646464u;
+    const uint32_t a = __byte_perm(m, e, 0x4140u);   // [m.0, 0x64, m.1, 0x64]
+    const uint32_t b = __byte_perm(m, e, 0x4342u);   // [m.2, 0x64, m.3, 0x64]
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+// Offset of byte `col` of stage row `row` in a 128-byte-swizzled [64][128] code tile.
+__device__ __forceinline__ uint32_t code_offset(int row, int col)
+{
+    return static_cast<uint32_t>(row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15));
+}
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 3)
+    paged_decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v, const Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRingBytes);
+    uint64_t *empty = full + kStages;
+
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int s = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int P = a.page_size;
+    int ctx = a.context_lens[s];
+    if (ctx > a.bt_stride * P) {
+        if (threadIdx.x == 0 && split == 0)
+            atomicOr(&g_decode_int8_errors, kErrContextRange);
+        ctx = a.bt_stride * P;
+    }
+    const int k_begin = split * a.chunk;
+    const int k_end = min(ctx, k_begin + a.chunk);
+    const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
+
+    if (k_begin >= k_end) {
+        if (SPLIT) {
+            if (threadIdx.x < G)
+                a.part_lse[(row0 + threadIdx.x) * a.n_split + split] = -INFINITY;
+        } else {
+            for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+                store_out(a.out, a.out_f32, row0 * D + i, 0.0f);
+        }
+        return;
+    }
+
+    const int n_blocks = (k_end - k_begin + kStageKeys - 1) / kStageKeys;
+    const int first_page = k_begin / P;
+    const int n_pages = (k_end - k_begin + P - 1) / P;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------ producer (whole warp) -------------------------------------
+        const int32_t *bt_row =
+            a.block_table + static_cast<size_t>(s) * a.bt_stride + first_page;
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+        const uint64_t policy = l2_policy_evict_first();
+        int cached_base = -32;
+        int cached_page = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int b = 0; b < n_blocks; ++b) {
+            const int st = b % kStages;
+            if (b >= kStages &&
+                !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((b / kStages) - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            const int rel0 = b * kStageKeys;
+            const int keys = min(kStageKeys, k_end - k_begin - rel0);
+            const int np = (keys + P - 1) / P;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[st],
+                                      static_cast<uint32_t>(np * P * (2 * D + 2 * 4)));
+            __syncwarp();
+            uint8_t *stage = smem + st * kStageBytes;
+            const int lp0 = rel0 / P;
+            if (lp0 + np > cached_base + 32) {
+                cached_base = lp0;
+                cached_page = (lp0 + lane < n_pages) ? bt_row[lp0 + lane] : 0;
+            }
+            // lane 4 i + op: page i's K codes, V codes, K scales, V scales
+            const int i = lane >> 2;
+            const int op = lane & 3;
+            const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
+            if (i < np) {
+                if (op == 0) {
+                    tma_load_3d(stage + i * P * D, &tmap_k, 0, kvh, page * P, &full[st], policy);
+                } else if (op == 1) {
+                    tma_load_3d(stage + kOffV + i * P * D, &tmap_v, 0, kvh, page * P, &full[st],
+                                policy);
+                } else {
+                    const float *src = (op == 2 ? a.k_scales : a.v_scales) +
+                                       (static_cast<size_t>(page) * a.kv_heads + kvh) * P;
+                    bulk_load(stage + (op == 2 ? kOffKs : kOffVs) + i * P * 4, src, P * 4,
+                              &full[st]);
+                }
+            }
+            issued = b + 1;
+        }
+        if (!ok && lane == 0) {
+            atomicOr(&g_decode_int8_errors, kErrDecodeEmptyWait);
+            for (int b = max(0, issued - kStages); b < issued; ++b)
+                if (!mbar_wait(&full[b % kStages], (b / kStages) & 1))
+                    atomicOr(&g_decode_int8_errors, kErrDrainWait);
+        }
+        return;
+    }
+
+    // --------------------------------- consumers -----------------------------------------
+    const int r = lane >> 2;   // fragment row = q head of the group (rows >= G: padding)
+    const int t = lane & 3;
+    // Q pairs in the contraction order (k-step kk uses dims 32 t + 4 kk + {0, 1} and {2, 3}),
+    // as fp16.  A power of two q_pow brings the largest |q| of the group below 2^14 when it
+    // is above, and is folded back into the score scale (exact either way).
+    uint32_t qa[D / 16][2];
+    float sl2 = a.scale_log2;
+    {
+        const __nv_bfloat16 *qrow = a.q + (row0 + r) * D + 32 * t;
+        float qv[D / 4];
+        float qmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) {
+            qv[i] = r < G ? __bfloat162float(qrow[i]) : 0.0f;
+            qmax = fmaxf(qmax, fabsf(qv[i]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+        float q_pow = 1.0f;
+        while (qmax * q_pow > 16384.0f)
+            q_pow *= 0.5f;
+        sl2 = sl2 / q_pow;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qa[kk][0] = pack_f16x2(qv[4 * kk] * q_pow, qv[4 * kk + 1] * q_pow);
+            qa[kk][1] = pack_f16x2(qv[4 * kk + 2] * q_pow, qv[4 * kk + 3] * q_pow);
+        }
+    }
+    // O^T accumulators: tile dt holds dims pi(dt, m) x query rows n, this thread rows 2t,
+    // 2t + 1 of dims pi(dt, r) (c0, c1) and pi(dt, r + 8) (c2, c3), where
+    // pi(dt, r + 8 h) = 32 (dt >> 1) + 4 r + 2 (dt & 1) + h
+    float o[D / 16][4];
+#pragma unroll
+    for (int n = 0; n < D / 16; ++n)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    float m_run = -INFINITY;
+    float l_run = 0.0f;
+    const int wrow = warp * kKeysPerWarp;   // first stage row of this warp
+    // Stage-independent offsets.  K: the two 16-byte halves of this thread's 32 bytes in rows
+    // wrow + r and wrow + 8 + r.  V: the word of dims 4 r .. 4 r + 3 in each of the thread's
+    // four positions; dims 32 q + 4 r lie at that offset xor (q << 5), since the swizzle only
+    // permutes 16-byte chunks within a row and q moves the chunk index by 2 q.
+    uint32_t k_off[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        k_off[nt][0] = code_offset(wrow + 8 * nt + r, 32 * t);
+        k_off[nt][1] = code_offset(wrow + 8 * nt + r, 32 * t + 16);
+    }
+    const int key[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    uint32_t v_off[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v_off[i] = kOffV + code_offset(wrow + key[i], 4 * r);
+    bool ok = true;
+
+    for (int b = 0; b < n_blocks; ++b) {
+        const int st = b % kStages;
+        if (!mbar_wait(&full[st], (b / kStages) & 1)) {
+            ok = false;
+            break;
+        }
+        const uint8_t *stage = smem + st * kStageBytes;
+        const float *ks = reinterpret_cast<const float *>(stage + kOffKs) + wrow;
+        const float *vs = reinterpret_cast<const float *>(stage + kOffVs) + wrow;
+        const int n_valid = k_end - (k_begin + b * kStageKeys + wrow);
+        if (n_valid > 0) {
+            // S = Q K^T: B column r of n-tile nt is position 8 nt + r of this warp
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const uint4 lo = *reinterpret_cast<const uint4 *>(stage + k_off[nt][0]);
+                const uint4 hi = *reinterpret_cast<const uint4 *>(stage + k_off[nt][1]);
+                const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint32_t b0, b1;   // codes 0, 1 and codes 2, 3 of the word
+                    word_f16x2(w[kk], b0, b1);
+                    mma_f16_16816(sc[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                }
+            }
+            // scores of positions 2t, 2t+1 (tile 0) and 8+2t, 9+2t (tile 1), key-scaled
+            float x[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                x[i] = key[i] < n_valid ? x[i] * ks[key[i]] * sl2 : -INFINITY;
+            float mb = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            const float m_new = fmaxf(m_run, mb);
+            if (__any_sync(0xffffffffu, m_new > m_run)) {
+                const float alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_new);
+                // this thread's accumulators are rows 2t and 2t + 1 (held by lanes 8t, 8t + 4)
+                const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+                const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+                for (int n = 0; n < D / 16; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a1;
+                    o[n][2] *= a0;
+                    o[n][3] *= a1;
+                }
+                l_run *= alpha;
+                m_run = m_new;
+            }
+            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+            float p[4], pv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                p[i] = fast_exp2(x[i] - m_use);
+                pv[i] = key[i] < n_valid ? p[i] * vs[key[i]] : 0.0f;
+            }
+            l_run += (p[0] + p[1]) + (p[2] + p[3]);
+            const uint32_t pa0 = pack_f16x2(pv[0], pv[1]);   // positions 2t, 2t+1
+            const uint32_t pa2 = pack_f16x2(pv[2], pv[3]);   // positions 8+2t, 9+2t
+            // O^T += V^T P'^T: A = V^T (16 dims x 16 positions), B = P'^T, whose fragment is
+            // exactly this thread's (pa0, pa2); thread r reads one word (dims 32 q + 4 r .. + 3)
+            // of each of its four positions per q
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t vw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    vw[i] = *reinterpret_cast<const uint32_t *>(stage + (v_off[i] ^ (q << 5)));
+                mma_f16_16816(o[2 * q], codes_f16x2<0>(vw[0], vw[1]), codes_f16x2<1>(vw[0], vw[1]),
+                              codes_f16x2<0>(vw[2], vw[3]), codes_f16x2<1>(vw[2], vw[3]), pa0,
+                              pa2);
+                mma_f16_16816(o[2 * q + 1], codes_f16x2<2>(vw[0], vw[1]),
+                              codes_f16x2<3>(vw[0], vw[1]), codes_f16x2<2>(vw[2], vw[3]),
+                              codes_f16x2<3>(vw[2], vw[3]), pa0, pa2);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[st]);
+    }
+    if (!ok)
+        atomicOr(&g_decode_int8_errors, kErrDecodeFullWait);
+
+    // ------------------------- combine the 4 warps' partial results -----------------------
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    named_barrier(1, kConsumerWarps * 32);
+    float *red_o = reinterpret_cast<float *>(smem);               // [W][8][D]
+    float *red_m = red_o + kConsumerWarps * kMaxGroup * D;         // [W][8]
+    float *red_l = red_m + kConsumerWarps * kMaxGroup;             // [W][8]
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {   // query rows 2t and 2t + 1
+        const int row = 2 * t + e;
+        if (row < G) {
+            float *dst = red_o + (warp * kMaxGroup + row) * D;
+#pragma unroll
+            for (int n = 0; n < D / 16; ++n) {
+                const int dim = 32 * (n >> 1) + 4 * r + 2 * (n & 1);
+                dst[dim] = o[n][e];
+                dst[dim + 1] = o[n][2 + e];
+            }
+        }
+    }
+    if (r < G && t == 0) {
+        red_m[warp * kMaxGroup + r] = m_run;
+        red_l[warp * kMaxGroup + r] = l_run;
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+        const int row = idx / D;
+        const int d = idx - row * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+            M = fmaxf(M, red_m[w * kMaxGroup + row]);
+        float L = 0.0f, O = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = red_m[w * kMaxGroup + row];
+            const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
+            L += f * red_l[w * kMaxGroup + row];
+            O += f * red_o[(w * kMaxGroup + row) * D + d];
+        }
+        const float val = (L > 0.0f) ? O / L : 0.0f;
+        if (SPLIT) {
+            const size_t prow = (row0 + row) * a.n_split + split;
+            a.part_o[prow * D + d] = val;
+            if (d == 0)
+                a.part_lse[prow] = (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+        } else {
+            store_out(a.out, a.out_f32, (row0 + row) * D + d, val);
+        }
+    }
+}
+
+template <bool SPLIT>
+cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUtensorMap &tv,
+                     cudaStream_t stream)
+{
+    Args a;
+    a.q = static_cast<const __nv_bfloat16 *>(l.q);
+    a.k_scales = l.k_scales;
+    a.v_scales = l.v_scales;
+    a.out = l.out;
+    a.out_f32 = l.out_f32;
+    a.part_o = l.part_o;
+    a.part_lse = l.part_lse;
+    a.block_table = l.block_table;
+    a.bt_stride = l.bt_stride;
+    a.context_lens = l.context_lens;
+    a.q_heads = l.q_heads;
+    a.kv_heads = l.kv_heads;
+    a.group = l.q_heads / l.kv_heads;
+    a.page_size = l.page_size;
+    a.chunk = l.chunk;
+    a.n_split = l.n_split;
+    a.scale_log2 = l.scale * 1.4426950408889634f;
+    auto kernel = paged_decode_int8_kernel<SPLIT>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmemBytes));
+    if (err != cudaSuccess)
+        return err;
+    dim3 grid(l.n_split, l.kv_heads, l.num_seqs);
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tmap_k,
+                               const CUtensorMap &tmap_v, cudaStream_t stream)
+{
+    if (l.num_seqs == 0)
+        return cudaSuccess;
+    return l.n_split > 1 ? launch_t<true>(l, tmap_k, tmap_v, stream)
+                         : launch_t<false>(l, tmap_k, tmap_v, stream);
+}
+
+cudaError_t read_and_clear_decode_int8_errors(uint32_t *flags)
+{
+    uint32_t zero = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(flags, g_decode_int8_errors, sizeof(uint32_t));
+    if (err != cudaSuccess)
+        return err;
+    return cudaMemcpyToSymbol(g_decode_int8_errors, &zero, sizeof(uint32_t));
+}
+
+}  // namespace kvc

@@ -27,6 +27,25 @@ struct DecodeLaunch {
     int split_stride = 0;   // 0: n_split
 };
 
+// Decode over INT8 pages (head_dim 128): codes like a bf16 pool, scales [pages][Hkv][P].
+struct DecodeInt8Launch {
+    const void *q;
+    const float *k_scales, *v_scales;
+    void *out;
+    int out_f32;
+    float *part_o;            // [S][Hq][n_split][D] when n_split > 1
+    float *part_lse;          // [S][Hq][n_split]
+    const int32_t *block_table;
+    int bt_stride;
+    const int32_t *context_lens;
+    int num_seqs, q_heads, kv_heads, page_size;
+    int chunk, n_split;
+    float scale;
+};
+cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tmap_k,
+                               const CUtensorMap &tmap_v, cudaStream_t stream);
+cudaError_t read_and_clear_decode_int8_errors(uint32_t *flags);
+
 // Grouped decode over a shared prefix: for each group, the first prefix_len[g] positions are
 // the same pages for every member (the leader's block-table row lists them).
 struct GroupedPrefixLaunch {
@@ -75,6 +94,10 @@ cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int 
 cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
                          int num_slots, const void *k_new, const void *v_new,
                          const int32_t *slots, int num_tokens, cudaStream_t stream);
+cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                              int kv_heads, int head_dim, int page_size, int num_slots,
+                              const void *k_new, const void *v_new, const int32_t *slots,
+                              int num_tokens, cudaStream_t stream);
 cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,
                               int kv_heads, int head_dim, const int32_t *src_pages,
                               const int32_t *dst_pages, int num_copies, cudaStream_t stream);

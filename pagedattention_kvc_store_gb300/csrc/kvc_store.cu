@@ -101,6 +101,76 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
     }
 }
 
+// INT8 store (TileInfer.jl "KV cache", "INT8 cache"): one warp per (token, kv head) vector of
+// D = 32 * E values.  scale = max|x| / 127 and code = rint(x / scale) clamped to [-127, 127],
+// both in fp32 with round-to-nearest division, so the codes are the ones the quantiser's
+// definition gives; an all-zero vector stores scale 0 and codes 0.  Codes land in the pool
+// like bf16 values do ([slot][kv head][D]); scales at [page][kv head][offset].
+template <int E>
+__global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_codes,
+                                                         int8_t *__restrict__ v_codes,
+                                                         float *__restrict__ k_scales,
+                                                         float *__restrict__ v_scales,
+                                                         const __nv_bfloat16 *__restrict__ k_new,
+                                                         const __nv_bfloat16 *__restrict__ v_new,
+                                                         const int32_t *__restrict__ slots,
+                                                         int num_tokens, int kv_heads,
+                                                         int page_size, int num_slots)
+{
+    constexpr int D = 32 * E;
+    const int lane = threadIdx.x & 31;
+    const long long vectors = static_cast<long long>(num_tokens) * kv_heads;
+    const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         w < vectors; w += step) {
+        const int t = static_cast<int>(w / kv_heads);
+        const int g = static_cast<int>(w - static_cast<long long>(t) * kv_heads);
+        const int slot = __ldg(slots + t);
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {
+            if (lane == 0 && g == 0)
+                atomicOr(&g_store_errors, kErrSlotRange);
+            continue;
+        }
+        const size_t src = static_cast<size_t>(w) * D + lane * E;
+        const size_t dst = (static_cast<size_t>(slot) * kv_heads + g) * D + lane * E;
+        const int page = slot / page_size;
+        const size_t sidx = (static_cast<size_t>(page) * kv_heads + g) * page_size +
+                            (slot - page * page_size);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const __nv_bfloat16 *x = (which == 0 ? k_new : v_new) + src;
+            float f[E];
+            float m = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                f[e] = __bfloat162float(x[e]);
+                m = fmaxf(m, fabsf(f[e]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            const float scale = __fdiv_rn(m, 127.0f);
+            uint32_t packed = 0;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                int c = 0;
+                if (scale != 0.0f)
+                    c = max(-127, min(127, __float2int_rn(__fdiv_rn(f[e], scale))));
+                packed |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+            }
+            int8_t *codes = (which == 0 ? k_codes : v_codes) + dst;
+            if (E == 4)
+                *reinterpret_cast<uint32_t *>(codes) = packed;
+            else
+                *reinterpret_cast<uint16_t *>(codes) = static_cast<uint16_t>(packed);
+            if (lane == 0)
+                (which == 0 ? k_scales : v_scales)[sidx] = scale;
+        }
+    }
+}
+
 // Copy-on-write: whole pages of both pools, src_pages[i] -> dst_pages[i].  chunks = 16-byte
 // chunks per page (page_size * kv_heads * head_dim * 2 / 16); a grid-stride loop over
 // (copy, chunk), so consecutive threads stream consecutive bytes of one page.
@@ -185,6 +255,33 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
         static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
         num_tokens, chunks, num_slots);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                              int kv_heads, int head_dim, int page_size, int num_slots,
+                              const void *k_new, const void *v_new, const int32_t *slots,
+                              int num_tokens, cudaStream_t stream)
+{
+    if (num_tokens == 0)
+        return cudaSuccess;
+    const long long vectors = static_cast<long long>(num_tokens) * kv_heads;
+    const int threads = 256;
+    const long long wanted = (vectors + 7) / 8;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    const int blocks = static_cast<int>(wanted < cap ? wanted : cap);
+    auto *kc = static_cast<int8_t *>(k_codes);
+    auto *vc = static_cast<int8_t *>(v_codes);
+    auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
+    auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
+    if (head_dim == 128)
+        store_int8_kernel<4><<<blocks, threads, 0, stream>>>(kc, vc, k_scales, v_scales, kn, vn,
+                                                             slots, num_tokens, kv_heads,
+                                                             page_size, num_slots);
+    else
+        store_int8_kernel<2><<<blocks, threads, 0, stream>>>(kc, vc, k_scales, v_scales, kn, vn,
+                                                             slots, num_tokens, kv_heads,
+                                                             page_size, num_slots);
     return cudaGetLastError();
 }
 

@@ -28,7 +28,8 @@ KVC_ERR_OUT_OF_RANGE = 6
 EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store",
            "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
-           "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages")
+           "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
+           "kvc_decode_int8", "kvc_decode_int8_plan")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -96,6 +97,15 @@ def lib() -> ctypes.CDLL:
                                                         ctypes.POINTER(sz)]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.kvc_store_int8.restype = ctypes.c_int
+            L.kvc_store_int8.argtypes = [p, p, p, p, PoolDesc, p, p, p, i32, p]
+            L.kvc_decode_int8_plan.restype = ctypes.c_int
+            L.kvc_decode_int8_plan.argtypes = [i32, i32, PoolDesc, i32, i32,
+                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                               ctypes.POINTER(sz)]
+            L.kvc_decode_int8.restype = ctypes.c_int
+            L.kvc_decode_int8.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, i32, i32,
+                                          i32, f, i32, p, sz, p]
             L.kvc_copy_pages.restype = ctypes.c_int
             L.kvc_copy_pages.argtypes = [p, p, PoolDesc, p, p, i32, p]
             L.kvc_validate_workspace_size.restype = ctypes.c_int
@@ -174,6 +184,66 @@ def kvc_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
     _check("kvc_store", lib().kvc_store(
         _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool), _ptr(k_new), _ptr(v_new),
         _ptr(slot_mapping), int(slot_mapping.shape[0]), _stream(stream)))
+
+
+def int8_pool_desc(k_codes: torch.Tensor) -> PoolDesc:
+    """Descriptor of a [num_pages, page_size, kv_heads, head_dim] int8 code pool."""
+    if k_codes.dim() != 4 or k_codes.dtype != torch.int8:
+        raise ValueError("INT8 codes are an int8 [num_pages, page_size, kv_heads, head_dim]")
+    n, p, h, d = (int(x) for x in k_codes.shape)
+    return PoolDesc(n, p, h, d)
+
+
+def _int8_pools(k_codes, v_codes, k_scales, v_scales):
+    pool = int8_pool_desc(k_codes)
+    for name, t, dt in (("k_codes", k_codes, torch.int8), ("v_codes", v_codes, torch.int8),
+                        ("k_scales", k_scales, torch.float32),
+                        ("v_scales", v_scales, torch.float32)):
+        _cuda(name, t, dt)
+    want = (pool.num_pages, pool.kv_heads, pool.page_size)
+    if tuple(k_scales.shape) != want or tuple(v_scales.shape) != want:
+        raise ValueError(f"scales are [num_pages, kv_heads, page_size] = {want}")
+    return pool
+
+
+def kvc_store_int8(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch.Tensor,
+                   v_scales: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   slot_mapping: torch.Tensor, stream=None) -> None:
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+    _cuda("k_new", k_new, torch.bfloat16)
+    _cuda("v_new", v_new, torch.bfloat16)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    _check("kvc_store_int8", lib().kvc_store_int8(
+        _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), pool, _ptr(k_new),
+        _ptr(v_new), _ptr(slot_mapping), int(slot_mapping.numel()), _stream(stream)))
+
+
+def kvc_decode_int8_plan(num_seqs: int, q_heads: int, pool: PoolDesc, max_ctx: int,
+                         num_splits: int = 0) -> Tuple[int, int, int]:
+    """(splits, chunk, workspace_bytes) that kvc_decode_int8 will use."""
+    splits, chunk, ws = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    _check("kvc_decode_int8_plan", lib().kvc_decode_int8_plan(
+        int(num_seqs), int(q_heads), pool, int(max_ctx), int(num_splits), ctypes.byref(splits),
+        ctypes.byref(chunk), ctypes.byref(ws)))
+    return splits.value, chunk.value, ws.value
+
+
+def kvc_decode_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
+                    v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                    block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
+                    scale: float = 0.0, num_splits: int = 0,
+                    workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("kvc_decode_int8", lib().kvc_decode_int8(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+        _ptr(v_scales), pool, _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
+        int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
+        int(num_splits), _ptr(workspace), ws, _stream(stream)))
 
 
 def kvc_copy_pages(k_pool: torch.Tensor, v_pool: torch.Tensor, src_pages: torch.Tensor,

@@ -1,0 +1,129 @@
+"""INT8 pages on the GPU against the oracle (TileInfer.jl "KV cache", section "INT8 cache").
+
+The cached positions of a seeded bf16 case are quantised into INT8 pages by the oracle; every
+slot that holds no position keeps random codes and a NaN scale (so a masked position that
+leaked into a sum would show).  The new tokens are then quantised and stored by
+kvc_store_int8 (codes and scales bit-exact against the oracle's store) and kvc_decode_int8
+attends over the pages (within the attention tolerance of the oracle's fp64 attention over
+scale * code)."""
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_kvc_store_gb300 as kvc
+from harness import assert_attention_close, out_to_f64, sample_seqs
+from oracle import oracle
+from workloads import build_case, config_case
+from workloads.device import bf16_tensor, i32_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def int8_pages(case, seed=0):
+    """INT8 pools holding the case's cached positions (every live position except the new
+    tokens'), poisoned elsewhere: random codes, NaN scales."""
+    rng = np.random.default_rng(seed)
+    pages, P, H, D = case.k_pool.shape
+    kc = rng.integers(-128, 128, size=(pages, P, H, D)).astype(np.int8)
+    vc = rng.integers(-128, 128, size=(pages, P, H, D)).astype(np.int8)
+    ks = np.full((pages, H, P), np.nan, np.float32)
+    vs = np.full((pages, H, P), np.nan, np.float32)
+    slots = []
+    for s in range(case.num_seqs):
+        q_len = case.q_indptr[s + 1] - case.q_indptr[s]
+        for p in range(case.context_lens[s] - q_len):
+            slots.append(oracle.slot_of_position(case.block_table, s, p, P))
+    slots = np.array(slots, dtype=np.int64)
+    flat_k = case.k_pool.reshape(pages * P, H, D)
+    flat_v = case.v_pool.reshape(pages * P, H, D)
+    oracle.store_int8(kc, vc, ks, vs, flat_k[slots], flat_v[slots], slots)
+    return kc, vc, ks, vs
+
+
+def run_int8(case, num_splits=0, out_dtype=torch.float32):
+    kc, vc, ks, vs = int8_pages(case)
+    dev = dict(kc=torch.from_numpy(kc).cuda(), vc=torch.from_numpy(vc).cuda(),
+               ks=torch.from_numpy(ks).cuda(), vs=torch.from_numpy(vs).cuda())
+    bt, ctx = i32_tensor(case.block_table, "cuda"), i32_tensor(case.context_lens, "cuda")
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device="cuda")
+    kvc.kvc_slot_mapping(slots, bt, ctx, None, case.page_size)
+    kvc.kvc_store_int8(dev["kc"], dev["vc"], dev["ks"], dev["vs"],
+                       bf16_tensor(case.k_new, "cuda"), bf16_tensor(case.v_new, "cuda"), slots)
+    oracle.store_int8(kc, vc, ks, vs, case.k_new, case.v_new,
+                      slots.cpu().numpy().astype(np.int64))
+    assert np.array_equal(dev["kc"].cpu().numpy(), kc), "K codes differ from the oracle's"
+    assert np.array_equal(dev["vc"].cpu().numpy(), vc), "V codes differ from the oracle's"
+    for name, ref in (("ks", ks), ("vs", vs)):
+        got = dev[name].cpu().numpy()
+        assert np.array_equal(np.isnan(got), np.isnan(ref)), f"{name}: NaN pattern"
+        assert np.array_equal(got[~np.isnan(ref)], ref[~np.isnan(ref)]), f"{name} differs"
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=out_dtype,
+                      device="cuda")
+    pool = kvc.int8_pool_desc(dev["kc"])
+    _, _, ws = kvc.kvc_decode_int8_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
+                                        num_splits)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    kvc.kvc_decode_int8(out, bf16_tensor(case.q, "cuda"), dev["kc"], dev["vc"], dev["ks"],
+                        dev["vs"], bt, ctx, case.max_ctx, num_splits=num_splits, workspace=work)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    return out, (kc, vc, ks, vs)
+
+
+def oracle_int8(case, pools, seqs=None):
+    kc, vc, ks, vs = pools
+    if seqs is None:
+        seqs = np.arange(case.num_seqs)
+    ind = np.arange(len(seqs) + 1, dtype=np.int32)
+    ref, _ = oracle.attention_int8(case.q[seqs], kc, vc, ks, vs, case.block_table[seqs],
+                                   case.context_lens[seqs], ind, num_threads=16)
+    return ref
+
+
+@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_int8_decode_ragged(P, G):
+    case = build_case(700 + P + G, name="int8", page_size=P, q_heads=2 * G, kv_heads=2,
+                      head_dim=128, context_lens=lambda rng: rng.integers(1, 700, size=24),
+                      q_lens=lambda ctx: np.ones_like(ctx))
+    for splits in (1, 3, 0):
+        out, pools = run_int8(case, num_splits=splits)
+        assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
+                               f"INT8 decode P={P} G={G} splits={splits}")
+
+
+def test_int8_decode_batched_workload():
+    """The batched-decode workload (64 sequences, ctx U[512, 4096], 32/8 heads, D 128, P 16)
+    on INT8 pages, bf16 output, checked on sampled sequences."""
+    case = config_case(2)
+    out, pools = run_int8(case, out_dtype=torch.bfloat16)
+    seqs = sample_seqs(case.num_seqs, 12)
+    assert_attention_close(out_to_f64(out)[seqs], oracle_int8(case, pools, seqs),
+                           "INT8 batched decode")
+
+
+def test_int8_head_dim_64_is_refused():
+    case = config_case(1)   # head_dim 64
+    kc = torch.zeros(case.num_pages, case.page_size, case.kv_heads, 64, dtype=torch.int8,
+                     device="cuda")
+    sc = torch.zeros(case.num_pages, case.kv_heads, case.page_size, device="cuda")
+    out = torch.empty(case.num_seqs, case.q_heads, 64, device="cuda")
+    with pytest.raises(kvc.KvcError, match="UNSUPPORTED"):
+        kvc.kvc_decode_int8(out, bf16_tensor(case.q, "cuda"), kc, kc, sc, sc,
+                            i32_tensor(case.block_table, "cuda"),
+                            i32_tensor(case.context_lens, "cuda"), case.max_ctx)
+
+
+def test_int8_single_position_is_its_stored_vector():
+    case = build_case(77, name="one", page_size=16, q_heads=4, kv_heads=2, head_dim=128,
+                      context_lens=lambda rng: np.array([1, 1, 2]),
+                      q_lens=lambda ctx: np.ones_like(ctx))
+    out, (kc, vc, ks, vs) = run_int8(case)
+    for s in (0, 1):
+        slot = oracle.slot_of_position(case.block_table, s, 0, 16)
+        page, off = divmod(slot, 16)
+        for h in range(case.q_heads):
+            g = h // 2
+            want = vs[page, g, off] * vc[page, off, g].astype(np.float64)
+            # the probability 1 times the value scale enters the PV product as bf16
+            np.testing.assert_allclose(out_to_f64(out)[s, h], want, rtol=2.0 ** -8, atol=1e-6)
