@@ -89,10 +89,28 @@ def slot_mapping(block_table, context_lens, q_indptr, page_size: int) -> np.ndar
     return out
 
 
-def store(k_pool, v_pool, k_new, v_new, slots) -> None:
-    """In place on k_pool / v_pool (uint16 bf16 bit patterns, [pages, P, Hkv, D])."""
+def hnd_to_nhd(pool):
+    """A pool in the HND layout [pages, Hkv, P, D] (TileInfer.jl "KV cache", "Pages and block
+    tables": its Julia (head_dim, page_size, kv_heads, num_pages) array, column-major) as the
+    same values in the NHD layout [pages, P, Hkv, D].  Layout only: no value changes."""
+    return np.ascontiguousarray(pool.transpose(0, 2, 1, 3))
+
+
+def nhd_to_hnd(pool):
+    return np.ascontiguousarray(pool.transpose(0, 2, 1, 3))
+
+
+def store(k_pool, v_pool, k_new, v_new, slots, layout: str = "nhd") -> None:
+    """In place on k_pool / v_pool (uint16 bf16 bit patterns, [pages, P, Hkv, D], or
+    [pages, Hkv, P, D] with layout "hnd")."""
     assert k_pool.dtype == np.uint16 and k_pool.flags.c_contiguous
     assert v_pool.dtype == np.uint16 and v_pool.flags.c_contiguous
+    if layout == "hnd":
+        kp, vp = hnd_to_nhd(k_pool), hnd_to_nhd(v_pool)
+        store(kp, vp, k_new, v_new, slots)
+        k_pool[...] = nhd_to_hnd(kp)
+        v_pool[...] = nhd_to_hnd(vp)
+        return
     kn = _c(k_new, np.uint16)
     vn = _c(v_new, np.uint16)
     sl = _c(slots, np.int64)
@@ -165,8 +183,11 @@ def copy_pages(k_pool, v_pool, src_pages, dst_pages) -> None:
 
 
 def attention(q, k_pool, v_pool, block_table, context_lens, q_indptr, scale=None,
-              key_lo=None, key_hi=None, num_threads: int = 1):
-    """fp64 paged attention; returns (out [T, Hq, D] float64, lse [T, Hq] float64)."""
+              key_lo=None, key_hi=None, num_threads: int = 1, layout: str = "nhd"):
+    """fp64 paged attention; returns (out [T, Hq, D] float64, lse [T, Hq] float64).  Pools
+    are NHD [pages, P, Hkv, D], or HND [pages, Hkv, P, D] with layout "hnd"."""
+    if layout == "hnd":
+        k_pool, v_pool = hnd_to_nhd(k_pool), hnd_to_nhd(v_pool)
     q = _c(q, np.uint16)
     kp = _c(k_pool, np.uint16)
     vp = _c(v_pool, np.uint16)

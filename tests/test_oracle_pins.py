@@ -410,3 +410,39 @@ def test_slot_mapping_marks_tokens_without_a_position_as_padding():
     bt = np.array([[3, 0, 5, 0]], dtype=np.int32)
     slots = oracle.slot_mapping(bt, np.array([1]), np.array([0, 3]), 4)
     assert slots.tolist() == [-1, -1, 12]
+
+
+def test_hnd_layout_address_rule():
+    """HND pools (TileInfer.jl's (head_dim, page_size, kv_heads, num_pages) column-major array):
+    the worked addresses of tests/golden/hnd_layout.txt, and the oracle's layout conversion
+    puts every value at its NHD address."""
+    P, H, D, pages = 4, 2, 3, 3
+    hnd = np.arange(pages * H * P * D, dtype=np.uint16).reshape(pages, H, P, D)
+    nhd = oracle.hnd_to_nhd(hnd)
+    for line in golden_lines("hnd_layout.txt"):
+        p, h, o, d, flat_hnd, flat_nhd = (int(v) for v in line.split(" | "))
+        assert hnd.reshape(-1)[flat_hnd] == hnd[p, h, o, d]
+        assert nhd.reshape(-1)[flat_nhd] == hnd[p, h, o, d]
+    assert np.array_equal(oracle.nhd_to_hnd(nhd), hnd)
+
+
+def test_hnd_store_and_attention_match_nhd():
+    """The same logical cache in either layout: the store writes the same values and
+    attention gives bit-identical fp64 results."""
+    from workloads import build_case
+
+    case = build_case(51, name="hnd", page_size=16, q_heads=8, kv_heads=2, head_dim=64,
+                      context_lens=lambda rng: rng.integers(1, 90, size=6),
+                      q_lens=lambda ctx: np.minimum(ctx, 3))
+    slots = oracle.slot_mapping(case.block_table, case.context_lens, case.q_indptr,
+                                case.page_size)
+    k_n, v_n = case.k_pool.copy(), case.v_pool.copy()
+    oracle.store(k_n, v_n, case.k_new, case.v_new, slots)
+    k_h, v_h = oracle.nhd_to_hnd(case.k_pool), oracle.nhd_to_hnd(case.v_pool)
+    oracle.store(k_h, v_h, case.k_new, case.v_new, slots, layout="hnd")
+    assert np.array_equal(oracle.hnd_to_nhd(k_h), k_n)
+    assert np.array_equal(oracle.hnd_to_nhd(v_h), v_n)
+    a_n = oracle.attention(case.q, k_n, v_n, case.block_table, case.context_lens, case.q_indptr)
+    a_h = oracle.attention(case.q, k_h, v_h, case.block_table, case.context_lens, case.q_indptr,
+                           layout="hnd")
+    assert np.array_equal(a_n[0], a_h[0]) and np.array_equal(a_n[1], a_h[1], equal_nan=True)
