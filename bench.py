@@ -362,6 +362,34 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     }
     del d, out, work, slots, kc, vc, ks, vs, all_slots
     torch.cuda.empty_cache()
+    # HND pools (one contiguous block per page and kv head): the batched-decode batch
+    case = config_case(2, seed=rank_seed(2, rank))
+    d = to_device(case, dev)
+    kh = d.k_pool.permute(0, 2, 1, 3).contiguous()
+    vh = d.v_pool.permute(0, 2, 1, 3).contiguous()
+    del d.k_pool, d.v_pool
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+    kvc.kvc_store(kh, vh, d.k_new, d.v_new, slots, layout="hnd")
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    pool = kvc.pool_desc(kh, "hnd")
+    splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        t = time_graph(torch, lambda: kvc.kvc_decode(
+            out, d.q, kh, vh, d.block_table, d.context_lens, case.max_ctx, num_splits=0,
+            workspace=work, layout="hnd"), stream, flush, args.leg_steps)
+    b = decode_bytes(case)
+    legs["hnd_decode"] = {
+        "workload": "batched decode on HND pools: 64 seqs, ctx U[512,4096], 32/8 heads, D 128, "
+                    "P 16",
+        "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
+        "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
+        "gpu_launches_per_step": 2 if splits > 1 else 1,
+    }
+    del d, out, work, slots, kh, vh
+    torch.cuda.empty_cache()
     # copy-on-write page copies: 4,096 pages of P 16 x 8 kv heads x D 128 (32 KB per pool)
     # from one half of a 16,384-page pool to shuffled pages of the other half
     n_pages, n_copy = 16384, 4096

@@ -11,7 +11,9 @@
  * ----------------------------------------
  * Pools.  One K pool and one V pool per layer, each bf16 [num_pages][page_size][kv_heads]
  *   [head_dim], row-major (the (position, kv head) vector is head_dim contiguous values).
- *   Viewed by slot it is [num_pages * page_size][kv_heads][head_dim].
+ *   Viewed by slot it is [num_pages * page_size][kv_heads][head_dim].  pool.layout = KVC_HND
+ *   selects [num_pages][kv_heads][page_size][head_dim] instead (see kvc_layout); INT8 pages
+ *   are NHD only.
  * Address rule.  Position p (0-based) of sequence s lives in page block_table[s][p /
  *   page_size] at offset p % page_size; its slot is page * page_size + offset.
  * Block table.  int32 [num_seqs][bt_stride], row-major.  Entries past a sequence's last
@@ -63,11 +65,21 @@ typedef enum kvc_dtype {
     KVC_F32 = 1
 } kvc_dtype;
 
+typedef enum kvc_layout {
+    KVC_NHD = 0,              /* [num_pages][page_size][kv_heads][head_dim] (default)       */
+    KVC_HND = 1               /* [num_pages][kv_heads][page_size][head_dim]: one contiguous
+                                 block per (page, kv head) -- TileInfer.jl "KV cache", "Pages
+                                 and block tables", its (head_dim, page_size, kv_heads,
+                                 num_pages) column-major array; bf16 pools only             */
+} kvc_layout;
+
 typedef struct kvc_pool_desc {
     int32_t num_pages;
     int32_t page_size;        /* positions per page                                       */
     int32_t kv_heads;
     int32_t head_dim;
+    int32_t layout;           /* kvc_layout; slots (page * page_size + offset) mean the same
+                                 positions in either layout                                 */
 } kvc_pool_desc;
 
 /* Human-readable name of a status, and the reason for the last failure on this thread. */

@@ -51,7 +51,15 @@ kvc_status check_pool(const kvc_pool_desc &pool)
                     pool.page_size);
     if (static_cast<int64_t>(pool.num_pages) * pool.page_size >= (int64_t(1) << 31))
         return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
+    if (pool.layout != KVC_NHD && pool.layout != KVC_HND)
+        return fail(KVC_ERR_INVALID_ARG, "layout %d (KVC_NHD or KVC_HND)", pool.layout);
     return KVC_OK;
+}
+
+kvc_status check_nhd(const kvc_pool_desc &pool)
+{
+    return pool.layout == KVC_NHD ? KVC_OK
+                                  : fail(KVC_ERR_UNSUPPORTED, "INT8 pages are NHD only");
 }
 
 kvc_status check_group(const kvc_pool_desc &pool, int32_t q_heads)
@@ -216,6 +224,17 @@ kvc_status pool_tensor_map_halves(const void *base, const kvc_pool_desc &pool, C
     k.ptr = base;
     k.rank = 3;
     k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
+    if (pool.layout == KVC_HND) {
+        // {head_dim, offset, page * kv_heads + kv head}: box {64, page_size, 1}
+        k.dims[1] = static_cast<cuuint64_t>(pool.page_size);
+        k.dims[2] = static_cast<cuuint64_t>(pool.num_pages) * pool.kv_heads;
+        k.strides[0] = static_cast<cuuint64_t>(pool.head_dim) * 2;
+        k.strides[1] = static_cast<cuuint64_t>(pool.page_size) * pool.head_dim * 2;
+        k.box[0] = 64;
+        k.box[1] = static_cast<cuuint32_t>(pool.page_size);
+        k.box[2] = 1;
+        return tensor_map(k, out);
+    }
     k.dims[1] = static_cast<cuuint64_t>(pool.kv_heads);
     k.dims[2] = static_cast<cuuint64_t>(pool.num_pages) * pool.page_size;
     k.strides[0] = static_cast<cuuint64_t>(pool.head_dim) * 2;
@@ -255,6 +274,22 @@ kvc_status pool_tensor_map(const void *base, const kvc_pool_desc &pool, CUtensor
     MapKey k{};
     k.ptr = base;
     k.rank = 4;
+    if (pool.layout == KVC_HND) {
+        // {64 columns, offset, column half, page * kv_heads + kv head}: box {64, page_size,
+        // head_dim / 64, 1} is one contiguous (page, kv head) block, [half][row][64] in smem
+        k.dims[0] = 64;
+        k.dims[1] = static_cast<cuuint64_t>(pool.page_size);
+        k.dims[2] = static_cast<cuuint64_t>(pool.head_dim / 64);
+        k.dims[3] = static_cast<cuuint64_t>(pool.num_pages) * pool.kv_heads;
+        k.strides[0] = static_cast<cuuint64_t>(pool.head_dim) * 2;                   // row
+        k.strides[1] = 128;                                                          // half
+        k.strides[2] = static_cast<cuuint64_t>(pool.page_size) * pool.head_dim * 2;  // block
+        k.box[0] = 64;
+        k.box[1] = static_cast<cuuint32_t>(pool.page_size);
+        k.box[2] = static_cast<cuuint32_t>(pool.head_dim / 64);
+        k.box[3] = 1;
+        return tensor_map(k, out);
+    }
     k.dims[0] = 64;
     k.dims[1] = static_cast<cuuint64_t>(pool.num_pages) * pool.page_size;
     k.dims[2] = static_cast<cuuint64_t>(pool.head_dim / 64);
@@ -417,10 +452,13 @@ kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void 
         return fail(KVC_ERR_INVALID_ARG, "pools and new K/V must be 16-byte aligned");
     if (static_cast<int64_t>(pool.num_pages) * pool.page_size >= (int64_t(1) << 31))
         return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
+    if (pool.layout != KVC_NHD && pool.layout != KVC_HND)
+        return fail(KVC_ERR_INVALID_ARG, "layout %d (KVC_NHD or KVC_HND)", pool.layout);
     cudaError_t err = kvc::launch_store(k_pool, v_pool, pool.kv_heads, pool.head_dim,
                                         pool.num_pages * pool.page_size, k_new,
                                         v_new, slot_mapping, num_tokens,
-                                        static_cast<cudaStream_t>(stream));
+                                        static_cast<cudaStream_t>(stream),
+                                        pool.layout == KVC_HND, pool.page_size);
     return err == cudaSuccess ? ok() : cuda_fail(err, "store launch");
 }
 
@@ -448,7 +486,7 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
                           const int32_t *slot_mapping, int32_t num_tokens, void *stream)
 {
     kvc_status st = check_pool(pool);
-    if (st != KVC_OK)
+    if (st != KVC_OK || (st = check_nhd(pool)) != KVC_OK)
         return st;
     if (num_tokens < 0)
         return fail(KVC_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
@@ -481,6 +519,8 @@ kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const vo
     if (pool.head_dim != 128)
         return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
                     pool.head_dim);
+    if ((st = check_nhd(pool)) != KVC_OK)
+        return st;
     if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
         return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
     if (num_splits < 0)
@@ -622,6 +662,7 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
     l.chunk = p.chunk;
     l.n_split = p.splits;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    l.hnd = pool.layout == KVC_HND;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = kvc::launch_decode(l, tk, tv, s);
     if (err != cudaSuccess)
@@ -726,6 +767,7 @@ kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
         p.n_split = g.n_prefix;
         p.split_stride = g.stride;
         p.scale = sc;
+        p.hnd = pool.layout == KVC_HND;
         if ((err = kvc::launch_grouped_prefix(p, tk, tv, s)) != cudaSuccess)
             return cuda_fail(err, "grouped prefix launch");
     }
@@ -749,6 +791,7 @@ kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
     l.key_start = key_start;
     l.split_base = g.n_prefix;
     l.split_stride = g.stride;
+    l.hnd = pool.layout == KVC_HND;
     if ((err = kvc::launch_decode(l, tk, tv, s)) != cudaSuccess)
         return cuda_fail(err, "suffix decode launch");
     if ((err = kvc::launch_merge(out, l.out_f32, part_o, part_lse, num_seqs * q_heads, g.stride,
@@ -822,6 +865,7 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
     l.head_dim = pool.head_dim;
     l.page_size = pool.page_size;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    l.hnd = pool.layout == KVC_HND;
     cudaError_t err = kvc::launch_append_tc(l, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");
 }

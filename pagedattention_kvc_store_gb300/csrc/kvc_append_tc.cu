@@ -81,6 +81,7 @@ struct Args {
     const int32_t *context_lens;
     int kv_heads, q_heads, group, page_size, pairs_per_seq, num_items;
     float scale_log2;
+    int hnd;   // HND pools: half boxes addressed by (offset, page * kv_heads + kv head)
 };
 
 enum BarIndex : int {
@@ -291,9 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int h = lane % kHalves;
                     const int page =
                         __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
+                    // NHD maps {head_dim, kv head, slot}; HND maps {head_dim, offset, block}
                     if (i < np)
-                        tma_load_3d(dst + h * kBN * 128 + i * P * 128, map, h * 64, x.kvh,
-                                    page * P, &bars[kBarKvFull + st], policy);
+                        tma_load_3d(dst + h * kBN * 128 + i * P * 128, map, h * 64,
+                                    a.hnd ? 0 : x.kvh, a.hnd ? page * a.kv_heads + x.kvh : page * P,
+                                    &bars[kBarKvFull + st], policy);
                 }
             }
             if (!ok)
@@ -690,6 +693,7 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     a.q_heads = l.q_heads;
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
+    a.hnd = l.hnd ? 1 : 0;
     const int tiles = (l.max_q_len * a.group + kM - 1) / kM;
     a.pairs_per_seq = (tiles + 1) / 2;
     const long long items = static_cast<long long>(a.pairs_per_seq) * l.kv_heads * l.num_seqs;

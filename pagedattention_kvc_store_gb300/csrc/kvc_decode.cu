@@ -63,11 +63,12 @@ struct Args {
     int bt_stride;
     const int32_t *context_lens;
     const int32_t *key_start;   // optional [S]: positions below it are another kernel's
-    int q_heads, group, page_size;
+    int q_heads, kv_heads, group, page_size;
     int chunk, n_split;
     int split_base, split_stride;   // partial j of this launch is split split_base + j of
                                     // split_stride per row
     float scale_log2;
+    int hnd;                        // HND pools: page boxes addressed by (page, kv head) block
 };
 
 __device__ __forceinline__ void store_out(void *out, int out_f32, size_t idx, float v)
@@ -178,10 +179,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
             if (i < np) {
                 const int off = i * P * D * 2;
+                // NHD maps {64, slot, half, kv head}; HND maps {64, offset, half, block}
+                const int c1 = a.hnd ? 0 : page * P;
+                const int c3 = a.hnd ? page * a.kv_heads + kvh : kvh;
                 if (lane & 1)
-                    tma_load_4d_hint(vdst + off, &tmap_v, 0, page * P, 0, kvh, &full[st], policy);
+                    tma_load_4d_hint(vdst + off, &tmap_v, 0, c1, 0, c3, &full[st], policy);
                 else
-                    tma_load_4d_hint(kdst + off, &tmap_k, 0, page * P, 0, kvh, &full[st], policy);
+                    tma_load_4d_hint(kdst + off, &tmap_k, 0, c1, 0, c3, &full[st], policy);
             }
             issued = b + 1;
         }
@@ -415,6 +419,8 @@ cudaError_t launch_decode_t(const DecodeLaunch &l, const CUtensorMap &tk, const 
     a.context_lens = l.context_lens;
     a.key_start = l.key_start;
     a.q_heads = l.q_heads;
+    a.kv_heads = l.kv_heads;
+    a.hnd = l.hnd ? 1 : 0;
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
     a.chunk = l.chunk;

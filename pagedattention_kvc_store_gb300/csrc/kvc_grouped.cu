@@ -53,9 +53,10 @@ struct Args {
     const int32_t *group_indptr;
     const int32_t *group_seqs;
     const int32_t *prefix_len;
-    int q_heads, group, page_size;
+    int q_heads, kv_heads, group, page_size;
     int chunk, split_stride;
     float scale_log2;
+    int hnd;   // HND pools: page boxes addressed by (page, kv head) block
 };
 
 __global__ void grouped_setup_kernel(float *__restrict__ part_lse, int32_t *__restrict__ key_start,
@@ -173,10 +174,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
             if (i < np) {
                 const int off = i * P * D * 2;
+                // NHD maps {64, slot, half, kv head}; HND maps {64, offset, half, block}
+                const int c1 = a.hnd ? 0 : page * P;
+                const int c3 = a.hnd ? page * a.kv_heads + kvh : kvh;
                 if (lane & 1)
-                    tma_load_4d_hint(vdst + off, &tmap_v, 0, page * P, 0, kvh, &full[st], policy);
+                    tma_load_4d_hint(vdst + off, &tmap_v, 0, c1, 0, c3, &full[st], policy);
                 else
-                    tma_load_4d_hint(kdst + off, &tmap_k, 0, page * P, 0, kvh, &full[st], policy);
+                    tma_load_4d_hint(kdst + off, &tmap_k, 0, c1, 0, c3, &full[st], policy);
             }
             issued = b + 1;
         }
@@ -403,6 +407,8 @@ cudaError_t launch_t(const GroupedPrefixLaunch &l, const CUtensorMap &tk, const 
     a.group_seqs = l.group_seqs;
     a.prefix_len = l.prefix_len;
     a.q_heads = l.q_heads;
+    a.kv_heads = l.kv_heads;
+    a.hnd = l.hnd ? 1 : 0;
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
     a.chunk = l.chunk;

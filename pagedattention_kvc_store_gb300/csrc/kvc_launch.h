@@ -25,6 +25,7 @@ struct DecodeLaunch {
     const int32_t *key_start = nullptr;
     int split_base = 0;
     int split_stride = 0;   // 0: n_split
+    bool hnd = false;       // pools in the HND layout (the tensor maps follow it too)
 };
 
 // Decode over INT8 pages (head_dim 128): codes like a bf16 pool, scales [pages][Hkv][P].
@@ -61,6 +62,7 @@ struct GroupedPrefixLaunch {
     int num_seqs, q_heads, kv_heads, head_dim, page_size;
     int chunk, n_split, split_stride;
     float scale;
+    bool hnd = false;
 };
 
 struct AppendLaunch {
@@ -73,6 +75,7 @@ struct AppendLaunch {
     const int32_t *context_lens;
     int num_seqs, num_tokens, max_q_len, q_heads, kv_heads, head_dim, page_size;
     float scale;
+    bool hnd = false;
 };
 
 // kvc_validate: the smallest offending index of each check (INT32_MAX when it passed), then two
@@ -93,7 +96,8 @@ cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int 
                                 cudaStream_t stream);
 cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
                          int num_slots, const void *k_new, const void *v_new,
-                         const int32_t *slots, int num_tokens, cudaStream_t stream);
+                         const int32_t *slots, int num_tokens, cudaStream_t stream,
+                         bool hnd = false, int page_size = 1);
 cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
                               int kv_heads, int head_dim, int page_size, int num_slots,
                               const void *k_new, const void *v_new, const int32_t *slots,

@@ -72,13 +72,18 @@ __device__ __forceinline__ uint4 load_streaming(const uint4 *p)
 }
 
 // chunks = kv_heads * head_dim * 2 / 16 per token row.
+// HND pools (hnd = true): the chunk's kv head h = c / row_chunks is its own block per page,
+// [page][h][offset][head_dim], so the destination is ((page * Hkv + h) * P + offset) rows of
+// head_dim values.
 __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
                                                     uint4 *__restrict__ v_pool,
                                                     const uint4 *__restrict__ k_new,
                                                     const uint4 *__restrict__ v_new,
                                                     const int32_t *__restrict__ slots,
-                                                    int num_tokens, int chunks, int num_slots)
+                                                    int num_tokens, int chunks, int num_slots,
+                                                    bool hnd, int kv_heads, int page_size)
 {
+    const int row_chunks = chunks / kv_heads;   // 16-byte chunks of one head_dim vector
     const size_t total = static_cast<size_t>(num_tokens) * chunks;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -93,7 +98,14 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
                 atomicOr(&g_store_errors, kErrSlotRange);
             continue;
         }
-        const size_t dst = static_cast<size_t>(slot) * chunks + c;
+        size_t dst = static_cast<size_t>(slot) * chunks + c;
+        if (hnd) {
+            const int page = slot / page_size;
+            const int h = c / row_chunks;
+            dst = ((static_cast<size_t>(page) * kv_heads + h) * page_size + (slot - page * page_size)) *
+                      row_chunks +
+                  (c - h * row_chunks);
+        }
         const uint4 kv = load_streaming(k_new + i);
         const uint4 vv = load_streaming(v_new + i);
         k_pool[dst] = kv;
@@ -241,7 +253,8 @@ cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int 
 
 cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
                          int num_slots, const void *k_new, const void *v_new,
-                         const int32_t *slots, int num_tokens, cudaStream_t stream)
+                         const int32_t *slots, int num_tokens, cudaStream_t stream, bool hnd,
+                         int page_size)
 {
     if (num_tokens == 0)
         return cudaSuccess;
@@ -254,7 +267,7 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
     store_kernel<<<blocks, threads, 0, stream>>>(
         static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
-        num_tokens, chunks, num_slots);
+        num_tokens, chunks, num_slots, hnd, kv_heads, page_size);
     return cudaGetLastError();
 }
 

@@ -42,9 +42,15 @@ class KvcError(RuntimeError):
         self.status = status
 
 
+KVC_NHD = 0
+KVC_HND = 1
+LAYOUTS = {"nhd": KVC_NHD, "hnd": KVC_HND}
+
+
 class PoolDesc(ctypes.Structure):
     _fields_ = [("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("layout", ctypes.c_int32)]
 
 
 _lib = None
@@ -152,12 +158,16 @@ def _out_dtype(out: torch.Tensor) -> int:
     raise TypeError(f"out must be bfloat16 or float32, got {out.dtype}")
 
 
-def pool_desc(k_pool: torch.Tensor) -> PoolDesc:
-    """Descriptor of a [num_pages, page_size, kv_heads, head_dim] bf16 pool."""
+def pool_desc(k_pool: torch.Tensor, layout: str = "nhd") -> PoolDesc:
+    """Descriptor of a bf16 pool: [num_pages, page_size, kv_heads, head_dim] (layout "nhd")
+    or [num_pages, kv_heads, page_size, head_dim] (layout "hnd")."""
     if k_pool.dim() != 4:
-        raise ValueError("a pool is [num_pages, page_size, kv_heads, head_dim]")
-    n, P, h, d = (int(x) for x in k_pool.shape)
-    return PoolDesc(n, P, h, d)
+        raise ValueError("a pool is a 4-D tensor")
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout {layout!r}: 'nhd' or 'hnd'")
+    n, a, b, d = (int(x) for x in k_pool.shape)
+    page_size, kv_heads = (a, b) if layout == "nhd" else (b, a)
+    return PoolDesc(n, page_size, kv_heads, d, LAYOUTS[layout])
 
 
 def kvc_slot_mapping(slot_mapping: torch.Tensor, block_table: torch.Tensor,
@@ -176,13 +186,14 @@ def kvc_slot_mapping(slot_mapping: torch.Tensor, block_table: torch.Tensor,
 
 
 def kvc_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
-              v_new: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+              v_new: torch.Tensor, slot_mapping: torch.Tensor, stream=None,
+              layout: str = "nhd") -> None:
     for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_new", k_new),
                     ("v_new", v_new)):
         _cuda(name, t, torch.bfloat16)
     _cuda("slot_mapping", slot_mapping, torch.int32)
     _check("kvc_store", lib().kvc_store(
-        _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool), _ptr(k_new), _ptr(v_new),
+        _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool, layout), _ptr(k_new), _ptr(v_new),
         _ptr(slot_mapping), int(slot_mapping.shape[0]), _stream(stream)))
 
 
@@ -247,7 +258,8 @@ def kvc_decode_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
 
 
 def kvc_copy_pages(k_pool: torch.Tensor, v_pool: torch.Tensor, src_pages: torch.Tensor,
-                   dst_pages: torch.Tensor, stream=None) -> None:
+                   dst_pages: torch.Tensor, stream=None,
+                   layout: str = "nhd") -> None:
     """Copy-on-write: page dst_pages[i] of both pools receives page src_pages[i]."""
     _cuda("k_pool", k_pool, torch.bfloat16)
     _cuda("v_pool", v_pool, torch.bfloat16)
@@ -256,7 +268,8 @@ def kvc_copy_pages(k_pool: torch.Tensor, v_pool: torch.Tensor, src_pages: torch.
     if src_pages.numel() != dst_pages.numel():
         raise ValueError("src_pages and dst_pages differ in length")
     _check("kvc_copy_pages", lib().kvc_copy_pages(
-        _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool), _ptr(src_pages), _ptr(dst_pages),
+        _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool, layout), _ptr(src_pages),
+        _ptr(dst_pages),
         int(src_pages.numel()), _stream(stream)))
 
 
@@ -273,7 +286,8 @@ def kvc_decode_plan(num_seqs: int, q_heads: int, pool: PoolDesc, max_ctx: int,
 def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
                scale: float = 0.0, num_splits: int = 0,
-               workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+               workspace: Optional[torch.Tensor] = None, stream=None,
+               layout: str = "nhd") -> None:
     _cuda("out", out)
     _cuda("q", q, torch.bfloat16)
     _cuda("k_pool", k_pool, torch.bfloat16)
@@ -285,7 +299,8 @@ def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
         _cuda("workspace", workspace)
         ws_bytes = workspace.numel() * workspace.element_size()
     _check("kvc_decode", lib().kvc_decode(
-        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        pool_desc(k_pool, layout),
         _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
@@ -307,7 +322,8 @@ def kvc_merge(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Ten
 
 def kvc_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                block_table: torch.Tensor, q_indptr: torch.Tensor, context_lens: torch.Tensor,
-               max_q_len: int, max_ctx: int, scale: float = 0.0, stream=None) -> None:
+               max_q_len: int, max_ctx: int, scale: float = 0.0, stream=None,
+               layout: str = "nhd") -> None:
     _cuda("out", out)
     _cuda("q", q, torch.bfloat16)
     _cuda("k_pool", k_pool, torch.bfloat16)
@@ -316,7 +332,8 @@ def kvc_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
     _cuda("q_indptr", q_indptr, torch.int32)
     _cuda("context_lens", context_lens, torch.int32)
     _check("kvc_append", lib().kvc_append(
-        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        pool_desc(k_pool, layout),
         _ptr(block_table), int(block_table.shape[1]), _ptr(q_indptr), _ptr(context_lens),
         int(context_lens.shape[0]), int(q.shape[0]), int(max_q_len), int(max_ctx),
         int(q.shape[1]), float(scale), _stream(stream)))
@@ -325,7 +342,8 @@ def kvc_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
 def kvc_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
                        v_pool: torch.Tensor, block_table: torch.Tensor,
                        context_lens: torch.Tensor, max_ctx: int, scale: float = 0.0,
-                       num_splits: int = 0, stream=None) -> None:
+                       num_splits: int = 0, stream=None,
+                       layout: str = "nhd") -> None:
     """kvc_decode without a workspace, for callers that may not allocate device memory:
     the split partials go to scratch memory the library owns (NOALLOC_SCRATCH_BYTES on
     every GPU that loads it).  Plans needing more scratch than that raise KvcError
@@ -339,7 +357,8 @@ def kvc_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     _cuda("block_table", block_table, torch.int32)
     _cuda("context_lens", context_lens, torch.int32)
     _check("kvc_decode_noalloc", lib().kvc_decode_noalloc(
-        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        pool_desc(k_pool, layout),
         _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         int(num_splits), _stream(stream)))
@@ -360,7 +379,8 @@ def kvc_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
                              context_lens: torch.Tensor, max_ctx: int,
                              group_indptr: torch.Tensor, group_seqs: torch.Tensor,
                              prefix_len: torch.Tensor, max_group_size: int, max_prefix_len: int,
-                             workspace: torch.Tensor, scale: float = 0.0, stream=None) -> None:
+                             workspace: torch.Tensor, scale: float = 0.0, stream=None,
+                             layout: str = "nhd") -> None:
     _cuda("out", out)
     _cuda("q", q, torch.bfloat16)
     _cuda("k_pool", k_pool, torch.bfloat16)
@@ -372,7 +392,8 @@ def kvc_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
         _cuda(name, t, torch.int32)
     _cuda("workspace", workspace)
     _check("kvc_decode_shared_prefix", lib().kvc_decode_shared_prefix(
-        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool),
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        pool_desc(k_pool, layout),
         _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         _ptr(group_indptr), _ptr(group_seqs), _ptr(prefix_len), int(prefix_len.shape[0]),
