@@ -89,10 +89,12 @@ def store_bytes(case) -> int:
     return case.num_tokens * (2 * row * 2 + 8)
 
 
-def append_work(case):
+def append_work(case, int8: bool = False):
     """(bytes, flops) of one append: K/V of each sequence's visible positions read once, Q
-    read, O written; 4*D flops per (query head, visible key) pair (QK and PV)."""
-    per_pos = 2 * case.kv_heads * case.head_dim * 2
+    read, O written; 4*D flops per (query head, visible key) pair (QK and PV).  INT8 pages:
+    D one-byte codes and a 4-byte scale per cached vector."""
+    vec = case.head_dim + 4 if int8 else case.head_dim * 2
+    per_pos = 2 * case.kv_heads * vec
     q_lens = case.q_lens.astype(np.int64)
     ctx = case.context_lens.astype(np.int64)
     kv = int(ctx.sum()) * per_pos
@@ -641,7 +643,31 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "traffic": (traffic_from_profile("append_rewind_p16", "kvc_append_tc.cu")
                         if P == 16 and args.append_docs == 1000 else None),
         }
-        del d, out, slots, g1, g2
+        del g1, g2
+        # the same append over INT8 pages: every slot of the bf16 pools quantised by
+        # kvc_store_int8, then kvc_append_int8 (132 B per cached vector instead of 256)
+        pages, _, H, D = (int(x) for x in d.k_pool.shape)
+        kc = torch.empty(pages, P, H, D, dtype=torch.int8, device=dev)
+        vc = torch.empty_like(kc)
+        ks = torch.empty(pages, H, P, dtype=torch.float32, device=dev)
+        vs = torch.empty_like(ks)
+        all_slots = torch.arange(pages * P, dtype=torch.int32, device=dev)
+        kvc.kvc_store_int8(kc, vc, ks, vs, d.k_pool.view(pages * P, H, D),
+                           d.v_pool.view(pages * P, H, D), all_slots)
+        with torch.cuda.stream(stream):
+            t8 = time_graph(torch, lambda: kvc.kvc_append_int8(
+                out, d.q, kc, vc, ks, vs, d.block_table, d.q_indptr, d.context_lens,
+                case.max_q_len, case.max_ctx), stream, flush, args.append_steps) / 1e3
+        b8 = append_work(case, int8=True)[0]
+        t8_roof = max(flops / (peaks["bf16_sustained"] * 1e12), b8 / (peaks["hbm"] * 1e9))
+        result[f"p{P}"]["int8"] = {
+            "kernel": "paged_append_int8_kernel (kvc_append_int8)",
+            "ms": round(t8 * 1e3, 4), "tflops": round(flops / t8 / 1e12, 2),
+            "gbs": round(b8 / t8 / 1e9, 1), "bytes": b8,
+            "roofline_frac": round(t8_roof / t8, 4), "speedup_vs_bf16": round(t / t8, 3),
+            "gpu_launches": args.append_steps,
+        }
+        del d, out, slots, kc, vc, ks, vs, all_slots
         torch.cuda.empty_cache()
     result["workload"] = (f"rewind-append: {args.append_docs:,} docs x 50 new tokens over 300 "
                           "cached, 32 q / 8 kv heads, head_dim 128")

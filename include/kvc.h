@@ -309,6 +309,24 @@ kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const vo
                            size_t workspace_bytes, void *stream);
 
 /*
+ * kvc_append_int8 -- kvc_append over INT8 pages (same arguments and outputs; the new tokens'
+ * codes and scales must already be stored, kvc_store_int8).  The score of position p is
+ * q . k_code[p] * k_scale[p] * scale and the value it weighs is v_scale[p] * v_code[p].  The
+ * codes are exact operands of the tensor-core products (K as bf16 against the bf16 query, V
+ * as fp16); the probability times the value scale enters the PV product as fp16 and the
+ * softmax denominator sums the unrounded probabilities.  fp16's range limits value scales to
+ * 4000 (|v| up to 5.08e5): a larger one sets a kvc_device_errors bit and its results are not
+ * valid.  Positions past a sequence's context may hold any codes and NaN scales.  head_dim 128
+ * only, NHD only (others: KVC_ERR_UNSUPPORTED).
+ */
+kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
+                           const void *v_codes, const float *k_scales, const float *v_scales,
+                           kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                           const int32_t *q_indptr, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                           int32_t max_ctx, int32_t q_heads, float scale, void *stream);
+
+/*
  * kvc_copy_pages -- copy-on-write page copy ("KV Cache Management and PagedAttention", "Split
  * shared blocks when a write is needed": before a sequence writes into a page that other
  * sequences still reference, the page is copied to a new one and the writer's block-table

@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkvc.so")
 
 SOURCES = ["kvc_api.cu", "kvc_store.cu", "kvc_decode.cu", "kvc_grouped.cu", "kvc_append_tc.cu",
-           "kvc_noalloc.cu", "kvc_validate.cu", "kvc_decode_int8.cu"]
+           "kvc_noalloc.cu", "kvc_validate.cu", "kvc_decode_int8.cu",
+           "kvc_append_int8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I", INCLUDE, "-I", CSRC]

@@ -870,6 +870,60 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
     return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");
 }
 
+kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
+                           const void *v_codes, const float *k_scales, const float *v_scales,
+                           kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                           const int32_t *q_indptr, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                           int32_t max_ctx, int32_t q_heads, float scale, void *stream)
+{
+    kvc_status st = check_attention_args(out, out_dtype, q, k_codes, v_codes, pool, block_table,
+                                         bt_stride, context_lens, num_seqs, max_ctx, q_heads);
+    if (st != KVC_OK)
+        return st;
+    if (pool.head_dim != 128)
+        return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
+                    pool.head_dim);
+    if ((st = check_nhd(pool)) != KVC_OK)
+        return st;
+    if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
+        return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
+    if (num_tokens < 0 || max_q_len < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_tokens %d, max_q_len %d", num_tokens, max_q_len);
+    if (num_seqs > 0 && q_indptr == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "q_indptr is required");
+    if (static_cast<int64_t>(max_q_len) * (q_heads / pool.kv_heads) > (int64_t(1) << 30))
+        return fail(KVC_ERR_INVALID_ARG, "max_q_len too large");
+    if (num_seqs == 0 || num_tokens == 0 || max_q_len == 0)
+        return ok();
+    CUtensorMap tq, tk, tv;
+    if ((st = pool_tensor_map_int8(k_codes, pool, &tk)) != KVC_OK)
+        return st;
+    if ((st = pool_tensor_map_int8(v_codes, pool, &tv)) != KVC_OK)
+        return st;
+    if ((st = query_tensor_map(q, num_tokens, pool.kv_heads, q_heads / pool.kv_heads,
+                               pool.head_dim, &tq)) != KVC_OK)
+        return st;
+    kvc::AppendInt8Launch l;
+    l.out = out;
+    l.out_f32 = out_dtype == KVC_F32;
+    l.k_scales = k_scales;
+    l.v_scales = v_scales;
+    l.block_table = block_table;
+    l.bt_stride = bt_stride;
+    l.q_indptr = q_indptr;
+    l.context_lens = context_lens;
+    l.num_seqs = num_seqs;
+    l.num_tokens = num_tokens;
+    l.max_q_len = max_q_len;
+    l.q_heads = q_heads;
+    l.kv_heads = pool.kv_heads;
+    l.page_size = pool.page_size;
+    l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    cudaError_t err = kvc::launch_append_int8(l, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "append_int8 launch");
+}
+
 kvc_status kvc_device_errors(uint32_t *flags_out)
 {
     if (flags_out == nullptr)
@@ -886,6 +940,9 @@ kvc_status kvc_device_errors(uint32_t *flags_out)
     uint32_t f = 0;
     if (err == cudaSuccess)
         err = kvc::read_and_clear_decode_int8_errors(&f);
+    e |= f;
+    if (err == cudaSuccess)
+        err = kvc::read_and_clear_append_int8_errors(&f);
     e |= f;
     if (err != cudaSuccess)
         return cuda_fail(err, "reading the device error word");

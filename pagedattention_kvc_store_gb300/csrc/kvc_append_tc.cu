@@ -37,6 +37,7 @@
 // slots, and each tile's blocks and items), so they line up across items.
 #include <math.h>
 
+#include "kvc_append_items.cuh"
 #include "kvc_device.cuh"
 #include "kvc_launch.h"
 
@@ -46,8 +47,11 @@ namespace {
 
 __device__ uint32_t g_append_tc_errors;
 
-constexpr int kM = 128;           // rows per tile
-constexpr int kBN = 128;          // positions per K or V stage (the N of S = Q K^T)
+using append::Item;
+using append::kBN;   // positions per K or V stage (the N of S = Q K^T)
+using append::kM;    // rows per tile
+using append::seq_of;
+using append::Walker;
 constexpr int kRoleWarps = 3;     // K/V loads, MMA issue, query loads
 constexpr int kSoftmaxWarps = 8;  // two groups of four
 constexpr int kThreads = (kRoleWarps + kSoftmaxWarps) * 32;
@@ -94,100 +98,6 @@ enum BarIndex : int {
     kBarPvDone = kBarPFull + 2,             // [tile], once per item
     kBarDrain = kBarPvDone + 2,
     kBarCount
-};
-
-// One work item: tiles 2 tp and 2 tp + 1 of one (sequence, kv head).
-struct Item {
-    int s, kvh, tp;
-    int tok0, q_len, ctx, rows, row_begin;   // row_begin: first row of tile 2 tp
-    bool has_b;                              // tile 2 tp + 1 exists
-    int n_keys, n_blocks;                    // positions the item's later tile sees
-};
-
-// The fields of item `it` from its sequence's query offsets and context length (no loads).
-__device__ __forceinline__ bool make_item(const Args &a, int it, int tok0, int tok1, int ctx,
-                                          Item &x)
-{
-    x.tp = it % a.pairs_per_seq;
-    const int rest = it / a.pairs_per_seq;
-    x.kvh = rest % a.kv_heads;
-    x.s = rest / a.kv_heads;
-    x.tok0 = tok0;
-    x.q_len = tok1 - tok0;
-    x.ctx = ctx;
-    if (x.ctx > a.bt_stride * a.page_size) {
-        if (threadIdx.x == 0)
-            atomicOr(&g_append_tc_errors, kErrContextRange);
-        x.ctx = a.bt_stride * a.page_size;
-    }
-    x.rows = x.q_len * a.group;
-    x.row_begin = x.tp * 2 * kM;
-    if (x.row_begin >= x.rows)
-        return false;
-    x.has_b = x.row_begin + kM < x.rows;
-    const int row_last = min(x.rows, x.row_begin + 2 * kM) - 1;
-    x.n_keys = min(x.ctx, x.ctx - x.q_len + row_last / a.group + 1);
-    if (x.n_keys <= 0)
-        return false;
-    x.n_blocks = (x.n_keys + kBN - 1) / kBN;
-    return true;
-}
-
-__device__ __forceinline__ int seq_of(const Args &a, int it)
-{
-    return it / a.pairs_per_seq / a.kv_heads;
-}
-
-// Walks this CTA's items: it = blockIdx.x, blockIdx.x + gridDim.x, ..., skipping empty ones.
-// A global load under a full memory pipe takes microseconds, so the metadata of the next
-// item index is requested one item ahead (its registers are read only at the next step).
-struct Walker {
-    int it;
-    bool done;
-    Item x;
-    int pit;                  // index whose metadata is in flight in p_*
-    int p_tok0, p_tok1, p_ctx;
-    __device__ __forceinline__ void prefetch(const Args &a, int idx)
-    {
-        pit = idx;
-        if (idx < a.num_items) {
-            const int s = seq_of(a, idx);
-            p_tok0 = a.q_indptr[s];
-            p_tok1 = a.q_indptr[s + 1];
-            p_ctx = a.context_lens[s];
-        }
-    }
-    __device__ __forceinline__ void next(const Args &a)
-    {
-        for (;;) {
-            it += gridDim.x;
-            if (it >= a.num_items) {
-                done = true;
-                return;
-            }
-            int tok0, tok1, ctx;
-            if (it == pit) {
-                tok0 = p_tok0;
-                tok1 = p_tok1;
-                ctx = p_ctx;
-            } else {
-                const int s = seq_of(a, it);
-                tok0 = a.q_indptr[s];
-                tok1 = a.q_indptr[s + 1];
-                ctx = a.context_lens[s];
-            }
-            if (make_item(a, it, tok0, tok1, ctx, x))
-                break;
-        }
-        prefetch(a, it + gridDim.x);
-    }
-    __device__ __forceinline__ void start(const Args &a)
-    {
-        it = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
-        done = false;
-        pit = -1;
-        next(a);
-    }
 };
 
 template <int D>
@@ -239,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t policy = l2_policy_evict_first();
         Walker w;
-        w.start(a);
+        w.start(a, &g_append_tc_errors);
         // block-table entries 0 .. 31 of the current item's sequence, one per lane, requested
         // one item ahead like the item metadata
         auto bt_head = [&](int idx) {
@@ -301,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
-            w.next(a);
+            w.next(a, &g_append_tc_errors);
         }
         if (!ok && lane == 0) {
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
@@ -315,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
             prefetch_tensormap(&tmap_q);
         Walker w;
-        w.start(a);
+        w.start(a, &g_append_tc_errors);
         int qi[2] = {0, 0};   // items whose query tile t was requested
         while (ok && !w.done) {
             const Item &x = w.x;
@@ -340,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
-            w.next(a);
+            w.next(a, &g_append_tc_errors);
         }
         if (!ok && lane == 0) {
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
@@ -380,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         Walker w;
-        w.start(a);
+        w.start(a, &g_append_tc_errors);
         int n0 = 0;             // ring index of the item's first slot
         int qi[2] = {0, 0};     // items of tile 0 / tile 1
         int tb[2] = {0, 0};     // blocks of tile 0 / tile 1
@@ -482,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < nt; ++t)
                 ++qi[t];
             n0 += 2 * nb;
-            w.next(a);
+            w.next(a, &g_append_tc_errors);
         }
         if (!ok && lane == 0)
             atomicOr(&g_append_tc_errors, kErrAppendTcWait);
@@ -503,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tmem_s = tmem + t * 256 + Geom::kColS + lane_off;
         const float sl2 = a.scale_log2;
         Walker w;
-        w.start(a);
+        w.start(a, &g_append_tc_errors);
         int tb = 0;   // blocks of this tile so far
         int ti = 0;   // items of this tile so far
-        for (; ok && !w.done; w.next(a)) {
+        for (; ok && !w.done; w.next(a, &g_append_tc_errors)) {
             const Item &x = w.x;
             if (t == 1 && !x.has_b)
                 continue;

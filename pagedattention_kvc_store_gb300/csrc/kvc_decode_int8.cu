@@ -96,21 +96,6 @@ __device__ __forceinline__ uint32_t codes_f16x2(uint32_t a, uint32_t b)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Both fp16 pairs of one word of int8 codes (codes 0, 1 and codes 2, 3), exact: the word's
-// sign bits flipped (m = code + 128), the bytes put under exponent 0x64 and 1152 subtracted.
-__device__ __forceinline__ void word_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi)
-{
-    const uint32_t m = w ^ 0x80808080u;
-    const uint32_t e = 0x64646464u;
-    const uint32_t a = __byte_perm(m, e, 0x4140u);   // [m.0, 0x64, m.1, 0x64]
-    const uint32_t b = __byte_perm(m, e, 0x4342u);   // [m.2, 0x64, m.3, 0x64]
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
-    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
-    lo = *reinterpret_cast<const uint32_t *>(&ha);
-    hi = *reinterpret_cast<const uint32_t *>(&hb);
-}
-
 // Offset of byte `col` of stage row `row` in a 128-byte-swizzled [64][128] code tile.
 __device__ __forceinline__ uint32_t code_offset(int row, int col)
 {
@@ -308,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     uint32_t b0, b1;   // codes 0, 1 and codes 2, 3 of the word
-                    word_f16x2(w[kk], b0, b1);
+                    codes_word_f16x2(w[kk], b0, b1);
                     mma_f16_16816(sc[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
                 }
             }

@@ -28,6 +28,7 @@ enum DeviceErrorBits : uint32_t {
     kErrAppendTcWait = 1u << 8,    // the tcgen05 append gave up a wait
     kErrSmemAlign = 1u << 9,       // dynamic shared memory not 1024-byte aligned: no work done
     kErrPageRange = 1u << 10,      // a page copy named a page outside the pool: skipped
+    kErrScaleRange = 1u << 11,     // INT8 append: a value scale above its fp16 limit (4000)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -221,6 +222,13 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_byte_addr, uin
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int b_mn)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with fp16 A and B (type field 0).
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int b_mn)
+{
+    return (1u << 4) | (static_cast<uint32_t>(b_mn) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -419,10 +427,117 @@ __device__ __forceinline__ float exp2_fma(float x)
     return x == -INFINITY ? 0.0f : r;
 }
 
+// Paired fp32 arithmetic of the sm_100 family: two fp32 lanes in one 64-bit register, one
+// instruction for both (round-to-nearest, like the scalar operations).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// max(a, b, c) in one instruction (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// exp2_fma on a pair, in paired arithmetic.  -inf gives 2^-125 rather than 0 (no select):
+// callers use it where a term that small is as good as 0 (a probability summed with at least
+// one term of 1, or rounded to fp16).
+__device__ __forceinline__ uint64_t exp2_fma2(uint64_t x)
+{
+    float a, b;
+    f2_unpack(x, a, b);
+    const uint64_t xc = f2_pack(fmaxf(a, -125.0f), fmaxf(b, -125.0f));
+    const uint64_t big = f2_pack(12582912.0f, 12582912.0f);
+    const uint64_t t = f2_add(xc, big);
+    const uint64_t f = f2_sub(xc, f2_sub(t, big));
+    uint64_t p = f2_fma(f2_pack(5.517132143e-2f, 5.517132143e-2f), f,
+                        f2_pack(2.426105423e-1f, 2.426105423e-1f));
+    p = f2_fma(p, f, f2_pack(6.932609856e-1f, 6.932609856e-1f));
+    p = f2_fma(p, f, f2_pack(9.999281094e-1f, 9.999281094e-1f));
+    float pa, pb, ta, tb;
+    f2_unpack(p, pa, pb);
+    f2_unpack(t, ta, tb);
+    // n sits in t's low mantissa bits; (t_bits - 0x4B400000) << 23 == t_bits << 23 (mod 2^32)
+    return f2_pack(__int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23)),
+                   __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23)));
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Both fp16 pairs of one word of int8 codes (codes 0, 1 and codes 2, 3), exact: the word's
+// sign bits flipped (m = code + 128), the bytes put under exponent 0x64 and 1152 subtracted.
+__device__ __forceinline__ void codes_word_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t m = w ^ 0x80808080u;
+    const uint32_t e = 0x64646464u;
+    const uint32_t a = __byte_perm(m, e, 0x4140u);   // [m.0, 0x64, m.1, 0x64]
+    const uint32_t b = __byte_perm(m, e, 0x4342u);   // [m.2, 0x64, m.3, 0x64]
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+// Both bf16 pairs of one word of int8 codes (codes 0, 1 and codes 2, 3), exact.  A code's low
+// seven bits m go under the exponent of 128 (bf16 128 + m: the step is 1 on [128, 256)); the
+// code is then 128 + m minus 128, or minus 256 where its sign bit is set (two's complement).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ void codes_word_bf16x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t e = 0x43434343u;
+    const uint32_t a = __byte_perm(w, e, 0x4140u);   // [c.0, 0x43, c.1, 0x43]
+    const uint32_t b = __byte_perm(w, e, 0x4342u);   // [c.2, 0x43, c.3, 0x43]
+    lo = bf16x2_sub(a & 0xFF7FFF7Fu, (a & 0x00800080u) | 0x43004300u);
+    hi = bf16x2_sub(b & 0xFF7FFF7Fu, (b & 0x00800080u) | 0x43004300u);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)

@@ -78,6 +78,19 @@ struct AppendLaunch {
     bool hnd = false;
 };
 
+// kvc_append_int8: AppendLaunch over INT8 pages (head_dim 128, NHD) plus the scale arrays.
+struct AppendInt8Launch {
+    void *out;
+    int out_f32;
+    const float *k_scales, *v_scales;   // [num_pages][kv_heads][page_size]
+    const int32_t *block_table;
+    int bt_stride;
+    const int32_t *q_indptr;
+    const int32_t *context_lens;
+    int num_seqs, num_tokens, max_q_len, q_heads, kv_heads, page_size;
+    float scale;
+};
+
 // kvc_validate: the smallest offending index of each check (INT32_MAX when it passed), then two
 // bitmaps over the pool's slots.
 constexpr int kValidateChecks = 4;
@@ -123,12 +136,17 @@ cudaError_t launch_grouped_prefix(const GroupedPrefixLaunch &a, const CUtensorMa
 cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
                              const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                              cudaStream_t stream);
+// tmap_q as for launch_append_tc; tmap_k / tmap_v are the INT8 page maps (one box per page).
+cudaError_t launch_append_int8(const AppendInt8Launch &a, const CUtensorMap &tmap_q,
+                               const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                               cudaStream_t stream);
 
 // Device error words, one per translation unit that owns bounded waits.
 cudaError_t read_and_clear_decode_errors(uint32_t *flags);
 cudaError_t read_and_clear_store_errors(uint32_t *flags);
 cudaError_t read_and_clear_append_tc_errors(uint32_t *flags);
 cudaError_t read_and_clear_grouped_errors(uint32_t *flags);
+cudaError_t read_and_clear_append_int8_errors(uint32_t *flags);
 
 // Record a failure reason for kvc_last_error() from another translation unit.
 int set_last_error(int status, const char *message);

@@ -29,7 +29,7 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
-           "kvc_decode_int8", "kvc_decode_int8_plan")
+           "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -112,6 +112,9 @@ def lib() -> ctypes.CDLL:
             L.kvc_decode_int8.restype = ctypes.c_int
             L.kvc_decode_int8.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, i32, i32,
                                           i32, f, i32, p, sz, p]
+            L.kvc_append_int8.restype = ctypes.c_int
+            L.kvc_append_int8.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, p, i32,
+                                          i32, i32, i32, i32, f, p]
             L.kvc_copy_pages.restype = ctypes.c_int
             L.kvc_copy_pages.argtypes = [p, p, PoolDesc, p, p, i32, p]
             L.kvc_validate_workspace_size.restype = ctypes.c_int
@@ -255,6 +258,25 @@ def kvc_decode_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
         _ptr(v_scales), pool, _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         int(num_splits), _ptr(workspace), ws, _stream(stream)))
+
+
+def kvc_append_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
+                    v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                    block_table: torch.Tensor, q_indptr: torch.Tensor,
+                    context_lens: torch.Tensor, max_q_len: int, max_ctx: int,
+                    scale: float = 0.0, stream=None) -> None:
+    """kvc_append over INT8 pages (codes int8 [pages, P, Hkv, D], scales fp32 [pages, Hkv, P])."""
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("q_indptr", q_indptr, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    _check("kvc_append_int8", lib().kvc_append_int8(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+        _ptr(v_scales), pool, _ptr(block_table), int(block_table.shape[1]), _ptr(q_indptr),
+        _ptr(context_lens), int(context_lens.shape[0]), int(q.shape[0]), int(max_q_len),
+        int(max_ctx), int(q.shape[1]), float(scale), _stream(stream)))
 
 
 def kvc_copy_pages(k_pool: torch.Tensor, v_pool: torch.Tensor, src_pages: torch.Tensor,

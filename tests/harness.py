@@ -98,3 +98,24 @@ def sample_seqs(n_total: int, n: int, seed: int = 0):
 
 def pools_bits(run: GpuRun):
     return bf16_bits_of(run.d.k_pool), bf16_bits_of(run.d.v_pool)
+
+
+def int8_pages(case, seed=0):
+    """INT8 pools holding the case's cached positions (every live position except the new
+    tokens'), poisoned elsewhere: random codes, NaN scales."""
+    rng = np.random.default_rng(seed)
+    pages, P, H, D = case.k_pool.shape
+    kc = rng.integers(-128, 128, size=(pages, P, H, D)).astype(np.int8)
+    vc = rng.integers(-128, 128, size=(pages, P, H, D)).astype(np.int8)
+    ks = np.full((pages, H, P), np.nan, np.float32)
+    vs = np.full((pages, H, P), np.nan, np.float32)
+    slots = []
+    for s in range(case.num_seqs):
+        q_len = case.q_indptr[s + 1] - case.q_indptr[s]
+        for p in range(case.context_lens[s] - q_len):
+            slots.append(oracle.slot_of_position(case.block_table, s, p, P))
+    slots = np.array(slots, dtype=np.int64)
+    flat_k = case.k_pool.reshape(pages * P, H, D)
+    flat_v = case.v_pool.reshape(pages * P, H, D)
+    oracle.store_int8(kc, vc, ks, vs, flat_k[slots], flat_v[slots], slots)
+    return kc, vc, ks, vs

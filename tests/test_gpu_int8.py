@@ -11,33 +11,12 @@ import pytest
 import torch
 
 import pagedattention_kvc_store_gb300 as kvc
-from harness import assert_attention_close, out_to_f64, sample_seqs
+from harness import assert_attention_close, int8_pages, out_to_f64, sample_seqs
 from oracle import oracle
 from workloads import build_case, config_case
 from workloads.device import bf16_tensor, i32_tensor
 
 pytestmark = pytest.mark.gpu
-
-
-def int8_pages(case, seed=0):
-    """INT8 pools holding the case's cached positions (every live position except the new
-    tokens'), poisoned elsewhere: random codes, NaN scales."""
-    rng = np.random.default_rng(seed)
-    pages, P, H, D = case.k_pool.shape
-    kc = rng.integers(-128, 128, size=(pages, P, H, D)).astype(np.int8)
-    vc = rng.integers(-128, 128, size=(pages, P, H, D)).astype(np.int8)
-    ks = np.full((pages, H, P), np.nan, np.float32)
-    vs = np.full((pages, H, P), np.nan, np.float32)
-    slots = []
-    for s in range(case.num_seqs):
-        q_len = case.q_indptr[s + 1] - case.q_indptr[s]
-        for p in range(case.context_lens[s] - q_len):
-            slots.append(oracle.slot_of_position(case.block_table, s, p, P))
-    slots = np.array(slots, dtype=np.int64)
-    flat_k = case.k_pool.reshape(pages * P, H, D)
-    flat_v = case.v_pool.reshape(pages * P, H, D)
-    oracle.store_int8(kc, vc, ks, vs, flat_k[slots], flat_v[slots], slots)
-    return kc, vc, ks, vs
 
 
 def run_int8(case, num_splits=0, out_dtype=torch.float32):
