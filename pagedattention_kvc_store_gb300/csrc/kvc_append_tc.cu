@@ -450,17 +450,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float mx = -INFINITY;
                     if (__all_sync(0xffffffffu, n_vis == kBN)) {
 #pragma unroll
-                        for (int j = 0; j < kBN; ++j)
-                            mx = fmaxf(mx, xs[j >> 5][j & 31]);
+                        for (int j = 0; j < kBN; j += 2)
+                            mx = fmax3(mx, xs[j >> 5][j & 31], xs[j >> 5][(j & 31) + 1]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
+                            for (int j = 0; j < 32; ++j)
                                 if (32 * c + j >= n_vis)
                                     xs[c][j] = -INFINITY;
-                                mx = fmaxf(mx, xs[c][j]);
-                            }
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2)
+                                mx = fmax3(mx, xs[c][j], xs[c][j + 1]);
                             tmem_st32(tmem_s + 32 * c, xs[c]);
                         }
                         tmem_wait_st();
@@ -488,11 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // pass 2, 32 columns at a time (a short loop body keeps the instruction
-                // footprint small): p = 2^(s * scale * log2(e) - m), every fourth column on the
-                // FMA pipe; the bf16 pairs of chunk c go to S columns [16 c, 16 c + 16), which
-                // hold only chunks already read.
+                // footprint small), in paired fp32 arithmetic: p = 2^(s * scale * log2(e) - m),
+                // one pair in four on the FMA pipe; the bf16 pairs of chunk c go to S columns
+                // [16 c, 16 c + 16), which hold only chunks already read; the sum takes the
+                // rounded bf16 values.
                 const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
-                float psum = 0.0f;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t nm2 = f2_pack(neg_mu, neg_mu);
+                uint64_t psum2 = f2_pack(0.0f, 0.0f);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
@@ -502,11 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float e0 = fast_exp2(fmaf(v[2 * j], sl2, neg_mu));
-                            const float y1 = fmaf(v[2 * j + 1], sl2, neg_mu);
-                            const float e1 = (j & 1) ? exp2_fma(y1) : fast_exp2(y1);
+                            const uint64_t y = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sl2x2, nm2);
+                            float e0, e1;
+                            if ((j & 3) == 3) {
+                                f2_unpack(exp2_fma2<true>(y), e0, e1);
+                            } else {
+                                f2_unpack(y, e0, e1);
+                                e0 = fast_exp2(e0);
+                                e1 = fast_exp2(e1);
+                            }
                             pk[j] = pack_bf16x2(e0, e1);
-                            psum += bf16x2_sum(pk[j]);
+                            psum2 = f2_add(psum2, f2_pack(__uint_as_float(pk[j] << 16),
+                                                          __uint_as_float(pk[j] & 0xFFFF0000u)));
                         }
                     } else {
 #pragma unroll
@@ -515,6 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_st16u(tmem_s + 16 * c, pk);
                 }
+                float ps0, ps1;
+                f2_unpack(psum2, ps0, ps1);
+                const float psum = ps0 + ps1;
                 l_sum = l_sum * alpha + psum;
                 tmem_wait_st();
                 tc_fence_before_sync();

@@ -477,9 +477,10 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return r;
 }
 
-// exp2_fma on a pair, in paired arithmetic.  -inf gives 2^-125 rather than 0 (no select):
-// callers use it where a term that small is as good as 0 (a probability summed with at least
-// one term of 1, or rounded to fp16).
+// exp2_fma on a pair, in paired arithmetic.  With kExactZero false, -inf gives 2^-125 rather
+// than 0 (no select): for callers where a term that small is as good as 0 (a probability summed
+// with at least one term of 1, and rounded to fp16, where it becomes 0).
+template <bool kExactZero = false>
 __device__ __forceinline__ uint64_t exp2_fma2(uint64_t x)
 {
     float a, b;
@@ -496,8 +497,13 @@ __device__ __forceinline__ uint64_t exp2_fma2(uint64_t x)
     f2_unpack(p, pa, pb);
     f2_unpack(t, ta, tb);
     // n sits in t's low mantissa bits; (t_bits - 0x4B400000) << 23 == t_bits << 23 (mod 2^32)
-    return f2_pack(__int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23)),
-                   __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23)));
+    float ra = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
+    float rb = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
+    if (kExactZero) {
+        ra = a == -INFINITY ? 0.0f : ra;
+        rb = b == -INFINITY ? 0.0f : rb;
+    }
+    return f2_pack(ra, rb);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
