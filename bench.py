@@ -666,6 +666,8 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "gbs": round(b8 / t8 / 1e9, 1), "bytes": b8,
             "roofline_frac": round(t8_roof / t8, 4), "speedup_vs_bf16": round(t / t8, 3),
             "gpu_launches": args.append_steps,
+            "traffic": (traffic_from_profile("append_int8_rewind_p16", "kvc_append_int8.cu")
+                        if P == 16 and args.append_docs == 1000 else None),
         }
         del d, out, slots, kc, vc, ks, vs, all_slots
         torch.cuda.empty_cache()

@@ -665,11 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(tmem_o + c0, o);
                     }
                 }
-                // pass 2: p = 2^(x - m) in paired arithmetic (one pair in four on the FMA
-                // pipe, the rest on MUFU); P' = p * v_scale as fp16 pairs over S columns
-                // [16 c, 16 c + 16), which hold only chunks already read.  A masked x is -inf:
-                // its p is 0 or (on the FMA pipe) 2^-125, which rounds to an fp16 P' of 0 and is
-                // nothing beside the row's p of at least 1.
+                // pass 2: p = 2^(x - m) on MUFU, the rest in paired arithmetic; P' = p * v_scale
+                // as fp16 pairs over S columns [16 c, 16 c + 16), which hold only chunks already
+                // read.  A masked x is -inf: its p is 0.
                 const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
                 const uint64_t nm2 = f2_pack(neg_mu, neg_mu);
                 uint64_t psum2 = f2_pack(0.0f, 0.0f);
@@ -685,13 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float *v8 = &v[8 * j8];
                             float e[8];
 #pragma unroll
-                            for (int q = 0; q < 3; ++q) {
+                            for (int q = 0; q < 4; ++q) {
                                 f2_unpack(f2_add(f2_pack(v8[2 * q], v8[2 * q + 1]), nm2),
                                           e[2 * q], e[2 * q + 1]);
                                 e[2 * q] = fast_exp2(e[2 * q]);
                                 e[2 * q + 1] = fast_exp2(e[2 * q + 1]);
                             }
-                            f2_unpack(exp2_fma2(f2_add(f2_pack(v8[6], v8[7]), nm2)), e[6], e[7]);
                             const float4 sa = vs4[8 * c + 2 * j8];
                             const float4 sb = vs4[8 * c + 2 * j8 + 1];
                             const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};

@@ -489,10 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // pass 2, 32 columns at a time (a short loop body keeps the instruction
-                // footprint small), in paired fp32 arithmetic: p = 2^(s * scale * log2(e) - m),
-                // one pair in four on the FMA pipe; the bf16 pairs of chunk c go to S columns
-                // [16 c, 16 c + 16), which hold only chunks already read; the sum takes the
-                // rounded bf16 values.
+                // footprint small), in paired fp32 arithmetic: p = 2^(s * scale * log2(e) - m)
+                // on MUFU (measured: moving a share of the exponentials to an FMA-pipe
+                // polynomial costs more issue slots than it saves); the bf16 pairs of chunk c go
+                // to S columns [16 c, 16 c + 16), which hold only chunks already read; the sum
+                // takes the rounded bf16 values.
                 const float neg_mu = (m_used == -INFINITY) ? 0.0f : -m_used;
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 const uint64_t nm2 = f2_pack(neg_mu, neg_mu);
@@ -506,16 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const uint64_t y = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sl2x2, nm2);
                             float e0, e1;
-                            if ((j & 3) == 3) {
-                                f2_unpack(exp2_fma2<true>(y), e0, e1);
-                            } else {
-                                f2_unpack(y, e0, e1);
-                                e0 = fast_exp2(e0);
-                                e1 = fast_exp2(e1);
-                            }
-                            pk[j] = pack_bf16x2(e0, e1);
+                            f2_unpack(f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sl2x2, nm2), e0, e1);
+                            pk[j] = pack_bf16x2(fast_exp2(e0), fast_exp2(e1));
                             psum2 = f2_add(psum2, f2_pack(__uint_as_float(pk[j] << 16),
                                                           __uint_as_float(pk[j] & 0xFFFF0000u)));
                         }

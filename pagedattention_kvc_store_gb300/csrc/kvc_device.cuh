@@ -407,26 +407,6 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
-// 2^x on the FMA pipe, for the share of a softmax's exponentials that would otherwise queue on
-// the MUFU unit.  x is rounded to the nearest integer n by adding 1.5 * 2^23 (the low mantissa
-// bits of the sum then hold n), 2^(x - n) with x - n in [-1/2, 1/2] is a cubic, and n is added
-// to the exponent field.  The cubic is a relative-error least-squares fit of 2^f on [-1/2, 1/2]
-// (Lawson-reweighted), max relative error 7.5e-5 -- far below the bf16 rounding the
-// probabilities get next.  x = -inf (a masked position) gives exactly 0; x is clamped at -125 so
-// the result stays a normal number.
-__device__ __forceinline__ float exp2_fma(float x)
-{
-    const float xc = fmaxf(x, -125.0f);
-    const float t = xc + 12582912.0f;
-    const float n = t - 12582912.0f;
-    const float f = xc - n;
-    const float p = fmaf(fmaf(fmaf(5.517132143e-2f, f, 2.426105423e-1f), f, 6.932609856e-1f), f,
-                         9.999281094e-1f);
-    const int e = (__float_as_int(t) - 0x4B400000) << 23;
-    const float r = __int_as_float(__float_as_int(p) + e);
-    return x == -INFINITY ? 0.0f : r;
-}
-
 // Paired fp32 arithmetic of the sm_100 family: two fp32 lanes in one 64-bit register, one
 // instruction for both (round-to-nearest, like the scalar operations).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
@@ -475,35 +455,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
-}
-
-// exp2_fma on a pair, in paired arithmetic.  With kExactZero false, -inf gives 2^-125 rather
-// than 0 (no select): for callers where a term that small is as good as 0 (a probability summed
-// with at least one term of 1, and rounded to fp16, where it becomes 0).
-template <bool kExactZero = false>
-__device__ __forceinline__ uint64_t exp2_fma2(uint64_t x)
-{
-    float a, b;
-    f2_unpack(x, a, b);
-    const uint64_t xc = f2_pack(fmaxf(a, -125.0f), fmaxf(b, -125.0f));
-    const uint64_t big = f2_pack(12582912.0f, 12582912.0f);
-    const uint64_t t = f2_add(xc, big);
-    const uint64_t f = f2_sub(xc, f2_sub(t, big));
-    uint64_t p = f2_fma(f2_pack(5.517132143e-2f, 5.517132143e-2f), f,
-                        f2_pack(2.426105423e-1f, 2.426105423e-1f));
-    p = f2_fma(p, f, f2_pack(6.932609856e-1f, 6.932609856e-1f));
-    p = f2_fma(p, f, f2_pack(9.999281094e-1f, 9.999281094e-1f));
-    float pa, pb, ta, tb;
-    f2_unpack(p, pa, pb);
-    f2_unpack(t, ta, tb);
-    // n sits in t's low mantissa bits; (t_bits - 0x4B400000) << 23 == t_bits << 23 (mod 2^32)
-    float ra = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
-    float rb = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
-    if (kExactZero) {
-        ra = a == -INFINITY ? 0.0f : ra;
-        rb = b == -INFINITY ? 0.0f : rb;
-    }
-    return f2_pack(ra, rb);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
