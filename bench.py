@@ -89,6 +89,15 @@ def store_bytes(case) -> int:
     return case.num_tokens * (2 * row * 2 + 8)
 
 
+def fused_work(case) -> int:
+    """Bytes of one kvc_append_store: the chunk's K/V read once and written to the pools, the
+    cached positions' K/V read, Q read, O written."""
+    row = 2 * case.kv_heads * case.head_dim * 2          # K and V of one position
+    cached = int((case.context_lens - case.q_lens).clip(min=0).sum())
+    qo = 2 * case.num_tokens * case.q_heads * case.head_dim * 2
+    return 2 * case.num_tokens * row + cached * row + qo
+
+
 def append_work(case, int8: bool = False):
     """(bytes, flops) of one append: K/V of each sequence's visible positions read once, Q
     read, O written; 4*D flops per (query head, visible key) pair (QK and PV).  INT8 pages:
@@ -644,6 +653,21 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
                         if P == 16 and args.append_docs == 1000 else None),
         }
         del g1, g2
+        # fused store + append (kvc_append_store) on the same inputs: the chunk's K/V read once
+        # from k_new / v_new; the pools end as the separate store leaves them
+        with torch.cuda.stream(stream):
+            tf = time_graph(torch, lambda: kvc.kvc_append_store(
+                out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table, d.q_indptr,
+                d.context_lens, case.max_q_len, case.max_ctx), stream, flush,
+                args.append_steps) / 1e3
+        sep = (statistics.mean(st_ms) + statistics.mean(ap_ms)) / 1e3
+        bf = fused_work(case)
+        result[f"p{P}"]["fused_store"] = {
+            "kernel": "store_boundary_kernel + paged_append_tc_kernel (kvc_append_store)",
+            "ms": round(tf * 1e3, 4), "bytes": bf, "gbs": round(bf / tf / 1e9, 1),
+            "separate_ms": round(sep * 1e3, 4), "speedup_vs_separate": round(sep / tf, 3),
+            "gpu_launches": 2 * args.append_steps,
+        }
         # the same append over INT8 pages: every slot of the bf16 pools quantised by
         # kvc_store_int8, then kvc_append_int8 (132 B per cached vector instead of 256)
         pages, _, H, D = (int(x) for x in d.k_pool.shape)

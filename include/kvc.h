@@ -263,6 +263,27 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
                       void *stream);
 
 /*
+ * kvc_append_store -- kvc_slot_mapping + kvc_store + kvc_append in one pass over the chunk
+ * (TileInfer.jl "KV cache": the store is fused into the kernel that stages K/V for attention).
+ * Stores every new token's k_new / v_new row at the slot its position gets from the block
+ * table (exactly what kvc_store with kvc_slot_mapping's slots writes), and returns kvc_append's
+ * output for the same arguments.  The chunk's K/V are read once from k_new / v_new: the pages
+ * that hold only new tokens are attended from there and written to the pools by the attention
+ * kernel itself; the new tokens that share a page with cached positions (the chunk's first
+ * page when ctx - q_len is not a multiple of page_size) are stored by a small kernel first.
+ *   k_new, v_new   bf16 [num_tokens][kv_heads][head_dim], row t = token t of q (q_indptr)
+ *   k_pool, v_pool written (the new tokens' slots only) and read
+ * Other arguments as kvc_append.  A token whose position is negative (context_lens[s] <
+ * q_len_s) is not stored.  Two launches on `stream`.
+ */
+kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                            const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,
+                            const int32_t *block_table, int32_t bt_stride,
+                            const int32_t *q_indptr, const int32_t *context_lens,
+                            int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                            int32_t max_ctx, int32_t q_heads, float scale, void *stream);
+
+/*
  * kvc_device_errors -- read and clear the device-side error word.  Kernels bound every wait
  * (about one second); a wait that runs out sets a bit here and the kernel returns early,
  * leaving its outputs undefined.  Synchronises with the device.  *flags_out = 0 when no

@@ -245,6 +245,26 @@ kvc_status pool_tensor_map_halves(const void *base, const kvc_pool_desc &pool, C
     return tensor_map(k, out);
 }
 
+// New tokens' K or V [num_tokens][kv_heads][head_dim] bf16 viewed as {head_dim, kv head, token};
+// one box {64, 1, page_size} is one column half of page_size consecutive tokens of one kv head,
+// landing in shared memory exactly as a page box of an NHD pool does.
+kvc_status new_tokens_tensor_map(const void *base, int32_t num_tokens, const kvc_pool_desc &pool,
+                                 CUtensorMap *out)
+{
+    MapKey k{};
+    k.ptr = base;
+    k.rank = 3;
+    k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
+    k.dims[1] = static_cast<cuuint64_t>(pool.kv_heads);
+    k.dims[2] = static_cast<cuuint64_t>(num_tokens);
+    k.strides[0] = static_cast<cuuint64_t>(pool.head_dim) * 2;
+    k.strides[1] = static_cast<cuuint64_t>(pool.kv_heads) * pool.head_dim * 2;
+    k.box[0] = 64;
+    k.box[1] = 1;
+    k.box[2] = static_cast<cuuint32_t>(pool.page_size);
+    return tensor_map(k, out);
+}
+
 // INT8 codes [num_pages * page_size][kv_heads][head_dim] viewed as the 3-D tensor
 // {head_dim, kv head, slot} of bytes; one box {head_dim, 1, page_size} is one page of one kv
 // head, [page_size rows][head_dim bytes] (128 bytes at head_dim 128, one swizzle row).
@@ -867,6 +887,70 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     l.hnd = pool.layout == KVC_HND;
     cudaError_t err = kvc::launch_append_tc(l, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");
+}
+
+kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                            const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,
+                            const int32_t *block_table, int32_t bt_stride,
+                            const int32_t *q_indptr, const int32_t *context_lens,
+                            int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                            int32_t max_ctx, int32_t q_heads, float scale, void *stream)
+{
+    kvc_status st = check_attention_args(out, out_dtype, q, k_pool, v_pool, pool, block_table,
+                                         bt_stride, context_lens, num_seqs, max_ctx, q_heads);
+    if (st != KVC_OK)
+        return st;
+    if (num_tokens < 0 || max_q_len < 0)
+        return fail(KVC_ERR_INVALID_ARG, "num_tokens %d, max_q_len %d", num_tokens, max_q_len);
+    if (num_seqs > 0 && q_indptr == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "q_indptr is required");
+    if (num_tokens > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return fail(KVC_ERR_INVALID_ARG, "k_new / v_new missing or not 16-byte aligned");
+    if (static_cast<int64_t>(max_q_len) * (q_heads / pool.kv_heads) > (int64_t(1) << 30))
+        return fail(KVC_ERR_INVALID_ARG, "max_q_len too large");
+    if (num_seqs == 0 || num_tokens == 0 || max_q_len == 0)
+        return ok();
+    CUtensorMap tq, tk, tv, tkn, tvn;
+    if ((st = pool_tensor_map_halves(k_pool, pool, &tk)) != KVC_OK)
+        return st;
+    if ((st = pool_tensor_map_halves(v_pool, pool, &tv)) != KVC_OK)
+        return st;
+    if ((st = new_tokens_tensor_map(k_new, num_tokens, pool, &tkn)) != KVC_OK)
+        return st;
+    if ((st = new_tokens_tensor_map(v_new, num_tokens, pool, &tvn)) != KVC_OK)
+        return st;
+    if ((st = query_tensor_map(q, num_tokens, pool.kv_heads, q_heads / pool.kv_heads,
+                               pool.head_dim, &tq)) != KVC_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = kvc::launch_store_boundary(
+        k_pool, v_pool, pool.kv_heads, pool.head_dim, pool.page_size,
+        pool.num_pages * pool.page_size, pool.layout == KVC_HND, k_new, v_new, block_table,
+        bt_stride, q_indptr, context_lens, num_seqs, s);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "boundary store launch");
+    kvc::AppendLaunch l;
+    l.q = q;
+    l.out = out;
+    l.out_f32 = out_dtype == KVC_F32;
+    l.block_table = block_table;
+    l.bt_stride = bt_stride;
+    l.q_indptr = q_indptr;
+    l.context_lens = context_lens;
+    l.num_seqs = num_seqs;
+    l.num_tokens = num_tokens;
+    l.max_q_len = max_q_len;
+    l.q_heads = q_heads;
+    l.kv_heads = pool.kv_heads;
+    l.head_dim = pool.head_dim;
+    l.page_size = pool.page_size;
+    l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    l.hnd = pool.layout == KVC_HND;
+    l.fused = true;
+    l.k_pool_w = k_pool;
+    l.v_pool_w = v_pool;
+    err = kvc::launch_append_tc(l, tq, tk, tv, s, &tkn, &tvn);
     return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");
 }
 

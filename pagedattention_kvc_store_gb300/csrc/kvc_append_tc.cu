@@ -31,6 +31,9 @@
 //               lane r; warp w reaches lanes 32 (w % 4) ..): reads its S row, applies the
 //               scale and the causal limit, keeps a running max / sum, writes P (bf16 pairs)
 //               over the first half of the S columns, and at the end of the item writes O / l.
+//   (kvc_append_store) warp 2 also writes the chunk's rows from the ring slots they landed in
+//               (read from k_new / v_new there) to the pools, and releases each slot on a
+//               barrier of its own that the K/V producer waits for as well.
 // The running max is updated lazily: O is rescaled (in TMEM) only when a row's max grows by
 // more than 2^8.  The result is exact either way; probabilities are then at most 2^8 before
 // normalisation.  Barrier phases follow counters kept identically by every role (items, ring
@@ -67,7 +70,7 @@ struct TcGeom {
     static constexpr int kStages = D == 128 ? 5 : 8;
     static constexpr int kOffStages = 2 * kQBytes;           // Q: [tile]
     static constexpr int kOffBar = kOffStages + kStages * kStageBytes;
-    static constexpr size_t kSmemBytes = kOffBar + 256;      // base is 1024-aligned
+    static constexpr size_t kSmemBytes = kOffBar + 512;      // base is 1024-aligned
     // TMEM, per tile w at w * 256: O [0, D), S [D, D + 128); P overwrites S [D, D + 64).
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = D;
@@ -86,6 +89,11 @@ struct Args {
     int kv_heads, q_heads, group, page_size, pairs_per_seq, num_items;
     float scale_log2;
     int hnd;   // HND pools: half boxes addressed by (offset, page * kv_heads + kv head)
+    // Fused store (kvc_append_store): the chunk's pages are read from k_new / v_new and written
+    // to the pools by this kernel, except the tokens that share a page with cached positions
+    // (stored before the launch).
+    int fused;
+    uint8_t *k_pool_w, *v_pool_w;   // the pools, for rows of a partly filled last page
 };
 
 enum BarIndex : int {
@@ -97,14 +105,17 @@ enum BarIndex : int {
     kBarPFull = kBarSFull + 2,              // [tile], 128 arrivals
     kBarPvDone = kBarPFull + 2,             // [tile], once per item
     kBarDrain = kBarPvDone + 2,
-    kBarCount
+    kBarKvStored = kBarDrain + 1,           // [ring slot], fused store: its pages written
+    kBarCount = kBarKvStored + kMaxStages
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_append_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                            const __grid_constant__ CUtensorMap tmap_k,
-                           const __grid_constant__ CUtensorMap tmap_v, const Args a)
+                           const __grid_constant__ CUtensorMap tmap_v,
+                           const __grid_constant__ CUtensorMap tmap_kn,
+                           const __grid_constant__ CUtensorMap tmap_vn, const Args a)
 {
     using Geom = TcGeom<D>;
     constexpr int kHalves = D / 64;
@@ -169,6 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             head_it = w.it + static_cast<int>(gridDim.x);   // the next index, if not skipped
             head_page = bt_head(head_it);
             const int nb = x.n_blocks;
+            const int base = x.ctx - x.q_len;   // position of the chunk's first token
+            const int first_new = base > 0 ? (base + P - 1) / P : 0;
             for (int j = 0; j < 2 * nb; ++j, ++n) {
                 // Fill order K(0), K(1), V(0), K(2), V(1), ..., V(nb - 1): K runs one block
                 // ahead, so V(b) lands about when PV(b) needs it, next to K(b + 1).
@@ -179,8 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {
                     const int st = n % kStages;
                     if (n >= kStages &&
-                        !__all_sync(0xffffffffu,
-                                    mbar_wait(&bars[kBarKvEmpty + st], ((n / kStages) - 1) & 1))) {
+                        (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvEmpty + st],
+                                                            ((n / kStages) - 1) & 1)) ||
+                         (a.fused && !__all_sync(0xffffffffu,
+                                                 mbar_wait(&bars[kBarKvStored + st],
+                                                           ((n / kStages) - 1) & 1))))) {
                         ok = false;
                         break;
                     }
@@ -202,8 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int h = lane % kHalves;
                     const int page =
                         __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
-                    // NHD maps {head_dim, kv head, slot}; HND maps {head_dim, offset, block}
-                    if (i < np)
+                    // NHD maps {head_dim, kv head, slot}; HND maps {head_dim, offset, block}.
+                    // Fused store: a page that holds only the chunk's tokens comes from
+                    // k_new / v_new ({head_dim, kv head, token}), its first token at
+                    // tok0 + lp * P - (ctx - q_len).
+                    const int lp = lp0 + i;
+                    if (i < np && a.fused && lp >= first_new)
+                        tma_load_3d(dst + h * kBN * 128 + i * P * 128, is_k ? &tmap_kn : &tmap_vn,
+                                    h * 64, x.kvh, x.tok0 + lp * P - base, &bars[kBarKvFull + st],
+                                    policy);
+                    else if (i < np)
                         tma_load_3d(dst + h * kBN * 128 + i * P * 128, map, h * 64,
                                     a.hnd ? 0 : x.kvh, a.hnd ? page * a.kv_heads + x.kvh : page * P,
                                     &bars[kBarKvFull + st], policy);
@@ -221,12 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicOr(&g_append_tc_errors, kErrDrainWait);
         }
     } else if (warp == 2) {
-        // ------------------------------ query loads --------------------------------------
+        // ------------------------------ query loads (and the fused store) -----------------
         if (lane == 0)
             prefetch_tensormap(&tmap_q);
         Walker w;
         w.start(a, &g_append_tc_errors);
         int qi[2] = {0, 0};   // items whose query tile t was requested
+        int n = 0;
         while (ok && !w.done) {
             const Item &x = w.x;
             // Tile t of the next item loads as soon as tile t of this one has had its last S
@@ -247,6 +272,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(q_tile(t) + lane * kM * 128, &tmap_q, lane * 64, 0, x.kvh,
                                 x.tok0 + (x.row_begin + t * kM) / G, &bars[kBarQFull + t]);
                 ++qi[t];
+            }
+            if (!ok)
+                break;
+            if (a.fused) {
+                // Fused store: write the chunk's positions that this tile pair sees and no
+                // earlier pair of its (sequence, kv head) saw, [p_lo, p_hi), row by row from
+                // the ring slots they landed in (16-byte loads and stores; measured as fast as
+                // TMA stores of whole pages, and a slot is free once its rows are in registers).
+                // Rows at or past p_hi = n_keys may be zeroed by the MMA warp for the last PV
+                // product; they are never read here.  Positions in the page of the chunk's first
+                // token that also holds cached ones were stored before the launch.  Every slot
+                // gets its arrival on kBarKvStored once it has landed: a parity wait cannot
+                // tell a phase from the one two later, so this warp must not run two phases of
+                // kBarKvStored ahead of the producer's waits.
+                const int nb = x.n_blocks;
+                const int base = x.ctx - x.q_len;
+                const int first_new = base > 0 ? (base + P - 1) / P : 0;
+                int p_lo = first_new * P;
+                if (x.tp > 0)
+                    p_lo = max(p_lo, min(x.ctx, base + (x.row_begin - 1) / G + 1));
+                const int p_hi = x.n_keys;
+                const int32_t *bt_row = a.block_table + static_cast<size_t>(x.s) * a.bt_stride;
+                for (int j = 0; j < 2 * nb; ++j, ++n) {
+                    const bool is_k = j == 0 || (j < 2 * nb - 1 && (j & 1));
+                    const int b = is_k ? (j + 1) / 2 : (j == 2 * nb - 1 ? nb - 1 : j / 2 - 1);
+                    const int st = n % kStages;
+                    const int lp0 = b * kBN / P;
+                    const int np = (min(kBN, x.n_keys - b * kBN) + P - 1) / P;
+                    const int s_lo = max(lp0, p_lo / P);   // pages of the block to write
+                    const int s_hi = min(lp0 + np, (p_hi + P - 1) / P);
+                    const bool write = p_lo < p_hi && s_lo < s_hi;
+                    const int my_page = (write && s_lo + lane < s_hi) ? bt_row[s_lo + lane] : 0;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bars[kBarKvFull + st], (n / kStages) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    if (write) {
+                        const uint8_t *stage = sStages + st * Geom::kStageBytes;
+                        uint8_t *pool = is_k ? a.k_pool_w : a.v_pool_w;
+                        for (int lp = s_lo; lp < s_hi; ++lp) {
+                            const int page = __shfl_sync(0xffffffffu, my_page, lp - s_lo);
+                            const int i = lp - lp0;
+                            const int r_lo = max(p_lo - lp * P, 0);
+                            const int r_hi = min(p_hi - lp * P, P);
+                            // rows r_lo .. r_hi - 1; 16-byte chunk c of row r sits at chunk
+                            // (c % 8) ^ (r % 8) of its 128-byte line
+                            for (int idx = lane; idx < (r_hi - r_lo) * (D / 8); idx += 32) {
+                                const int c = idx % (D / 8);
+                                const int r = r_lo + idx / (D / 8);
+                                const uint4 v = *reinterpret_cast<const uint4 *>(
+                                    stage + (c >> 3) * kBN * 128 + (i * P + r) * 128 +
+                                    (((c & 7) ^ (r & 7)) << 4));
+                                const size_t row =
+                                    a.hnd ? (static_cast<size_t>(page) * a.kv_heads + x.kvh) * P +
+                                                r
+                                          : (static_cast<size_t>(page) * P + r) * a.kv_heads +
+                                                x.kvh;
+                                *reinterpret_cast<uint4 *>(pool + row * (D * 2) + c * 16) = v;
+                            }
+                        }
+                        __syncwarp();
+                    }
+                    if (lane == 0)
+                        mbar_arrive(&bars[kBarKvStored + st]);
+                }
+                if (!ok)
+                    break;
             }
             if (!ok)
                 break;
@@ -598,7 +691,8 @@ int sm_count()
 
 template <int D>
 cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, cudaStream_t stream)
+                     const CUtensorMap &tv, const CUtensorMap &tkn, const CUtensorMap &tvn,
+                     cudaStream_t stream)
 {
     Args a;
     a.out = l.out;
@@ -612,6 +706,9 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
     a.hnd = l.hnd ? 1 : 0;
+    a.fused = l.fused ? 1 : 0;
+    a.k_pool_w = static_cast<uint8_t *>(l.k_pool_w);
+    a.v_pool_w = static_cast<uint8_t *>(l.v_pool_w);
     const int tiles = (l.max_q_len * a.group + kM - 1) / kM;
     a.pairs_per_seq = (tiles + 1) / 2;
     const long long items = static_cast<long long>(a.pairs_per_seq) * l.kv_heads * l.num_seqs;
@@ -626,7 +723,7 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     if (err != cudaSuccess)
         return err;
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
-    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, a);
+    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tkn, tvn, a);
     return cudaGetLastError();
 }
 
@@ -634,12 +731,17 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
 
 cudaError_t launch_append_tc(const AppendLaunch &l, const CUtensorMap &tmap_q,
                              const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                             cudaStream_t stream)
+                             cudaStream_t stream, const CUtensorMap *tmap_kn,
+                             const CUtensorMap *tmap_vn)
 {
     if (l.num_seqs == 0 || l.num_tokens == 0 || l.max_q_len == 0)
         return cudaSuccess;
-    return l.head_dim == 128 ? launch_t<128>(l, tmap_q, tmap_k, tmap_v, stream)
-                             : launch_t<64>(l, tmap_q, tmap_k, tmap_v, stream);
+    if (l.fused && (tmap_kn == nullptr || tmap_vn == nullptr))
+        return cudaErrorInvalidValue;
+    const CUtensorMap &kn = tmap_kn ? *tmap_kn : tmap_k;   // unused unless fused
+    const CUtensorMap &vn = tmap_vn ? *tmap_vn : tmap_v;
+    return l.head_dim == 128 ? launch_t<128>(l, tmap_q, tmap_k, tmap_v, kn, vn, stream)
+                             : launch_t<64>(l, tmap_q, tmap_k, tmap_v, kn, vn, stream);
 }
 
 cudaError_t read_and_clear_append_tc_errors(uint32_t *flags)

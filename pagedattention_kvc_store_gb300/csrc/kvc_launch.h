@@ -76,6 +76,11 @@ struct AppendLaunch {
     int num_seqs, num_tokens, max_q_len, q_heads, kv_heads, head_dim, page_size;
     float scale;
     bool hnd = false;
+    // kvc_append_store: the chunk's K/V come from k_new / v_new (tmap_kn / tmap_vn) and the
+    // kernel writes them to the pools (k_pool_w / v_pool_w), except the boundary tokens
+    // launch_store_boundary wrote before.
+    bool fused = false;
+    void *k_pool_w = nullptr, *v_pool_w = nullptr;
 };
 
 // kvc_append_int8: AppendLaunch over INT8 pages (head_dim 128, NHD) plus the scale arrays.
@@ -132,10 +137,19 @@ cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int3
                                  cudaStream_t stream);
 cudaError_t launch_grouped_prefix(const GroupedPrefixLaunch &a, const CUtensorMap &tmap_k,
                                   const CUtensorMap &tmap_v, cudaStream_t stream);
-// tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes.
+// tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes; tmap_kn / tmap_vn (fused
+// only) view k_new / v_new as {head_dim, kv head, token} with {64, 1, page_size} boxes.
 cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
                              const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const CUtensorMap *tmap_kn = nullptr,
+                             const CUtensorMap *tmap_vn = nullptr);
+// The new tokens that share a page with cached positions (the chunk's first page when
+// (ctx - q_len) % page_size != 0), stored at their slots from the block table.
+cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int head_dim,
+                                  int page_size, int num_slots, bool hnd, const void *k_new,
+                                  const void *v_new, const int32_t *block_table, int bt_stride,
+                                  const int32_t *q_indptr, const int32_t *context_lens,
+                                  int num_seqs, cudaStream_t stream);
 // tmap_q as for launch_append_tc; tmap_k / tmap_v are the INT8 page maps (one box per page).
 cudaError_t launch_append_int8(const AppendInt8Launch &a, const CUtensorMap &tmap_q,
                                const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,

@@ -113,6 +113,50 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
     }
 }
 
+// Fused store + append, first part: the chunk's tokens in the page of its first token when
+// that page also holds cached positions (positions base .. min(ctx, (base / P + 1) P) - 1 with
+// base = ctx - q_len not a multiple of P), stored at their slots; the fused append reads that
+// page from the pool and writes every later page of the chunk itself.  One CTA per sequence
+// (grid-stride), one thread per 16-byte chunk of a token row; addressing as store_kernel.
+__global__ void __launch_bounds__(256) store_boundary_kernel(
+    uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, const uint4 *__restrict__ k_new,
+    const uint4 *__restrict__ v_new, const int32_t *__restrict__ block_table, int bt_stride,
+    const int32_t *__restrict__ q_indptr, const int32_t *__restrict__ context_lens, int num_seqs,
+    int chunks, int kv_heads, int page_size, int num_slots, bool hnd)
+{
+    const int row_chunks = chunks / kv_heads;
+    for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
+        const int tok0 = __ldg(q_indptr + s);
+        const int q_len = __ldg(q_indptr + s + 1) - tok0;
+        const int ctx = min(__ldg(context_lens + s), bt_stride * page_size);
+        const int base = ctx - q_len;
+        if (q_len <= 0 || base <= 0 || base % page_size == 0)
+            continue;
+        const int n_tok = min(ctx, (base / page_size + 1) * page_size) - base;
+        const int page = __ldg(block_table + static_cast<size_t>(s) * bt_stride + base / page_size);
+        for (int i = threadIdx.x; i < n_tok * chunks; i += blockDim.x) {
+            const int t = i / chunks;
+            const int c = i - t * chunks;
+            const long long slot =
+                static_cast<long long>(page) * page_size + base % page_size + t;
+            if (slot < 0 || slot >= num_slots) {   // a page outside the pool: skip, flag
+                if (c == 0)
+                    atomicOr(&g_store_errors, kErrSlotRange);
+                continue;
+            }
+            size_t dst = static_cast<size_t>(slot) * chunks + c;
+            if (hnd) {
+                const int h = c / row_chunks;
+                dst = ((static_cast<size_t>(page) * kv_heads + h) * page_size +
+                       (base % page_size + t)) * row_chunks + (c - h * row_chunks);
+            }
+            const size_t src = static_cast<size_t>(tok0 + t) * chunks + c;
+            k_pool[dst] = load_streaming(k_new + src);
+            v_pool[dst] = load_streaming(v_new + src);
+        }
+    }
+}
+
 // INT8 store (TileInfer.jl "KV cache", "INT8 cache"): one warp per (token, kv head) vector of
 // D = 32 * E values.  scale = max|x| / 127 and code = rint(x / scale) clamped to [-127, 127],
 // both in fp32 with round-to-nearest division, so the codes are the ones the quantiser's
@@ -268,6 +312,24 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
         static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
         num_tokens, chunks, num_slots, hnd, kv_heads, page_size);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int head_dim,
+                                  int page_size, int num_slots, bool hnd, const void *k_new,
+                                  const void *v_new, const int32_t *block_table, int bt_stride,
+                                  const int32_t *q_indptr, const int32_t *context_lens,
+                                  int num_seqs, cudaStream_t stream)
+{
+    if (num_seqs == 0)
+        return cudaSuccess;
+    const int cap = sm_count() * 8;
+    const int blocks = num_seqs < cap ? num_seqs : cap;
+    store_boundary_kernel<<<blocks, 256, 0, stream>>>(
+        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), block_table,
+        bt_stride, q_indptr, context_lens, num_seqs, kv_heads * head_dim * 2 / 16, kv_heads,
+        page_size, num_slots, hnd);
     return cudaGetLastError();
 }
 

@@ -29,7 +29,8 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_decode", "kvc_decode_plan", "kvc_merge", "kvc_append", "kvc_device_errors",
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
-           "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8")
+           "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8",
+           "kvc_append_store")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -115,6 +116,9 @@ def lib() -> ctypes.CDLL:
             L.kvc_append_int8.restype = ctypes.c_int
             L.kvc_append_int8.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, p, i32,
                                           i32, i32, i32, i32, f, p]
+            L.kvc_append_store.restype = ctypes.c_int
+            L.kvc_append_store.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, p, i32,
+                                           i32, i32, i32, i32, f, p]
             L.kvc_copy_pages.restype = ctypes.c_int
             L.kvc_copy_pages.argtypes = [p, p, PoolDesc, p, p, i32, p]
             L.kvc_validate_workspace_size.restype = ctypes.c_int
@@ -359,6 +363,29 @@ def kvc_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
         _ptr(block_table), int(block_table.shape[1]), _ptr(q_indptr), _ptr(context_lens),
         int(context_lens.shape[0]), int(q.shape[0]), int(max_q_len), int(max_ctx),
         int(q.shape[1]), float(scale), _stream(stream)))
+
+
+def kvc_append_store(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor,
+                     v_new: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                     block_table: torch.Tensor, q_indptr: torch.Tensor,
+                     context_lens: torch.Tensor, max_q_len: int, max_ctx: int,
+                     scale: float = 0.0, stream=None, layout: str = "nhd") -> None:
+    """Store the chunk's K/V at their slots and attend (kvc_slot_mapping + kvc_store +
+    kvc_append in one pass over the chunk)."""
+    _cuda("out", out)
+    _cuda("q", q, torch.bfloat16)
+    _cuda("k_new", k_new, torch.bfloat16)
+    _cuda("v_new", v_new, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("q_indptr", q_indptr, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    _check("kvc_append_store", lib().kvc_append_store(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+        _ptr(v_pool), pool_desc(k_pool, layout), _ptr(block_table), int(block_table.shape[1]),
+        _ptr(q_indptr), _ptr(context_lens), int(context_lens.shape[0]), int(q.shape[0]),
+        int(max_q_len), int(max_ctx), int(q.shape[1]), float(scale), _stream(stream)))
 
 
 def kvc_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
