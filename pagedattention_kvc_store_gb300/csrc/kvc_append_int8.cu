@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_addr(smem) & 1023u) != 0) {
         if (threadIdx.x == 0)
@@ -819,8 +821,8 @@ cudaError_t launch_append_int8(const AppendInt8Launch &l, const CUtensorMap &tma
     if (err != cudaSuccess)
         return err;
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
-    paged_append_int8_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmap_q, tmap_k, tmap_v, a);
-    return cudaGetLastError();
+    return launch_pdl(paged_append_int8_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream,
+                      tmap_q, tmap_k, tmap_v, a);
 }
 
 cudaError_t read_and_clear_append_int8_errors(uint32_t *flags)

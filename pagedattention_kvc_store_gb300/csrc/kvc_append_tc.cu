@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tmap_kn,
                            const __grid_constant__ CUtensorMap tmap_vn, const Args a)
 {
+    pdl_wait();
+    pdl_trigger();
     using Geom = TcGeom<D>;
     constexpr int kHalves = D / 64;
     constexpr int kStages = Geom::kStages;
@@ -723,8 +725,7 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     if (err != cudaSuccess)
         return err;
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
-    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tkn, tvn, a);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, tkn, tvn, a);
 }
 
 }  // namespace

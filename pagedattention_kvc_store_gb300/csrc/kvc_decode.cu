@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
+    pdl_wait();
+    pdl_trigger();
     using Geom = DecodeGeom<D>;
 
     extern __shared__ uint8_t smem_raw[];
@@ -352,6 +354,8 @@ __global__ void __launch_bounds__(128) merge_kernel(void *out, int out_f32,
                                                     const float *__restrict__ part_lse,
                                                     int rows, int n_split, float *lse_out)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = D / 32;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -436,8 +440,7 @@ cudaError_t launch_decode_t(const DecodeLaunch &l, const CUtensorMap &tk, const 
     if (err != cudaSuccess)
         return err;
     dim3 grid(l.n_split, l.kv_heads, l.num_seqs);
-    kernel<<<grid, kThreads, smem, stream>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_pdl(kernel, grid, dim3(kThreads), smem, stream, tk, tv, a);
 }
 
 }  // namespace
@@ -463,12 +466,10 @@ cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const floa
         return cudaSuccess;
     const int blocks = (rows + 3) / 4;
     if (head_dim == 128)
-        merge_kernel<128><<<blocks, 128, 0, stream>>>(out, out_f32, part_o, part_lse, rows,
-                                                       n_split, lse_out);
-    else
-        merge_kernel<64><<<blocks, 128, 0, stream>>>(out, out_f32, part_o, part_lse, rows,
-                                                      n_split, lse_out);
-    return cudaGetLastError();
+        return launch_pdl(merge_kernel<128>, dim3(blocks), dim3(128), 0, stream, out, out_f32,
+                          part_o, part_lse, rows, n_split, lse_out);
+    return launch_pdl(merge_kernel<64>, dim3(blocks), dim3(128), 0, stream, out, out_f32, part_o,
+                      part_lse, rows, n_split, lse_out);
 }
 
 cudaError_t read_and_clear_decode_errors(uint32_t *flags)

@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     paged_decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -435,8 +437,7 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     if (err != cudaSuccess)
         return err;
     dim3 grid(l.n_split, l.kv_heads, l.num_seqs);
-    kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, tk, tv, a);
 }
 
 }  // namespace

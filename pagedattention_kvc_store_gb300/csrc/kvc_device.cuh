@@ -36,6 +36,21 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  Every kvc kernel starts with pdl_wait() -- it returns once
+// the grids this launch depends on have completed and their writes are visible (at once when
+// the launch has no such dependency) -- and then pdl_trigger(), which lets the next launch on
+// the stream start its CTAs as this grid's last ones are scheduled; they wait in their own
+// pdl_wait().  The next kernel's launch and prologue so overlap this one's tail.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------

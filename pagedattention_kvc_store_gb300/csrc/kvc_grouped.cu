@@ -62,6 +62,8 @@ struct Args {
 __global__ void grouped_setup_kernel(float *__restrict__ part_lse, int32_t *__restrict__ key_start,
                                      int num_seqs, int q_heads, int n_prefix, int split_stride)
 {
+    pdl_wait();
+    pdl_trigger();
     const size_t total = static_cast<size_t>(num_seqs) * q_heads * n_prefix;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -81,6 +83,8 @@ __global__ void grouped_members_kernel(int32_t *__restrict__ key_start,
                                        const int32_t *__restrict__ prefix_len, int page_size,
                                        int bt_stride)
 {
+    pdl_wait();
+    pdl_trigger();
     const int g = blockIdx.x;
     int pre = (prefix_len[g] / page_size) * page_size;   // whole pages only
     pre = min(max(pre, 0), bt_stride * page_size);
@@ -93,6 +97,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     grouped_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
+    pdl_wait();
+    pdl_trigger();
     using Geom = GroupGeom<D>;
     constexpr int kWarpsPerTile = kConsumerWarps / NMT;   // warps sharing one 16-row tile
     constexpr int kKeysPerWarp = kStageKeys / kWarpsPerTile;
@@ -421,8 +427,7 @@ cudaError_t launch_t(const GroupedPrefixLaunch &l, const CUtensorMap &tk, const 
     if (err != cudaSuccess)
         return err;
     dim3 grid(l.n_split, l.kv_heads, l.num_groups);
-    kernel<<<grid, kThreads, smem, stream>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_pdl(kernel, grid, dim3(kThreads), smem, stream, tk, tv, a);
 }
 
 template <int D>
@@ -447,13 +452,13 @@ cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int3
     const size_t total = static_cast<size_t>(num_seqs) * q_heads * n_prefix_splits;
     const size_t want = (total + 255) / 256;
     const int blocks = static_cast<int>(want < 1024 ? (want > 0 ? want : 1) : 1024);
-    grouped_setup_kernel<<<blocks, 256, 0, stream>>>(part_lse, key_start, num_seqs, q_heads,
-                                                     n_prefix_splits, split_stride);
-    if (num_groups > 0)
-        grouped_members_kernel<<<num_groups, 128, 0, stream>>>(key_start, group_indptr,
-                                                               group_seqs, prefix_len, page_size,
-                                                               bt_stride);
-    return cudaGetLastError();
+    cudaError_t err = launch_pdl(grouped_setup_kernel, dim3(blocks), dim3(256), 0, stream,
+                                 part_lse, key_start, num_seqs, q_heads, n_prefix_splits,
+                                 split_stride);
+    if (err == cudaSuccess && num_groups > 0)
+        err = launch_pdl(grouped_members_kernel, dim3(num_groups), dim3(128), 0, stream,
+                         key_start, group_indptr, group_seqs, prefix_len, page_size, bt_stride);
+    return err;
 }
 
 cudaError_t launch_grouped_prefix(const GroupedPrefixLaunch &l, const CUtensorMap &tk,

@@ -24,6 +24,8 @@ __global__ void slot_mapping_decode_kernel(int32_t *__restrict__ slots,
                                            const int32_t *__restrict__ context_lens,
                                            int num_seqs, int page_size)
 {
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= num_seqs)
         return;
@@ -46,6 +48,8 @@ __global__ void slot_mapping_ragged_kernel(int32_t *__restrict__ slots,
                                            const int32_t *__restrict__ q_indptr,
                                            int page_size)
 {
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x;
     const int first = q_indptr[s];
     const int q_len = q_indptr[s + 1] - first;
@@ -83,6 +87,8 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
                                                     int num_tokens, int chunks, int num_slots,
                                                     bool hnd, int kv_heads, int page_size)
 {
+    pdl_wait();
+    pdl_trigger();
     const int row_chunks = chunks / kv_heads;   // 16-byte chunks of one head_dim vector
     const size_t total = static_cast<size_t>(num_tokens) * chunks;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -124,6 +130,8 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
     const int32_t *__restrict__ q_indptr, const int32_t *__restrict__ context_lens, int num_seqs,
     int chunks, int kv_heads, int page_size, int num_slots, bool hnd)
 {
+    pdl_wait();
+    pdl_trigger();
     const int row_chunks = chunks / kv_heads;
     for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
         const int tok0 = __ldg(q_indptr + s);
@@ -173,6 +181,8 @@ __global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_
                                                          int num_tokens, int kv_heads,
                                                          int page_size, int num_slots)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int D = 32 * E;
     const int lane = threadIdx.x & 31;
     const long long vectors = static_cast<long long>(num_tokens) * kv_heads;
@@ -236,6 +246,8 @@ __global__ void __launch_bounds__(256) copy_pages_kernel(uint4 *__restrict__ k_p
                                                          const int32_t *__restrict__ dst_pages,
                                                          int num_copies, int chunks, int num_pages)
 {
+    pdl_wait();
+    pdl_trigger();
     const size_t total = static_cast<size_t>(num_copies) * chunks;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -284,15 +296,15 @@ cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int 
         return cudaSuccess;
     if (q_indptr == nullptr) {
         const int threads = 128;
-        slot_mapping_decode_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
-            slots, block_table, bt_stride, context_lens, num_seqs, page_size);
+        return launch_pdl(slot_mapping_decode_kernel, dim3((num_seqs + threads - 1) / threads),
+                          dim3(threads), 0, stream, slots, block_table, bt_stride, context_lens,
+                          num_seqs, page_size);
     } else {
         int threads = ((max_q_len + 31) / 32) * 32;
         threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
-        slot_mapping_ragged_kernel<<<num_seqs, threads, 0, stream>>>(
-            slots, block_table, bt_stride, context_lens, q_indptr, page_size);
+        return launch_pdl(slot_mapping_ragged_kernel, dim3(num_seqs), dim3(threads), 0, stream,
+                          slots, block_table, bt_stride, context_lens, q_indptr, page_size);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
@@ -308,11 +320,10 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
     const size_t wanted = (total + threads - 1) / threads;
     const size_t cap = static_cast<size_t>(sm_count()) * 8;
     const int blocks = static_cast<int>(wanted < cap ? wanted : cap);
-    store_kernel<<<blocks, threads, 0, stream>>>(
-        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
-        num_tokens, chunks, num_slots, hnd, kv_heads, page_size);
-    return cudaGetLastError();
+    return launch_pdl(store_kernel, dim3(blocks), dim3(threads), 0, stream,
+                      static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
+                      num_tokens, chunks, num_slots, hnd, kv_heads, page_size);
 }
 
 cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int head_dim,
@@ -325,12 +336,11 @@ cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int 
         return cudaSuccess;
     const int cap = sm_count() * 8;
     const int blocks = num_seqs < cap ? num_seqs : cap;
-    store_boundary_kernel<<<blocks, 256, 0, stream>>>(
-        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), block_table,
-        bt_stride, q_indptr, context_lens, num_seqs, kv_heads * head_dim * 2 / 16, kv_heads,
-        page_size, num_slots, hnd);
-    return cudaGetLastError();
+    return launch_pdl(store_boundary_kernel, dim3(blocks), dim3(256), 0, stream,
+                      static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+                      block_table, bt_stride, q_indptr, context_lens, num_seqs,
+                      kv_heads * head_dim * 2 / 16, kv_heads, page_size, num_slots, hnd);
 }
 
 cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
@@ -350,14 +360,13 @@ cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, flo
     auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
     auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
     if (head_dim == 128)
-        store_int8_kernel<4><<<blocks, threads, 0, stream>>>(kc, vc, k_scales, v_scales, kn, vn,
-                                                             slots, num_tokens, kv_heads,
-                                                             page_size, num_slots);
+        return launch_pdl(store_int8_kernel<4>, dim3(blocks), dim3(threads), 0, stream, kc, vc,
+                          k_scales, v_scales, kn, vn, slots, num_tokens, kv_heads, page_size,
+                          num_slots);
     else
-        store_int8_kernel<2><<<blocks, threads, 0, stream>>>(kc, vc, k_scales, v_scales, kn, vn,
-                                                             slots, num_tokens, kv_heads,
-                                                             page_size, num_slots);
-    return cudaGetLastError();
+        return launch_pdl(store_int8_kernel<2>, dim3(blocks), dim3(threads), 0, stream, kc, vc,
+                          k_scales, v_scales, kn, vn, slots, num_tokens, kv_heads, page_size,
+                          num_slots);
 }
 
 cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,
@@ -372,10 +381,9 @@ cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int pag
     const size_t wanted = (total + threads - 1) / threads;
     const size_t cap = static_cast<size_t>(sm_count()) * 8;
     const int blocks = static_cast<int>(wanted < cap ? wanted : cap);
-    copy_pages_kernel<<<blocks, threads, 0, stream>>>(
-        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), src_pages, dst_pages,
-        num_copies, chunks, num_pages);
-    return cudaGetLastError();
+    return launch_pdl(copy_pages_kernel, dim3(blocks), dim3(threads), 0, stream,
+                      static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), src_pages,
+                      dst_pages, num_copies, chunks, num_pages);
 }
 
 cudaError_t read_and_clear_store_errors(uint32_t *flags)
