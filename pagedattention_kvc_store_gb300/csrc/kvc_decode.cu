@@ -101,14 +101,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int G = a.group;
     const int P = a.page_size;
+    const int k_first = a.key_start ? a.key_start[s] : 0;   // a multiple of page_size
+    const int k_begin = k_first + split * a.chunk;
+    // The producer's first 32 page ids are requested together with the context length (the
+    // chunk's first page does not depend on it), one memory round trip less before the first
+    // TMA copy; entries past the sequence's pages are read but never used.
+    int pre_page = 0;
+    if (warp == kConsumerWarps && k_begin / P + lane < a.bt_stride)
+        pre_page = a.block_table[static_cast<size_t>(s) * a.bt_stride + k_begin / P + lane];
     int ctx = a.context_lens[s];
     if (ctx > a.bt_stride * a.page_size) {   // the block-table row cannot hold it
         if (threadIdx.x == 0 && split == 0)
             atomicOr(&g_decode_errors, kErrContextRange);
         ctx = a.bt_stride * a.page_size;
     }
-    const int k_first = a.key_start ? a.key_start[s] : 0;   // a multiple of page_size
-    const int k_begin = k_first + split * a.chunk;
     const int k_end = min(ctx, k_begin + a.chunk);
     const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
 
@@ -149,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             prefetch_tensormap(&tmap_v);
         }
         const uint64_t policy = l2_policy_evict_first();
-        int cached_base = -32;
-        int cached_page = 0;
+        int cached_base = 0;
+        int cached_page = pre_page;
         int issued = 0;
         bool ok = true;
         for (int b = 0; b < n_blocks; ++b) {
