@@ -303,7 +303,7 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
         "grouped_frac_of_hbm": round(unique_b / (t_g / 1e3) / 1e9 / peaks["hbm"], 4),
         "plain_unique_gbs": round(unique_b / (t_p / 1e3) / 1e9, 1),
         "plain_effective_gbs": round(logical_b / (t_p / 1e3) / 1e9, 1),
-        "gpu_launches_per_step": {"grouped": 5, "plain": 2},
+        "gpu_launches_per_step": {"grouped": 3, "plain": 2},
     }
     del d, out, work_g, work_p, slots
     torch.cuda.empty_cache()

@@ -775,31 +775,27 @@ kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
                                                 s);
     if (err != cudaSuccess)
         return cuda_fail(err, "grouped setup launch");
-    if (g.n_prefix > 0) {
-        kvc::GroupedPrefixLaunch p;
-        p.q = q;
-        p.part_o = part_o;
-        p.part_lse = part_lse;
-        p.block_table = block_table;
-        p.bt_stride = bt_stride;
-        p.group_indptr = group_indptr;
-        p.group_seqs = group_seqs;
-        p.prefix_len = prefix_len;
-        p.num_groups = num_groups;
-        p.max_rows = max_group_size * G;
-        p.num_seqs = num_seqs;
-        p.q_heads = q_heads;
-        p.kv_heads = pool.kv_heads;
-        p.head_dim = pool.head_dim;
-        p.page_size = pool.page_size;
-        p.chunk = g.prefix_chunk;
-        p.n_split = g.n_prefix;
-        p.split_stride = g.stride;
-        p.scale = sc;
-        p.hnd = pool.layout == KVC_HND;
-        if ((err = kvc::launch_grouped_prefix(p, tk, tv, s)) != cudaSuccess)
-            return cuda_fail(err, "grouped prefix launch");
-    }
+    kvc::GroupedPrefixLaunch p;
+    p.q = q;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.block_table = block_table;
+    p.bt_stride = bt_stride;
+    p.group_indptr = group_indptr;
+    p.group_seqs = group_seqs;
+    p.prefix_len = prefix_len;
+    p.num_groups = num_groups;
+    p.max_rows = max_group_size * G;
+    p.num_seqs = num_seqs;
+    p.q_heads = q_heads;
+    p.kv_heads = pool.kv_heads;
+    p.head_dim = pool.head_dim;
+    p.page_size = pool.page_size;
+    p.chunk = g.prefix_chunk;
+    p.n_split = g.n_prefix;
+    p.split_stride = g.stride;
+    p.scale = sc;
+    p.hnd = pool.layout == KVC_HND;
     kvc::DecodeLaunch l;
     l.q = q;
     l.out = out;
@@ -821,8 +817,10 @@ kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
     l.split_base = g.n_prefix;
     l.split_stride = g.stride;
     l.hnd = pool.layout == KVC_HND;
-    if ((err = kvc::launch_decode(l, tk, tv, s)) != cudaSuccess)
-        return cuda_fail(err, "suffix decode launch");
+    if (g.n_prefix == 0)
+        p.num_groups = 0;   // no prefix CTAs
+    if ((err = kvc::launch_grouped_decode(p, l, tk, tv, s)) != cudaSuccess)
+        return cuda_fail(err, "grouped prefix + suffix decode launch");
     if ((err = kvc::launch_merge(out, l.out_f32, part_o, part_lse, num_seqs * q_heads, g.stride,
                                  pool.head_dim, nullptr, s)) != cudaSuccess)
         return cuda_fail(err, "merge launch");

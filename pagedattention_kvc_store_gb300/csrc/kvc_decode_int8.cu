@@ -56,7 +56,8 @@ constexpr int kOffKs = 2 * kCodeBytes;
 constexpr int kOffVs = kOffKs + kScaleBytes;
 constexpr int kStageBytes = ((2 * kCodeBytes + 2 * kScaleBytes) + 1023) & ~1023;
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kCombineBytes = kConsumerWarps * kMaxGroup * (D + 2) * 4;
+constexpr int kCombineBytes =   // o rows, m, l per warp; weights per row
+    kConsumerWarps * kMaxGroup * (D + 4) * 4 + 3 * kConsumerWarps * kMaxGroup * 4;
 static_assert(kCombineBytes <= kRingBytes, "combine area aliases the ring");
 constexpr size_t kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8;
 
@@ -74,14 +75,6 @@ struct Args {
     int chunk, n_split;
     float scale_log2;
 };
-
-__device__ __forceinline__ void store_out(void *out, int out_f32, size_t idx, float v)
-{
-    if (out_f32)
-        static_cast<float *>(out)[idx] = v;
-    else
-        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
-}
 
 // fp16 pair (low: byte c of a, high: byte c of b) of two words of int8 codes, exact.  The
 // bytes are moved under exponent bits 0x64 (fp16 1024 + m for m in 0..255) with the sign bit
@@ -358,22 +351,26 @@ __global__ void __launch_bounds__(kThreads, 3)
         atomicOr(&g_decode_int8_errors, kErrDecodeFullWait);
 
     // ------------------------- combine the 4 warps' partial results -----------------------
+    // Each warp leaves its unnormalised o rows (D + 4 floats apart: 16-byte aligned rows),
+    // running max and row sum; one thread per query head folds them into weights
+    // 2^(m_w - M) / L, and the output is written as float4 (bf16x4) pieces.
+    constexpr int kRowStride = D + 4;
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     named_barrier(1, kConsumerWarps * 32);
-    float *red_o = reinterpret_cast<float *>(smem);               // [W][8][D]
-    float *red_m = red_o + kConsumerWarps * kMaxGroup * D;         // [W][8]
-    float *red_l = red_m + kConsumerWarps * kMaxGroup;             // [W][8]
+    float *red_o = reinterpret_cast<float *>(smem);                      // [W][8][D + 4]
+    float *red_m = red_o + kConsumerWarps * kMaxGroup * kRowStride;       // [W][8]
+    float *red_l = red_m + kConsumerWarps * kMaxGroup;                    // [W][8]
+    float *row_w = red_l + kConsumerWarps * kMaxGroup;                    // [8][W]
 #pragma unroll
     for (int e = 0; e < 2; ++e) {   // query rows 2t and 2t + 1
         const int row = 2 * t + e;
         if (row < G) {
-            float *dst = red_o + (warp * kMaxGroup + row) * D;
+            float *dst = red_o + (warp * kMaxGroup + row) * kRowStride;
 #pragma unroll
             for (int n = 0; n < D / 16; ++n) {
                 const int dim = 32 * (n >> 1) + 4 * r + 2 * (n & 1);
-                dst[dim] = o[n][e];
-                dst[dim + 1] = o[n][2 + e];
+                *reinterpret_cast<float2 *>(dst + dim) = make_float2(o[n][e], o[n][2 + e]);
             }
         }
     }
@@ -382,29 +379,49 @@ __global__ void __launch_bounds__(kThreads, 3)
         red_l[warp * kMaxGroup + r] = l_run;
     }
     named_barrier(1, kConsumerWarps * 32);
-    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
-        const int row = idx / D;
-        const int d = idx - row * D;
+    if (threadIdx.x < G) {
+        const int row = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w)
             M = fmaxf(M, red_m[w * kMaxGroup + row]);
-        float L = 0.0f, O = 0.0f;
+        float f[kConsumerWarps];
+        float L = 0.0f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
             const float mw = red_m[w * kMaxGroup + row];
-            const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
-            L += f * red_l[w * kMaxGroup + row];
-            O += f * red_o[(w * kMaxGroup + row) * D + d];
+            f[w] = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
+            L += f[w] * red_l[w * kMaxGroup + row];
         }
-        const float val = (L > 0.0f) ? O / L : 0.0f;
+        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+            row_w[row * kConsumerWarps + w] = f[w] * inv;
+        if (SPLIT)
+            a.part_lse[(row0 + row) * a.n_split + split] =
+                (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    constexpr int kVec = D / 4;
+    for (int idx = threadIdx.x; idx < G * kVec; idx += kConsumerWarps * 32) {
+        const int row = idx / kVec;
+        const int c = (idx - row * kVec) * 4;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float wt = row_w[row * kConsumerWarps + w];
+            const float4 v = *reinterpret_cast<const float4 *>(
+                red_o + (w * kMaxGroup + row) * kRowStride + c);
+            acc.x = fmaf(wt, v.x, acc.x);
+            acc.y = fmaf(wt, v.y, acc.y);
+            acc.z = fmaf(wt, v.z, acc.z);
+            acc.w = fmaf(wt, v.w, acc.w);
+        }
         if (SPLIT) {
             const size_t prow = (row0 + row) * a.n_split + split;
-            a.part_o[prow * D + d] = val;
-            if (d == 0)
-                a.part_lse[prow] = (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+            *reinterpret_cast<float4 *>(a.part_o + prow * D + c) = acc;
         } else {
-            store_out(a.out, a.out_f32, (row0 + row) * D + d, val);
+            store_out4(a.out, a.out_f32, (row0 + row) * D + c, acc);
         }
     }
 }

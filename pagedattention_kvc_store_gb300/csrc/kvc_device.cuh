@@ -518,6 +518,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// One output element, fp32 or bf16 (round to nearest even) as the caller's out_f32 says.
+__device__ __forceinline__ void store_out(void *out, int out_f32, size_t idx, float v)
+{
+    if (out_f32)
+        static_cast<float *>(out)[idx] = v;
+    else
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// Four consecutive outputs from element idx (a multiple of 4): one 16- or 8-byte store.
+__device__ __forceinline__ void store_out4(void *out, int out_f32, size_t idx, float4 v)
+{
+    if (out_f32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = v;
+    } else {
+        uint2 packed;
+        packed.x = pack_bf16x2(v.x, v.y);
+        packed.y = pack_bf16x2(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + idx) = packed;
+    }
+}
+
 // Sum of the two bf16 values packed in v (exact widening to fp32).  Softmax sums are taken
 // over the rounded probabilities that the PV product actually uses, so that numerator and
 // denominator weigh every position the same.

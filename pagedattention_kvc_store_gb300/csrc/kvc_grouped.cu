@@ -7,17 +7,22 @@
 // only the reading of the shared pages is done once per group instead of once per member.
 //
 // Decomposition (all partials are normalised fp32 pieces with their log-sum-exp):
+//   setup   grouped_setup_kernel: each sequence's key start (the end of its group's prefix,
+//           whole pages; 0 outside groups) and every prefix partial marked empty;
 //   prefix  one CTA per (prefix chunk, kv head, group): the chunk's pages, read once, against
 //           the query rows of every member of the group (members x G rows, at most 64), on
-//           mma.sync tiles of 16 rows -- this kernel;
-//   suffix  each member's positions from the end of the prefix, with the decode kernel
-//           (kvc_decode.cu, started at key_start[s]);
+//           mma.sync tiles of 16 rows;
+//   suffix  one decode CTA (kvc_decode_cta.cuh) per (split, kv head, member) over the
+//           member's positions from its key start;
 //   merge   log-sum-exp over prefix and suffix partials (merge_kernel).
-// A TMA producer warp streams the prefix pages (one box per page) into a 3-deep swizzled
-// ring; four consumer warps cover 1, 2 or 4 row tiles, the warps of one tile splitting each
-// 64-position stage between them and combining through shared memory at the end.
+// Prefix and suffix CTAs are one grid (grouped_decode_kernel), prefix CTAs first: the suffix
+// CTAs take the SMs as the prefix CTAs drain.  A TMA producer warp streams the prefix pages
+// (one box per page) into a 3-deep swizzled ring; four consumer warps cover 1, 2 or 4 row
+// tiles, the warps of one tile splitting each 64-position stage between them and combining
+// through shared memory at the end.
 #include <math.h>
 
+#include "kvc_decode_cta.cuh"
 #include "kvc_device.cuh"
 #include "kvc_launch.h"
 
@@ -39,7 +44,9 @@ struct GroupGeom {
     static constexpr int kTileBytes = kStageKeys * D * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kCombineBytes = kConsumerWarps * 16 * (D + 2) * 4;
+    static constexpr int kCombineBytes =
+        kConsumerWarps * 16 * (D + 8) * 4 + 2 * kConsumerWarps * 16 * 4 +
+        kMaxRows * kConsumerWarps * 4 + kMaxRows * 8;
     static_assert(kCombineBytes <= kRingBytes, "combine area aliases the ring");
     static constexpr size_t kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8;
 };
@@ -54,65 +61,61 @@ struct Args {
     const int32_t *group_seqs;
     const int32_t *prefix_len;
     int q_heads, kv_heads, group, page_size;
-    int chunk, split_stride;
+    int chunk, n_split, split_stride;
     float scale_log2;
     int hnd;   // HND pools: page boxes addressed by (page, kv head) block
 };
 
+// Block 0 sets every sequence's key start: 0, then, for each group member, the end of the
+// group's prefix in whole pages (the two phases separated by the block barrier).  The other
+// blocks mark every prefix split of every row empty (lse -inf): prefix CTAs overwrite the
+// splits that hold positions of a member.
 __global__ void grouped_setup_kernel(float *__restrict__ part_lse, int32_t *__restrict__ key_start,
-                                     int num_seqs, int q_heads, int n_prefix, int split_stride)
+                                     const int32_t *__restrict__ group_indptr,
+                                     const int32_t *__restrict__ group_seqs,
+                                     const int32_t *__restrict__ prefix_len, int num_groups,
+                                     int num_seqs, int q_heads, int n_prefix, int split_stride,
+                                     int page_size, int bt_stride)
 {
     pdl_wait();
     pdl_trigger();
+    if (blockIdx.x == 0) {
+        for (int s = threadIdx.x; s < num_seqs; s += blockDim.x)
+            key_start[s] = 0;
+        __syncthreads();
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int g = warp; g < num_groups; g += blockDim.x >> 5) {
+            int pre = (prefix_len[g] / page_size) * page_size;   // whole pages only
+            pre = min(max(pre, 0), bt_stride * page_size);
+            for (int i = group_indptr[g] + lane; i < group_indptr[g + 1]; i += 32)
+                key_start[group_seqs[i]] = pre;
+        }
+        return;
+    }
     const size_t total = static_cast<size_t>(num_seqs) * q_heads * n_prefix;
-    const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+    const size_t step = static_cast<size_t>(gridDim.x - 1) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < total;
          i += step) {
         const size_t row = i / n_prefix;
         const size_t j = i - row * n_prefix;
         part_lse[row * split_stride + j] = -INFINITY;
     }
-    for (size_t s = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-         s < static_cast<size_t>(num_seqs); s += step)
-        key_start[s] = 0;
 }
 
-__global__ void grouped_members_kernel(int32_t *__restrict__ key_start,
-                                       const int32_t *__restrict__ group_indptr,
-                                       const int32_t *__restrict__ group_seqs,
-                                       const int32_t *__restrict__ prefix_len, int page_size,
-                                       int bt_stride)
-{
-    pdl_wait();
-    pdl_trigger();
-    const int g = blockIdx.x;
-    int pre = (prefix_len[g] / page_size) * page_size;   // whole pages only
-    pre = min(max(pre, 0), bt_stride * page_size);
-    for (int i = group_indptr[g] + threadIdx.x; i < group_indptr[g + 1]; i += blockDim.x)
-        key_start[group_seqs[i]] = pre;
-}
-
+// One prefix CTA: chunk `split` of the shared prefix of group `grp`, kv head `kvh`.
 template <int D, int NMT>
-__global__ void __launch_bounds__(kThreads, 2)
-    grouped_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v, const Args a)
+__device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
+                                           const Args &a, const int split, const int kvh,
+                                           const int grp, uint8_t *smem)
 {
-    pdl_wait();
-    pdl_trigger();
     using Geom = GroupGeom<D>;
     constexpr int kWarpsPerTile = kConsumerWarps / NMT;   // warps sharing one 16-row tile
     constexpr int kKeysPerWarp = kStageKeys / kWarpsPerTile;
     constexpr int kNT = kKeysPerWarp / 8;                  // n-tiles of S per warp and stage
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Geom::kRingBytes);
     uint64_t *empty = full + kStages;
 
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int grp = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.group;
@@ -144,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int32_t *bt_row =
             a.block_table + static_cast<size_t>(leader) * a.bt_stride + first_page;
         if (lane == 0) {
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
+            prefetch_tensormap(tmap_k);
+            prefetch_tensormap(tmap_v);
         }
         const uint64_t policy = l2_policy_evict_first();
         int cached_base = -32;
@@ -184,9 +187,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int c1 = a.hnd ? 0 : page * P;
                 const int c3 = a.hnd ? page * a.kv_heads + kvh : kvh;
                 if (lane & 1)
-                    tma_load_4d_hint(vdst + off, &tmap_v, 0, c1, 0, c3, &full[st], policy);
+                    tma_load_4d_hint(vdst + off, tmap_v, 0, c1, 0, c3, &full[st], policy);
                 else
-                    tma_load_4d_hint(kdst + off, &tmap_k, 0, c1, 0, c3, &full[st], policy);
+                    tma_load_4d_hint(kdst + off, tmap_k, 0, c1, 0, c3, &full[st], policy);
             }
             issued = b + 1;
         }
@@ -229,13 +232,37 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int n = 0; n < D / 8; ++n)
         o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
+    float m_a = -INFINITY, m_b = -INFINITY;
 
+    // ldmatrix addresses.  Inside a stage tile, row `row` of half `h` starts at
+    // ((row / P) * (D / 64) + h) * P * 128 + (row % P) * 128, and 16-byte chunk c of it sits
+    // at chunk c ^ (row & 7).  Every row a lane addresses has row & 7 equal to lane & 7, so the
+    // swizzled chunk of column tile j is (2 (j % 4) + c0) ^ (lane & 7), i.e. (32 (j % 4)) ^ x
+    // bytes for a per-lane x: one add per ldmatrix once the row's offset is known.
     const int log2p = __ffs(P) - 1;
+    const int half_bytes = P * 128;
+    constexpr int kHalves = D / 64;
+    constexpr int kPairs = kNT / 2;             // 16-key groups of a warp's slice
     const int k_row = ksl * kKeysPerWarp + (lane & 7) + ((lane >> 4) << 3);
-    const int k_col = ((lane >> 3) & 1) << 3;
     const int v_row = ksl * kKeysPerWarp + (lane & 7) + (((lane >> 3) & 1) << 3);
-    const int v_col = (lane >> 4) << 3;
+    auto row_offset = [&](int row) {
+        return static_cast<uint32_t>(((row >> log2p) * kHalves) * half_bytes +
+                                     (row & (P - 1)) * 128);
+    };
+    uint32_t k_x[4], v_x[4];
+    {
+        const uint32_t xk = static_cast<uint32_t>((((lane >> 3) & 1) ^ (lane & 7)) << 4);
+        const uint32_t xv = static_cast<uint32_t>(((lane >> 4) ^ (lane & 7)) << 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            k_x[j] = (32u * j) ^ xk;
+            v_x[j] = (32u * j) ^ xv;
+        }
+    }
+    // Row sums of the bf16 probabilities come out of the P.V products: one more n-tile
+    // whose B operand is all ones sums P's rows exactly as the products see them.
+    constexpr uint32_t kOnes = 0x3F803F80u;   // two bf16 1.0
+    float o_l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const float sl2 = a.scale_log2;
     bool ok = true;
 
@@ -254,30 +281,38 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int n = 0; n < kNT; ++n)
                 sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
 #pragma unroll
-            for (int pr = 0; pr < kNT / 2; ++pr) {
+            for (int pr = 0; pr < kPairs; ++pr) {
+                const uint32_t krow = kbase + row_offset(pr * 16 + k_row);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbase + page_tile_offset<D>(pr * 16 + k_row, kk * 16 + k_col, log2p),
-                            b0, b1, b2, b3);
+                    ldsm_x4(krow + (kk / 4) * half_bytes + k_x[kk % 4], b0, b1, b2, b3);
                     mma_bf16_16816(sc[2 * pr], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0,
                                    b1);
                     mma_bf16_16816(sc[2 * pr + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
                                    b2, b3);
                 }
             }
-            float mx_a = -INFINITY, mx_b = -INFINITY;
+            if (n_valid < kKeysPerWarp) {   // warp-uniform: only the last slice of a chunk
 #pragma unroll
-            for (int n = 0; n < kNT; ++n) {
+                for (int n = 0; n < kNT; ++n) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    if (n * 8 + cq + e >= n_valid) {
-                        sc[n][e] = -INFINITY;
-                        sc[n][2 + e] = -INFINITY;
+                    for (int e = 0; e < 2; ++e) {
+                        if (n * 8 + cq + e >= n_valid) {
+                            sc[n][e] = -INFINITY;
+                            sc[n][2 + e] = -INFINITY;
+                        }
                     }
-                    mx_a = fmaxf(mx_a, sc[n][e]);
-                    mx_b = fmaxf(mx_b, sc[n][2 + e]);
                 }
+            }
+            float mx_a = fmax3(sc[0][0], sc[0][1], sc[1][0]);
+            float mx_b = fmax3(sc[0][2], sc[0][3], sc[1][2]);
+            mx_a = fmaxf(mx_a, sc[1][1]);
+            mx_b = fmaxf(mx_b, sc[1][3]);
+#pragma unroll
+            for (int n = 2; n < kNT; ++n) {
+                mx_a = fmax3(mx_a, sc[n][0], sc[n][1]);
+                mx_b = fmax3(mx_b, sc[n][2], sc[n][3]);
             }
             mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
             mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
@@ -294,8 +329,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     o[n][2] *= al_b;
                     o[n][3] *= al_b;
                 }
-                l_a *= al_a;
-                l_b *= al_b;
+                o_l[0] *= al_a;
+                o_l[1] *= al_a;
+                o_l[2] *= al_b;
+                o_l[3] *= al_b;
                 m_a = mn_a;
                 m_b = mn_b;
             }
@@ -308,20 +345,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                                        fast_exp2(fmaf(sc[n][1], sl2, nu_a)));
                 pa[n][1] = pack_bf16x2(fast_exp2(fmaf(sc[n][2], sl2, nu_b)),
                                        fast_exp2(fmaf(sc[n][3], sl2, nu_b)));
-                l_a += bf16x2_sum(pa[n][0]);
-                l_b += bf16x2_sum(pa[n][1]);
             }
 #pragma unroll
-            for (int ks = 0; ks < kKeysPerWarp / 16; ++ks) {
+            for (int ks = 0; ks < kPairs; ++ks) {
                 if (ks * 16 >= n_valid)
                     break;
+                const bool partial = n_valid < (ks + 1) * 16;
+                const uint32_t vrow = vbase + row_offset(ks * 16 + v_row);
 #pragma unroll
                 for (int dt = 0; dt < D / 16; ++dt) {
                     uint32_t v0, v1, v2, v3;
-                    ldsm_x4_trans(vbase + page_tile_offset<D>(ks * 16 + v_row, dt * 16 + v_col,
-                                                              log2p),
-                                  v0, v1, v2, v3);
-                    if (n_valid < (ks + 1) * 16) {
+                    ldsm_x4_trans(vrow + (dt / 4) * half_bytes + v_x[dt % 4], v0, v1, v2, v3);
+                    if (partial) {
                         v0 = keep_keys(v0, ks * 16 + cq, n_valid);
                         v1 = keep_keys(v1, ks * 16 + 8 + cq, n_valid);
                         v2 = keep_keys(v2, ks * 16 + cq, n_valid);
@@ -332,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mma_bf16_16816(o[2 * dt + 1], pa[2 * ks][0], pa[2 * ks][1],
                                    pa[2 * ks + 1][0], pa[2 * ks + 1][1], v2, v3);
                 }
+                mma_bf16_16816(o_l, pa[2 * ks][0], pa[2 * ks][1], pa[2 * ks + 1][0],
+                               pa[2 * ks + 1][1], kOnes, kOnes);
             }
         }
         __syncwarp();
@@ -342,24 +379,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         atomicOr(&g_grouped_errors, kErrDecodeFullWait);
 
     // ------------------- combine the warps of each tile, write partials --------------------
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    // Warp w of tile t leaves its unnormalised o (rows of D + 8 floats: the pad spreads the
+    // 8 rows a store instruction touches over distinct banks), its running max and row sum.
+    // One thread per output row then folds the tile's warps into weights 2^(m_w - M) / L
+    // and finds the row's partial slot; the write-out is float4 loads and stores.
+    constexpr int kRowStride = D + 8;
+    const float l_a = o_l[0], l_b = o_l[2];   // every column of the ones tile holds the sum
     named_barrier(1, kConsumerWarps * 32);   // every warp is done with the ring
-    float *red_o = reinterpret_cast<float *>(smem);                    // [W][16][D]
-    float *red_m = red_o + kConsumerWarps * 16 * D;                     // [W][16]
-    float *red_l = red_m + kConsumerWarps * 16;                         // [W][16]
+    float *red_o = reinterpret_cast<float *>(smem);                        // [W][16][D + 8]
+    float *red_m = red_o + kConsumerWarps * 16 * kRowStride;                // [W][16]
+    float *red_l = red_m + kConsumerWarps * 16;                             // [W][16]
+    float *row_w = red_l + kConsumerWarps * 16;                             // [rows][W / tile]
+    long long *row_slot = reinterpret_cast<long long *>(row_w + kMaxRows * kWarpsPerTile);
     {
         const int la = lane >> 2, lb = la + 8;
-        float *dst_a = red_o + (warp * 16 + la) * D;
-        float *dst_b = red_o + (warp * 16 + lb) * D;
+        float *dst_a = red_o + (warp * 16 + la) * kRowStride + cq;
+        float *dst_b = red_o + (warp * 16 + lb) * kRowStride + cq;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
-            dst_a[n * 8 + cq] = o[n][0];
-            dst_a[n * 8 + cq + 1] = o[n][1];
-            dst_b[n * 8 + cq] = o[n][2];
-            dst_b[n * 8 + cq + 1] = o[n][3];
+            *reinterpret_cast<float2 *>(dst_a + n * 8) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2 *>(dst_b + n * 8) = make_float2(o[n][2], o[n][3]);
         }
         if ((lane & 3) == 0) {
             red_m[warp * 16 + la] = m_a;
@@ -369,76 +408,136 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     named_barrier(1, kConsumerWarps * 32);
-    for (int idx = threadIdx.x; idx < rows * D; idx += kConsumerWarps * 32) {
-        const int r = idx / D;
-        const int d = idx - r * D;
-        const int tile = r >> 4;
-        const int rr = r & 15;
+    for (int r = threadIdx.x; r < rows; r += kConsumerWarps * 32) {
+        const int slot0 = (r >> 4) * kWarpsPerTile * 16 + (r & 15);
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarpsPerTile; ++w)
-            M = fmaxf(M, red_m[(tile * kWarpsPerTile + w) * 16 + rr]);
-        float L = 0.0f, O = 0.0f;
+            M = fmaxf(M, red_m[slot0 + w * 16]);
+        float f[kWarpsPerTile];
+        float L = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarpsPerTile; ++w) {
-            const int slot = (tile * kWarpsPerTile + w) * 16 + rr;
-            const float mw = red_m[slot];
-            const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
-            L += f * red_l[slot];
-            O += f * red_o[slot * D + d];
+            const float mw = red_m[slot0 + w * 16];
+            f[w] = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
+            L += f[w] * red_l[slot0 + w * 16];
         }
+        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerTile; ++w)
+            row_w[r * kWarpsPerTile + w] = f[w] * inv;
         const int m = r / G;
         const int gh = r - m * G;
         const int seq = a.group_seqs[m0 + m];
-        const size_t prow =
-            (static_cast<size_t>(seq) * a.q_heads + static_cast<size_t>(kvh) * G + gh) *
+        const long long prow =
+            (static_cast<long long>(seq) * a.q_heads + static_cast<long long>(kvh) * G + gh) *
                 a.split_stride + split;
-        a.part_o[prow * D + d] = (L > 0.0f) ? O / L : 0.0f;
-        if (d == 0)
-            a.part_lse[prow] = (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+        row_slot[r] = prow;
+        a.part_lse[prow] = (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    constexpr int kVec = D / 4;
+    for (int idx = threadIdx.x; idx < rows * kVec; idx += kConsumerWarps * 32) {
+        const int r = idx / kVec;
+        const int c = (idx - r * kVec) * 4;
+        const float *src = red_o + ((r >> 4) * kWarpsPerTile * 16 + (r & 15)) * kRowStride + c;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int w = 0; w < kWarpsPerTile; ++w) {
+            const float wt = row_w[r * kWarpsPerTile + w];
+            const float4 v = *reinterpret_cast<const float4 *>(src + w * 16 * kRowStride);
+            acc.x = fmaf(wt, v.x, acc.x);
+            acc.y = fmaf(wt, v.y, acc.y);
+            acc.z = fmaf(wt, v.z, acc.z);
+            acc.w = fmaf(wt, v.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(a.part_o + row_slot[r] * D + c) = acc;
+    }
+}
+
+// The whole shared-prefix decode in one grid: CTAs [0, n_prefix) are prefix CTAs ordered
+// (split, kv head, group), the rest the members' suffix decode ordered (split, kv head,
+// sequence).  CTAs start roughly in index order, so the suffix CTAs fill the SMs as the prefix
+// CTAs drain instead of waiting for the last of them.
+template <int D, int NMT>
+__global__ void __launch_bounds__(kThreads, 2)
+    grouped_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const Args a,
+                          const dec::Args da, const int n_prefix_ctas)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int idx = blockIdx.x;
+    if (idx < n_prefix_ctas) {
+        const int split = idx % a.n_split;
+        const int rest = idx / a.n_split;
+        prefix_cta<D, NMT>(&tmap_k, &tmap_v, a, split, rest % a.kv_heads, rest / a.kv_heads,
+                           smem);
+    } else {
+        const int j = idx - n_prefix_ctas;
+        const int split = j % da.n_split;
+        const int rest = j / da.n_split;
+        dec::decode_cta<D, true>(&tmap_k, &tmap_v, da, split, rest % da.kv_heads,
+                                 rest / da.kv_heads, smem, &g_grouped_errors);
     }
 }
 
 template <int D, int NMT>
-cudaError_t launch_t(const GroupedPrefixLaunch &l, const CUtensorMap &tk, const CUtensorMap &tv,
-                     cudaStream_t stream)
+cudaError_t launch_t(const GroupedPrefixLaunch &p, const DecodeLaunch &l, const CUtensorMap &tk,
+                     const CUtensorMap &tv, cudaStream_t stream)
 {
+    static_assert(kThreads == dec::kThreads, "prefix and suffix CTAs share the block shape");
     Args a;
-    a.q = static_cast<const __nv_bfloat16 *>(l.q);
-    a.part_o = l.part_o;
-    a.part_lse = l.part_lse;
-    a.block_table = l.block_table;
-    a.bt_stride = l.bt_stride;
-    a.group_indptr = l.group_indptr;
-    a.group_seqs = l.group_seqs;
-    a.prefix_len = l.prefix_len;
-    a.q_heads = l.q_heads;
-    a.kv_heads = l.kv_heads;
-    a.hnd = l.hnd ? 1 : 0;
-    a.group = l.q_heads / l.kv_heads;
-    a.page_size = l.page_size;
-    a.chunk = l.chunk;
-    a.split_stride = l.split_stride;
-    a.scale_log2 = l.scale * kLog2e;
-    const size_t smem = GroupGeom<D>::kSmemBytes;
-    auto kernel = grouped_prefix_kernel<D, NMT>;
+    a.q = static_cast<const __nv_bfloat16 *>(p.q);
+    a.part_o = p.part_o;
+    a.part_lse = p.part_lse;
+    a.block_table = p.block_table;
+    a.bt_stride = p.bt_stride;
+    a.group_indptr = p.group_indptr;
+    a.group_seqs = p.group_seqs;
+    a.prefix_len = p.prefix_len;
+    a.q_heads = p.q_heads;
+    a.kv_heads = p.kv_heads;
+    a.hnd = p.hnd ? 1 : 0;
+    a.group = p.q_heads / p.kv_heads;
+    a.page_size = p.page_size;
+    a.chunk = p.chunk;
+    a.n_split = p.n_split > 0 ? p.n_split : 1;
+    a.split_stride = p.split_stride;
+    a.scale_log2 = p.scale * kLog2e;
+    const dec::Args da = dec::make_args(l);
+    const long long n_prefix =
+        p.num_groups > 0 ? static_cast<long long>(p.n_split) * p.kv_heads * p.num_groups : 0;
+    const long long n_ctas =
+        n_prefix + static_cast<long long>(l.n_split) * l.kv_heads * l.num_seqs;
+    if (n_ctas == 0)
+        return cudaSuccess;
+    if (n_ctas > 0x7FFFFFFFLL)
+        return cudaErrorInvalidConfiguration;
+    const size_t smem = GroupGeom<D>::kSmemBytes > dec::DecodeGeom<D>::kSmemBytes
+                            ? GroupGeom<D>::kSmemBytes
+                            : dec::DecodeGeom<D>::kSmemBytes;
+    auto kernel = grouped_decode_kernel<D, NMT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess)
         return err;
-    dim3 grid(l.n_split, l.kv_heads, l.num_groups);
-    return launch_pdl(kernel, grid, dim3(kThreads), smem, stream, tk, tv, a);
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(n_ctas)), dim3(kThreads), smem, stream,
+                      tk, tv, a, da, static_cast<int>(n_prefix));
 }
 
 template <int D>
-cudaError_t launch_d(const GroupedPrefixLaunch &l, const CUtensorMap &tk, const CUtensorMap &tv,
-                     cudaStream_t stream)
+cudaError_t launch_d(const GroupedPrefixLaunch &p, const DecodeLaunch &l, const CUtensorMap &tk,
+                     const CUtensorMap &tv, cudaStream_t stream)
 {
-    if (l.max_rows <= 16)
-        return launch_t<D, 1>(l, tk, tv, stream);
-    if (l.max_rows <= 32)
-        return launch_t<D, 2>(l, tk, tv, stream);
-    return launch_t<D, 4>(l, tk, tv, stream);
+    if (p.max_rows <= 16)
+        return launch_t<D, 1>(p, l, tk, tv, stream);
+    if (p.max_rows <= 32)
+        return launch_t<D, 2>(p, l, tk, tv, stream);
+    return launch_t<D, 4>(p, l, tk, tv, stream);
 }
 
 }  // namespace
@@ -451,22 +550,18 @@ cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int3
 {
     const size_t total = static_cast<size_t>(num_seqs) * q_heads * n_prefix_splits;
     const size_t want = (total + 255) / 256;
-    const int blocks = static_cast<int>(want < 1024 ? (want > 0 ? want : 1) : 1024);
-    cudaError_t err = launch_pdl(grouped_setup_kernel, dim3(blocks), dim3(256), 0, stream,
-                                 part_lse, key_start, num_seqs, q_heads, n_prefix_splits,
-                                 split_stride);
-    if (err == cudaSuccess && num_groups > 0)
-        err = launch_pdl(grouped_members_kernel, dim3(num_groups), dim3(128), 0, stream,
-                         key_start, group_indptr, group_seqs, prefix_len, page_size, bt_stride);
-    return err;
+    const int blocks = 1 + static_cast<int>(want < 1024 ? want : 1024);
+    return launch_pdl(grouped_setup_kernel, dim3(blocks), dim3(256), 0, stream, part_lse,
+                      key_start, group_indptr, group_seqs, prefix_len, num_groups, num_seqs,
+                      q_heads, n_prefix_splits, split_stride, page_size, bt_stride);
 }
 
-cudaError_t launch_grouped_prefix(const GroupedPrefixLaunch &l, const CUtensorMap &tk,
-                                  const CUtensorMap &tv, cudaStream_t stream)
+cudaError_t launch_grouped_decode(const GroupedPrefixLaunch &p, const DecodeLaunch &l,
+                                  const CUtensorMap &tk, const CUtensorMap &tv,
+                                  cudaStream_t stream)
 {
-    if (l.num_groups == 0 || l.n_split == 0)
-        return cudaSuccess;
-    return l.head_dim == 128 ? launch_d<128>(l, tk, tv, stream) : launch_d<64>(l, tk, tv, stream);
+    return p.head_dim == 128 ? launch_d<128>(p, l, tk, tv, stream)
+                             : launch_d<64>(p, l, tk, tv, stream);
 }
 
 cudaError_t read_and_clear_grouped_errors(uint32_t *flags)

@@ -155,8 +155,11 @@ cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int3
                                  int num_groups, int num_seqs, int q_heads, int n_prefix_splits,
                                  int split_stride, int page_size, int bt_stride,
                                  cudaStream_t stream);
-cudaError_t launch_grouped_prefix(const GroupedPrefixLaunch &a, const CUtensorMap &tmap_k,
-                                  const CUtensorMap &tmap_v, cudaStream_t stream);
+// The prefix CTAs of `p` and the suffix decode of `l` (key_start set, partials after the
+// prefix splits) in one grid.
+cudaError_t launch_grouped_decode(const GroupedPrefixLaunch &p, const DecodeLaunch &l,
+                                  const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                  cudaStream_t stream);
 // tmap_q views q as [T][kv_heads][G][head_dim] with 128-row boxes; tmap_kn / tmap_vn (fused
 // only) view k_new / v_new as {head_dim, kv head, token} with {64, 1, page_size} boxes.
 cudaError_t launch_append_tc(const AppendLaunch &a, const CUtensorMap &tmap_q,
