@@ -55,6 +55,10 @@ def parse_args():
     p.add_argument("--no-legs", action="store_true",
                    help="skip the shared-prefix and long-context decode legs")
     p.add_argument("--leg-steps", type=int, default=30)
+    p.add_argument("--legs", type=lambda v: v.split(","),
+                   default=["shared_prefix", "long_decode", "int8_decode", "hnd_decode",
+                            "page_copy"],
+                   help="comma-separated decode legs to run (default: all)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -213,9 +217,26 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def traffic_from_profile(kernel_tag: str, source_file: str):
-    """DRAM bytes per launch recorded by ncu for this kernel, if the kernel source has not
-    changed since (the summary records the source's sha256 prefix)."""
+# Sources (under the package's csrc/) that make up each profiled kernel, hashed in this order.
+PROFILE_SOURCES = {
+    "decode_batched": ("kvc_decode.cu", "kvc_decode_cta.cuh", "kvc_device.cuh"),
+    "grouped_shared_prefix": ("kvc_grouped.cu", "kvc_decode_cta.cuh", "kvc_device.cuh"),
+    "decode_int8_batched": ("kvc_decode_int8.cu", "kvc_device.cuh"),
+    "append_rewind_p16": ("kvc_append_tc.cu", "kvc_append_items.cuh", "kvc_device.cuh"),
+    "append_int8_rewind_p16": ("kvc_append_int8.cu", "kvc_append_items.cuh", "kvc_device.cuh"),
+}
+
+
+def profile_digest(kernel_tag: str) -> str:
+    h = hashlib.sha256()
+    for f in PROFILE_SOURCES[kernel_tag]:
+        h.update(open(os.path.join(ROOT, "pagedattention_kvc_store_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def traffic_from_profile(kernel_tag: str):
+    """DRAM bytes per launch recorded by ncu for this kernel, if none of its sources has
+    changed since (the summary records their sha256 prefix)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     try:
         text = open(path).read()
@@ -225,9 +246,7 @@ def traffic_from_profile(kernel_tag: str, source_file: str):
                   text)
     if not m:
         return None
-    src = os.path.join(ROOT, "pagedattention_kvc_store_gb300", "csrc", source_file)
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m.group(1)) if digest.startswith(m.group(2)) else None
+    return float(m.group(1)) if profile_digest(kernel_tag).startswith(m.group(2)) else None
 
 
 # ---------------------------------------------------------------------------------------
@@ -266,160 +285,167 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     legs = {}
     per_pos = lambda c: 2 * c.kv_heads * c.head_dim * 2
     qo = lambda c: 2 * c.num_seqs * c.q_heads * c.head_dim * 2
-    # shared prefix: 32 groups x 8 sequences over 2,048 shared positions
-    case = config_case(3, seed=rank_seed(3, rank))
-    d = to_device(case, dev)
-    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
-    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
-    kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
-    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
-                      device=dev)
-    indptr = np.arange(0, case.num_seqs + 1, 8, dtype=np.int32)
-    prefix = np.full(len(case.groups), case.shared_positions, np.int32)
-    gi, gs, gp = (i32_tensor(indptr, dev), i32_tensor(np.concatenate(case.groups), dev),
-                  i32_tensor(prefix, dev))
-    pool = kvc.pool_desc(d.k_pool)
-    ws_g = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
-                                             len(case.groups), int(prefix.max()))
-    work_g = torch.empty(ws_g, dtype=torch.uint8, device=dev)
-    _, _, ws_p = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
-    work_p = torch.empty(max(ws_p, 16), dtype=torch.uint8, device=dev)
-    with torch.cuda.stream(stream):
-        t_g = time_graph(torch, lambda: kvc.kvc_decode_shared_prefix(
-            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx, gi, gs,
-            gp, 8, int(prefix.max()), work_g), stream, flush, args.leg_steps)
-        t_p = time_graph(torch, lambda: kvc.kvc_decode(
-            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
-            num_splits=0, workspace=work_p), stream, flush, args.leg_steps)
-    unique_pos = int(case.context_lens.sum()) - 7 * len(case.groups) * int(prefix[0])
-    unique_b = unique_pos * per_pos(case) + qo(case)
-    logical_b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
-    legs["shared_prefix"] = {
-        "workload": "32 groups x 8 seqs, 2,048 shared positions + U[64,512] own, 32/8 heads, "
-                    "D 128, P 16",
-        "grouped_us": round(t_g * 1e3, 1), "plain_us": round(t_p * 1e3, 1),
-        "unique_bytes": unique_b, "logical_bytes": logical_b,
-        "grouped_unique_gbs": round(unique_b / (t_g / 1e3) / 1e9, 1),
-        "grouped_frac_of_hbm": round(unique_b / (t_g / 1e3) / 1e9 / peaks["hbm"], 4),
-        "plain_unique_gbs": round(unique_b / (t_p / 1e3) / 1e9, 1),
-        "plain_effective_gbs": round(logical_b / (t_p / 1e3) / 1e9, 1),
-        "gpu_launches_per_step": {"grouped": 3, "plain": 2},
-    }
-    del d, out, work_g, work_p, slots
-    torch.cuda.empty_cache()
-    # long context: 8 sequences of 32k..128k positions
-    case = config_case(5, seed=rank_seed(5, rank))
-    d = to_device(case, dev)
-    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
-    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
-    kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
-    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
-                      device=dev)
-    pool = kvc.pool_desc(d.k_pool)
-    splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
-    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-    with torch.cuda.stream(stream):
-        t = time_graph(torch, lambda: kvc.kvc_decode(
-            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
-            num_splits=0, workspace=work), stream, flush, args.leg_steps)
-    b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
-    legs["long_decode"] = {
-        "workload": "8 seqs, ctx U[32768,131072], 64/8 heads, D 128, P 64, split-K + merge",
-        "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
-        "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
-        "chunk": chunk, "gpu_launches_per_step": 2,
-    }
-    del d, out, work, slots
-    torch.cuda.empty_cache()
-    # INT8 pages: the batched-decode batch quantised by kvc_store_int8 (every slot of the bf16
-    # pools, as if each were a new token), decoded by kvc_decode_int8 beside kvc_decode
-    case = config_case(2, seed=rank_seed(2, rank))
-    d = to_device(case, dev)
-    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
-    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
-    kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
-    pages, P, H, D = (int(x) for x in d.k_pool.shape)
-    kc = torch.empty(pages, P, H, D, dtype=torch.int8, device=dev)
-    vc = torch.empty_like(kc)
-    ks = torch.empty(pages, H, P, dtype=torch.float32, device=dev)
-    vs = torch.empty_like(ks)
-    all_slots = torch.arange(pages * P, dtype=torch.int32, device=dev)
-    kvc.kvc_store_int8(kc, vc, ks, vs, d.k_pool.view(pages * P, H, D),
-                       d.v_pool.view(pages * P, H, D), all_slots)
-    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
-                      device=dev)
-    pool = kvc.pool_desc(d.k_pool)
-    splits, chunk, ws = kvc.kvc_decode_int8_plan(case.num_seqs, case.q_heads, pool,
-                                                 case.max_ctx, 0)
-    _, _, ws16 = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
-    work = torch.empty(max(ws, ws16, 16), dtype=torch.uint8, device=dev)
-    with torch.cuda.stream(stream):
-        t8 = time_graph(torch, lambda: kvc.kvc_decode_int8(
-            out, d.q, kc, vc, ks, vs, d.block_table, d.context_lens, case.max_ctx,
-            num_splits=0, workspace=work), stream, flush, args.leg_steps)
-        t16 = time_graph(torch, lambda: kvc.kvc_decode(
-            out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
-            num_splits=0, workspace=work), stream, flush, args.leg_steps)
-    b8 = int(case.context_lens.sum()) * 2 * H * (D + 4) + qo(case)
-    b16 = decode_bytes(case)
-    legs["int8_decode"] = {
-        "workload": "batched decode on INT8 pages: 64 seqs, ctx U[512,4096], 32/8 heads, D 128, "
-                    "P 16 (132 B per vector)",
-        "us": round(t8 * 1e3, 1), "bytes": b8, "gbs": round(b8 / (t8 / 1e3) / 1e9, 1),
-        "frac_of_hbm": round(b8 / (t8 / 1e3) / 1e9 / peaks["hbm"], 4),
-        "bf16_us": round(t16 * 1e3, 1), "bf16_bytes": b16,
-        "speedup_vs_bf16": round(t16 / t8, 3), "splits": splits,
-        "gpu_launches_per_step": 2 if splits > 1 else 1,
-    }
-    del d, out, work, slots, kc, vc, ks, vs, all_slots
-    torch.cuda.empty_cache()
-    # HND pools (one contiguous block per page and kv head): the batched-decode batch
-    case = config_case(2, seed=rank_seed(2, rank))
-    d = to_device(case, dev)
-    kh = d.k_pool.permute(0, 2, 1, 3).contiguous()
-    vh = d.v_pool.permute(0, 2, 1, 3).contiguous()
-    del d.k_pool, d.v_pool
-    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
-    kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
-    kvc.kvc_store(kh, vh, d.k_new, d.v_new, slots, layout="hnd")
-    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
-                      device=dev)
-    pool = kvc.pool_desc(kh, "hnd")
-    splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
-    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-    with torch.cuda.stream(stream):
-        t = time_graph(torch, lambda: kvc.kvc_decode(
-            out, d.q, kh, vh, d.block_table, d.context_lens, case.max_ctx, num_splits=0,
-            workspace=work, layout="hnd"), stream, flush, args.leg_steps)
-    b = decode_bytes(case)
-    legs["hnd_decode"] = {
-        "workload": "batched decode on HND pools: 64 seqs, ctx U[512,4096], 32/8 heads, D 128, "
-                    "P 16",
-        "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
-        "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
-        "gpu_launches_per_step": 2 if splits > 1 else 1,
-    }
-    del d, out, work, slots, kh, vh
-    torch.cuda.empty_cache()
-    # copy-on-write page copies: 4,096 pages of P 16 x 8 kv heads x D 128 (32 KB per pool)
-    # from one half of a 16,384-page pool to shuffled pages of the other half
-    n_pages, n_copy = 16384, 4096
-    rng = np.random.default_rng(rank_seed(6, rank) or 6)
-    kp = torch.empty(n_pages, 16, 8, 128, dtype=torch.bfloat16, device=dev).normal_()
-    vp = torch.empty_like(kp).normal_()
-    perm = rng.permutation(n_pages).astype(np.int32)
-    src, dst = i32_tensor(perm[:n_copy], dev), i32_tensor(perm[n_copy:2 * n_copy], dev)
-    with torch.cuda.stream(stream):
-        t = time_graph(torch, lambda: kvc.kvc_copy_pages(kp, vp, src, dst), stream, flush,
-                       args.leg_steps)
-    b = 2 * 2 * n_copy * 16 * 8 * 128 * 2          # K and V, read and written
-    legs["page_copy"] = {
-        "workload": "copy-on-write of 4,096 pages (P 16, 8 kv heads, D 128) in a 16,384-page pool",
-        "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
-        "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "gpu_launches_per_step": 1,
-    }
-    del kp, vp
-    torch.cuda.empty_cache()
+    if "shared_prefix" in args.legs:
+        # shared prefix: 32 groups x 8 sequences over 2,048 shared positions
+        case = config_case(3, seed=rank_seed(3, rank))
+        d = to_device(case, dev)
+        slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+        kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+        kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+        out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                          device=dev)
+        indptr = np.arange(0, case.num_seqs + 1, 8, dtype=np.int32)
+        prefix = np.full(len(case.groups), case.shared_positions, np.int32)
+        gi, gs, gp = (i32_tensor(indptr, dev), i32_tensor(np.concatenate(case.groups), dev),
+                      i32_tensor(prefix, dev))
+        pool = kvc.pool_desc(d.k_pool)
+        ws_g = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
+                                                 len(case.groups), int(prefix.max()))
+        work_g = torch.empty(ws_g, dtype=torch.uint8, device=dev)
+        _, _, ws_p = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+        work_p = torch.empty(max(ws_p, 16), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            t_g = time_graph(torch, lambda: kvc.kvc_decode_shared_prefix(
+                out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx, gi, gs,
+                gp, 8, int(prefix.max()), work_g), stream, flush, args.leg_steps)
+            t_p = time_graph(torch, lambda: kvc.kvc_decode(
+                out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+                num_splits=0, workspace=work_p), stream, flush, args.leg_steps)
+        unique_pos = int(case.context_lens.sum()) - 7 * len(case.groups) * int(prefix[0])
+        unique_b = unique_pos * per_pos(case) + qo(case)
+        logical_b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
+        legs["shared_prefix"] = {
+            "workload": "32 groups x 8 seqs, 2,048 shared positions + U[64,512] own, 32/8 heads, "
+                        "D 128, P 16",
+            "grouped_us": round(t_g * 1e3, 1), "plain_us": round(t_p * 1e3, 1),
+            "unique_bytes": unique_b, "logical_bytes": logical_b,
+            "grouped_unique_gbs": round(unique_b / (t_g / 1e3) / 1e9, 1),
+            "grouped_frac_of_hbm": round(unique_b / (t_g / 1e3) / 1e9 / peaks["hbm"], 4),
+            "plain_unique_gbs": round(unique_b / (t_p / 1e3) / 1e9, 1),
+            "plain_effective_gbs": round(logical_b / (t_p / 1e3) / 1e9, 1),
+            "gpu_launches_per_step": {"grouped": 3, "plain": 2},
+            "traffic_grouped_decode_kernel": traffic_from_profile("grouped_shared_prefix"),
+        }
+        del d, out, work_g, work_p, slots
+        torch.cuda.empty_cache()
+    if "long_decode" in args.legs:
+        # long context: 8 sequences of 32k..128k positions
+        case = config_case(5, seed=rank_seed(5, rank))
+        d = to_device(case, dev)
+        slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+        kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+        kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+        out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                          device=dev)
+        pool = kvc.pool_desc(d.k_pool)
+        splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+        work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            t = time_graph(torch, lambda: kvc.kvc_decode(
+                out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+                num_splits=0, workspace=work), stream, flush, args.leg_steps)
+        b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
+        legs["long_decode"] = {
+            "workload": "8 seqs, ctx U[32768,131072], 64/8 heads, D 128, P 64, split-K + merge",
+            "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
+            "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
+            "chunk": chunk, "gpu_launches_per_step": 2,
+        }
+        del d, out, work, slots
+        torch.cuda.empty_cache()
+    if "int8_decode" in args.legs:
+        # INT8 pages: the batched-decode batch quantised by kvc_store_int8 (every slot of the bf16
+        # pools, as if each were a new token), decoded by kvc_decode_int8 beside kvc_decode
+        case = config_case(2, seed=rank_seed(2, rank))
+        d = to_device(case, dev)
+        slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+        kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+        kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+        pages, P, H, D = (int(x) for x in d.k_pool.shape)
+        kc = torch.empty(pages, P, H, D, dtype=torch.int8, device=dev)
+        vc = torch.empty_like(kc)
+        ks = torch.empty(pages, H, P, dtype=torch.float32, device=dev)
+        vs = torch.empty_like(ks)
+        all_slots = torch.arange(pages * P, dtype=torch.int32, device=dev)
+        kvc.kvc_store_int8(kc, vc, ks, vs, d.k_pool.view(pages * P, H, D),
+                           d.v_pool.view(pages * P, H, D), all_slots)
+        out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                          device=dev)
+        pool = kvc.pool_desc(d.k_pool)
+        splits, chunk, ws = kvc.kvc_decode_int8_plan(case.num_seqs, case.q_heads, pool,
+                                                     case.max_ctx, 0)
+        _, _, ws16 = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+        work = torch.empty(max(ws, ws16, 16), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            t8 = time_graph(torch, lambda: kvc.kvc_decode_int8(
+                out, d.q, kc, vc, ks, vs, d.block_table, d.context_lens, case.max_ctx,
+                num_splits=0, workspace=work), stream, flush, args.leg_steps)
+            t16 = time_graph(torch, lambda: kvc.kvc_decode(
+                out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+                num_splits=0, workspace=work), stream, flush, args.leg_steps)
+        b8 = int(case.context_lens.sum()) * 2 * H * (D + 4) + qo(case)
+        b16 = decode_bytes(case)
+        legs["int8_decode"] = {
+            "workload": "batched decode on INT8 pages: 64 seqs, ctx U[512,4096], 32/8 heads, D 128, "
+                        "P 16 (132 B per vector)",
+            "us": round(t8 * 1e3, 1), "bytes": b8, "gbs": round(b8 / (t8 / 1e3) / 1e9, 1),
+            "frac_of_hbm": round(b8 / (t8 / 1e3) / 1e9 / peaks["hbm"], 4),
+            "bf16_us": round(t16 * 1e3, 1), "bf16_bytes": b16,
+            "speedup_vs_bf16": round(t16 / t8, 3), "splits": splits,
+            "gpu_launches_per_step": 2 if splits > 1 else 1,
+            "traffic_decode_int8_kernel": traffic_from_profile("decode_int8_batched"),
+        }
+        del d, out, work, slots, kc, vc, ks, vs, all_slots
+        torch.cuda.empty_cache()
+    if "hnd_decode" in args.legs:
+        # HND pools (one contiguous block per page and kv head): the batched-decode batch
+        case = config_case(2, seed=rank_seed(2, rank))
+        d = to_device(case, dev)
+        kh = d.k_pool.permute(0, 2, 1, 3).contiguous()
+        vh = d.v_pool.permute(0, 2, 1, 3).contiguous()
+        del d.k_pool, d.v_pool
+        slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+        kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+        kvc.kvc_store(kh, vh, d.k_new, d.v_new, slots, layout="hnd")
+        out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                          device=dev)
+        pool = kvc.pool_desc(kh, "hnd")
+        splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+        work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            t = time_graph(torch, lambda: kvc.kvc_decode(
+                out, d.q, kh, vh, d.block_table, d.context_lens, case.max_ctx, num_splits=0,
+                workspace=work, layout="hnd"), stream, flush, args.leg_steps)
+        b = decode_bytes(case)
+        legs["hnd_decode"] = {
+            "workload": "batched decode on HND pools: 64 seqs, ctx U[512,4096], 32/8 heads, D 128, "
+                        "P 16",
+            "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
+            "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
+            "gpu_launches_per_step": 2 if splits > 1 else 1,
+        }
+        del d, out, work, slots, kh, vh
+        torch.cuda.empty_cache()
+    if "page_copy" in args.legs:
+        # copy-on-write page copies: 4,096 pages of P 16 x 8 kv heads x D 128 (32 KB per pool)
+        # from one half of a 16,384-page pool to shuffled pages of the other half
+        n_pages, n_copy = 16384, 4096
+        rng = np.random.default_rng(rank_seed(6, rank) or 6)
+        kp = torch.empty(n_pages, 16, 8, 128, dtype=torch.bfloat16, device=dev).normal_()
+        vp = torch.empty_like(kp).normal_()
+        perm = rng.permutation(n_pages).astype(np.int32)
+        src, dst = i32_tensor(perm[:n_copy], dev), i32_tensor(perm[n_copy:2 * n_copy], dev)
+        with torch.cuda.stream(stream):
+            t = time_graph(torch, lambda: kvc.kvc_copy_pages(kp, vp, src, dst), stream, flush,
+                           args.leg_steps)
+        b = 2 * 2 * n_copy * 16 * 8 * 128 * 2          # K and V, read and written
+        legs["page_copy"] = {
+            "workload": "copy-on-write of 4,096 pages (P 16, 8 kv heads, D 128) in a 16,384-page pool",
+            "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
+            "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "gpu_launches_per_step": 1,
+        }
+        del kp, vp
+        torch.cuda.empty_cache()
     return legs
 
 
@@ -533,7 +559,7 @@ def run_kvc(args):
                      "peak_source": f"of {peaks['source']} (copy bandwidth)",
                      "kernel": "paged_decode_kernel + merge_kernel (one kvc_decode call)",
                      "bytes_per_launch": dec_b,
-                     "traffic": traffic_from_profile("decode_batched", "kvc_decode.cu")},
+                     "traffic": traffic_from_profile("decode_batched")},
         "gpu_launches": K * launches_per_step,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
@@ -682,7 +708,7 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "roofline_frac": round(t_roof / t, 4),
             "store_gbs": round(store_bytes(case) / (statistics.mean(st_ms) / 1e3) / 1e9, 1),
             "gpu_launches": args.append_steps * 3,
-            "traffic": (traffic_from_profile("append_rewind_p16", "kvc_append_tc.cu")
+            "traffic": (traffic_from_profile("append_rewind_p16")
                         if P == 16 and args.append_docs == 1000 else None),
         }
         del g1, g2
@@ -723,7 +749,7 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "gbs": round(b8 / t8 / 1e9, 1), "bytes": b8,
             "roofline_frac": round(t8_roof / t8, 4), "speedup_vs_bf16": round(t / t8, 3),
             "gpu_launches": args.append_steps,
-            "traffic": (traffic_from_profile("append_int8_rewind_p16", "kvc_append_int8.cu")
+            "traffic": (traffic_from_profile("append_int8_rewind_p16")
                         if P == 16 and args.append_docs == 1000 else None),
         }
         del d, out, slots, kc, vc, ks, vs, all_slots
