@@ -26,7 +26,8 @@
  * Scale.  Scores are q.k * scale; scale <= 0 selects 1/sqrt(head_dim).
  * Memory.  Every pointer argument named *pool, q, k_new, v_new, out, block_table,
  *   context_lens, q_indptr, slot_mapping, partial_*, workspace is a DEVICE pointer owned by
- *   the caller.  The library allocates no memory, holds no pointer after a call returns,
+ *   the caller (the decode calls' out may also be pinned host memory, see kvc_decode).
+ *   The library allocates no memory, holds no pointer after a call returns,
  *   and never synchronises: each call only enqueues kernels on `stream` (a cudaStream_t;
  *   NULL is the legacy default stream).  Device arrays are not read on the host, so per-step
  *   values may change between replays of a captured graph.
@@ -134,7 +135,12 @@ kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void 
  * fp32 partial, normalised over its own keys, and its log-sum-exp into the workspace, and
  * kvc_merge (enqueued by this call) combines them.  The result does not depend on the
  * split count beyond fp32 rounding.
- *   out           [num_seqs][q_heads][head_dim], out_dtype KVC_BF16 or KVC_F32
+ *   out           [num_seqs][q_heads][head_dim], out_dtype KVC_BF16 or KVC_F32.  Device
+ *                 memory, or pinned host memory that the device reaches at its host
+ *                 address (cudaHostAlloc / cudaHostRegister on a UVA system): the kernel
+ *                 that finishes each row then writes it straight to host memory, so the
+ *                 result is on the host when the call's work completes, with no copy to
+ *                 enqueue.  Any other host pointer: KVC_ERR_INVALID_ARG, nothing enqueued.
  *   q             bf16 [num_seqs][q_heads][head_dim]
  *   max_ctx       host upper bound on every context_lens[s] (sizes the launch)
  *   num_splits    0 = choose automatically, 1 = no split, n > 1 = at most n chunks
@@ -232,7 +238,8 @@ kvc_status kvc_decode_noalloc(void *out, int32_t out_dtype, const void *q,
  *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M);
  *   out[r] = sum_j w_j partial_o[r][j] / sum_j w_j;   lse_out[r] = M + log(sum_j w_j).
  * Splits with lse = -inf hold no key: their partial_o is not read.  A row whose splits are
- * all empty gets out = 0 and lse_out = -inf.  (The pages leave partitioning and combining
+ * all empty gets out = 0 and lse_out = -inf.  out may be pinned host memory, as for
+ * kvc_decode.  (The pages leave partitioning and combining
  * inside the kernel open -- "KV Cache Management and PagedAttention", "Compute attention
  * over scattered KV"; this is the plain combination of softmax-normalised pieces.)
  *   partial_o    fp32 [rows][num_splits][head_dim]

@@ -388,6 +388,26 @@ GroupPlan make_group_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc
     return g;
 }
 
+// `out` of the decode entry points may be device (or managed) memory, or pinned host memory
+// that the device reaches at the same address (cudaHostAlloc / cudaHostRegister on a UVA
+// system): the kernel that finishes a row then writes it straight to host memory.
+kvc_status check_decode_out(const void *out)
+{
+    if (out == nullptr)
+        return KVC_OK;   // num_seqs == 0, checked by the caller
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, out) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(KVC_ERR_INVALID_ARG, "out: not a CUDA-visible pointer");
+    }
+    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
+        return KVC_OK;
+    if (attr.type == cudaMemoryTypeHost && attr.devicePointer == out)
+        return KVC_OK;
+    return fail(KVC_ERR_INVALID_ARG,
+                "out must be device memory or pinned host memory mapped at its host address");
+}
+
 kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *q,
                                 const void *k_pool, const void *v_pool,
                                 const kvc_pool_desc &pool, const int32_t *block_table,
@@ -667,6 +687,8 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
         if (!aligned16(workspace))
             return fail(KVC_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     }
+    if ((st = check_decode_out(out)) != KVC_OK)
+        return st;
     CUtensorMap tk, tv;
     if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
         return st;
@@ -843,6 +865,8 @@ kvc_status kvc_merge(void *out, int32_t out_dtype, const float *partial_o,
         return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
     if (!aligned16(partial_o) || !aligned16(out))
         return fail(KVC_ERR_INVALID_ARG, "partial_o and out must be 16-byte aligned");
+    if (kvc_status st = check_decode_out(out); st != KVC_OK)
+        return st;
     cudaError_t err = kvc::launch_merge(out, out_dtype == KVC_F32, partial_o, partial_lse, rows,
                                         num_splits, head_dim, lse_out,
                                         static_cast<cudaStream_t>(stream));

@@ -99,9 +99,11 @@ __global__ void __launch_bounds__(128) merge_kernel(void *out, int out_f32,
     }
     const float inv = (sum > 0.0f) ? 1.0f / sum : 0.0f;
     const size_t base = static_cast<size_t>(row) * D + lane * V;
-#pragma unroll
-    for (int v = 0; v < V; ++v)
-        store_out(out, out_f32, base + v, acc[v] * inv);
+    if constexpr (V == 4)
+        store_out4(out, out_f32, base,
+                   make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv));
+    else
+        store_out2(out, out_f32, base, make_float2(acc[0] * inv, acc[1] * inv));
     if (lse_out != nullptr && lane == 0)
         lse_out[row] = (M == -INFINITY) ? -INFINITY : M + logf(sum);
 }

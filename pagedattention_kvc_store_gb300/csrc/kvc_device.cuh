@@ -527,6 +527,16 @@ __device__ __forceinline__ void store_out(void *out, int out_f32, size_t idx, fl
         static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
 }
 
+// Two consecutive outputs from element idx (even): one 8- or 4-byte store.
+__device__ __forceinline__ void store_out2(void *out, int out_f32, size_t idx, float2 v)
+{
+    if (out_f32)
+        *reinterpret_cast<float2 *>(static_cast<float *>(out) + idx) = v;
+    else
+        *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(out) + idx) =
+            pack_bf16x2(v.x, v.y);
+}
+
 // Four consecutive outputs from element idx (a multiple of 4): one 16- or 8-byte store.
 __device__ __forceinline__ void store_out4(void *out, int out_f32, size_t idx, float4 v)
 {

@@ -152,6 +152,18 @@ def _cuda(name: str, t: torch.Tensor, dtype=None, contiguous=True) -> torch.Tens
     return t
 
 
+def _decode_out(t: torch.Tensor) -> torch.Tensor:
+    """`out` of the decode calls: a CUDA tensor, or a pinned host tensor that the kernels
+    write directly (the result lands in host memory with no separate copy)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError("out must be a CUDA tensor or a pinned host tensor")
+        if not t.is_contiguous():
+            raise ValueError("out must be contiguous")
+        return t
+    return _cuda("out", t)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -314,7 +326,7 @@ def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
                scale: float = 0.0, num_splits: int = 0,
                workspace: Optional[torch.Tensor] = None, stream=None,
                layout: str = "nhd") -> None:
-    _cuda("out", out)
+    _decode_out(out)
     _cuda("q", q, torch.bfloat16)
     _cuda("k_pool", k_pool, torch.bfloat16)
     _cuda("v_pool", v_pool, torch.bfloat16)
@@ -335,7 +347,7 @@ def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
 def kvc_merge(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,
               lse_out: Optional[torch.Tensor] = None, stream=None) -> None:
     """partial_o [rows, splits, D] fp32, partial_lse [rows, splits] fp32 -> out [rows, D]."""
-    _cuda("out", out)
+    _decode_out(out)
     _cuda("partial_o", partial_o, torch.float32)
     _cuda("partial_lse", partial_lse, torch.float32)
     if lse_out is not None:
@@ -399,7 +411,7 @@ def kvc_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     (KVC_ERR_WORKSPACE).  Calls share that scratch, so calls whose kernels could overlap
     on the GPU must be ordered by the caller; call it once on a device before any stream
     capture."""
-    _cuda("out", out)
+    _decode_out(out)
     _cuda("q", q, torch.bfloat16)
     _cuda("k_pool", k_pool, torch.bfloat16)
     _cuda("v_pool", v_pool, torch.bfloat16)

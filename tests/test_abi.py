@@ -107,3 +107,14 @@ def test_binding_refuses_cpu_tensors():
     t = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         kvc.kvc_store(t, t, t, t, torch.zeros(4, dtype=torch.int32))
+
+
+def test_binding_refuses_pageable_decode_out():
+    """The decode calls take a CUDA or a pinned host out; pageable host memory is refused."""
+    import torch
+    t = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    lens = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="pinned"):
+        kvc.kvc_decode(t, t, t, t, torch.zeros(4, 1, dtype=torch.int32), lens, 16)
+    with pytest.raises(ValueError, match="pinned"):
+        kvc.kvc_merge(t, torch.zeros(4, 2, 64), torch.zeros(4, 2))

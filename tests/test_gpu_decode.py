@@ -1,4 +1,6 @@
 """GPU parity of paged decode (split-K and merge) against the fp64 oracle."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -173,3 +175,56 @@ def test_physical_placement_gives_identical_bits():
 def test_no_device_errors_were_raised():
     torch.cuda.synchronize()
     assert kvc.kvc_device_errors() == 0
+
+
+@pytest.mark.parametrize("num_splits", [1, 0])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_decode_into_pinned_host_out(num_splits, out_dtype):
+    """out may be pinned host memory: the kernel that finishes each row (the decode itself
+    with one split, the merge otherwise) writes it there, bit for bit what a device out
+    receives; kvc_merge accepts a pinned host out the same way."""
+    case = config_case(2, num_seqs=16)
+    g = GpuRun(case, decode=True)
+    g.store()
+    dev_out = g.attend(out_dtype, num_splits)
+    host_out = torch.full(tuple(dev_out.shape), float("nan"), dtype=out_dtype).pin_memory()
+    c, d = g.case, g.d
+    kvc.kvc_decode(host_out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, c.max_ctx,
+                   num_splits=num_splits, workspace=g.workspace)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    assert torch.equal(host_out, dev_out.cpu())
+
+
+def test_merge_into_pinned_host_out():
+    rng = np.random.default_rng(3)
+    rows, splits, D = 37, 5, 128
+    po = torch.tensor(rng.standard_normal((rows, splits, D)), dtype=torch.float32, device="cuda")
+    lse = torch.tensor(rng.standard_normal((rows, splits)), dtype=torch.float32, device="cuda")
+    lse[3, :] = float("-inf")   # a row with no key
+    dev_out = torch.empty(rows, D, dtype=torch.bfloat16, device="cuda")
+    host_out = torch.empty(rows, D, dtype=torch.bfloat16).pin_memory()
+    kvc.kvc_merge(dev_out, po, lse)
+    kvc.kvc_merge(host_out, po, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(host_out, dev_out.cpu())
+    assert not host_out[3].float().any()
+
+
+def test_decode_refuses_pageable_host_out():
+    """A host pointer the device cannot reach at that address is refused before anything is
+    enqueued (the C entry point, bypassing the binding's own check)."""
+    from pagedattention_kvc_store_gb300.kvc import lib, pool_desc, _ptr
+    case = config_case(1)
+    g = GpuRun(case, decode=True)
+    g.store()
+    c, d = g.case, g.d
+    host = np.zeros(c.num_seqs * c.q_heads * c.head_dim + 8, dtype=np.float32)
+    addr = (host.ctypes.data + 15) // 16 * 16
+    st = lib().kvc_decode(ctypes.c_void_p(addr), 1, _ptr(d.q), _ptr(d.k_pool), _ptr(d.v_pool),
+                          pool_desc(d.k_pool), _ptr(d.block_table), int(d.block_table.shape[1]),
+                          _ptr(d.context_lens), c.num_seqs, c.max_ctx, c.q_heads, 0.0, 1, None,
+                          0, None)
+    assert st == 1 and b"pinned host" in lib().kvc_last_error()
+    torch.cuda.synchronize()
+    assert not host.any()
