@@ -101,3 +101,27 @@ def test_rejects_groups_with_too_many_rows():
 def test_no_device_errors_were_raised():
     torch.cuda.synchronize()
     assert kvc.kvc_device_errors() == 0
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_no_groups_runs_suffix_only(out_dtype):
+    """No groups at all: the grid holds only suffix CTAs, each from position 0, and the result
+    is the oracle's plain attention."""
+    case = build_case(77, name="no-groups", page_size=16, q_heads=32, kv_heads=8, head_dim=128,
+                      context_lens=lambda rng: rng.integers(1, 700, size=19),
+                      q_lens=np.ones_like)
+    g = GpuRun(case, decode=True)
+    g.store()
+    pool = kvc.pool_desc(g.d.k_pool)
+    ws = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=out_dtype,
+                      device="cuda")
+    none = i32_tensor(np.zeros(1, np.int32), "cuda")
+    kvc.kvc_decode_shared_prefix(out, g.d.q, g.d.k_pool, g.d.v_pool, g.d.block_table,
+                                 g.d.context_lens, case.max_ctx, none, none,
+                                 i32_tensor(np.zeros(1, np.int32), "cuda")[:0], 1, 0, work)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    ref, _ = OracleRun(case).attention()
+    assert_attention_close(out_to_f64(out), ref, "shared-prefix call without groups")
