@@ -168,6 +168,34 @@ kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool
                            int32_t *chunk_out, size_t *workspace_bytes_out);
 
 /*
+ * kvc_shared_prefix_groups -- find the groups for kvc_decode_shared_prefix from the block
+ * tables alone (an opt-in prepass; the caller may build the groups itself instead).
+ * Sequences s - 1 and s are linked when their block-table rows agree on at least the first
+ * page both can share; a sequence can share only whole pages before the page of its last
+ * position (its newest token goes to a page of its own): floor((ctx - 1) / page_size) pages,
+ * at most bt_stride.  A group is a maximal run of linked sequences, cut into consecutive
+ * chunks of at most max_members (2 .. 64; kvc_decode_shared_prefix takes members *
+ * q_heads / kv_heads <= 64); a chunk of one sequence is no group.  A group's prefix is the
+ * smallest agreement between adjacent members, in positions (pages * page_size).  Integer
+ * work, one CTA; the result is exact (tested against the oracle's groups).
+ *   block_table    int32 [num_seqs][bt_stride];  context_lens int32 [num_seqs] (device)
+ *   group_indptr   int32 [num_seqs / 2 + 1] (out, device): members of group g are
+ *                  group_seqs[group_indptr[g] .. group_indptr[g + 1])
+ *   group_seqs     int32 [num_seqs] (out, device), ascending within and across groups
+ *   prefix_len     int32 [num_seqs / 2] (out, device)
+ *   num_groups     int32 [1] (out, device): the number of groups found
+ * Slots g >= *num_groups of the capacity num_seqs / 2 are written as empty groups with a
+ * zero prefix, so the outputs can go to kvc_decode_shared_prefix with num_groups =
+ * num_seqs / 2 and max_prefix_len = max_ctx without reading the count back (empty groups
+ * cost a CTA that exits at once), or with the count read back for a tighter launch.
+ */
+kvc_status kvc_shared_prefix_groups(const int32_t *block_table, int32_t bt_stride,
+                                    const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t page_size, int32_t max_members,
+                                    int32_t *group_indptr, int32_t *group_seqs,
+                                    int32_t *prefix_len, int32_t *num_groups, void *stream);
+
+/*
  * kvc_decode_shared_prefix -- kvc_decode for batches in which groups of sequences begin with
  * the same physical pages ("KV Cache Management and PagedAttention", "Share common KV across
  * responses": several block tables point at one copy of the common KV; each response still

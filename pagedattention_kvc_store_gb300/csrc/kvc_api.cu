@@ -727,6 +727,28 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
     return ok();
 }
 
+kvc_status kvc_shared_prefix_groups(const int32_t *block_table, int32_t bt_stride,
+                                    const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t page_size, int32_t max_members,
+                                    int32_t *group_indptr, int32_t *group_seqs,
+                                    int32_t *prefix_len, int32_t *num_groups, void *stream)
+{
+    if (num_seqs < 0 || num_seqs > 65535)
+        return fail(KVC_ERR_INVALID_ARG, "num_seqs %d (0 .. 65535)", num_seqs);
+    if (page_size <= 0 || bt_stride <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "page_size %d, bt_stride %d", page_size, bt_stride);
+    if (max_members < 2 || max_members > 64)
+        return fail(KVC_ERR_INVALID_ARG, "max_members %d (2 .. 64)", max_members);
+    if (!group_indptr || !num_groups || (num_seqs > 0 && (!block_table || !context_lens ||
+                                                          !group_seqs)) ||
+        (num_seqs > 1 && !prefix_len))
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    const cudaError_t err = kvc::launch_group_detect(
+        block_table, bt_stride, context_lens, num_seqs, page_size, max_members, group_indptr,
+        group_seqs, prefix_len, num_groups, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "group detection launch");
+}
+
 kvc_status kvc_decode_shared_prefix_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
                                          int32_t max_ctx, int32_t num_groups,
                                          int32_t max_prefix_len, size_t *workspace_bytes_out)

@@ -102,6 +102,161 @@ __global__ void grouped_setup_kernel(float *__restrict__ part_lse, int32_t *__re
     }
 }
 
+// ------------------------------- group detection --------------------------------------
+// Groups from the block tables alone: adjacent sequences s - 1, s are linked when their
+// tables agree on at least the first page that both can share (pages wholly before the page
+// of the last position); a group is a maximal run of linked sequences cut into chunks of at
+// most max_members, chunks of one sequence dropped; its prefix is the smallest agreement
+// inside the chunk.  One CTA of kDetectThreads threads walks the sequences in tiles; each
+// warp measures the agreement of one pair at a time, 32 table entries per step.
+constexpr int kDetectThreads = 1024;
+constexpr int kDetectTile = kDetectThreads;
+constexpr int kDetectMaxMembers = 64;
+
+__device__ int pair_agreement(const int32_t *__restrict__ bt, int bt_stride,
+                              const int32_t *__restrict__ ctx, int page_size, int s, int lane)
+{
+    if (s == 0)
+        return 0;
+    const int sh0 = min(max(ctx[s - 1] - 1, 0) / page_size, bt_stride);
+    const int sh1 = min(max(ctx[s] - 1, 0) / page_size, bt_stride);
+    const int lim = min(sh0, sh1);
+    const int32_t *a = bt + static_cast<size_t>(s - 1) * bt_stride;
+    const int32_t *b = bt + static_cast<size_t>(s) * bt_stride;
+    for (int k0 = 0; k0 < lim; k0 += 32) {
+        const int k = k0 + lane;
+        const unsigned diff = __ballot_sync(0xffffffffu, k < lim && a[k] != b[k]);
+        if (diff != 0u)
+            return k0 + __ffs(diff) - 1;
+    }
+    return lim;
+}
+
+// Inclusive max / exclusive sum over the block (all kDetectThreads threads call them).
+__device__ int block_max_scan(int v, int *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off)
+            v = max(v, o);
+    }
+    if (lane == 31)
+        red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = red[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off)
+                w = max(w, o);
+        }
+        red[lane] = w;
+    }
+    __syncthreads();
+    const int r = warp > 0 ? max(v, red[warp - 1]) : v;
+    __syncthreads();
+    return r;
+}
+
+__device__ int block_sum_scan_excl(int v, int *red, int *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += o;
+    }
+    if (lane == 31)
+        red[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = red[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off)
+                w += o;
+        }
+        red[lane] = w;
+    }
+    __syncthreads();
+    const int r = x - v + (warp > 0 ? red[warp - 1] : 0);
+    *total = red[31];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kDetectThreads, 1)
+    group_detect_kernel(const int32_t *__restrict__ bt, int bt_stride,
+                        const int32_t *__restrict__ ctx, int num_seqs, int page_size,
+                        int max_members, int capacity, int32_t *__restrict__ group_indptr,
+                        int32_t *__restrict__ group_seqs, int32_t *__restrict__ prefix_len,
+                        int32_t *__restrict__ num_groups)
+{
+    pdl_wait();
+    pdl_trigger();
+    // agreement of sequences t0 .. t0 + kDetectTile + max_members - 1 of the current tile: a
+    // chunk starting in the tile reads its members' agreements past the tile's end
+    __shared__ int agree[kDetectTile + kDetectMaxMembers];
+    __shared__ int red[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int carry_run = 0, carry_members = 0, carry_groups = 0;
+    for (int t0 = 0; t0 < num_seqs; t0 += kDetectTile) {
+        const int n_ext = min(kDetectTile + max_members, num_seqs - t0);
+        for (int i = warp; i < n_ext; i += kDetectThreads / 32) {
+            const int k = pair_agreement(bt, bt_stride, ctx, page_size, t0 + i, lane);
+            if (lane == 0)
+                agree[i] = k;
+        }
+        __syncthreads();
+        const int s = t0 + tid;
+        const bool valid = s < num_seqs;
+        // the start of s's run: the last r <= s that is 0 or not linked to r - 1
+        const int run = max(block_max_scan(valid && (s == 0 || agree[tid] == 0) ? s : -1, red),
+                            carry_run);
+        const bool chunk_start = valid && (s - run) % max_members == 0;
+        // s is in a group unless it starts a chunk that the next sequence does not continue
+        const bool continued =
+            s + 1 < num_seqs && tid + 1 < n_ext && agree[tid + 1] >= 1 && max_members >= 2;
+        const bool in_group = valid && (!chunk_start || continued);
+        const bool group_start = chunk_start && in_group;
+        int members_here, groups_here;
+        const int mi = carry_members + block_sum_scan_excl(in_group ? 1 : 0, red, &members_here);
+        const int gi = carry_groups + block_sum_scan_excl(group_start ? 1 : 0, red, &groups_here);
+        if (in_group)
+            group_seqs[mi] = s;
+        if (group_start && gi < capacity) {
+            int pre = agree[tid + 1];
+            for (int j = 2; j < max_members && s + j < num_seqs && agree[tid + j] >= 1; ++j)
+                pre = min(pre, agree[tid + j]);
+            group_indptr[gi] = mi;
+            prefix_len[gi] = pre * page_size;
+        }
+        // the run reaching into the next tile starts where the tile's last sequence's run does
+        if (tid == min(kDetectTile, num_seqs - t0) - 1)
+            red[0] = run;
+        __syncthreads();
+        carry_run = red[0];
+        carry_members += members_here;
+        carry_groups += groups_here;
+        __syncthreads();
+    }
+    // unused group slots: no members, no prefix (a decode over them does nothing); the end
+    // offset of the last group and of every unused slot, up to group_indptr[capacity]
+    for (int g = min(carry_groups, capacity) + tid; g <= capacity; g += kDetectThreads) {
+        group_indptr[g] = carry_members;
+        if (g < capacity)
+            prefix_len[g] = 0;
+    }
+    if (tid == 0)
+        *num_groups = carry_groups;
+}
+
 // One prefix CTA: chunk `split` of the shared prefix of group `grp`, kv head `kvh`.
 template <int D, int NMT>
 __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
@@ -554,6 +709,18 @@ cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int3
     return launch_pdl(grouped_setup_kernel, dim3(blocks), dim3(256), 0, stream, part_lse,
                       key_start, group_indptr, group_seqs, prefix_len, num_groups, num_seqs,
                       q_heads, n_prefix_splits, split_stride, page_size, bt_stride);
+}
+
+cudaError_t launch_group_detect(const int32_t *block_table, int bt_stride,
+                                const int32_t *context_lens, int num_seqs, int page_size,
+                                int max_members, int32_t *group_indptr, int32_t *group_seqs,
+                                int32_t *prefix_len, int32_t *num_groups, cudaStream_t stream)
+{
+    if (max_members < 2 || max_members > kDetectMaxMembers)
+        return cudaErrorInvalidValue;
+    return launch_pdl(group_detect_kernel, dim3(1), dim3(kDetectThreads), 0, stream,
+                      block_table, bt_stride, context_lens, num_seqs, page_size, max_members,
+                      num_seqs / 2, group_indptr, group_seqs, prefix_len, num_groups);
 }
 
 cudaError_t launch_grouped_decode(const GroupedPrefixLaunch &p, const DecodeLaunch &l,

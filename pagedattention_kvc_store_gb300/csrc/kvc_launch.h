@@ -155,6 +155,12 @@ cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int3
                                  int num_groups, int num_seqs, int q_heads, int n_prefix_splits,
                                  int split_stride, int page_size, int bt_stride,
                                  cudaStream_t stream);
+// Groups from block tables (adjacent sequences agreeing on leading shareable pages), one CTA:
+// group_indptr[num_seqs / 2 + 1], group_seqs[num_seqs], prefix_len[num_seqs / 2], num_groups[1].
+cudaError_t launch_group_detect(const int32_t *block_table, int bt_stride,
+                                const int32_t *context_lens, int num_seqs, int page_size,
+                                int max_members, int32_t *group_indptr, int32_t *group_seqs,
+                                int32_t *prefix_len, int32_t *num_groups, cudaStream_t stream);
 // The prefix CTAs of `p` and the suffix decode of `l` (key_start set, partials after the
 // prefix splits) in one grid.
 cudaError_t launch_grouped_decode(const GroupedPrefixLaunch &p, const DecodeLaunch &l,

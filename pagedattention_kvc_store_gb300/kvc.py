@@ -30,7 +30,7 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
            "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8",
-           "kvc_append_store")
+           "kvc_append_store", "kvc_shared_prefix_groups")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
             L.kvc_decode_shared_prefix.restype = ctypes.c_int
             L.kvc_decode_shared_prefix.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, i32,
                                                    i32, i32, f, p, p, p, i32, i32, i32, p, sz, p]
+            L.kvc_shared_prefix_groups.restype = ctypes.c_int
+            L.kvc_shared_prefix_groups.argtypes = [p, i32, p, i32, i32, i32, p, p, p, p, p]
             L.kvc_decode_shared_prefix_plan.restype = ctypes.c_int
             L.kvc_decode_shared_prefix_plan.argtypes = [i32, i32, PoolDesc, i32, i32, i32,
                                                         ctypes.POINTER(sz)]
@@ -460,6 +462,26 @@ def kvc_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
         _ptr(group_indptr), _ptr(group_seqs), _ptr(prefix_len), int(prefix_len.shape[0]),
         int(max_group_size), int(max_prefix_len), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kvc_shared_prefix_groups(group_indptr: torch.Tensor, group_seqs: torch.Tensor,
+                             prefix_len: torch.Tensor, num_groups: torch.Tensor,
+                             block_table: torch.Tensor, context_lens: torch.Tensor,
+                             page_size: int, max_members: int, stream=None) -> None:
+    """Groups for kvc_decode_shared_prefix from the block tables (device prepass).  Outputs:
+    group_indptr [S // 2 + 1], group_seqs [S], prefix_len [S // 2], num_groups [1], int32."""
+    for name, t in (("group_indptr", group_indptr), ("group_seqs", group_seqs),
+                    ("prefix_len", prefix_len), ("num_groups", num_groups),
+                    ("block_table", block_table), ("context_lens", context_lens)):
+        _cuda(name, t, torch.int32)
+    S = int(context_lens.shape[0])
+    if group_indptr.numel() < S // 2 + 1 or group_seqs.numel() < S or \
+            prefix_len.numel() < S // 2 or num_groups.numel() < 1:
+        raise ValueError("group outputs smaller than num_seqs / 2 groups need")
+    _check("kvc_shared_prefix_groups", lib().kvc_shared_prefix_groups(
+        _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens), S, int(page_size),
+        int(max_members), _ptr(group_indptr), _ptr(group_seqs), _ptr(prefix_len),
+        _ptr(num_groups), _stream(stream)))
 
 
 def kvc_device_errors() -> int:
