@@ -802,10 +802,19 @@ def cpu_baseline(case, seconds):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = (time.perf_counter() - t0) / reps
+    # the same oracle on one thread, over the first 8 sequences of the batch
+    few = np.arange(min(8, case.num_seqs))
+    kp1, vp1 = case.k_pool.copy(), case.v_pool.copy()
+    t1 = time.perf_counter()
+    _oracle_step(oracle, case, few, 1, kp1, vp1)
+    dt1 = time.perf_counter() - t1
     return {"value": round(_sub_bytes(case, seqs) / dt / 1e9, 4), "unit": "GB/s",
             "cores": threads, "kind": "oracle",
             "sample": f"the full 64-sequence batch, {reps} pass(es), {dt:.2f} s per pass "
-                      f"(fp64 C oracle: slot mapping, store, gathered attention)"}
+                      f"(fp64 C oracle: slot mapping, store, gathered attention)",
+            "value_1_thread": round(_sub_bytes(case, few) / dt1 / 1e9, 4),
+            "sample_1_thread": f"sequences 0-{len(few) - 1} of the batch on one thread, "
+                               f"{dt1:.2f} s"}
 
 
 def run_reference(args):

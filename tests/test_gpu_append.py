@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import pagedattention_kvc_store_gb300 as kvc
-from harness import GpuRun, OracleRun, assert_attention_close, out_to_f64, sample_seqs
+from harness import GpuRun, OracleRun, assert_attention_close, out_to_f64
 from workloads import bf16_bits, build_case, config_case, f32_from_bf16, normal_bf16
 from workloads.device import bf16_tensor, i32_tensor
 
@@ -13,14 +13,44 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("page_size", [16, 64])
-def test_rewind_append_full_size_sampled(page_size):
+def test_rewind_append_full_size(page_size):
+    """The rewind workload at full size (1,000 documents x 50 new tokens over 300 cached, 32 /
+    8 heads), every document against the oracle."""
     case = config_case(4, page_size=page_size)
     g = GpuRun(case, decode=False)
     g.store()
     out = out_to_f64(g.attend(torch.bfloat16))
-    seqs = sample_seqs(case.num_seqs, 48, seed=page_size)
-    ref, _, rows = OracleRun(case).attention(seqs)
-    assert_attention_close(out[rows], ref, f"rewind append P={page_size}")
+    ref, _ = OracleRun(case).attention()
+    assert_attention_close(out, ref, f"rewind append P={page_size}")
+
+
+def test_two_chunks_compose_to_one():
+    """Appending 50 tokens and then 50 more over the cached first 50 gives, row for row, what
+    one append of all 100 gives (the same keys and causal limits; different tiles, so within
+    fp32 rounding)."""
+    n, P, Hq, Hkv, D = 12, 16, 32, 8, 128
+    case = build_case(4321, name="compose", page_size=P, q_heads=Hq, kv_heads=Hkv, head_dim=D,
+                      context_lens=lambda rng: np.full(n, 100), q_lens=lambda c: np.full(n, 100))
+    g = GpuRun(case, decode=False)
+    g.store()                              # all 100 tokens of every document are now cached
+    d = g.d
+    whole = torch.empty(n * 100, Hq, D, dtype=torch.float32, device="cuda")
+    kvc.kvc_append(whole, d.q, d.k_pool, d.v_pool, d.block_table, d.q_indptr, d.context_lens,
+                   100, 100)
+    q = d.q.view(n, 100, Hq, D)
+    halves = []
+    for lo, ctx in ((0, 50), (50, 100)):
+        part = torch.empty(n * 50, Hq, D, dtype=torch.float32, device="cuda")
+        kvc.kvc_append(part, q[:, lo:lo + 50].contiguous().view(n * 50, Hq, D), d.k_pool,
+                       d.v_pool, d.block_table, i32_tensor(np.arange(0, n * 50 + 1, 50), "cuda"),
+                       i32_tensor(np.full(n, ctx), "cuda"), 50, ctx)
+        halves.append(part.view(n, 50, Hq, D))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    two = torch.cat(halves, dim=1).view(n * 100, Hq, D)
+    assert (two - whole).abs().max().item() < 2e-3
+    ref, _ = OracleRun(case).attention()
+    assert_attention_close(out_to_f64(whole), ref, "append of 100")
 
 
 @pytest.mark.parametrize("P,Hq,Hkv,D", [(16, 32, 8, 128), (32, 8, 8, 64), (64, 16, 2, 128),

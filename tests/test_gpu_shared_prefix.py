@@ -125,3 +125,31 @@ def test_no_groups_runs_suffix_only(out_dtype):
     assert kvc.kvc_device_errors() == 0
     ref, _ = OracleRun(case).attention()
     assert_attention_close(out_to_f64(out), ref, "shared-prefix call without groups")
+
+
+def test_shared_pages_and_private_copies_agree():
+    """Sharing is storage: tables whose members point at one copy of the prefix pages and
+    tables where every member of four groups has its own copy of them give bit-identical
+    kvc_decode output; the grouped decode over the shared tables agrees with both."""
+    case = config_case(3)
+    g1 = GpuRun(case, decode=True)
+    g1.store()
+    shared_out = g1.attend(torch.float32, 0)
+    grouped = _run_shared(case, g1)
+
+    case2 = config_case(3)
+    pages = case2.k_pool.shape[0]
+    n_sh = case2.shared_positions // case2.page_size
+    members = [m for grp in case2.groups[:4] for m in grp]
+    src = np.concatenate([case2.block_table[m, :n_sh] for m in members])
+    fresh = np.arange(pages, pages + len(src), dtype=np.int32)
+    case2.k_pool = np.concatenate([case2.k_pool, case2.k_pool[src]])
+    case2.v_pool = np.concatenate([case2.v_pool, case2.v_pool[src]])
+    for i, m in enumerate(members):
+        case2.block_table[m, :n_sh] = fresh[i * n_sh:(i + 1) * n_sh]
+    g2 = GpuRun(case2, decode=True)
+    g2.store()
+    private_out = g2.attend(torch.float32, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(private_out, shared_out)
+    assert np.abs(grouped - out_to_f64(private_out)).max() < 2e-3
