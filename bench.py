@@ -311,6 +311,32 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             t_p = time_graph(torch, lambda: kvc.kvc_decode(
                 out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
                 num_splits=0, workspace=work_p), stream, flush, args.leg_steps)
+        # the same step with the groups found on the device from the block tables: the prepass
+        # alone, and prepass + decode over its fixed-capacity group list (S / 2 slots, unused
+        # ones empty; at most 8 members; prefix bound max_ctx), with no host read of the count
+        cap = case.num_seqs // 2
+        di = torch.empty(cap + 1, dtype=torch.int32, device=dev)
+        ds = torch.empty(case.num_seqs, dtype=torch.int32, device=dev)
+        dp = torch.empty(cap, dtype=torch.int32, device=dev)
+        dn = torch.empty(1, dtype=torch.int32, device=dev)
+        ws_d = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
+                                                 cap, case.max_ctx)
+        work_d = torch.empty(ws_d, dtype=torch.uint8, device=dev)
+
+        def detect():
+            kvc.kvc_shared_prefix_groups(di, ds, dp, dn, d.block_table, d.context_lens,
+                                         case.page_size, 8)
+
+        def detect_and_decode():
+            detect()
+            kvc.kvc_decode_shared_prefix(out, d.q, d.k_pool, d.v_pool, d.block_table,
+                                         d.context_lens, case.max_ctx, di, ds, dp, 8,
+                                         case.max_ctx, work_d)
+        with torch.cuda.stream(stream):
+            t_det = time_graph(torch, detect, stream, flush, args.leg_steps)
+            t_gd = time_graph(torch, detect_and_decode, stream, flush, args.leg_steps)
+        torch.cuda.synchronize()
+        found = int(dn.item())
         unique_pos = int(case.context_lens.sum()) - 7 * len(case.groups) * int(prefix[0])
         unique_b = unique_pos * per_pos(case) + qo(case)
         logical_b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
@@ -323,10 +349,13 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             "grouped_frac_of_hbm": round(unique_b / (t_g / 1e3) / 1e9 / peaks["hbm"], 4),
             "plain_unique_gbs": round(unique_b / (t_p / 1e3) / 1e9, 1),
             "plain_effective_gbs": round(logical_b / (t_p / 1e3) / 1e9, 1),
-            "gpu_launches_per_step": {"grouped": 3, "plain": 2},
+            "gpu_launches_per_step": {"grouped": 3, "plain": 2, "device_groups": 5},
             "traffic_grouped_decode_kernel": traffic_from_profile("grouped_shared_prefix"),
+            "device_groups": {"groups_found": found, "detect_us": round(t_det * 1e3, 2),
+                              "detect_and_grouped_us": round(t_gd * 1e3, 1),
+                              "unique_gbs": round(unique_b / (t_gd / 1e3) / 1e9, 1)},
         }
-        del d, out, work_g, work_p, slots
+        del d, out, work_g, work_p, slots, work_d
         torch.cuda.empty_cache()
     if "long_decode" in args.legs:
         # long context: 8 sequences of 32k..128k positions

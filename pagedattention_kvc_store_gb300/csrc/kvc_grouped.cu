@@ -107,8 +107,12 @@ __global__ void grouped_setup_kernel(float *__restrict__ part_lse, int32_t *__re
 // tables agree on at least the first page that both can share (pages wholly before the page
 // of the last position); a group is a maximal run of linked sequences cut into chunks of at
 // most max_members, chunks of one sequence dropped; its prefix is the smallest agreement
-// inside the chunk.  One CTA of kDetectThreads threads walks the sequences in tiles; each
-// warp measures the agreement of one pair at a time, 32 table entries per step.
+// inside the chunk.  group_agree_kernel measures every adjacent pair's agreement (a warp per
+// pair, 32 table entries per step) into group_seqs, which serves as scratch; then one CTA of
+// kDetectThreads threads walks the sequences in tiles of kDetectTile, reading a tile's
+// agreements (and the next max_members ones) before it writes any output.  Its writes to
+// group_seqs land at member offsets <= the sequence index, below every agreement a later
+// tile still has to read.
 constexpr int kDetectThreads = 1024;
 constexpr int kDetectTile = kDetectThreads;
 constexpr int kDetectMaxMembers = 64;
@@ -191,12 +195,27 @@ __device__ int block_sum_scan_excl(int v, int *red, int *total)
     return r;
 }
 
+constexpr int kAgreeWarps = 8;
+
+__global__ void __launch_bounds__(kAgreeWarps * 32)
+    group_agree_kernel(const int32_t *__restrict__ bt, int bt_stride,
+                       const int32_t *__restrict__ ctx, int num_seqs, int page_size,
+                       int32_t *__restrict__ agree_out)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int s = blockIdx.x * kAgreeWarps + (threadIdx.x >> 5);
+    if (s >= num_seqs)
+        return;   // warp-uniform
+    const int k = pair_agreement(bt, bt_stride, ctx, page_size, s, threadIdx.x & 31);
+    if ((threadIdx.x & 31) == 0)
+        agree_out[s] = k;
+}
+
 __global__ void __launch_bounds__(kDetectThreads, 1)
-    group_detect_kernel(const int32_t *__restrict__ bt, int bt_stride,
-                        const int32_t *__restrict__ ctx, int num_seqs, int page_size,
-                        int max_members, int capacity, int32_t *__restrict__ group_indptr,
-                        int32_t *__restrict__ group_seqs, int32_t *__restrict__ prefix_len,
-                        int32_t *__restrict__ num_groups)
+    group_detect_kernel(int num_seqs, int page_size, int max_members, int capacity,
+                        int32_t *__restrict__ group_indptr, int32_t *group_seqs,
+                        int32_t *__restrict__ prefix_len, int32_t *__restrict__ num_groups)
 {
     pdl_wait();
     pdl_trigger();
@@ -204,15 +223,12 @@ __global__ void __launch_bounds__(kDetectThreads, 1)
     // chunk starting in the tile reads its members' agreements past the tile's end
     __shared__ int agree[kDetectTile + kDetectMaxMembers];
     __shared__ int red[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     int carry_run = 0, carry_members = 0, carry_groups = 0;
     for (int t0 = 0; t0 < num_seqs; t0 += kDetectTile) {
         const int n_ext = min(kDetectTile + max_members, num_seqs - t0);
-        for (int i = warp; i < n_ext; i += kDetectThreads / 32) {
-            const int k = pair_agreement(bt, bt_stride, ctx, page_size, t0 + i, lane);
-            if (lane == 0)
-                agree[i] = k;
-        }
+        for (int i = tid; i < n_ext; i += kDetectThreads)
+            agree[i] = group_seqs[t0 + i];   // the agreements group_agree_kernel left here
         __syncthreads();
         const int s = t0 + tid;
         const bool valid = s < num_seqs;
@@ -718,9 +734,17 @@ cudaError_t launch_group_detect(const int32_t *block_table, int bt_stride,
 {
     if (max_members < 2 || max_members > kDetectMaxMembers)
         return cudaErrorInvalidValue;
-    return launch_pdl(group_detect_kernel, dim3(1), dim3(kDetectThreads), 0, stream,
-                      block_table, bt_stride, context_lens, num_seqs, page_size, max_members,
-                      num_seqs / 2, group_indptr, group_seqs, prefix_len, num_groups);
+    if (num_seqs > 0) {
+        const cudaError_t err = launch_pdl(
+            group_agree_kernel, dim3((num_seqs + kAgreeWarps - 1) / kAgreeWarps),
+            dim3(kAgreeWarps * 32), 0, stream, block_table, bt_stride, context_lens, num_seqs,
+            page_size, group_seqs);
+        if (err != cudaSuccess)
+            return err;
+    }
+    return launch_pdl(group_detect_kernel, dim3(1), dim3(kDetectThreads), 0, stream, num_seqs,
+                      page_size, max_members, num_seqs / 2, group_indptr, group_seqs,
+                      prefix_len, num_groups);
 }
 
 cudaError_t launch_grouped_decode(const GroupedPrefixLaunch &p, const DecodeLaunch &l,
