@@ -609,38 +609,26 @@ def run_kvc(args):
 
 
 def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
-    """The same step through the public API with host buffers: the step's inputs copied from
-    pinned host memory, the three calls, and the output delivered to pinned host memory, all
-    inside the timed region.  The inputs sit back to back in one pinned buffer (one host ->
-    device copy); kvc_decode writes its output straight into a pinned host tensor (the merge
-    kernel's stores cross to the host; no separate device -> host copy).  The calls are issued
+    """The same step through the public API with host buffers, every step inside the timed
+    region: the step's inputs start in pinned host memory and its output ends there.  No copy
+    is enqueued: kvc_slot_mapping reads the tables, kvc_store the new keys and values and
+    kvc_decode the queries and tables straight from pinned host memory across the host link,
+    and kvc_decode writes its output into a pinned host tensor.  The calls are issued
     eagerly; the same step captured as one graph is reported beside it."""
-    names = ("q", "k_new", "v_new", "block_table", "context_lens")
+    names = ("q", "block_table", "context_lens", "k_new", "v_new")
     src = {name: getattr(d, name) for name in names}
-    offs, total = {}, 0
-    for name in names:
-        offs[name] = total
-        total += -(-src[name].numel() * src[name].element_size() // 256) * 256
-    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    dev_in = {}
-    for name in names:
-        t = src[name]
-        n = t.numel() * t.element_size()
-        host_buf[offs[name]:offs[name] + n].copy_(t.reshape(-1).view(torch.uint8).cpu())
-        dev_in[name] = dev_buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+    host_in = {name: t.cpu().pin_memory() for name, t in src.items()}
     out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
                       device=dev)
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
 
     def step():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        kvc.kvc_slot_mapping(slots, dev_in["block_table"], dev_in["context_lens"], None,
+        kvc.kvc_slot_mapping(slots, host_in["block_table"], host_in["context_lens"], None,
                              case.page_size)
-        kvc.kvc_store(d.k_pool, d.v_pool, dev_in["k_new"], dev_in["v_new"], slots)
-        kvc.kvc_decode(out_host, dev_in["q"], d.k_pool, d.v_pool, dev_in["block_table"],
-                       dev_in["context_lens"], case.max_ctx, num_splits=0, workspace=work)
+        kvc.kvc_store(d.k_pool, d.v_pool, host_in["k_new"], host_in["v_new"], slots)
+        kvc.kvc_decode(out_host, host_in["q"], d.k_pool, d.v_pool, host_in["block_table"],
+                       host_in["context_lens"], case.max_ctx, num_splits=0, workspace=work)
 
     for _ in range(5):
         step()
@@ -665,10 +653,10 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
     t_graph = timed(g.replay)
     t_eager = timed(step)
     torch.cuda.synchronize()
-    kvc.kvc_decode(out, dev_in["q"], d.k_pool, d.v_pool, dev_in["block_table"],
-                   dev_in["context_lens"], case.max_ctx, num_splits=0, workspace=work)
+    kvc.kvc_decode(out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
+                   num_splits=0, workspace=work)
     torch.cuda.synchronize()
-    assert torch.equal(out_host, out.cpu()), "host-delivered output differs from device output"
+    assert torch.equal(out_host, out.cpu()), "host-fed output differs from device-fed output"
     h2d = sum(t.numel() * t.element_size() for t in src.values())
     d2h = out_host.numel() * out_host.element_size()
     step_b = decode_bytes(case) + store_bytes(case)
@@ -677,10 +665,10 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "graph_value": round(step_b / (t_graph / 1e3) / 1e9, 2),
             "graph_ms_per_step": round(t_graph, 5),
-            "path": "one pinned H2D of q/k_new/v_new/block_table/context_lens, "
-                    "kvc_slot_mapping, kvc_store, kvc_decode with out in pinned host memory "
-                    "(the merge kernel writes the result across to the host), issued eagerly "
-                    "(graph_value: the same step captured as one graph)"}
+            "path": "kvc_slot_mapping, kvc_store and kvc_decode reading q, block_table, "
+                    "context_lens, k_new and v_new straight from pinned host memory; kvc_decode "
+                    "writing its output into pinned host memory; no copy enqueued; issued "
+                    "eagerly (graph_value: the same step captured as one graph)"}
 
 
 def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):

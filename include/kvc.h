@@ -26,7 +26,9 @@
  * Scale.  Scores are q.k * scale; scale <= 0 selects 1/sqrt(head_dim).
  * Memory.  Every pointer argument named *pool, q, k_new, v_new, out, block_table,
  *   context_lens, q_indptr, slot_mapping, partial_*, workspace is a DEVICE pointer owned by
- *   the caller (the decode calls' out may also be pinned host memory, see kvc_decode).
+ *   the caller (kvc_decode's q, tables and out, kvc_merge's out, kvc_store's k_new / v_new
+ *   and kvc_slot_mapping's tables may also be pinned host memory mapped at its host
+ *   address, see each call).
  *   The library allocates no memory, holds no pointer after a call returns,
  *   and never synchronises: each call only enqueues kernels on `stream` (a cudaStream_t;
  *   NULL is the legacy default stream).  Device arrays are not read on the host, so per-step
@@ -100,6 +102,10 @@ const char *kvc_last_error(void);
  *   block_table   int32 [num_seqs][bt_stride]
  *   context_lens  int32 [num_seqs]
  *   q_indptr      int32 [num_seqs + 1] or NULL
+ * block_table, context_lens and q_indptr may also be pinned host memory that the device
+ * reaches at its host address (the kernel reads the few entries it needs across the host
+ * link, so a step's tables need not be copied first for this call); any other host pointer:
+ * KVC_ERR_INVALID_ARG, nothing enqueued.
  *   max_q_len     host upper bound on q_len_s (sizes the launch; 1 when q_indptr is NULL)
  */
 kvc_status kvc_slot_mapping(int32_t *slot_mapping, const int32_t *block_table,
@@ -116,7 +122,10 @@ kvc_status kvc_slot_mapping(int32_t *slot_mapping, const int32_t *block_table,
  * A raw 16-bit copy: NaN payloads and signed zeros are kept.  slot_mapping[t] < 0 skips
  * token t (padding).  Slots must be < num_pages * page_size and distinct within one call
  * (two writers of one slot is the race copy-on-write exists to prevent).
- *   k_new, v_new  bf16 [num_tokens][kv_heads][head_dim]
+ *   k_new, v_new  bf16 [num_tokens][kv_heads][head_dim]; device memory, or pinned host
+ *                 memory that the device reaches at its host address (the kernel reads the
+ *                 step's new keys and values across the host link); any other host pointer:
+ *                 KVC_ERR_INVALID_ARG, nothing enqueued.
  */
 kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void *k_new,
                      const void *v_new, const int32_t *slot_mapping, int32_t num_tokens,
@@ -142,6 +151,9 @@ kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void 
  *                 result is on the host when the call's work completes, with no copy to
  *                 enqueue.  Any other host pointer: KVC_ERR_INVALID_ARG, nothing enqueued.
  *   q             bf16 [num_seqs][q_heads][head_dim]
+ *   q, block_table, context_lens may also be pinned host memory mapped at its host address:
+ *                 the kernels read them across the host link (each CTA its query rows and
+ *                 page ids), so a step's inputs need no copy first.
  *   max_ctx       host upper bound on every context_lens[s] (sizes the launch)
  *   num_splits    0 = choose automatically, 1 = no split, n > 1 = at most n chunks
  *   workspace     device scratch of at least kvc_decode_plan(...)'s workspace bytes when

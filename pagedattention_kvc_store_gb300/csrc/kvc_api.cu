@@ -388,25 +388,29 @@ GroupPlan make_group_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc
     return g;
 }
 
-// `out` of the decode entry points may be device (or managed) memory, or pinned host memory
-// that the device reaches at the same address (cudaHostAlloc / cudaHostRegister on a UVA
-// system): the kernel that finishes a row then writes it straight to host memory.
-kvc_status check_decode_out(const void *out)
+// Arguments that may live in host memory (the decode calls' out; the per-step inputs of slot
+// mapping and store) must be device (or managed) memory, or pinned host memory that the
+// device reaches at the same address (cudaHostAlloc / cudaHostRegister on a UVA system):
+// kernels then read or write them across the host link directly.
+kvc_status check_reachable(const void *p, const char *name)
 {
-    if (out == nullptr)
-        return KVC_OK;   // num_seqs == 0, checked by the caller
+    if (p == nullptr)
+        return KVC_OK;   // optional, or nothing to do: checked by the caller
     cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, out) != cudaSuccess) {
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
         cudaGetLastError();
-        return fail(KVC_ERR_INVALID_ARG, "out: not a CUDA-visible pointer");
+        return fail(KVC_ERR_INVALID_ARG, "%s: not a CUDA-visible pointer", name);
     }
     if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
         return KVC_OK;
-    if (attr.type == cudaMemoryTypeHost && attr.devicePointer == out)
+    if (attr.type == cudaMemoryTypeHost && attr.devicePointer == p)
         return KVC_OK;
     return fail(KVC_ERR_INVALID_ARG,
-                "out must be device memory or pinned host memory mapped at its host address");
+                "%s must be device memory or pinned host memory mapped at its host address",
+                name);
 }
+
+kvc_status check_decode_out(const void *out) { return check_reachable(out, "out"); }
 
 kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *q,
                                 const void *k_pool, const void *v_pool,
@@ -476,6 +480,11 @@ kvc_status kvc_slot_mapping(int32_t *slot_mapping, const int32_t *block_table,
         return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
     if (num_seqs == 0 || num_tokens == 0)
         return ok();
+    kvc_status st;
+    if ((st = check_reachable(block_table, "block_table")) != KVC_OK ||
+        (st = check_reachable(context_lens, "context_lens")) != KVC_OK ||
+        (st = check_reachable(q_indptr, "q_indptr")) != KVC_OK)
+        return st;
     cudaError_t err = kvc::launch_slot_mapping(slot_mapping, block_table, bt_stride,
                                                context_lens, q_indptr, num_seqs, num_tokens,
                                                max_q_len, page_size,
@@ -503,6 +512,10 @@ kvc_status kvc_store(void *k_pool, void *v_pool, kvc_pool_desc pool, const void 
         return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
     if (pool.layout != KVC_NHD && pool.layout != KVC_HND)
         return fail(KVC_ERR_INVALID_ARG, "layout %d (KVC_NHD or KVC_HND)", pool.layout);
+    kvc_status st;
+    if ((st = check_reachable(k_new, "k_new")) != KVC_OK ||
+        (st = check_reachable(v_new, "v_new")) != KVC_OK)
+        return st;
     cudaError_t err = kvc::launch_store(k_pool, v_pool, pool.kv_heads, pool.head_dim,
                                         pool.num_pages * pool.page_size, k_new,
                                         v_new, slot_mapping, num_tokens,
@@ -687,7 +700,9 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
         if (!aligned16(workspace))
             return fail(KVC_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     }
-    if ((st = check_decode_out(out)) != KVC_OK)
+    if ((st = check_decode_out(out)) != KVC_OK || (st = check_reachable(q, "q")) != KVC_OK ||
+        (st = check_reachable(block_table, "block_table")) != KVC_OK ||
+        (st = check_reachable(context_lens, "context_lens")) != KVC_OK)
         return st;
     CUtensorMap tk, tv;
     if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)

@@ -154,16 +154,23 @@ def _cuda(name: str, t: torch.Tensor, dtype=None, contiguous=True) -> torch.Tens
     return t
 
 
-def _decode_out(t: torch.Tensor) -> torch.Tensor:
-    """`out` of the decode calls: a CUDA tensor, or a pinned host tensor that the kernels
-    write directly (the result lands in host memory with no separate copy)."""
+def _reachable(name: str, t: torch.Tensor, dtype=None) -> torch.Tensor:
+    """An argument the kernels may reach in host memory: a CUDA tensor, or a pinned host
+    tensor that they read or write across the host link directly."""
     if isinstance(t, torch.Tensor) and not t.is_cuda:
         if not t.is_pinned():
-            raise ValueError("out must be a CUDA tensor or a pinned host tensor")
+            raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
         if not t.is_contiguous():
-            raise ValueError("out must be contiguous")
+            raise ValueError(f"{name} must be contiguous")
         return t
-    return _cuda("out", t)
+    return _cuda(name, t, dtype)
+
+
+def _decode_out(t: torch.Tensor) -> torch.Tensor:
+    """`out` of the decode calls (a CUDA tensor or a pinned host tensor)."""
+    return _reachable("out", t)
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -195,10 +202,10 @@ def kvc_slot_mapping(slot_mapping: torch.Tensor, block_table: torch.Tensor,
                      context_lens: torch.Tensor, q_indptr: Optional[torch.Tensor],
                      page_size: int, max_q_len: int = 1, stream=None) -> None:
     _cuda("slot_mapping", slot_mapping, torch.int32)
-    _cuda("block_table", block_table, torch.int32)
-    _cuda("context_lens", context_lens, torch.int32)
+    _reachable("block_table", block_table, torch.int32)
+    _reachable("context_lens", context_lens, torch.int32)
     if q_indptr is not None:
-        _cuda("q_indptr", q_indptr, torch.int32)
+        _reachable("q_indptr", q_indptr, torch.int32)
     S = int(context_lens.shape[0])
     _check("kvc_slot_mapping", lib().kvc_slot_mapping(
         _ptr(slot_mapping), _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
@@ -209,9 +216,10 @@ def kvc_slot_mapping(slot_mapping: torch.Tensor, block_table: torch.Tensor,
 def kvc_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
               v_new: torch.Tensor, slot_mapping: torch.Tensor, stream=None,
               layout: str = "nhd") -> None:
-    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_new", k_new),
-                    ("v_new", v_new)):
-        _cuda(name, t, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _reachable("k_new", k_new, torch.bfloat16)
+    _reachable("v_new", v_new, torch.bfloat16)
     _cuda("slot_mapping", slot_mapping, torch.int32)
     _check("kvc_store", lib().kvc_store(
         _ptr(k_pool), _ptr(v_pool), pool_desc(k_pool, layout), _ptr(k_new), _ptr(v_new),
@@ -329,11 +337,11 @@ def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
                workspace: Optional[torch.Tensor] = None, stream=None,
                layout: str = "nhd") -> None:
     _decode_out(out)
-    _cuda("q", q, torch.bfloat16)
+    _reachable("q", q, torch.bfloat16)
     _cuda("k_pool", k_pool, torch.bfloat16)
     _cuda("v_pool", v_pool, torch.bfloat16)
-    _cuda("block_table", block_table, torch.int32)
-    _cuda("context_lens", context_lens, torch.int32)
+    _reachable("block_table", block_table, torch.int32)
+    _reachable("context_lens", context_lens, torch.int32)
     ws_bytes = 0
     if workspace is not None:
         _cuda("workspace", workspace)

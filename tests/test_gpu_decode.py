@@ -228,3 +228,21 @@ def test_decode_refuses_pageable_host_out():
     assert st == 1 and b"pinned host" in lib().kvc_last_error()
     torch.cuda.synchronize()
     assert not host.any()
+
+
+@pytest.mark.parametrize("num_splits", [1, 0])
+def test_decode_reads_pinned_host_inputs(num_splits):
+    """q, block_table and context_lens may sit in pinned host memory (with the output too):
+    the kernels read them across the host link and give the device-fed result bit for bit."""
+    case = config_case(2, num_seqs=24)
+    g = GpuRun(case, decode=True)
+    g.store()
+    dev_out = g.attend(torch.bfloat16, num_splits)
+    d = g.d
+    hq, hbt, hctx = (t.cpu().pin_memory() for t in (d.q, d.block_table, d.context_lens))
+    host_out = torch.empty(tuple(dev_out.shape), dtype=torch.bfloat16).pin_memory()
+    kvc.kvc_decode(host_out, hq, d.k_pool, d.v_pool, hbt, hctx, case.max_ctx,
+                   num_splits=num_splits, workspace=g.workspace)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    assert torch.equal(host_out, dev_out.cpu())

@@ -77,3 +77,41 @@ def test_slot_mapping_negative_position_gives_minus_one():
     slots = torch.empty(3, dtype=torch.int32, device="cuda")
     kvc.kvc_slot_mapping(slots, bt, ctx, indptr, 4, max_q_len=3)
     assert slots.cpu().tolist() == [-1, -1, 12]
+
+
+@pytest.mark.parametrize("decode,cfg", [(True, 2), (False, 4)])
+def test_store_and_slot_mapping_read_pinned_host_inputs(decode, cfg):
+    """kvc_slot_mapping's tables and kvc_store's new keys and values may sit in pinned host
+    memory: the slots and the pools come out bit for bit as from device inputs (and as the
+    oracle's)."""
+    case = config_case(cfg, num_seqs=96) if not decode else config_case(cfg)
+    g = GpuRun(case, decode=decode)
+    d = g.d
+    host = {n: getattr(d, n).cpu().pin_memory() for n in ("block_table", "context_lens",
+                                                           "q_indptr", "k_new", "v_new")}
+    kvc.kvc_slot_mapping(g.slots, host["block_table"], host["context_lens"],
+                         None if decode else host["q_indptr"], case.page_size,
+                         max_q_len=case.max_q_len)
+    kvc.kvc_store(d.k_pool, d.v_pool, host["k_new"], host["v_new"], g.slots)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    o = OracleRun(case)
+    np.testing.assert_array_equal(g.slots.cpu().numpy().astype(np.int64), o.slots)
+    k_bits, v_bits = pools_bits(g)
+    assert np.array_equal(k_bits, o.k_pool)
+    assert np.array_equal(v_bits, o.v_pool)
+
+
+def test_store_refuses_pageable_host_inputs():
+    from pagedattention_kvc_store_gb300.kvc import lib, pool_desc, _ptr
+    case = config_case(1)
+    g = GpuRun(case, decode=True)
+    d = g.d
+    kvc.kvc_slot_mapping(g.slots, d.block_table, d.context_lens, None, case.page_size)
+    host_k = np.zeros(d.k_new.numel() + 16, dtype=np.uint16)
+    addr = (host_k.ctypes.data + 15) // 16 * 16
+    import ctypes
+    st = lib().kvc_store(_ptr(d.k_pool), _ptr(d.v_pool), pool_desc(d.k_pool),
+                         ctypes.c_void_p(addr), _ptr(d.v_new), _ptr(g.slots),
+                         int(g.slots.shape[0]), None)
+    assert st == 1 and b"pinned host" in lib().kvc_last_error()
