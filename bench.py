@@ -509,18 +509,30 @@ def run_kvc(args):
         kvc.kvc_decode(out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens,
                        case.max_ctx, num_splits=0, workspace=work)
 
+    def fused_step():
+        # slot mapping + store + decode + merge through kvc_decode_store: the decode CTA that
+        # holds each sequence's newest position stores its new K / V first
+        kvc.kvc_decode_store(out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table,
+                             d.context_lens, case.max_ctx, num_splits=0, workspace=work)
+
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         store_part()
         decode_part()
         torch.cuda.synchronize()
         K, W = args.steps, args.warmup
-        # The step runs as one graph (slot mapping, store, decode, merge), as a serving loop
-        # replays it.  The roofline times the decode alone: a graph of the kvc_decode call,
-        # replayed in a second timed loop (an event node inside the step's graph would cost
-        # the step ~5 us of its own).
-        g_step, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        # The step (slot mapping, store, decode, merge: one kvc_decode_store call) runs as one
+        # graph, as a serving loop replays it.  The same work as the separate calls
+        # (kvc_slot_mapping, kvc_store, kvc_decode) is timed beside it, and the roofline times
+        # the decode alone: a graph of the kvc_decode call, replayed in a timed loop of its own
+        # (an event node inside the step's graph would cost the step ~5 us of its own).
+        fused_step()
+        torch.cuda.synchronize()
+        g_step, g_sep, g_decode = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                   torch.cuda.CUDAGraph())
         with torch.cuda.graph(g_step, stream=stream):
+            fused_step()
+        with torch.cuda.graph(g_sep, stream=stream):
             store_part()
             decode_part()
         with torch.cuda.graph(g_decode, stream=stream):
@@ -552,13 +564,14 @@ def run_kvc(args):
         barrier(world)
         clk = clocks.stop()
         dec_ms = timed_loop(g_decode, max(50, K // 10))
+        sep_ms = timed_loop(g_sep, max(50, K // 10))
         total_ms = max_over_ranks(sum(step_ms), world, dev)
 
         step_b = decode_bytes(case) + store_bytes(case)
         value = whole_job_value(world, step_b, K, total_ms)
         dec_b = decode_bytes(case)
         achieved = dec_b / (statistics.mean(dec_ms) / 1e3) / 1e9
-        launches_per_step = 2 + 1 + (1 if splits > 1 else 0)
+        launches_per_step = 1 + (1 if splits > 1 else 0)
 
         e2e = None
         if not args.no_e2e:
@@ -581,7 +594,12 @@ def run_kvc(args):
                    "sum_ctx": int(case.context_lens.sum()), "splits": splits,
                    "chunk": chunk, "l2": f"flushed between steps ({args.flush_mb} MB write)",
                    "timing": "CUDA events per step on the launching stream; the step is one "
-                             "graph; roofline from decode-only graph replays",
+                             "graph of one kvc_decode_store call; roofline from decode-only "
+                             "graph replays",
+                   "separate_calls": {
+                       "ms_per_step": round(statistics.mean(sep_ms), 5),
+                       "value": round(step_b / (statistics.mean(sep_ms) / 1e3) / 1e9, 2),
+                       "path": "kvc_slot_mapping + kvc_store + kvc_decode as one graph"},
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
@@ -611,10 +629,10 @@ def run_kvc(args):
 def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
     """The same step through the public API with host buffers, every step inside the timed
     region: the step's inputs start in pinned host memory and its output ends there.  No copy
-    is enqueued: kvc_slot_mapping reads the tables, kvc_store the new keys and values and
-    kvc_decode the queries and tables straight from pinned host memory across the host link,
-    and kvc_decode writes its output into a pinned host tensor.  The calls are issued
-    eagerly; the same step captured as one graph is reported beside it."""
+    is enqueued: kvc_decode_store reads the queries, tables and new keys and values straight
+    from pinned host memory across the host link and writes its output into a pinned host
+    tensor.  The call is issued eagerly; the same step captured as one graph is reported
+    beside it."""
     names = ("q", "block_table", "context_lens", "k_new", "v_new")
     src = {name: getattr(d, name) for name in names}
     host_in = {name: t.cpu().pin_memory() for name, t in src.items()}
@@ -624,11 +642,10 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
     slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
 
     def step():
-        kvc.kvc_slot_mapping(slots, host_in["block_table"], host_in["context_lens"], None,
-                             case.page_size)
-        kvc.kvc_store(d.k_pool, d.v_pool, host_in["k_new"], host_in["v_new"], slots)
-        kvc.kvc_decode(out_host, host_in["q"], d.k_pool, d.v_pool, host_in["block_table"],
-                       host_in["context_lens"], case.max_ctx, num_splits=0, workspace=work)
+        kvc.kvc_decode_store(out_host, host_in["q"], host_in["k_new"], host_in["v_new"],
+                             d.k_pool, d.v_pool, host_in["block_table"],
+                             host_in["context_lens"], case.max_ctx, num_splits=0,
+                             workspace=work)
 
     for _ in range(5):
         step()
@@ -665,10 +682,10 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "graph_value": round(step_b / (t_graph / 1e3) / 1e9, 2),
             "graph_ms_per_step": round(t_graph, 5),
-            "path": "kvc_slot_mapping, kvc_store and kvc_decode reading q, block_table, "
-                    "context_lens, k_new and v_new straight from pinned host memory; kvc_decode "
-                    "writing its output into pinned host memory; no copy enqueued; issued "
-                    "eagerly (graph_value: the same step captured as one graph)"}
+            "path": "kvc_decode_store reading q, block_table, context_lens, k_new and v_new "
+                    "straight from pinned host memory and writing its output into pinned host "
+                    "memory; no copy enqueued; issued eagerly (graph_value: the same step "
+                    "captured as one graph)"}
 
 
 def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):

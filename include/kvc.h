@@ -170,6 +170,25 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kvc_decode_store -- kvc_slot_mapping (one new token per sequence) + kvc_store + kvc_decode
+ * in one call: the decode CTA whose chunk ends at sequence s's newest position (ctx_s - 1)
+ * writes that token's key and value (k_new[s], v_new[s], bf16 [num_seqs][kv_heads][head_dim])
+ * for its kv head at the slot block_table[s][(ctx_s - 1) / page_size] * page_size +
+ * (ctx_s - 1) % page_size, before its own copy of that page, and the attention reads it
+ * there.  The pools end exactly as the three calls leave them and so does out (the same
+ * kernels read the same values in the same order).  Sequences with ctx_s = 0 store nothing;
+ * a slot past the pool is skipped and flagged (kvc_device_errors), as in kvc_store.  Two
+ * launches (decode, and merge when split) instead of four.  Arguments as kvc_decode, plus
+ * k_new / v_new (device or pinned host memory, 16-byte aligned); the pools are written.
+ */
+kvc_status kvc_decode_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                            const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,
+                            const int32_t *block_table, int32_t bt_stride,
+                            const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                            int32_t q_heads, float scale, int32_t num_splits, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
  * kvc_decode_plan -- the split plan kvc_decode will use for these scalars: the number of
  * splits (>= 1), the chunk length in positions (a multiple of 64 and of page_size; equal
  * to the padded max_ctx when splits == 1) and the workspace bytes it needs (0 when

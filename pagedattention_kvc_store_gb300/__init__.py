@@ -6,6 +6,7 @@ The product is the C-ABI library libkvc.so (include/kvc.h), built from ``csrc/``
 from .kvc import (EXPORTS, KVC_BF16, KVC_F32, KVC_HND, KVC_NHD, NOALLOC_SCRATCH_BYTES, KvcError,
                   PoolDesc,
                   kvc_append, kvc_append_store, kvc_copy_pages, kvc_decode, kvc_decode_noalloc, kvc_decode_plan,
+                  kvc_decode_store,
                   kvc_decode_shared_prefix, kvc_decode_shared_prefix_plan, kvc_shared_prefix_groups,
                   kvc_decode_int8, kvc_decode_int8_plan, kvc_append_int8, kvc_device_errors, kvc_merge, kvc_slot_mapping,
                   kvc_store, kvc_store_int8, int8_pool_desc,
@@ -14,6 +15,7 @@ from .kvc import (EXPORTS, KVC_BF16, KVC_F32, KVC_HND, KVC_NHD, NOALLOC_SCRATCH_
 __all__ = ["EXPORTS", "KVC_BF16", "KVC_F32", "KVC_HND", "KVC_NHD", "NOALLOC_SCRATCH_BYTES",
            "KvcError", "PoolDesc",
            "kvc_append", "kvc_append_store", "kvc_copy_pages", "kvc_decode", "kvc_decode_noalloc", "kvc_decode_plan",
+           "kvc_decode_store",
            "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan", "kvc_shared_prefix_groups",
            "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8", "kvc_device_errors", "kvc_merge", "kvc_slot_mapping",
            "kvc_store", "kvc_store_int8", "int8_pool_desc",

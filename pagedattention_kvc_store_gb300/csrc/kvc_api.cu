@@ -678,11 +678,18 @@ kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool
     return ok();
 }
 
-kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k_pool,
-                      const void *v_pool, kvc_pool_desc pool, const int32_t *block_table,
-                      int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs,
-                      int32_t max_ctx, int32_t q_heads, float scale, int32_t num_splits,
-                      void *workspace, size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+// kvc_decode, and kvc_decode_store when k_new / v_new are given (the decode CTAs store the
+// new tokens before reading their pages).
+kvc_status decode_impl(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                       const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,
+                       const int32_t *block_table, int32_t bt_stride,
+                       const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                       int32_t q_heads, float scale, int32_t num_splits, void *workspace,
+                       size_t workspace_bytes, void *stream)
 {
     kvc_status st = check_attention_args(out, out_dtype, q, k_pool, v_pool, pool, block_table,
                                          bt_stride, context_lens, num_seqs, max_ctx, q_heads);
@@ -704,6 +711,18 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
         (st = check_reachable(block_table, "block_table")) != KVC_OK ||
         (st = check_reachable(context_lens, "context_lens")) != KVC_OK)
         return st;
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    if (fused) {
+        if (!k_new || !v_new)
+            return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+        if (!aligned16(k_new) || !aligned16(v_new))
+            return fail(KVC_ERR_INVALID_ARG, "new K/V must be 16-byte aligned");
+        if (static_cast<int64_t>(pool.num_pages) * pool.page_size >= (int64_t(1) << 31))
+            return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
+        if ((st = check_reachable(k_new, "k_new")) != KVC_OK ||
+            (st = check_reachable(v_new, "v_new")) != KVC_OK)
+            return st;
+    }
     CUtensorMap tk, tv;
     if ((st = pool_tensor_map(k_pool, pool, &tk)) != KVC_OK)
         return st;
@@ -729,6 +748,13 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
     l.n_split = p.splits;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     l.hnd = pool.layout == KVC_HND;
+    if (fused) {
+        l.k_new = k_new;
+        l.v_new = v_new;
+        l.k_pool_w = k_pool;
+        l.v_pool_w = v_pool;
+        l.num_slots = pool.num_pages * pool.page_size;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = kvc::launch_decode(l, tk, tv, s);
     if (err != cudaSuccess)
@@ -740,6 +766,36 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
             return cuda_fail(err, "merge launch");
     }
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k_pool,
+                      const void *v_pool, kvc_pool_desc pool, const int32_t *block_table,
+                      int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs,
+                      int32_t max_ctx, int32_t q_heads, float scale, int32_t num_splits,
+                      void *workspace, size_t workspace_bytes, void *stream)
+{
+    return decode_impl(out, out_dtype, q, nullptr, nullptr, const_cast<void *>(k_pool),
+                       const_cast<void *>(v_pool), pool, block_table, bt_stride, context_lens,
+                       num_seqs, max_ctx, q_heads, scale, num_splits, workspace,
+                       workspace_bytes, stream);
+}
+
+kvc_status kvc_decode_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                            const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,
+                            const int32_t *block_table, int32_t bt_stride,
+                            const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                            int32_t q_heads, float scale, int32_t num_splits, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    return decode_impl(out, out_dtype, q, k_new, v_new, k_pool, v_pool, pool, block_table,
+                       bt_stride, context_lens, num_seqs, max_ctx, q_heads, scale, num_splits,
+                       workspace, workspace_bytes, stream);
 }
 
 kvc_status kvc_shared_prefix_groups(const int32_t *block_table, int32_t bt_stride,

@@ -52,6 +52,12 @@ struct Args {
                                     // split_stride per row
     float scale_log2;
     int hnd;                        // HND pools: page boxes addressed by (page, kv head) block
+    // Fused store (kvc_decode_store): the new token of every sequence, [S][Hkv][D], written
+    // into the pools (num_slots slots) by the CTA whose chunk ends at the newest position,
+    // before that CTA's copy of the page; null otherwise.
+    const uint4 *k_new, *v_new;
+    uint4 *k_pool, *v_pool;
+    int num_slots;
 };
 
 // Kernel arguments from the host-side launch description.
@@ -77,6 +83,11 @@ inline Args make_args(const DecodeLaunch &l)
     a.split_base = l.split_base;
     a.split_stride = l.split_stride > 0 ? l.split_stride : l.n_split;
     a.scale_log2 = l.scale * kLog2e;
+    a.k_new = static_cast<const uint4 *>(l.k_new);
+    a.v_new = static_cast<const uint4 *>(l.v_new);
+    a.k_pool = static_cast<uint4 *>(l.k_pool_w);
+    a.v_pool = static_cast<uint4 *>(l.v_pool_w);
+    a.num_slots = l.num_slots;
     return a;
 }
 
@@ -104,11 +115,23 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap *tmap_k, const CUte
     int pre_page = 0;
     if (warp == kConsumerWarps && k_begin / P + lane < a.bt_stride)
         pre_page = a.block_table[static_cast<size_t>(s) * a.bt_stride + k_begin / P + lane];
+    // Fused store: the producer's lanes fetch the sequence's new K / V row for this kv head
+    // (16 bytes each) together with the context length; only the CTA whose chunk ends at the
+    // newest position writes it.
+    constexpr int kRowChunks = D / 8;
+    uint4 k_row_new = make_uint4(0u, 0u, 0u, 0u), v_row_new = k_row_new;
+    if (a.k_new != nullptr && warp == kConsumerWarps && lane < kRowChunks) {
+        const size_t src = (static_cast<size_t>(s) * a.kv_heads + kvh) * kRowChunks + lane;
+        k_row_new = load_streaming(a.k_new + src);
+        v_row_new = load_streaming(a.v_new + src);
+    }
     int ctx = a.context_lens[s];
+    bool store_new = a.k_new != nullptr && ctx >= 1;
     if (ctx > a.bt_stride * a.page_size) {   // the block-table row cannot hold it
         if (threadIdx.x == 0 && split == 0)
             atomicOr(errors, kErrContextRange);
         ctx = a.bt_stride * a.page_size;
+        store_new = false;                    // no slot for the new token: stored nowhere
     }
     const int k_end = min(ctx, k_begin + a.chunk);
     const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
@@ -154,6 +177,12 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap *tmap_k, const CUte
         int cached_page = pre_page;
         int issued = 0;
         bool ok = true;
+        // this CTA writes the new token when its chunk ends at the newest position, in the
+        // sequence's last page: before the last stage's copies read that page
+        const bool writes_new = store_new && k_end == ctx;
+        const int new_page = writes_new ? a.block_table[static_cast<size_t>(s) * a.bt_stride +
+                                                        (ctx - 1) / P]
+                                        : 0;
         for (int b = 0; b < n_blocks; ++b) {
             const int st = b % kStages;
             if (b >= kStages) {
@@ -180,6 +209,27 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap *tmap_k, const CUte
             // several lanes reach a much higher TMA rate than one thread issuing them in turn.
             const int i = lane >> 1;
             const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
+            if (writes_new && b + 1 == n_blocks) {
+                const int off_new = (ctx - 1) % P;
+                const long long slot = static_cast<long long>(new_page) * P + off_new;
+                if (new_page >= 0 && slot < a.num_slots) {
+                    if (lane < kRowChunks) {
+                        const size_t dst =
+                            a.hnd ? ((static_cast<size_t>(new_page) * a.kv_heads + kvh) * P +
+                                     off_new) * kRowChunks + lane
+                                  : (static_cast<size_t>(slot) * a.kv_heads + kvh) * kRowChunks +
+                                        lane;
+                        a.k_pool[dst] = k_row_new;
+                        a.v_pool[dst] = v_row_new;
+                    }
+                } else if (lane == 0) {
+                    atomicOr(errors, kErrSlotRange);   // skipped, as kvc_store skips it
+                }
+                // the stores (generic proxy) before the copies (async proxy) that read them
+                fence_proxy_async_global();
+                __syncwarp();
+                fence_proxy_async_global();
+            }
             if (i < np) {
                 const int off = i * P * D * 2;
                 // NHD maps {64, slot, half, kv head}; HND maps {64, offset, half, block}

@@ -334,6 +334,23 @@ __device__ __forceinline__ void tc_fence_after_sync()
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (TMA, tensor cores).
+// A 16-byte read-only load that does not allocate in L1 (data read once).
+__device__ __forceinline__ uint4 load_streaming(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Orders this thread's earlier generic-proxy global accesses before its later async-proxy
+// (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

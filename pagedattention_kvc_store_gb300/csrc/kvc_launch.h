@@ -46,6 +46,10 @@ struct DecodeLaunch {
     int split_base = 0;
     int split_stride = 0;   // 0: n_split
     bool hnd = false;       // pools in the HND layout (the tensor maps follow it too)
+    // Fused store (kvc_decode_store): new K / V [S][Hkv][D] and the writable pools.
+    const void *k_new = nullptr, *v_new = nullptr;
+    void *k_pool_w = nullptr, *v_pool_w = nullptr;
+    int num_slots = 0;
 };
 
 // Decode over INT8 pages (head_dim 128): codes like a bf16 pool, scales [pages][Hkv][P].

@@ -66,15 +66,6 @@ __global__ void slot_mapping_ragged_kernel(int32_t *__restrict__ slots,
     }
 }
 
-__device__ __forceinline__ uint4 load_streaming(const uint4 *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 // chunks = kv_heads * head_dim * 2 / 16 per token row.
 // HND pools (hnd = true): the chunk's kv head h = c / row_chunks is its own block per page,
 // [page][h][offset][head_dim], so the destination is ((page * Hkv + h) * P + offset) rows of

@@ -30,7 +30,7 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
            "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8",
-           "kvc_append_store", "kvc_shared_prefix_groups")
+           "kvc_append_store", "kvc_shared_prefix_groups", "kvc_decode_store")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
             L.kvc_decode.restype = ctypes.c_int
             L.kvc_decode.argtypes = [p, i32, p, p, p, PoolDesc, p, i32, p, i32, i32, i32, f,
                                      i32, p, sz, p]
+            L.kvc_decode_store.restype = ctypes.c_int
+            L.kvc_decode_store.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, i32, i32,
+                                           i32, f, i32, p, sz, p]
             L.kvc_decode_plan.restype = ctypes.c_int
             L.kvc_decode_plan.argtypes = [i32, i32, PoolDesc, i32, i32,
                                           ctypes.POINTER(i32), ctypes.POINTER(i32),
@@ -352,6 +355,32 @@ def kvc_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool:
         _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def kvc_decode_store(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor,
+                     v_new: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                     block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
+                     scale: float = 0.0, num_splits: int = 0,
+                     workspace: Optional[torch.Tensor] = None, stream=None,
+                     layout: str = "nhd") -> None:
+    """Store each sequence's new token (k_new / v_new [S, Hkv, D]) and decode, in one call."""
+    _decode_out(out)
+    _reachable("q", q, torch.bfloat16)
+    _reachable("k_new", k_new, torch.bfloat16)
+    _reachable("v_new", v_new, torch.bfloat16)
+    _cuda("k_pool", k_pool, torch.bfloat16)
+    _cuda("v_pool", v_pool, torch.bfloat16)
+    _reachable("block_table", block_table, torch.int32)
+    _reachable("context_lens", context_lens, torch.int32)
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("kvc_decode_store", lib().kvc_decode_store(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+        _ptr(v_pool), pool_desc(k_pool, layout), _ptr(block_table), int(block_table.shape[1]),
+        _ptr(context_lens), int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]),
+        float(scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def kvc_merge(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,
