@@ -97,6 +97,13 @@ def test_empty_context_stores_nothing():
     out2 = torch.empty_like(out1)
     kvc.kvc_decode_store(out1, d1.q, d1.k_new, d1.v_new, d1.k_pool, d1.v_pool, d1.block_table,
                          d1.context_lens, case.max_ctx, num_splits=1)
+    # with two splits (partials and merge): the empty sequence's output is 0 as well
+    pool = kvc.pool_desc(d1.k_pool)
+    _, _, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 2)
+    out3 = torch.full_like(out1, float("nan"))
+    kvc.kvc_decode_store(out3, d1.q, d1.k_new, d1.v_new, d1.k_pool, d1.v_pool, d1.block_table,
+                         d1.context_lens, case.max_ctx, num_splits=2,
+                         workspace=torch.empty(ws, dtype=torch.uint8, device="cuda"))
     slots = torch.empty(case.num_seqs, dtype=torch.int32, device="cuda")
     kvc.kvc_slot_mapping(slots, d2.block_table, d2.context_lens, None, case.page_size)
     kvc.kvc_store(d2.k_pool, d2.v_pool, d2.k_new, d2.v_new, slots)
@@ -108,3 +115,35 @@ def test_empty_context_stores_nothing():
     assert np.array_equal(bf16_bits_of(d1.k_pool), bf16_bits_of(d2.k_pool))
     assert np.array_equal(bf16_bits_of(d1.v_pool), bf16_bits_of(d2.v_pool))
     assert torch.equal(out1, out2) and not out1[2].any()
+    assert not out3[2].any() and (out3 - out1).abs().max().item() < 2e-3
+
+
+def test_repeated_calls_and_graph_replay():
+    """Storing the same new tokens again leaves the pools and the output as they were:
+    repeated calls and replays of a captured graph give the same output."""
+    case = config_case(2)
+    d = to_device(case)
+    pool = kvc.pool_desc(d.k_pool)
+    sp, _, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device="cuda")
+
+    def call():
+        kvc.kvc_decode_store(out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table,
+                             d.context_lens, case.max_ctx, workspace=work)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    first = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for _ in range(3):
+        g.replay()
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    assert torch.equal(out, first)
