@@ -171,7 +171,10 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
 
 /*
  * kvc_decode_store -- kvc_slot_mapping (one new token per sequence) + kvc_store + kvc_decode
- * in one call: the decode CTA whose chunk ends at sequence s's newest position (ctx_s - 1)
+ * in one call ("KV Cache Management and PagedAttention", "Grow the allocation as generation
+ * proceeds" and "Compute attention over scattered KV"; TileInfer.jl "KV cache", "Pages and
+ * block tables": the step writes the new key and value at their slot, and TileInfer does that
+ * inside the kernel that prepares attention's inputs): the decode CTA whose chunk ends at sequence s's newest position (ctx_s - 1)
  * writes that token's key and value (k_new[s], v_new[s], bf16 [num_seqs][kv_heads][head_dim])
  * for its kv head at the slot block_table[s][(ctx_s - 1) / page_size] * page_size +
  * (ctx_s - 1) % page_size, before its own copy of that page, and the attention reads it
@@ -200,7 +203,10 @@ kvc_status kvc_decode_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool
 
 /*
  * kvc_shared_prefix_groups -- find the groups for kvc_decode_shared_prefix from the block
- * tables alone (an opt-in prepass; the caller may build the groups itself instead).
+ * tables alone (an opt-in prepass; the caller may build the groups itself instead).  Shared
+ * pages are those "KV Cache Management and PagedAttention", "Share common KV across
+ * responses" and Quail "KV", "Prefix sharing" / "The sharing plan" put in several block
+ * tables; this finds them again by comparing adjacent tables.
  * Sequences s - 1 and s are linked when their block-table rows agree on at least the first
  * page both can share; a sequence can share only whole pages before the page of its last
  * position (its newest token goes to a page of its own): floor((ctx - 1) / page_size) pages,
