@@ -302,7 +302,8 @@ kvc_status kvc_decode_noalloc(void *out, int32_t out_dtype, const void *q,
  * kvc_merge -- combine split partials by log-sum-exp.  For every row r:
  *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M);
  *   out[r] = sum_j w_j partial_o[r][j] / sum_j w_j;   lse_out[r] = M + log(sum_j w_j).
- * Splits with lse = -inf hold no key: their partial_o is not read.  A row whose splits are
+ * Splits with lse = -inf hold no key: their partial_o is not used (the first few splits'
+ * partials are loaded with the lse values, so partial_o must span every split).  A row whose splits are
  * all empty gets out = 0 and lse_out = -inf.  out may be pinned host memory, as for
  * kvc_decode.  (The pages leave partitioning and combining
  * inside the kernel open -- "KV Cache Management and PagedAttention", "Compute attention

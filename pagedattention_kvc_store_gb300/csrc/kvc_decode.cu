@@ -60,6 +60,28 @@ __global__ void __launch_bounds__(128) merge_kernel(void *out, int out_f32,
     if (row >= rows)
         return;
     const float *lse = part_lse + static_cast<size_t>(row) * n_split;
+    const float *po = part_o + static_cast<size_t>(row) * n_split * D + lane * V;
+    // The first kPre splits' partials are requested together with the lse values (one memory
+    // round trip instead of two on the step's critical path); an empty split's values are
+    // loaded but never used.
+    constexpr int kPre = 4;
+    float pre[kPre][V];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+        if (j < n_split) {
+            if constexpr (V == 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(po + static_cast<size_t>(j) * D);
+                pre[j][0] = t.x;
+                pre[j][1] = t.y;
+                pre[j][2] = t.z;
+                pre[j][3] = t.w;
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    pre[j][v] = po[static_cast<size_t>(j) * D + v];
+            }
+        }
+    }
     float M = -INFINITY;
     for (int j = lane; j < n_split; j += 32)
         M = fmaxf(M, lse[j]);
@@ -72,7 +94,6 @@ __global__ void __launch_bounds__(128) merge_kernel(void *out, int out_f32,
         acc[v] = 0.0f;
     float sum = 0.0f;
     if (M != -INFINITY) {
-        const float *po = part_o + static_cast<size_t>(row) * n_split * D + lane * V;
         for (int j0 = 0; j0 < n_split; j0 += 32) {
             const float mine = (j0 + lane < n_split) ? lse[j0 + lane] : -INFINITY;
             const int cnt = min(32, n_split - j0);
@@ -82,18 +103,31 @@ __global__ void __launch_bounds__(128) merge_kernel(void *out, int out_f32,
                     continue;   // empty split: its partial is not read
                 const float w = fast_exp2((lj - M) * kLog2e);
                 sum += w;
-                const float *src = po + static_cast<size_t>(j0 + jj) * D;
-                if constexpr (V == 4) {
-                    const float4 val = *reinterpret_cast<const float4 *>(src);
-                    acc[0] += w * val.x;
-                    acc[1] += w * val.y;
-                    acc[2] += w * val.z;
-                    acc[3] += w * val.w;
+                const int j = j0 + jj;
+                float val[V];
+                if (j < kPre) {   // select in registers (no dynamic index into pre)
+#pragma unroll
+                    for (int k = 0; k < kPre; ++k)
+                        if (k == j) {
+#pragma unroll
+                            for (int v = 0; v < V; ++v)
+                                val[v] = pre[k][v];
+                        }
+                } else if constexpr (V == 4) {
+                    const float4 t =
+                        *reinterpret_cast<const float4 *>(po + static_cast<size_t>(j) * D);
+                    val[0] = t.x;
+                    val[1] = t.y;
+                    val[2] = t.z;
+                    val[3] = t.w;
                 } else {
 #pragma unroll
                     for (int v = 0; v < V; ++v)
-                        acc[v] += w * src[v];
+                        val[v] = po[static_cast<size_t>(j) * D + v];
                 }
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    acc[v] += w * val[v];
             }
         }
     }
