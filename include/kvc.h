@@ -365,6 +365,14 @@ kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const v
 kvc_status kvc_device_errors(uint32_t *flags_out);
 
 /*
+ * kvc_selftest_wait -- a diagnostic of the failure path every kernel shares: one CTA waits on
+ * an mbarrier phase that nothing completes, with the same bounded wait the kernels use; after
+ * about a second it gives up, sets bit 1 << 12 of the device error word (kvc_device_errors)
+ * and returns.  Nothing faults or hangs, and later calls run as usual.
+ */
+kvc_status kvc_selftest_wait(void *stream);
+
+/*
  * INT8 pages (TileInfer.jl "KV cache", section "INT8 cache": the pools hold int8 codes with
  * one fp32 scale per cached vector -- one kv head at one position -- x ~ scale * code,
  * symmetric, scale = max|x| / 127, quantised once when the position is written; attention

@@ -1132,6 +1132,12 @@ kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const vo
     return err == cudaSuccess ? ok() : cuda_fail(err, "append_int8 launch");
 }
 
+kvc_status kvc_selftest_wait(void *stream)
+{
+    const cudaError_t err = kvc::launch_selftest_wait(static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? ok() : cuda_fail(err, "self-test launch");
+}
+
 kvc_status kvc_device_errors(uint32_t *flags_out)
 {
     if (flags_out == nullptr)

@@ -158,6 +158,21 @@ cudaError_t launch_decode_t(const DecodeLaunch &l, const CUtensorMap &tk, const 
     return launch_pdl(kernel, grid, dim3(kThreads), smem, stream, tk, tv, a);
 }
 
+// The bounded wait every kernel uses, on an mbarrier phase that nothing completes: it gives
+// up after kWaitLimitCycles and the CTA records kErrSelftestWait and returns, leaving the
+// context usable.  A diagnostic of the failure path, with no fault and no hang.
+__global__ void __launch_bounds__(32) selftest_wait_kernel()
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar, 0)) && threadIdx.x == 0)
+        atomicOr(&g_decode_errors, kErrSelftestWait);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeLaunch &l, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -185,6 +200,12 @@ cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const floa
                           part_o, part_lse, rows, n_split, lse_out);
     return launch_pdl(merge_kernel<64>, dim3(blocks), dim3(128), 0, stream, out, out_f32, part_o,
                       part_lse, rows, n_split, lse_out);
+}
+
+cudaError_t launch_selftest_wait(cudaStream_t stream)
+{
+    selftest_wait_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_decode_errors(uint32_t *flags)

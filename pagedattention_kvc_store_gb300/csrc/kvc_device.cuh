@@ -29,6 +29,7 @@ enum DeviceErrorBits : uint32_t {
     kErrSmemAlign = 1u << 9,       // dynamic shared memory not 1024-byte aligned: no work done
     kErrPageRange = 1u << 10,      // a page copy named a page outside the pool: skipped
     kErrScaleRange = 1u << 11,     // INT8 append: a value scale above its fp16 limit (4000)
+    kErrSelftestWait = 1u << 12,   // kvc_selftest_wait: its wait ran out, as it must
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)

@@ -190,6 +190,8 @@ cudaError_t launch_append_int8(const AppendInt8Launch &a, const CUtensorMap &tma
 
 // Device error words, one per translation unit that owns bounded waits.
 cudaError_t read_and_clear_decode_errors(uint32_t *flags);
+// One CTA whose bounded wait runs out (about a second): sets kErrSelftestWait.
+cudaError_t launch_selftest_wait(cudaStream_t stream);
 cudaError_t read_and_clear_store_errors(uint32_t *flags);
 cudaError_t read_and_clear_append_tc_errors(uint32_t *flags);
 cudaError_t read_and_clear_grouped_errors(uint32_t *flags);

@@ -30,7 +30,8 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_decode_noalloc", "kvc_decode_shared_prefix", "kvc_decode_shared_prefix_plan",
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
            "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8",
-           "kvc_append_store", "kvc_shared_prefix_groups", "kvc_decode_store")
+           "kvc_append_store", "kvc_shared_prefix_groups", "kvc_decode_store",
+           "kvc_selftest_wait")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -107,6 +108,8 @@ def lib() -> ctypes.CDLL:
             L.kvc_decode_shared_prefix_plan.restype = ctypes.c_int
             L.kvc_decode_shared_prefix_plan.argtypes = [i32, i32, PoolDesc, i32, i32, i32,
                                                         ctypes.POINTER(sz)]
+            L.kvc_selftest_wait.restype = ctypes.c_int
+            L.kvc_selftest_wait.argtypes = [p]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             L.kvc_store_int8.restype = ctypes.c_int
@@ -519,6 +522,12 @@ def kvc_shared_prefix_groups(group_indptr: torch.Tensor, group_seqs: torch.Tenso
         _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens), S, int(page_size),
         int(max_members), _ptr(group_indptr), _ptr(group_seqs), _ptr(prefix_len),
         _ptr(num_groups), _stream(stream)))
+
+
+def kvc_selftest_wait(stream=None) -> None:
+    """Enqueue the bounded-wait self-test (about a second); kvc_device_errors() then has bit
+    1 << 12 set."""
+    _check("kvc_selftest_wait", lib().kvc_selftest_wait(_stream(stream)))
 
 
 def kvc_device_errors() -> int:
