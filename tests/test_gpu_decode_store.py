@@ -61,7 +61,8 @@ def test_batched_decode_store(num_splits, out_dtype):
 def test_edges_and_hnd():
     """One-position contexts, a newest position at the first / last offset of its page,
     several page sizes; HND pools."""
-    for P, Hq, Hkv, D in ((16, 32, 8, 128), (32, 8, 2, 64), (64, 16, 8, 128)):
+    for P, Hq, Hkv, D in ((16, 32, 8, 128), (32, 8, 2, 64), (64, 16, 8, 128), (16, 8, 8, 128),
+                          (32, 64, 8, 64)):
         ctx = np.array([1, 2, P, P + 1, 2 * P, 3 * P - 1, 5 * P + 7, 700])
         case = build_case(P + D + Hq, name="decode-store-edges", page_size=P, q_heads=Hq,
                           kv_heads=Hkv, head_dim=D, context_lens=lambda rng: ctx,
@@ -147,3 +148,13 @@ def test_repeated_calls_and_graph_replay():
     torch.cuda.synchronize()
     assert kvc.kvc_device_errors() == 0
     assert torch.equal(out, first)
+
+
+def test_host_fed_hnd():
+    case = config_case(2, num_seqs=16)
+    dev = fused(case, torch.float32, 0, layout="hnd")
+    host = fused(case, torch.float32, 0, layout="hnd", host=True)
+    assert torch.equal(dev[0], host[0])
+    assert np.array_equal(dev[1], host[1]) and np.array_equal(dev[2], host[2])
+    o = OracleRun(case)
+    assert np.array_equal(dev[1], oracle.nhd_to_hnd(o.k_pool))
