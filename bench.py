@@ -412,6 +412,18 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             t16 = time_graph(torch, lambda: kvc.kvc_decode(
                 out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
                 num_splits=0, workspace=work), stream, flush, args.leg_steps)
+            # the whole INT8 step: quantise and store each sequence's new token, then decode
+            # (the pools already hold those tokens, so every replay writes the same bytes)
+            t8_fused = time_graph(torch, lambda: kvc.kvc_decode_int8_store(
+                out, d.q, d.k_new, d.v_new, kc, vc, ks, vs, d.block_table, d.context_lens,
+                case.max_ctx, num_splits=0, workspace=work), stream, flush, args.leg_steps)
+
+            def int8_separate():
+                kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+                kvc.kvc_store_int8(kc, vc, ks, vs, d.k_new, d.v_new, slots)
+                kvc.kvc_decode_int8(out, d.q, kc, vc, ks, vs, d.block_table, d.context_lens,
+                                    case.max_ctx, num_splits=0, workspace=work)
+            t8_sep = time_graph(torch, int8_separate, stream, flush, args.leg_steps)
         b8 = int(case.context_lens.sum()) * 2 * H * (D + 4) + qo(case)
         b16 = decode_bytes(case)
         legs["int8_decode"] = {
@@ -423,6 +435,10 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             "speedup_vs_bf16": round(t16 / t8, 3), "splits": splits,
             "gpu_launches_per_step": 2 if splits > 1 else 1,
             "traffic_decode_int8_kernel": traffic_from_profile("decode_int8_batched"),
+            "step_store_decode_us": {"fused": round(t8_fused * 1e3, 1),
+                                     "separate": round(t8_sep * 1e3, 1),
+                                     "launches": {"fused": 2 if splits > 1 else 1,
+                                                  "separate": 4 if splits > 1 else 3}},
         }
         del d, out, work, slots, kc, vc, ks, vs, all_slots
         torch.cuda.empty_cache()

@@ -411,6 +411,30 @@ kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const vo
                            size_t workspace_bytes, void *stream);
 
 /*
+ * kvc_decode_int8_store -- kvc_slot_mapping (one new token per sequence) + kvc_store_int8 +
+ * kvc_decode_int8 in one call, as kvc_decode_store is for 16-bit pages (TileInfer.jl "KV
+ * cache", "INT8 cache": a vector is quantised once, when it is written; "Pages and block
+ * tables": the step writes the new key and value at their slot).  The decode CTA whose chunk
+ * ends at sequence s's newest position (ctx_s - 1) quantises that token's key and value
+ * (k_new[s], v_new[s], bf16 [num_seqs][kv_heads][128]) for its kv head with kvc_store_int8's
+ * arithmetic, writes codes and scales at slot block_table[s][(ctx_s - 1) / page_size] *
+ * page_size + (ctx_s - 1) % page_size before its own copies of that page, and the attention
+ * reads them there.  Codes, scales and out end exactly as the three calls leave them.
+ * Sequences with ctx_s = 0 store nothing; a slot past the pool is skipped and flagged
+ * (kvc_device_errors).  Arguments as kvc_decode_int8 (split plan from kvc_decode_int8_plan),
+ * plus k_new / v_new (device or pinned host memory, 16-byte aligned); the code and scale
+ * pools are written.  out, q, block_table and context_lens may be pinned host memory, as for
+ * kvc_decode.
+ */
+kvc_status kvc_decode_int8_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                                 const void *v_new, void *k_codes, void *v_codes,
+                                 float *k_scales, float *v_scales, kvc_pool_desc pool,
+                                 const int32_t *block_table, int32_t bt_stride,
+                                 const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                                 int32_t q_heads, float scale, int32_t num_splits,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * kvc_append_int8 -- kvc_append over INT8 pages (same arguments and outputs; the new tokens'
  * codes and scales must already be stored, kvc_store_int8).  The score of position p is
  * q . k_code[p] * k_scale[p] * scale and the value it weighs is v_scale[p] * v_code[p].  The

@@ -567,12 +567,16 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
     return err == cudaSuccess ? ok() : cuda_fail(err, "store_int8 launch");
 }
 
-kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
-                           const void *v_codes, const float *k_scales, const float *v_scales,
-                           kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
-                           const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
-                           int32_t q_heads, float scale, int32_t num_splits, void *workspace,
-                           size_t workspace_bytes, void *stream)
+namespace {
+
+// kvc_decode_int8, and kvc_decode_int8_store when k_new / v_new are given (the decode CTAs
+// quantise and store the new tokens before reading their pages).
+kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                            const void *v_new, void *k_codes, void *v_codes, float *k_scales,
+                            float *v_scales, kvc_pool_desc pool, const int32_t *block_table,
+                            int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs,
+                            int32_t max_ctx, int32_t q_heads, float scale, int32_t num_splits,
+                            void *workspace, size_t workspace_bytes, void *stream)
 {
     kvc_status st = check_attention_args(out, out_dtype, q, k_codes, v_codes, pool, block_table,
                                          bt_stride, context_lens, num_seqs, max_ctx, q_heads);
@@ -596,6 +600,22 @@ kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const vo
                         p.ws_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
         if (!aligned16(workspace))
             return fail(KVC_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    }
+    if ((st = check_decode_out(out)) != KVC_OK || (st = check_reachable(q, "q")) != KVC_OK ||
+        (st = check_reachable(block_table, "block_table")) != KVC_OK ||
+        (st = check_reachable(context_lens, "context_lens")) != KVC_OK)
+        return st;
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    if (fused) {
+        if (!k_new || !v_new)
+            return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+        if (!aligned16(k_new) || !aligned16(v_new))
+            return fail(KVC_ERR_INVALID_ARG, "new K/V must be 16-byte aligned");
+        if (static_cast<int64_t>(pool.num_pages) * pool.page_size >= (int64_t(1) << 31))
+            return fail(KVC_ERR_UNSUPPORTED, "num_pages * page_size must be below 2^31");
+        if ((st = check_reachable(k_new, "k_new")) != KVC_OK ||
+            (st = check_reachable(v_new, "v_new")) != KVC_OK)
+            return st;
     }
     CUtensorMap tk, tv;
     if ((st = pool_tensor_map_int8(k_codes, pool, &tk)) != KVC_OK)
@@ -622,6 +642,15 @@ kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const vo
     l.chunk = p.chunk;
     l.n_split = p.splits;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
+    if (fused) {
+        l.k_new = k_new;
+        l.v_new = v_new;
+        l.k_codes_w = k_codes;
+        l.v_codes_w = v_codes;
+        l.k_scales_w = k_scales;
+        l.v_scales_w = v_scales;
+        l.num_slots = pool.num_pages * pool.page_size;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = kvc::launch_decode_int8(l, tk, tv, s);
     if (err != cudaSuccess)
@@ -633,6 +662,38 @@ kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const vo
             return cuda_fail(err, "merge launch");
     }
     return ok();
+}
+
+}  // namespace
+
+kvc_status kvc_decode_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
+                           const void *v_codes, const float *k_scales, const float *v_scales,
+                           kvc_pool_desc pool, const int32_t *block_table, int32_t bt_stride,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                           int32_t q_heads, float scale, int32_t num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    return decode_int8_impl(out, out_dtype, q, nullptr, nullptr, const_cast<void *>(k_codes),
+                            const_cast<void *>(v_codes), const_cast<float *>(k_scales),
+                            const_cast<float *>(v_scales), pool, block_table, bt_stride,
+                            context_lens, num_seqs, max_ctx, q_heads, scale, num_splits,
+                            workspace, workspace_bytes, stream);
+}
+
+kvc_status kvc_decode_int8_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
+                                 const void *v_new, void *k_codes, void *v_codes,
+                                 float *k_scales, float *v_scales, kvc_pool_desc pool,
+                                 const int32_t *block_table, int32_t bt_stride,
+                                 const int32_t *context_lens, int32_t num_seqs, int32_t max_ctx,
+                                 int32_t q_heads, float scale, int32_t num_splits,
+                                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return fail(KVC_ERR_INVALID_ARG, "null pointer argument");
+    return decode_int8_impl(out, out_dtype, q, k_new, v_new, k_codes, v_codes, k_scales,
+                            v_scales, pool, block_table, bt_stride, context_lens, num_seqs,
+                            max_ctx, q_heads, scale, num_splits, workspace, workspace_bytes,
+                            stream);
 }
 
 kvc_status kvc_copy_pages(void *k_pool, void *v_pool, kvc_pool_desc pool,

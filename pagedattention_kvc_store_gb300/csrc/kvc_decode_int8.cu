@@ -74,7 +74,47 @@ struct Args {
     int q_heads, kv_heads, group, page_size;
     int chunk, n_split;
     float scale_log2;
+    // kvc_decode_int8_store: sequence s's new key and value (bf16 [S][Hkv][D]), quantised and
+    // written to the code and scale pools (num_slots slots) by the CTA whose chunk ends at the
+    // newest position, before that CTA's copies of the page; null otherwise.
+    const __nv_bfloat16 *k_new, *v_new;
+    int8_t *k_codes_w, *v_codes_w;
+    float *k_scales_w, *v_scales_w;
+    int num_slots;
 };
+
+// Quantises one vector held as four bf16 values per lane (lane l: elements 4 l .. 4 l + 3)
+// and writes its codes and scale, with the arithmetic of kvc_store_int8 (TileInfer.jl "KV
+// cache", "INT8 cache": scale = max |x| / 127, codes rounded to nearest and clamped to +-127,
+// both quotients fp32 round-to-nearest), so both give the same bytes.
+__device__ __forceinline__ void quantise_store_row(uint2 x, int8_t *codes, float *scale_out,
+                                                   int lane)
+{
+    float f[4];
+    f[0] = __uint_as_float(x.x << 16);
+    f[1] = __uint_as_float(x.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(x.y << 16);
+    f[3] = __uint_as_float(x.y & 0xFFFF0000u);
+    float m = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        m = fmaxf(m, fabsf(f[e]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float scale = __fdiv_rn(m, 127.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        int c = 0;
+        if (scale != 0.0f)
+            c = max(-127, min(127, __float2int_rn(__fdiv_rn(f[e], scale))));
+        packed |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+    }
+    *reinterpret_cast<uint32_t *>(codes + lane * 4) = packed;
+    if (lane == 0)
+        *scale_out = scale;
+}
 
 // fp16 pair (low: byte c of a, high: byte c of b) of two words of int8 codes, exact.  The
 // bytes are moved under exponent bits 0x64 (fp16 1024 + m for m in 0..255) with the sign bit
@@ -115,11 +155,21 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int lane = threadIdx.x & 31;
     const int G = a.group;
     const int P = a.page_size;
+    // the new token's row, requested before anything else so that it is in registers by the
+    // time the producer writes it
+    uint2 k_row_new = make_uint2(0u, 0u), v_row_new = k_row_new;
+    if (a.k_new != nullptr && warp == kConsumerWarps) {
+        const size_t src = (static_cast<size_t>(s) * a.kv_heads + kvh) * (D / 4) + lane;
+        k_row_new = __ldg(reinterpret_cast<const uint2 *>(a.k_new) + src);
+        v_row_new = __ldg(reinterpret_cast<const uint2 *>(a.v_new) + src);
+    }
     int ctx = a.context_lens[s];
+    bool store_new = a.k_new != nullptr && ctx >= 1;
     if (ctx > a.bt_stride * P) {
         if (threadIdx.x == 0 && split == 0)
             atomicOr(&g_decode_int8_errors, kErrContextRange);
         ctx = a.bt_stride * P;
+        store_new = false;   // no slot for the new token: stored nowhere
     }
     const int k_begin = split * a.chunk;
     const int k_end = min(ctx, k_begin + a.chunk);
@@ -162,6 +212,12 @@ __global__ void __launch_bounds__(kThreads, 3)
         int cached_page = 0;
         int issued = 0;
         bool ok = true;
+        // this CTA writes the new token when its chunk ends at the newest position: before
+        // the last stage's copies read that page's codes and scales
+        const bool writes_new = store_new && k_end == ctx;
+        const int new_page = writes_new ? a.block_table[static_cast<size_t>(s) * a.bt_stride +
+                                                        (ctx - 1) / P]
+                                        : 0;
         for (int b = 0; b < n_blocks; ++b) {
             const int st = b % kStages;
             if (b >= kStages &&
@@ -186,6 +242,23 @@ __global__ void __launch_bounds__(kThreads, 3)
             const int i = lane >> 2;
             const int op = lane & 3;
             const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
+            if (writes_new && b + 1 == n_blocks) {
+                const int off_new = (ctx - 1) % P;
+                const long long slot = static_cast<long long>(new_page) * P + off_new;
+                if (new_page >= 0 && slot < a.num_slots) {
+                    const size_t row = (static_cast<size_t>(slot) * a.kv_heads + kvh) * D;
+                    const size_t sidx =
+                        (static_cast<size_t>(new_page) * a.kv_heads + kvh) * P + off_new;
+                    quantise_store_row(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx, lane);
+                    quantise_store_row(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx, lane);
+                } else if (lane == 0) {
+                    atomicOr(&g_decode_int8_errors, kErrSlotRange);   // skipped, as the store skips it
+                }
+                // the stores (generic proxy) before the copies (async proxy) that read them
+                fence_proxy_async_global();
+                __syncwarp();
+                fence_proxy_async_global();
+            }
             if (i < np) {
                 if (op == 0) {
                     tma_load_3d(stage + i * P * D, &tmap_k, 0, kvh, page * P, &full[st], policy);
@@ -448,6 +521,13 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.chunk = l.chunk;
     a.n_split = l.n_split;
     a.scale_log2 = l.scale * 1.4426950408889634f;
+    a.k_new = static_cast<const __nv_bfloat16 *>(l.k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(l.v_new);
+    a.k_codes_w = static_cast<int8_t *>(l.k_codes_w);
+    a.v_codes_w = static_cast<int8_t *>(l.v_codes_w);
+    a.k_scales_w = l.k_scales_w;
+    a.v_scales_w = l.v_scales_w;
+    a.num_slots = l.num_slots;
     auto kernel = paged_decode_int8_kernel<SPLIT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));

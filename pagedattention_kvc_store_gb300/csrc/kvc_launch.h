@@ -66,6 +66,11 @@ struct DecodeInt8Launch {
     int num_seqs, q_heads, kv_heads, page_size;
     int chunk, n_split;
     float scale;
+    // fused store (kvc_decode_int8_store): new K/V [S][Hkv][D] bf16 and the pools to write
+    const void *k_new = nullptr, *v_new = nullptr;
+    void *k_codes_w = nullptr, *v_codes_w = nullptr;
+    float *k_scales_w = nullptr, *v_scales_w = nullptr;
+    int num_slots = 0;
 };
 cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tmap_k,
                                const CUtensorMap &tmap_v, cudaStream_t stream);

@@ -31,7 +31,7 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
            "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8",
            "kvc_append_store", "kvc_shared_prefix_groups", "kvc_decode_store",
-           "kvc_selftest_wait")
+           "kvc_selftest_wait", "kvc_decode_int8_store")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -121,6 +121,9 @@ def lib() -> ctypes.CDLL:
             L.kvc_decode_int8.restype = ctypes.c_int
             L.kvc_decode_int8.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, i32, i32,
                                           i32, f, i32, p, sz, p]
+            L.kvc_decode_int8_store.restype = ctypes.c_int
+            L.kvc_decode_int8_store.argtypes = [p, i32, p, p, p, p, p, p, p, PoolDesc, p, i32, p,
+                                                i32, i32, i32, f, i32, p, sz, p]
             L.kvc_append_int8.restype = ctypes.c_int
             L.kvc_append_int8.argtypes = [p, i32, p, p, p, p, p, PoolDesc, p, i32, p, p, i32,
                                           i32, i32, i32, i32, f, p]
@@ -280,16 +283,42 @@ def kvc_decode_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
                     scale: float = 0.0, num_splits: int = 0,
                     workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
-    _cuda("out", out)
-    _cuda("q", q, torch.bfloat16)
-    _cuda("block_table", block_table, torch.int32)
-    _cuda("context_lens", context_lens, torch.int32)
+    _decode_out(out)
+    _reachable("q", q, torch.bfloat16)
+    _reachable("block_table", block_table, torch.int32)
+    _reachable("context_lens", context_lens, torch.int32)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("kvc_decode_int8", lib().kvc_decode_int8(
         _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
         _ptr(v_scales), pool, _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens),
         int(context_lens.shape[0]), int(max_ctx), int(q.shape[1]), float(scale),
         int(num_splits), _ptr(workspace), ws, _stream(stream)))
+
+
+def kvc_decode_int8_store(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor,
+                          v_new: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                          k_scales: torch.Tensor, v_scales: torch.Tensor,
+                          block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
+                          scale: float = 0.0, num_splits: int = 0,
+                          workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantise and store each sequence's new token (k_new / v_new bf16 [S, Hkv, D]) into the
+    INT8 pools and decode over them, in one call."""
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+    _decode_out(out)
+    _reachable("q", q, torch.bfloat16)
+    _reachable("k_new", k_new, torch.bfloat16)
+    _reachable("v_new", v_new, torch.bfloat16)
+    _reachable("block_table", block_table, torch.int32)
+    _reachable("context_lens", context_lens, torch.int32)
+    ws = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws = workspace.numel() * workspace.element_size()
+    _check("kvc_decode_int8_store", lib().kvc_decode_int8_store(
+        _ptr(out), _out_dtype(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_codes),
+        _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), pool, _ptr(block_table),
+        int(block_table.shape[1]), _ptr(context_lens), int(context_lens.shape[0]), int(max_ctx),
+        int(q.shape[1]), float(scale), int(num_splits), _ptr(workspace), ws, _stream(stream)))
 
 
 def kvc_append_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
