@@ -123,3 +123,41 @@ def test_null_new_rows_are_refused():
         int(bt.shape[1]), ctx.data_ptr(), case.num_seqs, case.max_ctx, case.q_heads, 0.0, 1,
         None, 0, None)
     assert st != 0
+
+
+def test_decode_int8_reads_pinned_host_memory():
+    """kvc_decode_int8 alone: q, the tables and out in pinned host memory give the device-fed
+    bytes (the pools hold the new tokens already, stored by the fused call)."""
+    case = config_case(2, num_seqs=16)
+    dev_out, pools = fused_int8(case, torch.bfloat16, num_splits=3)
+    kc, vc, ks, vs = (torch.from_numpy(a).cuda() for a in pools)
+    args = [bf16_tensor(case.q, "cuda"), i32_tensor(case.block_table, "cuda"),
+            i32_tensor(case.context_lens, "cuda")]
+    q, bt, ctx = (t.cpu().pin_memory() for t in args)
+    out = torch.empty(tuple(dev_out.shape), dtype=torch.bfloat16).pin_memory()
+    _, _, ws = kvc.kvc_decode_int8_plan(case.num_seqs, case.q_heads, kvc.int8_pool_desc(kc),
+                                        case.max_ctx, 3)
+    kvc.kvc_decode_int8(out, q, kc, vc, ks, vs, bt, ctx, case.max_ctx, num_splits=3,
+                        workspace=torch.empty(ws, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    assert torch.equal(out, dev_out)
+
+
+def test_decode_int8_refuses_pageable_host_out():
+    """A host pointer the device cannot reach at that address is refused before anything is
+    enqueued (the C entry point, bypassing the binding's own check)."""
+    import ctypes
+    case = config_case(2, num_seqs=4)
+    kc, vc, ks, vs = (torch.from_numpy(a).cuda() for a in int8_pages(case))
+    q = bf16_tensor(case.q, "cuda")
+    bt, ctx = i32_tensor(case.block_table, "cuda"), i32_tensor(case.context_lens, "cuda")
+    host = np.zeros(case.num_seqs * case.q_heads * case.head_dim + 8, dtype=np.float32)
+    addr = (host.ctypes.data + 15) // 16 * 16
+    st = kvc.lib().kvc_decode_int8(
+        ctypes.c_void_p(addr), kvc.KVC_F32, q.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+        ks.data_ptr(), vs.data_ptr(), kvc.int8_pool_desc(kc), bt.data_ptr(), int(bt.shape[1]),
+        ctx.data_ptr(), case.num_seqs, case.max_ctx, case.q_heads, 0.0, 1, None, 0, None)
+    assert st == 1 and b"pinned host" in kvc.lib().kvc_last_error()
+    torch.cuda.synchronize()
+    assert not host.any()
