@@ -174,8 +174,9 @@ kvc_status kvc_decode(void *out, int32_t out_dtype, const void *q, const void *k
  * in one call ("KV Cache Management and PagedAttention", "Grow the allocation as generation
  * proceeds" and "Compute attention over scattered KV"; TileInfer.jl "KV cache", "Pages and
  * block tables": the step writes the new key and value at their slot, and TileInfer does that
- * inside the kernel that prepares attention's inputs): the decode CTA whose chunk ends at sequence s's newest position (ctx_s - 1)
- * writes that token's key and value (k_new[s], v_new[s], bf16 [num_seqs][kv_heads][head_dim])
+ * inside the kernel that prepares attention's inputs): the decode CTA whose chunk ends at
+ * sequence s's newest position (ctx_s - 1) writes that token's key and value (k_new[s],
+ * v_new[s], bf16 [num_seqs][kv_heads][head_dim])
  * for its kv head at the slot block_table[s][(ctx_s - 1) / page_size] * page_size +
  * (ctx_s - 1) % page_size, before its own copy of that page, and the attention reads it
  * there.  The pools end exactly as the three calls leave them and so does out (the same
@@ -303,8 +304,8 @@ kvc_status kvc_decode_noalloc(void *out, int32_t out_dtype, const void *q,
  *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M);
  *   out[r] = sum_j w_j partial_o[r][j] / sum_j w_j;   lse_out[r] = M + log(sum_j w_j).
  * Splits with lse = -inf hold no key: their partial_o is not used (the first few splits'
- * partials are loaded with the lse values, so partial_o must span every split).  A row whose splits are
- * all empty gets out = 0 and lse_out = -inf.  out may be pinned host memory, as for
+ * partials are loaded with the lse values, so partial_o must span every split).  A row whose
+ * splits are all empty gets out = 0 and lse_out = -inf.  out may be pinned host memory, as for
  * kvc_decode.  (The pages leave partitioning and combining
  * inside the kernel open -- "KV Cache Management and PagedAttention", "Compute attention
  * over scattered KV"; this is the plain combination of softmax-normalised pieces.)

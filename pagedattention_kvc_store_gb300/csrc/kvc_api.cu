@@ -208,7 +208,8 @@ kvc_status tensor_map(MapKey key, CUtensorMap *out)
         return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     CUtensorMap map;
-    CUresult r = fn(&map, key.int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    CUresult r = fn(&map,
+                    key.int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     static_cast<cuuint32_t>(key.rank),
                     const_cast<void *>(key.ptr), key.dims, key.strides, key.box, elem_strides,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

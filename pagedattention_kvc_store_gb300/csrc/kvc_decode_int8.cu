@@ -18,7 +18,8 @@
 // Kernel design (head_dim 128): one CTA per (split, kv head, sequence), 4 consumer warps and a
 // producer warp, three CTAs per SM.  The producer streams 64-position stages -- per page one TMA
 // box of K codes, one of V codes (128-byte swizzle) and one bulk copy each of the K and V
-// scales, issued by parallel lanes -- through a 4-deep ring.  Consumer warp w takes positions 16 w .. 16 w + 15 of each stage:
+// scales, issued by parallel lanes -- through a 4-deep ring.  Consumer warp w takes positions
+// 16 w .. 16 w + 15 of each stage:
 //   S = Q K^T on mma.sync m16n8k16 (fp16; the G query heads padded to 16 rows).  The order
 //   in which head_dim is contracted is free, so thread (., t) takes dims 32 t + 4 kk .. + 3
 //   for k-step kk: its K codes for a position are 32 contiguous bytes (two 16-byte loads) and
@@ -30,6 +31,9 @@
 //   and the accumulators are put back in dim order when the warps combine.
 // Online softmax in base 2, masked positions excluded before the exponential and their
 // probabilities set to 0 by selection (a scale left in an unused slot may be NaN).
+// Fused store (kvc_decode_int8_store): the producer of the CTA whose chunk ends at a
+// sequence's newest position quantises that token's K/V row with the INT8 store's arithmetic
+// and writes its codes and scale before the copies of that page.
 #include <math.h>
 
 #include "kvc_device.cuh"
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                     quantise_store_row(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx, lane);
                     quantise_store_row(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx, lane);
                 } else if (lane == 0) {
-                    atomicOr(&g_decode_int8_errors, kErrSlotRange);   // skipped, as the store skips it
+                    atomicOr(&g_decode_int8_errors, kErrSlotRange);   // skipped, as in the store
                 }
                 // the stores (generic proxy) before the copies (async proxy) that read them
                 fence_proxy_async_global();

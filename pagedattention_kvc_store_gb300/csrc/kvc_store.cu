@@ -99,9 +99,9 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
         if (hnd) {
             const int page = slot / page_size;
             const int h = c / row_chunks;
-            dst = ((static_cast<size_t>(page) * kv_heads + h) * page_size + (slot - page * page_size)) *
-                      row_chunks +
-                  (c - h * row_chunks);
+            const size_t row =
+                (static_cast<size_t>(page) * kv_heads + h) * page_size + (slot - page * page_size);
+            dst = row * row_chunks + (c - h * row_chunks);
         }
         const uint4 kv = load_streaming(k_new + i);
         const uint4 vv = load_streaming(v_new + i);

@@ -30,7 +30,8 @@ __global__ void validate_tables_kernel(const int32_t *block_table, int bt_stride
         const int s = static_cast<int>(idx / bt_stride);
         const int i = static_cast<int>(idx % bt_stride);
         const int ctx = context_lens[s];
-        if (ctx < 0 || static_cast<long long>(ctx) > static_cast<long long>(bt_stride) * page_size) {
+        if (ctx < 0 ||
+            static_cast<long long>(ctx) > static_cast<long long>(bt_stride) * page_size) {
             if (i == 0)
                 atomicMin(&rec->first_bad[0], s);
             continue;
