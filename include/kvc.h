@@ -345,6 +345,8 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
  * that hold only new tokens are attended from there and written to the pools by the attention
  * kernel itself; the new tokens that share a page with cached positions (the chunk's first
  * page when ctx - q_len is not a multiple of page_size) are stored by a small kernel first.
+ * With page_size >= 64 that page holds most of a short chunk and the fused read gains nothing:
+ * there the small kernel stores the whole chunk and the plain append follows (same results).
  *   k_new, v_new   bf16 [num_tokens][kv_heads][head_dim], row t = token t of q (q_indptr)
  *   k_pool, v_pool written (the new tokens' slots only) and read
  * Other arguments as kvc_append.  A token whose position is negative (context_lens[s] <

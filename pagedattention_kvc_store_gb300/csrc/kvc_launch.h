@@ -187,7 +187,7 @@ cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int 
                                   int page_size, int num_slots, bool hnd, const void *k_new,
                                   const void *v_new, const int32_t *block_table, int bt_stride,
                                   const int32_t *q_indptr, const int32_t *context_lens,
-                                  int num_seqs, cudaStream_t stream);
+                                  int num_seqs, bool whole, cudaStream_t stream);
 // tmap_q as for launch_append_tc; tmap_k / tmap_v are the INT8 page maps (one box per page).
 cudaError_t launch_append_int8(const AppendInt8Launch &a, const CUtensorMap &tmap_q,
                                const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,

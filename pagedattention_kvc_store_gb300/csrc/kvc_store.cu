@@ -113,13 +113,15 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
 // Fused store + append, first part: the chunk's tokens in the page of its first token when
 // that page also holds cached positions (positions base .. min(ctx, (base / P + 1) P) - 1 with
 // base = ctx - q_len not a multiple of P), stored at their slots; the fused append reads that
-// page from the pool and writes every later page of the chunk itself.  One CTA per sequence
-// (grid-stride), one thread per 16-byte chunk of a token row; addressing as store_kernel.
+// page from the pool and writes every later page of the chunk itself.  With `whole`, every
+// token of the chunk (positions base .. ctx - 1, each at the page its block table lists) is
+// stored and the plain append follows.  One CTA per sequence (grid-stride), one thread per
+// 16-byte chunk of a token row; addressing as store_kernel.
 __global__ void __launch_bounds__(256) store_boundary_kernel(
     uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, const uint4 *__restrict__ k_new,
     const uint4 *__restrict__ v_new, const int32_t *__restrict__ block_table, int bt_stride,
     const int32_t *__restrict__ q_indptr, const int32_t *__restrict__ context_lens, int num_seqs,
-    int chunks, int kv_heads, int page_size, int num_slots, bool hnd)
+    int chunks, int kv_heads, int page_size, int num_slots, bool hnd, bool whole)
 {
     pdl_wait();
     pdl_trigger();
@@ -129,15 +131,19 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
         const int q_len = __ldg(q_indptr + s + 1) - tok0;
         const int ctx = min(__ldg(context_lens + s), bt_stride * page_size);
         const int base = ctx - q_len;
-        if (q_len <= 0 || base <= 0 || base % page_size == 0)
+        if (q_len <= 0 || (!whole && (base <= 0 || base % page_size == 0)))
             continue;
-        const int n_tok = min(ctx, (base / page_size + 1) * page_size) - base;
-        const int page = __ldg(block_table + static_cast<size_t>(s) * bt_stride + base / page_size);
+        const int n_tok = whole ? q_len : min(ctx, (base / page_size + 1) * page_size) - base;
+        const int32_t *bt_row = block_table + static_cast<size_t>(s) * bt_stride;
+        const int page0 = whole ? 0 : __ldg(bt_row + base / page_size);
         for (int i = threadIdx.x; i < n_tok * chunks; i += blockDim.x) {
             const int t = i / chunks;
             const int c = i - t * chunks;
-            const long long slot =
-                static_cast<long long>(page) * page_size + base % page_size + t;
+            const int pos = base + t;
+            if (pos < 0)
+                continue;   // a clamped context shorter than the chunk: no slot
+            const int page = whole ? __ldg(bt_row + pos / page_size) : page0;
+            const long long slot = static_cast<long long>(page) * page_size + pos % page_size;
             if (slot < 0 || slot >= num_slots) {   // a page outside the pool: skip, flag
                 if (c == 0)
                     atomicOr(&g_store_errors, kErrSlotRange);
@@ -147,7 +153,7 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
             if (hnd) {
                 const int h = c / row_chunks;
                 dst = ((static_cast<size_t>(page) * kv_heads + h) * page_size +
-                       (base % page_size + t)) * row_chunks + (c - h * row_chunks);
+                       pos % page_size) * row_chunks + (c - h * row_chunks);
             }
             const size_t src = static_cast<size_t>(tok0 + t) * chunks + c;
             k_pool[dst] = load_streaming(k_new + src);
@@ -321,7 +327,7 @@ cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int 
                                   int page_size, int num_slots, bool hnd, const void *k_new,
                                   const void *v_new, const int32_t *block_table, int bt_stride,
                                   const int32_t *q_indptr, const int32_t *context_lens,
-                                  int num_seqs, cudaStream_t stream)
+                                  int num_seqs, bool whole, cudaStream_t stream)
 {
     if (num_seqs == 0)
         return cudaSuccess;
@@ -331,7 +337,7 @@ cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int 
                       static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
                       block_table, bt_stride, q_indptr, context_lens, num_seqs,
-                      kv_heads * head_dim * 2 / 16, kv_heads, page_size, num_slots, hnd);
+                      kv_heads * head_dim * 2 / 16, kv_heads, page_size, num_slots, hnd, whole);
 }
 
 cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
