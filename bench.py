@@ -56,12 +56,14 @@ def parse_args():
                    help="skip the shared-prefix and long-context decode legs")
     p.add_argument("--leg-steps", type=int, default=30)
     p.add_argument("--legs", type=lambda v: v.split(","),
-                   default=["shared_prefix", "long_decode", "int8_decode", "hnd_decode",
-                            "page_copy"],
+                   default=["tiny_decode", "shared_prefix", "long_decode", "int8_decode",
+                            "hnd_decode", "page_copy"],
                    help="comma-separated decode legs to run (default: all)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-seconds", type=float, default=5.0,
+                   help="seconds of oracle passes over the headline batch (the other legs' "
+                        "oracle runs take one pass of their workload)")
     return p.parse_args()
 
 
@@ -254,7 +256,7 @@ def traffic_from_profile(kernel_tag: str):
 # ---------------------------------------------------------------------------------------
 
 def time_graph(torch, fn, stream, flush, steps):
-    """Capture fn in a CUDA graph; mean device time (ms) over `steps` replays, L2 flushed
+    """Capture fn in a CUDA graph; median device time (ms) over `steps` replays, L2 flushed
     between replays outside the timed events."""
     fn()
     torch.cuda.synchronize()
@@ -274,7 +276,51 @@ def time_graph(torch, fn, stream, flush, steps):
         e1.synchronize()
         ts.append(e0.elapsed_time(e1))
     del g
-    return statistics.mean(ts)
+    return statistics.median(ts)
+
+
+def host_rows(out):
+    """A GPU output as fp64 rows on the host (for the oracle comparison)."""
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def run_tiny(torch, kvc, args, dev, stream, flush, rank):
+    """The tiny decode (4 sequences of 1, 17, 33 and 100 positions, 4 / 2 heads, head_dim 64,
+    16-position pages in a 32-page pool): too small for a rate, so its step time is reported
+    (one kvc_decode_store call as a graph, and the separate slot mapping + store + decode),
+    with its output checked against the oracle."""
+    from workloads import config_case
+    from workloads.device import to_device
+
+    case = config_case(1, seed=rank_seed(1, rank))
+    d = to_device(case, dev)
+    out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    slots = torch.empty(case.num_tokens, dtype=torch.int32, device=dev)
+    pool = kvc.pool_desc(d.k_pool)
+    splits, chunk, ws = kvc.kvc_decode_plan(case.num_seqs, case.q_heads, pool, case.max_ctx, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def separate():
+        kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
+        kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+        kvc.kvc_decode(out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens,
+                       case.max_ctx, num_splits=0, workspace=work)
+    with torch.cuda.stream(stream):
+        t_sep = time_graph(torch, separate, stream, flush, args.leg_steps)
+        t = time_graph(torch, lambda: kvc.kvc_decode_store(
+            out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table, d.context_lens,
+            case.max_ctx, num_splits=0, workspace=work), stream, flush, args.leg_steps)
+    got = host_rows(out)
+    r = {"workload": "4 seqs, ctx {1,17,33,100}, 4/2 heads, D 64, P 16, 32-page pool; decode "
+                     "step with the store of the 4 new tokens",
+         "us": round(t * 1e3, 2), "separate_us": round(t_sep * 1e3, 2),
+         "bytes": decode_bytes(case) + store_bytes(case), "splits": splits,
+         "gpu_launches_per_step": 2 if splits > 1 else 1}
+    del d, out, work, slots
+    if args.cpu_on:
+        r["cpu_baseline"] = oracle_leg(case, got, "GB/s")
+    return r
 
 
 def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
@@ -308,9 +354,11 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             t_g = time_graph(torch, lambda: kvc.kvc_decode_shared_prefix(
                 out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx, gi, gs,
                 gp, 8, int(prefix.max()), work_g), stream, flush, args.leg_steps)
+            got_grouped = host_rows(out)
             t_p = time_graph(torch, lambda: kvc.kvc_decode(
                 out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
                 num_splits=0, workspace=work_p), stream, flush, args.leg_steps)
+            got_plain = host_rows(out)
         # the same step with the groups found on the device from the block tables: the prepass
         # alone, and prepass + decode over its fixed-capacity group list (S / 2 slots, unused
         # ones empty; at most 8 members; prefix bound max_ctx), with no host read of the count
@@ -336,6 +384,7 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             t_det = time_graph(torch, detect, stream, flush, args.leg_steps)
             t_gd = time_graph(torch, detect_and_decode, stream, flush, args.leg_steps)
         torch.cuda.synchronize()
+        got_device = host_rows(out)
         found = int(dn.item())
         unique_pos = int(case.context_lens.sum()) - 7 * len(case.groups) * int(prefix[0])
         unique_b = unique_pos * per_pos(case) + qo(case)
@@ -357,6 +406,12 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
         }
         del d, out, work_g, work_p, slots, work_d
         torch.cuda.empty_cache()
+        if args.cpu_on:
+            o = oracle_leg(case, got_grouped, "GB/s",
+                           also={"plain_decode": got_plain, "device_groups": got_device})
+            o["unit_note"] = "logical bytes (every sequence's positions, shared ones per member)"
+            legs["shared_prefix"]["cpu_baseline"] = o
+        del case
     if "long_decode" in args.legs:
         # long context: 8 sequences of 32k..128k positions
         case = config_case(5, seed=rank_seed(5, rank))
@@ -373,6 +428,7 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             t = time_graph(torch, lambda: kvc.kvc_decode(
                 out, d.q, d.k_pool, d.v_pool, d.block_table, d.context_lens, case.max_ctx,
                 num_splits=0, workspace=work), stream, flush, args.leg_steps)
+        got = host_rows(out)
         b = int(case.context_lens.sum()) * per_pos(case) + qo(case)
         legs["long_decode"] = {
             "workload": "8 seqs, ctx U[32768,131072], 64/8 heads, D 128, P 64, split-K + merge",
@@ -382,6 +438,9 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
         }
         del d, out, work, slots
         torch.cuda.empty_cache()
+        if args.cpu_on:
+            legs["long_decode"]["cpu_baseline"] = oracle_leg(case, got, "GB/s")
+        del case
     if "int8_decode" in args.legs:
         # INT8 pages: the batched-decode batch quantised by kvc_store_int8 (every slot of the bf16
         # pools, as if each were a new token), decoded by kvc_decode_int8 beside kvc_decode
@@ -494,6 +553,62 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
     return legs
 
 
+def headline_config(case, args, world):
+    """The headline workload's description, printed alike by both arms."""
+    return {"workload": WORKLOAD, "num_seqs": case.num_seqs, "q_heads": case.q_heads,
+            "kv_heads": case.kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
+            "sum_ctx": int(case.context_lens.sum()),
+            "l2": f"flushed between GPU steps ({args.flush_mb} MB write)",
+            "parallelism": f"replicas x{world} (sequences sharded, no collective)"}
+
+
+def summary_of(line):
+    """Each leg's headline figure, its roofline fraction, its oracle time and its parity, in
+    a few hundred bytes."""
+    def pick(d, *path):
+        for k in path:
+            if not isinstance(d, dict) or k not in d:
+                return None
+            d = d[k]
+        return d
+
+    def par(d):
+        p = pick(d, "cpu_baseline", "parity_vs_gpu")
+        return None if p is None else [p["max_abs"], p["mean_abs"]]
+
+    def osec(d):
+        return pick(d, "cpu_baseline", "seconds_per_pass")
+
+    legs = line.get("decode_legs") or {}
+    app = line.get("append") or {}
+    out = {"decode_step_gbs": line["value"], "decode_frac": line["roofline"]["frac"],
+           "decode_parity": par(line), "decode_oracle_s": osec(line)}
+    if "tiny_decode" in line:
+        t = line["tiny_decode"]
+        out["tiny_us"] = t["us"]
+        out["tiny_parity"] = par(t)
+    for P in ("p16", "p64"):
+        if P in app:
+            out[f"append_{P}_frac"] = app[P]["roofline_frac"]
+            out[f"append_{P}_tflops"] = app[P]["tflops"]
+            out[f"append_{P}_parity"] = par(app[P])
+            out[f"append_{P}_oracle_s"] = osec(app[P])
+            out[f"int8_append_{P}_frac"] = pick(app, P, "int8", "roofline_frac")
+    if "shared_prefix" in legs:
+        out["shared_prefix_frac"] = legs["shared_prefix"]["grouped_frac_of_hbm"]
+        out["shared_prefix_parity"] = par(legs["shared_prefix"])
+        out["shared_prefix_oracle_s"] = osec(legs["shared_prefix"])
+    if "long_decode" in legs:
+        out["long_decode_frac"] = legs["long_decode"]["frac_of_hbm"]
+        out["long_decode_parity"] = par(legs["long_decode"])
+        out["long_decode_oracle_s"] = osec(legs["long_decode"])
+    if "int8_decode" in legs:
+        out["int8_decode_frac"] = legs["int8_decode"]["frac_of_hbm"]
+    if "e2e" in line:
+        out["e2e_gbs"] = line["e2e"]["value"]
+    return out
+
+
 def run_kvc(args):
     import torch
 
@@ -505,6 +620,9 @@ def run_kvc(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
+    # the oracle (timed on the host cores, and compared with each leg's output) runs on rank 0
+    # of a 1-GPU run only
+    args.cpu_on = rank == 0 and world == 1 and not args.no_cpu_baseline
 
     # each rank decodes its own batch of 64 sequences (weak scaling, no collective)
     case = config_case(2, seed=rank_seed(2, rank))
@@ -581,18 +699,22 @@ def run_kvc(args):
         clk = clocks.stop()
         dec_ms = timed_loop(g_decode, max(50, K // 10))
         sep_ms = timed_loop(g_sep, max(50, K // 10))
+        got_headline = host_rows(out)
         total_ms = max_over_ranks(sum(step_ms), world, dev)
 
         step_b = decode_bytes(case) + store_bytes(case)
         value = whole_job_value(world, step_b, K, total_ms)
         dec_b = decode_bytes(case)
-        achieved = dec_b / (statistics.mean(dec_ms) / 1e3) / 1e9
+        achieved = dec_b / (statistics.median(dec_ms) / 1e3) / 1e9
         launches_per_step = 1 + (1 if splits > 1 else 0)
 
         e2e = None
         if not args.no_e2e:
             e2e = run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, max(20, K // 10))
 
+        tiny = None
+        if not args.no_legs and "tiny_decode" in args.legs:
+            tiny = run_tiny(torch, kvc, args, dev, stream, flush, rank)
         append = None
         if not args.no_append:
             append = run_append(torch, kvc, args, dev, stream, flush, peaks, rank)
@@ -605,36 +727,39 @@ def run_kvc(args):
         "steps": K, "warmup": W, "ms_per_step": round(total_ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q; no dataset, no weights)",
-        "config": {"workload": WORKLOAD, "num_seqs": S, "q_heads": Hq,
-                   "kv_heads": case.kv_heads, "head_dim": D, "page_size": case.page_size,
-                   "sum_ctx": int(case.context_lens.sum()), "splits": splits,
-                   "chunk": chunk, "l2": f"flushed between steps ({args.flush_mb} MB write)",
-                   "timing": "CUDA events per step on the launching stream; the step is one "
-                             "graph of one kvc_decode_store call; roofline from decode-only "
-                             "graph replays",
-                   "separate_calls": {
-                       "ms_per_step": round(statistics.mean(sep_ms), 5),
-                       "value": round(step_b / (statistics.mean(sep_ms) / 1e3) / 1e9, 2),
-                       "path": "kvc_slot_mapping + kvc_store + kvc_decode as one graph"},
-                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "config": headline_config(case, args, world),
+        "step": {"splits": splits, "chunk": chunk,
+                 "timing": "CUDA events per step on the launching stream; the step is one "
+                           "graph of one kvc_decode_store call; roofline from decode-only "
+                           "graph replays (median)",
+                 "separate_calls": {
+                     "ms_per_step": round(statistics.median(sep_ms), 5),
+                     "value": round(step_b / (statistics.median(sep_ms) / 1e3) / 1e9, 2),
+                     "path": "kvc_slot_mapping + kvc_store + kvc_decode as one graph"}},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                      "peak_source": f"of {peaks['source']} (copy bandwidth)",
                      "kernel": "paged_decode_kernel + merge_kernel (one kvc_decode call)",
                      "bytes_per_launch": dec_b,
-                     "traffic": traffic_from_profile("decode_batched")},
+                     "traffic": traffic_from_profile("decode_batched"),
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of one ncu "
+                                       "capture (profiles/decode_batched.md), used only while "
+                                       "the kernel's sources still match its sha256"},
         "gpu_launches": K * launches_per_step,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if tiny is not None:
+        line["tiny_decode"] = tiny
     if append is not None:
         line["append"] = append
     if legs is not None:
         line["decode_legs"] = legs
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if args.cpu_on:
+        line["cpu_baseline"] = cpu_baseline(case, got_headline, args.cpu_seconds)
+    line["summary"] = summary_of(line)   # last, so that a tail of the line keeps it
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -681,7 +806,7 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
             e1.record(stream)
             e1.synchronize()
             times.append(e0.elapsed_time(e1))
-        return statistics.mean(times)
+        return statistics.median(times)
 
     t_graph = timed(g.replay)
     t_eager = timed(step)
@@ -751,17 +876,18 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             e2.synchronize()
             st_ms.append(e0.elapsed_time(e1))
             ap_ms.append(e1.elapsed_time(e2))
+        got_append = host_rows(out)
         bytes_, flops = append_work(case)
-        t = statistics.mean(ap_ms) / 1e3
+        t = statistics.median(ap_ms) / 1e3
         t_roof = max(flops / (peaks["bf16_sustained"] * 1e12), bytes_ / (peaks["hbm"] * 1e9))
         bound = "tensor" if flops / (peaks["bf16_sustained"] * 1e12) > bytes_ / (peaks["hbm"] * 1e9) else "hbm"
         result[f"p{P}"] = {
             "tflops": round(flops / t / 1e12, 2), "gbs": round(bytes_ / t / 1e9, 1),
-            "ms": round(statistics.mean(ap_ms), 4),
-            "store_ms": round(statistics.mean(st_ms), 4),
+            "ms": round(statistics.median(ap_ms), 4),
+            "store_ms": round(statistics.median(st_ms), 4),
             "flops": flops, "bytes": bytes_, "roofline_bound": bound,
             "roofline_frac": round(t_roof / t, 4),
-            "store_gbs": round(store_bytes(case) / (statistics.mean(st_ms) / 1e3) / 1e9, 1),
+            "store_gbs": round(store_bytes(case) / (statistics.median(st_ms) / 1e3) / 1e9, 1),
             "gpu_launches": args.append_steps * 3,
             "traffic": (traffic_from_profile("append_rewind_p16")
                         if P == 16 and args.append_docs == 1000 else None),
@@ -774,7 +900,8 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
                 out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table, d.q_indptr,
                 d.context_lens, case.max_q_len, case.max_ctx), stream, flush,
                 args.append_steps) / 1e3
-        sep = (statistics.mean(st_ms) + statistics.mean(ap_ms)) / 1e3
+        got_fused = host_rows(out)
+        sep = (statistics.median(st_ms) + statistics.median(ap_ms)) / 1e3
         # kvc_append_store's plan: at pages of 64 positions or more it stores the whole chunk
         # first and runs the plain append (the chunk is then read twice)
         whole = P >= 64
@@ -814,6 +941,10 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
         }
         del d, out, slots, kc, vc, ks, vs, all_slots
         torch.cuda.empty_cache()
+        if args.cpu_on:
+            result[f"p{P}"]["cpu_baseline"] = oracle_leg(case, got_append, "TFLOP/s",
+                                                         also={"append_store": got_fused})
+        del case
     result["workload"] = (f"rewind-append: {args.append_docs:,} docs x 50 new tokens over 300 "
                           "cached, 32 q / 8 kv heads, head_dim 128")
     result["peaks"] = {"hbm_gbs": peaks["hbm"], "bf16_tflops": peaks["bf16_sustained"],
@@ -826,6 +957,8 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
 # ---------------------------------------------------------------------------------------
 
 def _oracle_step(oracle, case, seqs, threads, k_pool, v_pool):
+    """The oracle's step over sequences `seqs`: slot mapping, store of their new tokens, then
+    attention gathered through the block table; returns the output rows (fp64)."""
     bt = case.block_table[seqs]
     ctx = case.context_lens[seqs]
     q_lens = case.q_lens[seqs]
@@ -833,7 +966,9 @@ def _oracle_step(oracle, case, seqs, threads, k_pool, v_pool):
     rows = np.concatenate([np.arange(case.q_indptr[s], case.q_indptr[s + 1]) for s in seqs])
     slots = oracle.slot_mapping(bt, ctx, indptr, case.page_size)
     oracle.store(k_pool, v_pool, case.k_new[rows], case.v_new[rows], slots)
-    oracle.attention(case.q[rows], k_pool, v_pool, bt, ctx, indptr, num_threads=threads)
+    out, _ = oracle.attention(case.q[rows], k_pool, v_pool, bt, ctx, indptr,
+                              num_threads=threads)
+    return out
 
 
 def _sub_bytes(case, seqs):
@@ -844,7 +979,33 @@ def _sub_bytes(case, seqs):
             + 2 * n * case.q_heads * case.head_dim * 2 + n * (2 * row * 2 + 8))
 
 
-def cpu_baseline(case, seconds):
+def _sub_case_units(case, seqs, unit):
+    """Work of the oracle's step over `seqs`, in the leg's unit: bytes (GB/s) or FLOPs
+    (TFLOP/s) of the same definitions the GPU legs use."""
+    if unit == "TFLOP/s":
+        q_lens = case.q_lens[seqs].astype(np.int64)
+        ctx = case.context_lens[seqs].astype(np.int64)
+        pairs = int((q_lens * (ctx - q_lens) + q_lens * (q_lens + 1) // 2).sum())
+        return 4 * case.head_dim * case.q_heads * pairs / 1e12
+    return _sub_bytes(case, seqs) / 1e9
+
+
+def parity_of(got, ref):
+    """Element-wise comparison of GPU output rows with the oracle's (fp64), against the
+    attention tolerance the tests hold (max abs 1e-2, mean abs 1e-3)."""
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    mx, mean = float(err.max()), float(err.mean())
+    return {"max_abs": float(f"{mx:.3e}"), "mean_abs": float(f"{mean:.3e}"),
+            "elements": int(err.size), "ok": bool(mx <= 1e-2 and mean <= 1e-3)}
+
+
+def oracle_leg(case, got, unit, seconds=1.0, also=None):
+    """The oracle (fp64 C: slot mapping, store, attention gathered through the block table)
+    on the leg's whole workload, all host cores, repeated until `seconds` have passed (at least
+    once); the same oracle on one thread over the first sequences (about a second's worth,
+    scaled to the same unit); and the GPU output `got` (all rows, bf16 widened) against the
+    oracle's; `also` maps names to further GPU outputs of the same workload (other entry
+    points), each compared with the same oracle output."""
     from oracle import oracle
     threads = len(os.sched_getaffinity(0))
     seqs = np.arange(case.num_seqs)
@@ -852,24 +1013,34 @@ def cpu_baseline(case, seconds):
     t0 = time.perf_counter()
     reps = 0
     while True:
-        _oracle_step(oracle, case, seqs, threads, kp, vp)
+        ref = _oracle_step(oracle, case, seqs, threads, kp, vp)
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = (time.perf_counter() - t0) / reps
-    # the same oracle on one thread, over the first 8 sequences of the batch
-    few = np.arange(min(8, case.num_seqs))
+    n1 = int(np.clip(round(case.num_seqs / max(dt * threads, 1e-9)), 1, case.num_seqs))
+    few = np.arange(n1)
     kp1, vp1 = case.k_pool.copy(), case.v_pool.copy()
     t1 = time.perf_counter()
     _oracle_step(oracle, case, few, 1, kp1, vp1)
     dt1 = time.perf_counter() - t1
-    return {"value": round(_sub_bytes(case, seqs) / dt / 1e9, 4), "unit": "GB/s",
+    del kp, vp, kp1, vp1
+    return {"value": round(_sub_case_units(case, seqs, unit) / dt, 4), "unit": unit,
             "cores": threads, "kind": "oracle",
-            "sample": f"the full 64-sequence batch, {reps} pass(es), {dt:.2f} s per pass "
-                      f"(fp64 C oracle: slot mapping, store, gathered attention)",
-            "value_1_thread": round(_sub_bytes(case, few) / dt1 / 1e9, 4),
-            "sample_1_thread": f"sequences 0-{len(few) - 1} of the batch on one thread, "
-                               f"{dt1:.2f} s"}
+            "sample": f"the whole workload ({case.num_seqs} sequences), {reps} pass(es), "
+                      f"{dt:.3f} s per pass",
+            "seconds_per_pass": round(dt, 4),
+            "value_1_thread": round(_sub_case_units(case, few, unit) / dt1, 4),
+            "sample_1_thread": f"sequences 0-{n1 - 1} on one thread, {dt1:.2f} s",
+            "parity_vs_gpu": parity_of(got, ref),
+            **{f"parity_{k}": parity_of(v, ref) for k, v in (also or {}).items()}}
+
+
+def cpu_baseline(case, got, seconds):
+    """The headline's CPU baseline: the oracle over the full 64-sequence batch."""
+    r = oracle_leg(case, got, "GB/s", seconds)
+    r["sample"] += " (fp64 C oracle: slot mapping, store, gathered attention)"
+    return r
 
 
 def run_reference(args):
@@ -903,7 +1074,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD},
+            "config": headline_config(case, args, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -287,7 +287,9 @@ kvc_status kvc_decode_shared_prefix_plan(int32_t num_seqs, int32_t q_heads, kvc_
  * with KVC_ERR_WORKSPACE and nothing is enqueued: ask for fewer splits, or use kvc_decode
  * with a workspace of your own.  The first call on each device (the current device) looks
  * up where the scratch array lives on that device; make that first call before any stream
- * capture.  Every call uses the same array, which keeps what the last call wrote; nothing
+ * capture.  The address is kept with the id of the context it was found in; after a device
+ * reset (cudaDeviceReset) the next call finds a new context and looks it up again, so make
+ * that call outside a capture too.  Every call uses the same array, which keeps what the last call wrote; nothing
  * in it has to start at zero, but two calls whose kernels overlap on the GPU (launched on
  * different streams with no ordering between them) race on it, so the caller must order them.
  */
@@ -350,7 +352,11 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
  *   k_new, v_new   bf16 [num_tokens][kv_heads][head_dim], row t = token t of q (q_indptr)
  *   k_pool, v_pool written (the new tokens' slots only) and read
  * Other arguments as kvc_append.  A token whose position is negative (context_lens[s] <
- * q_len_s) is not stored.  Two launches on `stream`.
+ * q_len_s) is not stored.  A context longer than its block-table row (context_lens[s] >
+ * bt_stride * page_size) is an error the pools survive as they do kvc_slot_mapping +
+ * kvc_store: the chunk's tokens the row covers are stored at their slots, the others are
+ * skipped, and the device error word (kvc_device_errors) gets 1 << 7; that sequence's output
+ * is undefined.  Two launches on `stream`.
  */
 kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
                             const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,

@@ -4,16 +4,16 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: Quail "KV", section "The sharing plan": documents are sorted by token sequence,
 adjacent documents are compared for a common prefix, only complete pages are shared, the
-final token of every document is left to be computed, and when the preceding document
-reuses the whole shared prefix itself the plan follows parent links to the document that
-supplies those pages.
+final token of every document is left to be computed, and when the preceding document's
+own shared count already covers the current one, the plan follows parent links back to the
+document that supplies those pages.
 
 Readings where the section leaves a step open:
   * sorting is a stable lexicographic sort of the token sequences;
   * the final-token cap comes before rounding down to whole pages:
     shared = floor(min(lcp, len - 1) / page_size) * page_size;
-  * the preceding document "reuses the entire shared prefix" when its own shared count is
-    at least the current one; links are followed while that holds;
+  * the preceding document covers the current one when its own shared count is at least
+    the current one's; links are followed while that holds;
   * a document that shares nothing has parent None.
 """
 from __future__ import annotations

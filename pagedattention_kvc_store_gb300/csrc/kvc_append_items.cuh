@@ -23,6 +23,7 @@ struct Item {
     int tok0, q_len, ctx, rows, row_begin;   // row_begin: first row of tile 2 tp
     bool has_b;                              // tile 2 tp + 1 exists
     int n_keys, n_blocks;                    // positions the item's later tile sees
+    bool over;                               // context_lens[s] exceeded the block-table row
 };
 
 // The fields of item `it` from its sequence's query offsets and context length (no loads).
@@ -37,7 +38,8 @@ __device__ __forceinline__ bool make_item(const Args &a, int it, int tok0, int t
     x.tok0 = tok0;
     x.q_len = tok1 - tok0;
     x.ctx = ctx;
-    if (x.ctx > a.bt_stride * a.page_size) {
+    x.over = x.ctx > a.bt_stride * a.page_size;
+    if (x.over) {
         if (threadIdx.x == 0)
             atomicOr(err, kErrContextRange);
         x.ctx = a.bt_stride * a.page_size;

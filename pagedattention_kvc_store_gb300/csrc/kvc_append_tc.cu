@@ -304,7 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int np = (min(kBN, x.n_keys - b * kBN) + P - 1) / P;
                     const int s_lo = max(lp0, p_lo / P);   // pages of the block to write
                     const int s_hi = min(lp0 + np, (p_hi + P - 1) / P);
-                    const bool write = p_lo < p_hi && s_lo < s_hi;
+                    // (a context past its block-table row: the whole chunk was stored by
+                    // the boundary kernel at the slots the row covers, as slot mapping +
+                    // store would; nothing is written here)
+                    const bool write = !x.over && p_lo < p_hi && s_lo < s_hi;
                     const int my_page = (write && s_lo + lane < s_hi) ? bt_row[s_lo + lane] : 0;
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait(&bars[kBarKvFull + st], (n / kStages) & 1))) {

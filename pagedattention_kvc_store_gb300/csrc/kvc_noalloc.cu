@@ -4,7 +4,11 @@
 //
 // The scratch is one file-scope device array.  In host code its name is only a host-side
 // stand-in, so the device address is looked up with cudaGetSymbolAddress once per device
-// (with that device current) and that address is what the kernels receive.
+// (with that device current) and that address is what the kernels receive.  The address
+// belongs to the device's current context: it is kept together with that context's id
+// (unique for the life of the process), and looked up again when a device reset has replaced
+// the context, since the array may then live elsewhere.
+#include <cudaTypedefs.h>
 #include <stdio.h>
 
 #include <mutex>
@@ -21,9 +25,42 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_setup_mutex;
-void *g_scratch_address[kMaxDevices];   // device address of g_noalloc_scratch, per device
+struct ScratchSlot {
+    unsigned long long context_id;   // id of the context the address was looked up in
+    void *address;                   // device address of g_noalloc_scratch there
+};
+ScratchSlot g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up on first use).
+// Id of the calling thread's current context (0 if the driver cannot say): the driver's own
+// entry points, fetched once through the runtime.
+unsigned long long current_context_id()
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array on the current device (looked up on first use, and
+// again once the device's context has been replaced).
 kvc_status scratch_on_current_device(void **address)
 {
     int device = 0;
@@ -37,7 +74,11 @@ kvc_status scratch_on_current_device(void **address)
         return static_cast<kvc_status>(
             kvc::set_last_error(KVC_ERR_UNSUPPORTED, "device index beyond 63"));
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_address[device] == nullptr) {
+    ScratchSlot &slot = g_scratch[device];
+    if (slot.address == nullptr || slot.context_id == 0 ||
+        slot.context_id != current_context_id()) {
+        // cudaGetSymbolAddress also makes the device's context current if it is not yet, so
+        // the context id is read after it
         void *p = nullptr;
         err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess || p == nullptr) {
@@ -46,9 +87,10 @@ kvc_status scratch_on_current_device(void **address)
                      cudaGetErrorString(err));
             return static_cast<kvc_status>(kvc::set_last_error(KVC_ERR_CUDA, msg));
         }
-        g_scratch_address[device] = p;
+        slot.address = p;
+        slot.context_id = current_context_id();
     }
-    *address = g_scratch_address[device];
+    *address = slot.address;
     return KVC_OK;
 }
 

@@ -117,6 +117,11 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
 // token of the chunk (positions base .. ctx - 1, each at the page its block table lists) is
 // stored and the plain append follows.  One CTA per sequence (grid-stride), one thread per
 // 16-byte chunk of a token row; addressing as store_kernel.
+//
+// A context longer than the block-table row (ctx > bt_stride * P) is the caller's error; the
+// pools then end as slot mapping + store leave them: every chunk token whose position the row
+// covers is stored at its own slot (the whole chunk is handled here, and the fused append
+// writes nothing for that sequence), the others are skipped, and kErrContextRange is set.
 __global__ void __launch_bounds__(256) store_boundary_kernel(
     uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, const uint4 *__restrict__ k_new,
     const uint4 *__restrict__ v_new, const int32_t *__restrict__ block_table, int bt_stride,
@@ -126,23 +131,28 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
     pdl_wait();
     pdl_trigger();
     const int row_chunks = chunks / kv_heads;
+    const int capacity = bt_stride * page_size;   // positions a block-table row covers
     for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
         const int tok0 = __ldg(q_indptr + s);
         const int q_len = __ldg(q_indptr + s + 1) - tok0;
-        const int ctx = min(__ldg(context_lens + s), bt_stride * page_size);
+        const int ctx = __ldg(context_lens + s);
         const int base = ctx - q_len;
-        if (q_len <= 0 || (!whole && (base <= 0 || base % page_size == 0)))
+        const bool over = ctx > capacity;
+        const bool all = whole || over;   // every token of the chunk is stored here
+        if (over && threadIdx.x == 0)
+            atomicOr(&g_store_errors, kErrContextRange);
+        if (q_len <= 0 || (!all && (base <= 0 || base % page_size == 0)))
             continue;
-        const int n_tok = whole ? q_len : min(ctx, (base / page_size + 1) * page_size) - base;
+        const int n_tok = all ? q_len : min(ctx, (base / page_size + 1) * page_size) - base;
         const int32_t *bt_row = block_table + static_cast<size_t>(s) * bt_stride;
-        const int page0 = whole ? 0 : __ldg(bt_row + base / page_size);
+        const int page0 = all ? 0 : __ldg(bt_row + base / page_size);
         for (int i = threadIdx.x; i < n_tok * chunks; i += blockDim.x) {
             const int t = i / chunks;
             const int c = i - t * chunks;
             const int pos = base + t;
-            if (pos < 0)
-                continue;   // a clamped context shorter than the chunk: no slot
-            const int page = whole ? __ldg(bt_row + pos / page_size) : page0;
+            if (pos < 0 || pos >= capacity)
+                continue;   // no slot: before position 0, or past the block-table row
+            const int page = all ? __ldg(bt_row + pos / page_size) : page0;
             const long long slot = static_cast<long long>(page) * page_size + pos % page_size;
             if (slot < 0 || slot >= num_slots) {   // a page outside the pool: skip, flag
                 if (c == 0)

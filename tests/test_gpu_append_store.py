@@ -134,3 +134,57 @@ def test_append_store_bf16_output_and_graph_replay():
     assert np.array_equal(bf16_bits_of(d.v_pool), o.v_pool)
     ref, _ = o.attention()
     assert_attention_close(out_to_f64(out), ref, "append_store bf16 output")
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_append_store_context_past_the_row(P):
+    """A context longer than its block-table row (a caller error): kvc_append_store must leave
+    the pools exactly as kvc_slot_mapping + kvc_store do -- the chunk's tokens the row covers
+    at their own slots, the rest skipped -- and both paths flag bit 1 << 7.  Sequence 0 fills
+    its 16-entry row exactly (ctx = 16 P); on the device its context is then raised by 10, so
+    the chunk's last 10 tokens fall past the row and the others land on its own pages.  At
+    P = 64 the call stores the whole chunk first, at P = 16 the append writes the later pages."""
+    cap = 16 * P
+    ctx = np.array([cap, 200, 75, 211, 40])
+    qlen = np.array([50, 50, 9, 120, 40])
+    case = build_case(94 + P, name="append-store-over", page_size=P, q_heads=16, kv_heads=4,
+                      head_dim=128, context_lens=lambda rng: ctx, q_lens=lambda c: qlen,
+                      bt_width=16)
+    assert case.block_table.shape[1] * P == cap
+    over = case.context_lens.copy()
+    over[0] += 10
+
+    def run(fused_call):
+        d = to_device(case)
+        d.context_lens.copy_(torch.from_numpy(over.astype(np.int32)))
+        out = torch.zeros(case.num_tokens, case.q_heads, case.head_dim, dtype=torch.float32,
+                          device="cuda")
+        kvc.kvc_device_errors()
+        if fused_call:
+            kvc.kvc_append_store(out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table,
+                                 d.q_indptr, d.context_lens, case.max_q_len, cap)
+        else:
+            slots = torch.empty(case.num_tokens, dtype=torch.int32, device="cuda")
+            kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, d.q_indptr, P,
+                                 max_q_len=case.max_q_len)
+            kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+            kvc.kvc_append(out, d.q, d.k_pool, d.v_pool, d.block_table, d.q_indptr,
+                           d.context_lens, case.max_q_len, cap)
+        torch.cuda.synchronize()
+        flags = kvc.kvc_device_errors()
+        return out, bf16_bits_of(d.k_pool), bf16_bits_of(d.v_pool), flags
+
+    out_f, kf, vf, flags_f = run(True)
+    out_s, ks, vs, flags_s = run(False)
+    assert flags_f & (1 << 7) and flags_s & (1 << 7)
+    assert np.array_equal(kf, ks), "K pools differ from slot mapping + store"
+    assert np.array_equal(vf, vs), "V pools differ from slot mapping + store"
+    # the chunk's first 40 tokens of sequence 0 were stored (at positions cap - 40 .. cap - 1),
+    # its last 10 were not
+    pos = np.arange(cap - 40, cap)
+    slots0 = case.block_table[0][pos // P].astype(np.int64) * P + pos % P
+    flat_k = kf.reshape(-1, case.kv_heads, case.head_dim)
+    assert np.array_equal(flat_k[slots0], case.k_new[:40])
+    # the other sequences' outputs are untouched by sequence 0's error
+    rows = slice(int(case.q_indptr[1]), case.num_tokens)
+    assert torch.equal(out_f[rows], out_s[rows])

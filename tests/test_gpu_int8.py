@@ -81,6 +81,15 @@ def test_int8_decode_batched_workload():
                            "INT8 batched decode")
 
 
+def test_int8_decode_batched_workload_f32_every_sequence():
+    """The same workload with fp32 output: all 64 sequences, held to the plain attention
+    tolerance (no allowance for output rounding)."""
+    case = config_case(2)
+    out, pools = run_int8(case, out_dtype=torch.float32)
+    assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
+                           "INT8 batched decode, fp32 output, every sequence")
+
+
 def test_int8_head_dim_64_is_refused():
     case = config_case(1)   # head_dim 64
     kc = torch.zeros(case.num_pages, case.page_size, case.kv_heads, 64, dtype=torch.int8,

@@ -135,6 +135,17 @@ def test_int8_append_rewind_workload_sampled(P):
     assert_close_out(got[rows], ref, f"INT8 rewind append P={P}", torch.bfloat16)
 
 
+@pytest.mark.parametrize("P", [16, 64])
+def test_int8_append_rewind_workload_f32_every_document(P):
+    """The rewind-append workload with fp32 output: all 1,000 documents, held to the plain
+    attention tolerance (no allowance for output rounding)."""
+    case = config_case(4, page_size=P)
+    run = Int8AppendRun(case)
+    got = run.attend(torch.float32)
+    ref, rows = run.oracle()
+    assert_attention_close(got[rows], ref, f"INT8 rewind append P={P}, fp32, every document")
+
+
 def test_int8_append_single_position_is_its_stored_vector():
     case = build_case(80, name="int8-single", page_size=16, q_heads=4, kv_heads=2,
                       head_dim=128, context_lens=lambda rng: np.array([1, 1]),

@@ -5,17 +5,18 @@ inside an inference engine that planned all of its device memory at start-up, or
 loop that may not call cudaMalloc (which can synchronise the whole device) while it runs.
 They cannot pass kvc_decode a workspace, so kvc_decode_noalloc keeps the split partials in a
 fixed scratch array inside the library instead.  These tests call it through the C ABI and
-check it against kvc_decode, twice in a row (the scratch keeps the previous call's data),
-and check that a plan too large for the scratch is refused with a clear error.
-
-This file is named to be collected last.
+check it against kvc_decode and against the fp64 oracle, twice in a row (the scratch keeps
+the previous call's data), and check that a plan too large for the scratch is refused with
+a clear error.  Each test builds its own inputs, so the file passes alone in a fresh process
+as well as after the other tests; it is named to be collected last, so that a run stopping
+at its first failure has run every other test before it.
 """
 import numpy as np
 import pytest
 import torch
 
 import pagedattention_kvc_store_gb300 as kvc
-from harness import MAX_ABS, MEAN_ABS, GpuRun, out_to_f64
+from harness import MAX_ABS, MEAN_ABS, GpuRun, OracleRun, assert_attention_close, out_to_f64
 from workloads import config_case
 
 pytestmark = pytest.mark.gpu
@@ -44,6 +45,8 @@ def test_matches_decode_on_two_calls_in_a_row():
         assert np.isfinite(got).all()
         err = np.abs(got - ref)
         assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS
+        exact, _ = OracleRun(case).attention()
+        assert_attention_close(got, exact, f"kvc_decode_noalloc, {splits} splits")
 
 
 def test_plan_beyond_the_scratch_is_refused():
