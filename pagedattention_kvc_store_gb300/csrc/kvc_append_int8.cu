@@ -15,31 +15,26 @@
 // fp16's range bounds P': p <= 2^4 (the running max lags the true one by at most 2^4) and a
 // value scale above 4000 (|v| above 5.08e5) sets kErrScaleRange.
 //
-// Structure (persistent, one CTA per SM; a work item is a pair of 128-row tiles of one
-// (sequence, kv head), as in kvc_append_tc.cu), head_dim 128, 14 warps, keys in blocks of 64:
-//   warp 0      TMA: the int8 codes of each 64-position block (one box per page) through an
-//               8-deep ring, in the order K(0), K(1), V(0), K(2), V(1), K(3), ... (K two blocks
-//               ahead of V), and with each K block its K and V scale runs (one bulk copy each per
-//               page) into a scale ring;
-//   warp 1      TMEM and the MMA issue: S_t(b) = Q_t K(b)^T (bf16, N = 64) and O_t += P'_t(b) V(b)
-//               (fp16, K = 64, P' read from TMEM);
-//   warps 2, 3, 12, 13   converters 0-3: converter v turns rows 16 v .. 16 v + 15 of every code
-//               block into the same rows of a 16-bit operand slot (K: three slots, V: two; the
-//               MMA's 128-byte-swizzled [half][64 positions][64 dims]); converters 0 and 1 also
-//               load query tile 0 / 1 of each item, and converter 0 readies each block's scales
-//               (K scales times scale * log2(e), positions the item never sees set to 0);
-//   warps 4-7   softmax of tile 0, warps 8-11 of tile 1: the block's 64 scores in registers,
-//               x = S * k_scale' with the causal limit, lazy running max, p = 2^(x - m),
-//               P' = p * v_scale as fp16 pairs into the first 32 columns of the block's S buffer.
-// TMEM per tile t (at 256 t): O in columns [0, 128) and two S buffers of 64 columns,
-// [128, 192) and [192, 256), used by alternate blocks.  S_t(b + 2) goes into S_t(b)'s buffer
-// right behind the PV product that reads P'_t(b) from it (products of one thread run in issue
-// order), so the tensor core computes the scores of later blocks while the softmax works on
-// this one, and the softmax warps go from block to block without waiting on the tensor pipe.
-// O is rescaled (rarely: the running max is lazy) only once the previous block's PV product is
-// done.  The softmax denominator sums p (before the value scale).  A position the item never
-// sees may hold any codes and a NaN scale: its scales are replaced by 0 before the softmax reads
-// them, its scores are masked, and its operand rows are finite codes or never read.
+// Structure: kvc_append_tc.cu's (persistent, one CTA per SM; a work item is a pair of 128-row
+// tiles of one (sequence, kv head); fixed-order MMA issue; P in TMEM over S's columns), head_dim
+// 128, 14 warps:
+//   warp 0      TMA: int8 code half-slots of 64 positions (one box per page) through a 7-deep
+//               ring, in the order K(0), K(1), V(0), K(2), V(1), ..., and for each block the K
+//               and V scale runs (one bulk copy each per page) into a 6-deep scale ring;
+//   warp 1      TMEM and the MMA issue: S_t = Q_t K(b)^T (bf16) and O_t += P'_t V(b) (fp16);
+//   warps 2, 3, 12, 13   converters 0-3: converter v turns rows 32 (v / 2) .. + 31 of code
+//               half-slot v % 2 of each block into rows 64 (v % 2) + 32 (v / 2) .. of a 16-bit
+//               operand slot (two K slots, one V slot, the MMA's 128-byte-swizzled
+//               [half][128 positions][64 dims]); converter t < 2 also loads query tile t of
+//               each item, and converter 0 readies each block's scales (K scales times
+//               scale * log2(e), positions the item never sees set to 0);
+//   warps 4-7   softmax of tile 0, warps 8-11 of tile 1: x = S * k_scale' with the causal
+//               limit, lazy running max, p = 2^(x - m), P' = p * v_scale as fp16 pairs into TMEM.
+// The single V slot is released as soon as the last tile's PV product of a block is done; the
+// next V is converted while the softmax works on the S of the block after.  The softmax
+// denominator sums p (before the value scale).  A position the item never sees may hold any
+// codes and a NaN scale: its scales are replaced by 0 before the softmax reads them, its scores
+// are masked, and its operand rows are finite codes or never read.
 #include <math.h>
 
 #include "kvc_append_items.cuh"
