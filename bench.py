@@ -60,6 +60,10 @@ def parse_args():
                             "hnd_decode", "page_copy"],
                    help="comma-separated decode legs to run (default: all)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-headline", action="store_true",
+                   help="skip the batched-decode step and print only the legs (profiler captures)")
+    p.add_argument("--append-page-sizes", type=lambda v: [int(x) for x in v.split(",")],
+                   default=[16, 64], help="page sizes of the rewind-append leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=5.0,
                    help="seconds of oracle passes over the headline batch (the other legs' "
@@ -226,6 +230,10 @@ PROFILE_SOURCES = {
     "decode_int8_batched": ("kvc_decode_int8.cu", "kvc_device.cuh"),
     "append_rewind_p16": ("kvc_append_tc.cu", "kvc_append_items.cuh", "kvc_device.cuh"),
     "append_int8_rewind_p16": ("kvc_append_int8.cu", "kvc_append_items.cuh", "kvc_device.cuh"),
+    "append_rewind_p64": ("kvc_append_tc.cu", "kvc_append_items.cuh", "kvc_device.cuh"),
+    "long_decode": ("kvc_decode.cu", "kvc_decode_cta.cuh", "kvc_device.cuh"),
+    "merge_long_decode": ("kvc_decode.cu", "kvc_device.cuh"),
+    "store_rewind": ("kvc_store.cu", "kvc_device.cuh"),
 }
 
 
@@ -435,6 +443,8 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             "us": round(t * 1e3, 1), "bytes": b, "gbs": round(b / (t / 1e3) / 1e9, 1),
             "frac_of_hbm": round(b / (t / 1e3) / 1e9 / peaks["hbm"], 4), "splits": splits,
             "chunk": chunk, "gpu_launches_per_step": 2,
+            "traffic_decode_kernel": traffic_from_profile("long_decode"),
+            "traffic_merge_kernel": traffic_from_profile("merge_long_decode"),
         }
         del d, out, work, slots
         torch.cuda.empty_cache()
@@ -623,6 +633,20 @@ def run_kvc(args):
     # the oracle (timed on the host cores, and compared with each leg's output) runs on rank 0
     # of a 1-GPU run only
     args.cpu_on = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if args.no_headline:
+        # the legs alone (for profiler captures of one leg's kernels); not a bench line
+        flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            legs = {}
+            if not args.no_append:
+                legs["append"] = run_append(torch, kvc, args, dev, stream, flush, peaks, rank)
+            if not args.no_legs:
+                legs["decode_legs"] = run_decode_legs(torch, kvc, args, dev, stream, flush,
+                                                      peaks, rank)
+        if rank == 0:
+            print(json.dumps({"legs_only": True, **legs}), flush=True)
+        return
 
     # each rank decodes its own batch of 64 sequences (weak scaling, no collective)
     case = config_case(2, seed=rank_seed(2, rank))
@@ -835,7 +859,7 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
     from workloads.device import to_device
 
     result = {}
-    for P in (16, 64):
+    for P in args.append_page_sizes:
         case = config_case(4, page_size=P, num_seqs=args.append_docs,
                            seed=rank_seed(4, rank))
         d = to_device(case, dev)
@@ -889,8 +913,10 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
             "roofline_frac": round(t_roof / t, 4),
             "store_gbs": round(store_bytes(case) / (statistics.median(st_ms) / 1e3) / 1e9, 1),
             "gpu_launches": args.append_steps * 3,
-            "traffic": (traffic_from_profile("append_rewind_p16")
-                        if P == 16 and args.append_docs == 1000 else None),
+            "traffic": (traffic_from_profile(f"append_rewind_p{P}")
+                        if P in (16, 64) and args.append_docs == 1000 else None),
+            "store_traffic": (traffic_from_profile("store_rewind")
+                              if P == 16 and args.append_docs == 1000 else None),
         }
         del g1, g2
         # fused store + append (kvc_append_store) on the same inputs: the chunk's K/V read once
