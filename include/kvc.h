@@ -366,12 +366,30 @@ kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const v
                             int32_t max_ctx, int32_t q_heads, float scale, void *stream);
 
 /*
- * kvc_device_errors -- read and clear the device-side error word.  Kernels bound every wait
- * (about one second); a wait that runs out sets a bit here and the kernel returns early,
- * leaving its outputs undefined.  Synchronises with the device.  *flags_out = 0 when no
- * wait ever ran out.
+ * kvc_device_errors -- read and clear the library's own device-side error words.  Kernels
+ * bound every wait (about one second); a wait that runs out sets a bit and the kernel returns
+ * early, leaving its outputs undefined; range checks (a slot past the pool, a context longer
+ * than its block-table row, ...) set theirs and skip the offending token.  The bits of calls
+ * made while no caller word is set (kvc_set_error_word) land in these words, one per kernel
+ * family in each process, on the current device: calls from several threads or streams share
+ * them, and this read (which synchronises with the device) clears them for all.  *flags_out
+ * = 0 when nothing was flagged since the last read.
  */
 kvc_status kvc_device_errors(uint32_t *flags_out);
+
+/*
+ * kvc_set_error_word -- error reporting per caller.  Every later call from the calling host
+ * thread passes `device_word` to its kernels, which OR their error bits (the bits of
+ * kvc_device_errors) into it instead of into the library's own words; NULL restores those.
+ * The word belongs to the caller: device memory (or pinned host memory mapped at its host
+ * address) that stays valid while the calls that were given it run.  The library never reads
+ * or clears it -- the caller zeroes it and reads it back on its own stream (a captured CUDA
+ * graph keeps the word it was captured with).  Two callers with words of their own, on
+ * different threads or streams, never see each other's bits.  Host-side argument checks still
+ * return their status at once.  Returns KVC_ERR_INVALID_ARG for a word not 4-byte aligned.
+ * (No counterpart on the pages: it scopes this library's failure reports.)
+ */
+kvc_status kvc_set_error_word(uint32_t *device_word);
 
 /*
  * kvc_selftest_wait -- a diagnostic of the failure path every kernel shares: one CTA waits on

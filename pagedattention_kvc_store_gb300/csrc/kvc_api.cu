@@ -15,6 +15,7 @@
 namespace {
 
 thread_local std::string g_last_error;
+thread_local uint32_t *g_error_word = nullptr;   // kvc_set_error_word of this host thread
 
 kvc_status fail(kvc_status st, const char *fmt, ...)
 {
@@ -441,6 +442,13 @@ kvc_status check_attention_args(const void *out, int32_t out_dtype, const void *
 }
 
 }  // namespace
+
+namespace kvc {
+uint32_t *current_error_word()
+{
+    return g_error_word;
+}
+}  // namespace kvc
 
 int kvc::set_last_error(int status, const char *message)
 {
@@ -1204,6 +1212,14 @@ kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const vo
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     cudaError_t err = kvc::launch_append_int8(l, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? ok() : cuda_fail(err, "append_int8 launch");
+}
+
+kvc_status kvc_set_error_word(uint32_t *device_word)
+{
+    if ((reinterpret_cast<uintptr_t>(device_word) & 3u) != 0)
+        return fail(KVC_ERR_INVALID_ARG, "error word not 4-byte aligned");
+    g_error_word = device_word;
+    return ok();
 }
 
 kvc_status kvc_selftest_wait(void *stream)

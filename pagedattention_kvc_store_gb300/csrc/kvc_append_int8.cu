@@ -106,6 +106,7 @@ struct Args {
     const int32_t *context_lens;
     int kv_heads, q_heads, group, page_size, pairs_per_seq, num_items;
     float scale_log2;
+    uint32_t *err;   // the caller's device error word, or null (this file's own word)
 };
 
 // Fill order of an item's K / V blocks: j = 0 .. 2 nb - 1 is K(0), K(1), V(0), K(2), V(1), ...,
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_addr(smem) & 1023u) != 0) {
         if (threadIdx.x == 0)
-            atomicOr(&g_append_int8_errors, kErrSmemAlign);
+            atomicOr(a.err ? a.err : &g_append_int8_errors, kErrSmemAlign);
         return;
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto scale_slot = [&](int sb) {
         return reinterpret_cast<float *>(smem + kOffScale + (sb % kScaleSlots) * kScaleBytes);
     };
-    uint32_t *err = &g_append_int8_errors;
+    uint32_t *err = a.err ? a.err : &g_append_int8_errors;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -815,6 +816,7 @@ cudaError_t launch_append_int8(const AppendInt8Launch &l, const CUtensorMap &tma
         return cudaErrorInvalidValue;
     a.num_items = static_cast<int>(items);
     a.scale_log2 = l.scale * kLog2e;
+    a.err = current_error_word();
     cudaError_t err = cudaFuncSetAttribute(paged_append_int8_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));

@@ -94,6 +94,7 @@ struct Args {
     // (stored before the launch).
     int fused;
     uint8_t *k_pool_w, *v_pool_w;   // the pools, for rows of a partly filled last page
+    uint32_t *err;                  // the caller's device error word, or null (this file's own)
 };
 
 enum BarIndex : int {
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *const err_word = a.err ? a.err : &g_append_tc_errors;
     using Geom = TcGeom<D>;
     constexpr int kHalves = D / 64;
     constexpr int kStages = Geom::kStages;
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_addr(smem) & 1023u) != 0) {
         if (threadIdx.x == 0)
-            atomicOr(&g_append_tc_errors, kErrSmemAlign);
+            atomicOr(err_word, kErrSmemAlign);
         return;
     }
     uint8_t *sStages = smem + Geom::kOffStages;
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t policy = l2_policy_evict_first();
         Walker w;
-        w.start(a, &g_append_tc_errors);
+        w.start(a, err_word);
         // block-table entries 0 .. 31 of the current item's sequence, one per lane, requested
         // one item ahead like the item metadata
         auto bt_head = [&](int idx) {
@@ -237,21 +239,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
-            w.next(a, &g_append_tc_errors);
+            w.next(a, err_word);
         }
         if (!ok && lane == 0) {
-            atomicOr(&g_append_tc_errors, kErrAppendTcWait);
+            atomicOr(err_word, kErrAppendTcWait);
             // let every copy in flight land before the CTA can exit
             for (int m = max(0, n - kStages); m < n; ++m)
                 if (!mbar_wait(&bars[kBarKvFull + m % kStages], (m / kStages) & 1))
-                    atomicOr(&g_append_tc_errors, kErrDrainWait);
+                    atomicOr(err_word, kErrDrainWait);
         }
     } else if (warp == 2) {
         // ------------------------------ query loads (and the fused store) -----------------
         if (lane == 0)
             prefetch_tensormap(&tmap_q);
         Walker w;
-        w.start(a, &g_append_tc_errors);
+        w.start(a, err_word);
         int qi[2] = {0, 0};   // items whose query tile t was requested
         int n = 0;
         while (ok && !w.done) {
@@ -348,14 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
-            w.next(a, &g_append_tc_errors);
+            w.next(a, err_word);
         }
         if (!ok && lane == 0) {
-            atomicOr(&g_append_tc_errors, kErrAppendTcWait);
+            atomicOr(err_word, kErrAppendTcWait);
             // the last requests may still be in flight
             for (int t = 0; t < 2; ++t)
                 if (qi[t] > 0 && !mbar_wait(&bars[kBarQFull + t], (qi[t] - 1) & 1))
-                    atomicOr(&g_append_tc_errors, kErrDrainWait);
+                    atomicOr(err_word, kErrDrainWait);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issue ----------------------------------------
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         Walker w;
-        w.start(a, &g_append_tc_errors);
+        w.start(a, err_word);
         int n0 = 0;             // ring index of the item's first slot
         int qi[2] = {0, 0};     // items of tile 0 / tile 1
         int tb[2] = {0, 0};     // blocks of tile 0 / tile 1
@@ -490,15 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < nt; ++t)
                 ++qi[t];
             n0 += 2 * nb;
-            w.next(a, &g_append_tc_errors);
+            w.next(a, err_word);
         }
         if (!ok && lane == 0)
-            atomicOr(&g_append_tc_errors, kErrAppendTcWait);
+            atomicOr(err_word, kErrAppendTcWait);
         // Every MMA this thread issued must be complete before TMEM is released.
         if (lane == 0) {
             umma_commit(&bars[kBarDrain]);
             if (!mbar_wait(&bars[kBarDrain], 0))
-                atomicOr(&g_append_tc_errors, kErrDrainWait);
+                atomicOr(err_word, kErrDrainWait);
         }
         __syncwarp();
     } else {
@@ -511,10 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tmem_s = tmem + t * 256 + Geom::kColS + lane_off;
         const float sl2 = a.scale_log2;
         Walker w;
-        w.start(a, &g_append_tc_errors);
+        w.start(a, err_word);
         int tb = 0;   // blocks of this tile so far
         int ti = 0;   // items of this tile so far
-        for (; ok && !w.done; w.next(a, &g_append_tc_errors)) {
+        for (; ok && !w.done; w.next(a, err_word)) {
             const Item &x = w.x;
             if (t == 1 && !x.has_b)
                 continue;
@@ -669,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before_sync();
         }
         if (!ok)
-            atomicOr(&g_append_tc_errors, kErrAppendTcWait);
+            atomicOr(err_word, kErrAppendTcWait);
     }
 
     tc_fence_before_sync();
@@ -714,6 +716,7 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     a.fused = l.fused ? 1 : 0;
     a.k_pool_w = static_cast<uint8_t *>(l.k_pool_w);
     a.v_pool_w = static_cast<uint8_t *>(l.v_pool_w);
+    a.err = current_error_word();
     const int tiles = (l.max_q_len * a.group + kM - 1) / kM;
     a.pairs_per_seq = (tiles + 1) / 2;
     const long long items = static_cast<long long>(a.pairs_per_seq) * l.kv_heads * l.num_seqs;

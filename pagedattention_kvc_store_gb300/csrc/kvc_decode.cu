@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     decode_cta<D, SPLIT>(&tmap_k, &tmap_v, a, blockIdx.x, blockIdx.y, blockIdx.z, smem,
-                         &g_decode_errors);
+                         a.err ? a.err : &g_decode_errors);
 }
 
 // One warp per row: out[r] = sum_j exp(lse_j - M) o_j / sum_j exp(lse_j - M).
@@ -161,7 +161,7 @@ cudaError_t launch_decode_t(const DecodeLaunch &l, const CUtensorMap &tk, const 
 // The bounded wait every kernel uses, on an mbarrier phase that nothing completes: it gives
 // up after kWaitLimitCycles and the CTA records kErrSelftestWait and returns, leaving the
 // context usable.  A diagnostic of the failure path, with no fault and no hang.
-__global__ void __launch_bounds__(32) selftest_wait_kernel()
+__global__ void __launch_bounds__(32) selftest_wait_kernel(uint32_t *word)
 {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(32) selftest_wait_kernel()
     }
     __syncwarp();
     if (!__all_sync(0xffffffffu, mbar_wait(&bar, 0)) && threadIdx.x == 0)
-        atomicOr(&g_decode_errors, kErrSelftestWait);
+        atomicOr(word ? word : &g_decode_errors, kErrSelftestWait);
 }
 
 }  // namespace
@@ -204,7 +204,7 @@ cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const floa
 
 cudaError_t launch_selftest_wait(cudaStream_t stream)
 {
-    selftest_wait_kernel<<<1, 32, 0, stream>>>();
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(current_error_word());
     return cudaGetLastError();
 }
 

@@ -58,6 +58,7 @@ struct Args {
     const uint4 *k_new, *v_new;
     uint4 *k_pool, *v_pool;
     int num_slots;
+    uint32_t *err;   // the caller's device error word, or null (the kernel's own word)
 };
 
 // Kernel arguments from the host-side launch description.
@@ -88,6 +89,7 @@ inline Args make_args(const DecodeLaunch &l)
     a.k_pool = static_cast<uint4 *>(l.k_pool_w);
     a.v_pool = static_cast<uint4 *>(l.v_pool_w);
     a.num_slots = l.num_slots;
+    a.err = current_error_word();
     return a;
 }
 

@@ -85,6 +85,7 @@ struct Args {
     int8_t *k_codes_w, *v_codes_w;
     float *k_scales_w, *v_scales_w;
     int num_slots;
+    uint32_t *err;   // the caller's device error word, or null (this file's own word)
 };
 
 // Quantises one vector held as four bf16 values per lane (lane l: elements 4 l .. 4 l + 3)
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     bool store_new = a.k_new != nullptr && ctx >= 1;
     if (ctx > a.bt_stride * P) {
         if (threadIdx.x == 0 && split == 0)
-            atomicOr(&g_decode_int8_errors, kErrContextRange);
+            atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrContextRange);
         ctx = a.bt_stride * P;
         store_new = false;   // no slot for the new token: stored nowhere
     }
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                     quantise_store_row(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx, lane);
                     quantise_store_row(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx, lane);
                 } else if (lane == 0) {
-                    atomicOr(&g_decode_int8_errors, kErrSlotRange);   // skipped, as in the store
+                    atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrSlotRange);   // skipped, as in the store
                 }
                 // the stores (generic proxy) before the copies (async proxy) that read them
                 fence_proxy_async_global();
@@ -279,10 +280,10 @@ __global__ void __launch_bounds__(kThreads, 3)
             issued = b + 1;
         }
         if (!ok && lane == 0) {
-            atomicOr(&g_decode_int8_errors, kErrDecodeEmptyWait);
+            atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrDecodeEmptyWait);
             for (int b = max(0, issued - kStages); b < issued; ++b)
                 if (!mbar_wait(&full[b % kStages], (b / kStages) & 1))
-                    atomicOr(&g_decode_int8_errors, kErrDrainWait);
+                    atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrDrainWait);
         }
         return;
     }
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             mbar_arrive(&empty[st]);
     }
     if (!ok)
-        atomicOr(&g_decode_int8_errors, kErrDecodeFullWait);
+        atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrDecodeFullWait);
 
     // ------------------------- combine the 4 warps' partial results -----------------------
     // Each warp leaves its unnormalised o rows (D + 4 floats apart: 16-byte aligned rows),
@@ -532,6 +533,7 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.k_scales_w = l.k_scales_w;
     a.v_scales_w = l.v_scales_w;
     a.num_slots = l.num_slots;
+    a.err = current_error_word();
     auto kernel = paged_decode_int8_kernel<SPLIT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));

@@ -64,6 +64,7 @@ struct Args {
     int chunk, n_split, split_stride;
     float scale_log2;
     int hnd;   // HND pools: page boxes addressed by (page, kv head) block
+    uint32_t *err;   // the caller's device error word, or null (this file's own word)
 };
 
 // Block 0 sets every sequence's key start: 0, then, for each group member, the end of the
@@ -365,10 +366,10 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUte
             issued = b + 1;
         }
         if (!ok && lane == 0) {
-            atomicOr(&g_grouped_errors, kErrDecodeEmptyWait);
+            atomicOr(a.err ? a.err : &g_grouped_errors, kErrDecodeEmptyWait);
             for (int b = max(0, issued - kStages); b < issued; ++b)
                 if (!mbar_wait(&full[b % kStages], (b / kStages) & 1))
-                    atomicOr(&g_grouped_errors, kErrDrainWait);
+                    atomicOr(a.err ? a.err : &g_grouped_errors, kErrDrainWait);
         }
         return;
     }
@@ -547,7 +548,7 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUte
             mbar_arrive(&empty[st]);
     }
     if (!ok)
-        atomicOr(&g_grouped_errors, kErrDecodeFullWait);
+        atomicOr(a.err ? a.err : &g_grouped_errors, kErrDecodeFullWait);
 
     // ------------------- combine the warps of each tile, write partials --------------------
     // Warp w of tile t leaves its unnormalised o (rows of D + 8 floats: the pad spreads the
@@ -652,7 +653,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int split = j % da.n_split;
         const int rest = j / da.n_split;
         dec::decode_cta<D, true>(&tmap_k, &tmap_v, da, split, rest % da.kv_heads,
-                                 rest / da.kv_heads, smem, &g_grouped_errors);
+                                 rest / da.kv_heads, smem,
+                                 da.err ? da.err : &g_grouped_errors);
     }
 }
 
@@ -673,6 +675,7 @@ cudaError_t launch_t(const GroupedPrefixLaunch &p, const DecodeLaunch &l, const 
     a.q_heads = p.q_heads;
     a.kv_heads = p.kv_heads;
     a.hnd = p.hnd ? 1 : 0;
+    a.err = current_error_word();
     a.group = p.q_heads / p.kv_heads;
     a.page_size = p.page_size;
     a.chunk = p.chunk;

@@ -8,6 +8,10 @@
 
 namespace kvc {
 
+// The device word that the calling host thread named with kvc_set_error_word, or nullptr (the
+// kernels then set bits in their translation unit's own word, read by kvc_device_errors).
+uint32_t *current_error_word();
+
 // Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger in kvc_device.cuh):
 // the kernel may start before the previous launch on the stream has finished and waits for it
 // in its first instruction.

@@ -22,17 +22,18 @@ __global__ void slot_mapping_decode_kernel(int32_t *__restrict__ slots,
                                            const int32_t *__restrict__ block_table,
                                            int bt_stride,
                                            const int32_t *__restrict__ context_lens,
-                                           int num_seqs, int page_size)
+                                           int num_seqs, int page_size, uint32_t *word)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *err = word ? word : &g_store_errors;
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= num_seqs)
         return;
     const int position = context_lens[s] - 1;
     int slot = -1;
     if (position >= bt_stride * page_size) {
-        atomicOr(&g_store_errors, kErrContextRange);
+        atomicOr(err, kErrContextRange);
     } else if (position >= 0) {
         const int page = block_table[static_cast<size_t>(s) * bt_stride + position / page_size];
         slot = page * page_size + position % page_size;
@@ -46,10 +47,11 @@ __global__ void slot_mapping_ragged_kernel(int32_t *__restrict__ slots,
                                            int bt_stride,
                                            const int32_t *__restrict__ context_lens,
                                            const int32_t *__restrict__ q_indptr,
-                                           int page_size)
+                                           int page_size, uint32_t *word)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *err = word ? word : &g_store_errors;
     const int s = blockIdx.x;
     const int first = q_indptr[s];
     const int q_len = q_indptr[s + 1] - first;
@@ -59,7 +61,7 @@ __global__ void slot_mapping_ragged_kernel(int32_t *__restrict__ slots,
         const int position = ctx - q_len + i;
         int slot = -1;
         if (position >= bt_stride * page_size)
-            atomicOr(&g_store_errors, kErrContextRange);
+            atomicOr(err, kErrContextRange);
         else if (position >= 0)
             slot = row[position / page_size] * page_size + position % page_size;
         slots[first + i] = slot;
@@ -76,10 +78,12 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
                                                     const uint4 *__restrict__ v_new,
                                                     const int32_t *__restrict__ slots,
                                                     int num_tokens, int chunks, int num_slots,
-                                                    bool hnd, int kv_heads, int page_size)
+                                                    bool hnd, int kv_heads, int page_size,
+                                                    uint32_t *word)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *err = word ? word : &g_store_errors;
     const int row_chunks = chunks / kv_heads;   // 16-byte chunks of one head_dim vector
     const size_t total = static_cast<size_t>(num_tokens) * chunks;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(256) store_kernel(uint4 *__restrict__ k_pool,
             continue;
         if (slot >= num_slots) {   // past the pool: skip the token, flag the call
             if (c == 0)
-                atomicOr(&g_store_errors, kErrSlotRange);
+                atomicOr(err, kErrSlotRange);
             continue;
         }
         size_t dst = static_cast<size_t>(slot) * chunks + c;
@@ -126,10 +130,11 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
     uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, const uint4 *__restrict__ k_new,
     const uint4 *__restrict__ v_new, const int32_t *__restrict__ block_table, int bt_stride,
     const int32_t *__restrict__ q_indptr, const int32_t *__restrict__ context_lens, int num_seqs,
-    int chunks, int kv_heads, int page_size, int num_slots, bool hnd, bool whole)
+    int chunks, int kv_heads, int page_size, int num_slots, bool hnd, bool whole, uint32_t *word)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *err = word ? word : &g_store_errors;
     const int row_chunks = chunks / kv_heads;
     const int capacity = bt_stride * page_size;   // positions a block-table row covers
     for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
         const bool over = ctx > capacity;
         const bool all = whole || over;   // every token of the chunk is stored here
         if (over && threadIdx.x == 0)
-            atomicOr(&g_store_errors, kErrContextRange);
+            atomicOr(err, kErrContextRange);
         if (q_len <= 0 || (!all && (base <= 0 || base % page_size == 0)))
             continue;
         const int n_tok = all ? q_len : min(ctx, (base / page_size + 1) * page_size) - base;
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
             const long long slot = static_cast<long long>(page) * page_size + pos % page_size;
             if (slot < 0 || slot >= num_slots) {   // a page outside the pool: skip, flag
                 if (c == 0)
-                    atomicOr(&g_store_errors, kErrSlotRange);
+                    atomicOr(err, kErrSlotRange);
                 continue;
             }
             size_t dst = static_cast<size_t>(slot) * chunks + c;
@@ -186,10 +191,12 @@ __global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_
                                                          const __nv_bfloat16 *__restrict__ v_new,
                                                          const int32_t *__restrict__ slots,
                                                          int num_tokens, int kv_heads,
-                                                         int page_size, int num_slots)
+                                                         int page_size, int num_slots,
+                                                         uint32_t *word)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *err = word ? word : &g_store_errors;
     constexpr int D = 32 * E;
     const int lane = threadIdx.x & 31;
     const long long vectors = static_cast<long long>(num_tokens) * kv_heads;
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_
             continue;
         if (slot >= num_slots) {
             if (lane == 0 && g == 0)
-                atomicOr(&g_store_errors, kErrSlotRange);
+                atomicOr(err, kErrSlotRange);
             continue;
         }
         const size_t src = static_cast<size_t>(w) * D + lane * E;
@@ -251,10 +258,12 @@ __global__ void __launch_bounds__(256) copy_pages_kernel(uint4 *__restrict__ k_p
                                                          uint4 *__restrict__ v_pool,
                                                          const int32_t *__restrict__ src_pages,
                                                          const int32_t *__restrict__ dst_pages,
-                                                         int num_copies, int chunks, int num_pages)
+                                                         int num_copies, int chunks, int num_pages,
+                                                         uint32_t *word)
 {
     pdl_wait();
     pdl_trigger();
+    uint32_t *err = word ? word : &g_store_errors;
     const size_t total = static_cast<size_t>(num_copies) * chunks;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(256) copy_pages_kernel(uint4 *__restrict__ k_p
         const int dst = __ldg(dst_pages + n);
         if (src < 0 || src >= num_pages || dst < 0 || dst >= num_pages) {
             if (c == 0)
-                atomicOr(&g_store_errors, kErrPageRange);
+                atomicOr(err, kErrPageRange);
             continue;
         }
         const size_t from = static_cast<size_t>(src) * chunks + c;
@@ -305,12 +314,13 @@ cudaError_t launch_slot_mapping(int32_t *slots, const int32_t *block_table, int 
         const int threads = 128;
         return launch_pdl(slot_mapping_decode_kernel, dim3((num_seqs + threads - 1) / threads),
                           dim3(threads), 0, stream, slots, block_table, bt_stride, context_lens,
-                          num_seqs, page_size);
+                          num_seqs, page_size, current_error_word());
     } else {
         int threads = ((max_q_len + 31) / 32) * 32;
         threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
         return launch_pdl(slot_mapping_ragged_kernel, dim3(num_seqs), dim3(threads), 0, stream,
-                          slots, block_table, bt_stride, context_lens, q_indptr, page_size);
+                          slots, block_table, bt_stride, context_lens, q_indptr, page_size,
+                          current_error_word());
     }
 }
 
@@ -330,7 +340,8 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
     return launch_pdl(store_kernel, dim3(blocks), dim3(threads), 0, stream,
                       static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slots,
-                      num_tokens, chunks, num_slots, hnd, kv_heads, page_size);
+                      num_tokens, chunks, num_slots, hnd, kv_heads, page_size,
+                      current_error_word());
 }
 
 cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int head_dim,
@@ -347,7 +358,8 @@ cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int 
                       static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
                       block_table, bt_stride, q_indptr, context_lens, num_seqs,
-                      kv_heads * head_dim * 2 / 16, kv_heads, page_size, num_slots, hnd, whole);
+                      kv_heads * head_dim * 2 / 16, kv_heads, page_size, num_slots, hnd, whole,
+                      current_error_word());
 }
 
 cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
@@ -369,11 +381,11 @@ cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, flo
     if (head_dim == 128)
         return launch_pdl(store_int8_kernel<4>, dim3(blocks), dim3(threads), 0, stream, kc, vc,
                           k_scales, v_scales, kn, vn, slots, num_tokens, kv_heads, page_size,
-                          num_slots);
+                          num_slots, current_error_word());
     else
         return launch_pdl(store_int8_kernel<2>, dim3(blocks), dim3(threads), 0, stream, kc, vc,
                           k_scales, v_scales, kn, vn, slots, num_tokens, kv_heads, page_size,
-                          num_slots);
+                          num_slots, current_error_word());
 }
 
 cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,
@@ -390,7 +402,7 @@ cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int pag
     const int blocks = static_cast<int>(wanted < cap ? wanted : cap);
     return launch_pdl(copy_pages_kernel, dim3(blocks), dim3(threads), 0, stream,
                       static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), src_pages,
-                      dst_pages, num_copies, chunks, num_pages);
+                      dst_pages, num_copies, chunks, num_pages, current_error_word());
 }
 
 cudaError_t read_and_clear_store_errors(uint32_t *flags)

@@ -31,7 +31,7 @@ EXPORTS = ("kvc_status_string", "kvc_last_error", "kvc_slot_mapping", "kvc_store
            "kvc_validate_workspace_size", "kvc_validate", "kvc_copy_pages", "kvc_store_int8",
            "kvc_decode_int8", "kvc_decode_int8_plan", "kvc_append_int8",
            "kvc_append_store", "kvc_shared_prefix_groups", "kvc_decode_store",
-           "kvc_selftest_wait", "kvc_decode_int8_store")
+           "kvc_selftest_wait", "kvc_decode_int8_store", "kvc_set_error_word")
 
 # Size of the library's own split-partials scratch used by kvc_decode_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
             L.kvc_selftest_wait.argtypes = [p]
             L.kvc_device_errors.restype = ctypes.c_int
             L.kvc_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.kvc_set_error_word.restype = ctypes.c_int
+            L.kvc_set_error_word.argtypes = [p]
             L.kvc_store_int8.restype = ctypes.c_int
             L.kvc_store_int8.argtypes = [p, p, p, p, PoolDesc, p, p, p, i32, p]
             L.kvc_decode_int8_plan.restype = ctypes.c_int
@@ -557,6 +559,18 @@ def kvc_selftest_wait(stream=None) -> None:
     """Enqueue the bounded-wait self-test (about a second); kvc_device_errors() then has bit
     1 << 12 set."""
     _check("kvc_selftest_wait", lib().kvc_selftest_wait(_stream(stream)))
+
+
+def kvc_set_error_word(word) -> None:
+    """Route the error bits of this thread's later calls into `word` (a 4-byte int32/uint32
+    device tensor of one element, owned by the caller), or back to the library's own words with
+    None."""
+    if word is None:
+        _check("kvc_set_error_word", lib().kvc_set_error_word(None))
+        return
+    if word.numel() != 1 or word.element_size() != 4 or not word.is_cuda:
+        raise ValueError("the error word is one 4-byte element on the GPU")
+    _check("kvc_set_error_word", lib().kvc_set_error_word(word.data_ptr()))
 
 
 def kvc_device_errors() -> int:

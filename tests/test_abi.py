@@ -118,3 +118,11 @@ def test_binding_refuses_pageable_decode_out():
         kvc.kvc_decode(t, t, t, t, torch.zeros(4, 1, dtype=torch.int32), lens, 16)
     with pytest.raises(ValueError, match="pinned"):
         kvc.kvc_merge(t, torch.zeros(4, 2, 64), torch.zeros(4, 2))
+
+
+def test_error_word_setting_is_host_only():
+    """kvc_set_error_word stores a pointer for the calling thread: a misaligned one is refused,
+    NULL (the library's own words) is accepted, and neither touches the device."""
+    L = kvc.lib()
+    assert kvc.kvc.STATUS[L.kvc_set_error_word(ctypes.c_void_p(6))] == "KVC_ERR_INVALID_ARG"
+    assert L.kvc_set_error_word(None) == 0
