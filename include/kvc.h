@@ -12,8 +12,8 @@
  * Pools.  One K pool and one V pool per layer, each bf16 [num_pages][page_size][kv_heads]
  *   [head_dim], row-major (the (position, kv head) vector is head_dim contiguous values).
  *   Viewed by slot it is [num_pages * page_size][kv_heads][head_dim].  pool.layout = KVC_HND
- *   selects [num_pages][kv_heads][page_size][head_dim] instead (see kvc_layout); INT8 pages
- *   are NHD only.
+ *   selects [num_pages][kv_heads][page_size][head_dim] instead (see kvc_layout), for bf16 and
+ *   INT8 pages alike.
  * Address rule.  Position p (0-based) of sequence s lives in page block_table[s][p /
  *   page_size] at offset p % page_size; its slot is page * page_size + offset.
  * Block table.  int32 [num_seqs][bt_stride], row-major.  Entries past a sequence's last
@@ -406,7 +406,8 @@ kvc_status kvc_selftest_wait(void *stream);
  * does not dequantise: a key's scale multiplies its score, a value's scale its probability
  * before the PV product).  132 bytes per vector at head_dim 128 instead of 256.
  *   k_codes, v_codes   int8 [num_pages][page_size][kv_heads][head_dim] (the bf16 pools'
- *                      layout with one byte per value)
+ *                      layout with one byte per value), or [num_pages][kv_heads][page_size]
+ *                      [head_dim] with pool.layout = KVC_HND
  *   k_scales, v_scales fp32 [num_pages][kv_heads][page_size] (the scales of one page and kv
  *                      head are contiguous)
  * All four 16-byte aligned; `pool` describes them as it describes a bf16 pool.

@@ -57,12 +57,6 @@ kvc_status check_pool(const kvc_pool_desc &pool)
     return KVC_OK;
 }
 
-kvc_status check_nhd(const kvc_pool_desc &pool)
-{
-    return pool.layout == KVC_NHD ? KVC_OK
-                                  : fail(KVC_ERR_UNSUPPORTED, "INT8 pages are NHD only");
-}
-
 kvc_status check_group(const kvc_pool_desc &pool, int32_t q_heads)
 {
     if (q_heads <= 0 || q_heads % pool.kv_heads != 0)
@@ -278,13 +272,27 @@ kvc_status new_tokens_tensor_map(const void *base, int32_t num_tokens, const kvc
 
 // INT8 codes [num_pages * page_size][kv_heads][head_dim] viewed as the 3-D tensor
 // {head_dim, kv head, slot} of bytes; one box {head_dim, 1, page_size} is one page of one kv
-// head, [page_size rows][head_dim bytes] (128 bytes at head_dim 128, one swizzle row).
+// head, [page_size rows][head_dim bytes] (128 bytes at head_dim 128, one swizzle row).  HND
+// codes [num_pages][kv_heads][page_size][head_dim]: the tensor {head_dim, offset, page *
+// kv_heads + kv head}, whose box {head_dim, page_size, 1} is the same contiguous block and
+// lands in shared memory exactly as the NHD box does.
 kvc_status pool_tensor_map_int8(const void *base, const kvc_pool_desc &pool, CUtensorMap *out)
 {
     MapKey k{};
     k.ptr = base;
     k.rank = 3;
     k.int8 = true;
+    if (pool.layout == KVC_HND) {
+        k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
+        k.dims[1] = static_cast<cuuint64_t>(pool.page_size);
+        k.dims[2] = static_cast<cuuint64_t>(pool.num_pages) * pool.kv_heads;
+        k.strides[0] = static_cast<cuuint64_t>(pool.head_dim);
+        k.strides[1] = static_cast<cuuint64_t>(pool.page_size) * pool.head_dim;
+        k.box[0] = static_cast<cuuint32_t>(pool.head_dim);
+        k.box[1] = static_cast<cuuint32_t>(pool.page_size);
+        k.box[2] = 1;
+        return tensor_map(k, out);
+    }
     k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
     k.dims[1] = static_cast<cuuint64_t>(pool.kv_heads);
     k.dims[2] = static_cast<cuuint64_t>(pool.num_pages) * pool.page_size;
@@ -557,7 +565,7 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
                           const int32_t *slot_mapping, int32_t num_tokens, void *stream)
 {
     kvc_status st = check_pool(pool);
-    if (st != KVC_OK || (st = check_nhd(pool)) != KVC_OK)
+    if (st != KVC_OK)
         return st;
     if (num_tokens < 0)
         return fail(KVC_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
@@ -572,7 +580,8 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
                                              pool.kv_heads, pool.head_dim, pool.page_size,
                                              pool.num_pages * pool.page_size, k_new, v_new,
                                              slot_mapping, num_tokens,
-                                             static_cast<cudaStream_t>(stream));
+                                             static_cast<cudaStream_t>(stream),
+                                             pool.layout == KVC_HND);
     return err == cudaSuccess ? ok() : cuda_fail(err, "store_int8 launch");
 }
 
@@ -594,8 +603,6 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
     if (pool.head_dim != 128)
         return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
                     pool.head_dim);
-    if ((st = check_nhd(pool)) != KVC_OK)
-        return st;
     if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
         return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
     if (num_splits < 0)
@@ -648,6 +655,7 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
     l.q_heads = q_heads;
     l.kv_heads = pool.kv_heads;
     l.page_size = pool.page_size;
+    l.hnd = pool.layout == KVC_HND;
     l.chunk = p.chunk;
     l.n_split = p.splits;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
@@ -1174,8 +1182,6 @@ kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const vo
     if (pool.head_dim != 128)
         return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
                     pool.head_dim);
-    if ((st = check_nhd(pool)) != KVC_OK)
-        return st;
     if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
         return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
     if (num_tokens < 0 || max_q_len < 0)
@@ -1209,6 +1215,7 @@ kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const vo
     l.q_heads = q_heads;
     l.kv_heads = pool.kv_heads;
     l.page_size = pool.page_size;
+    l.hnd = pool.layout == KVC_HND;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     cudaError_t err = kvc::launch_append_int8(l, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? ok() : cuda_fail(err, "append_int8 launch");

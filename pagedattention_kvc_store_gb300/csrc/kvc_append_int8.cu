@@ -107,6 +107,7 @@ struct Args {
     int kv_heads, q_heads, group, page_size, pairs_per_seq, num_items;
     float scale_log2;
     uint32_t *err;   // the caller's device error word, or null (this file's own word)
+    int hnd;         // HND codes: page boxes addressed by (offset, page * kv_heads + kv head)
 };
 
 // Fill order of an item's K / V blocks: j = 0 .. 2 nb - 1 is K(0), K(1), V(0), K(2), V(1), ...,
@@ -285,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
                     if (lane < np_h) {
                         tma_load_3d(code_slot(m) + lane * P * D, is_k ? &tmap_k : &tmap_v, 0,
-                                    x.kvh, page * P, &bars[kBarCodeFull + cs], policy);
+                                    a.hnd ? 0 : x.kvh, a.hnd ? page * a.kv_heads + x.kvh : page * P,
+                                    &bars[kBarCodeFull + cs], policy);
                     } else if (scales && lane >= 8 && i < np) {
                         const int op = (lane - 8) & 1;
                         const float *src = (op == 0 ? a.k_scales : a.v_scales) +
@@ -817,6 +819,7 @@ cudaError_t launch_append_int8(const AppendInt8Launch &l, const CUtensorMap &tma
     a.num_items = static_cast<int>(items);
     a.scale_log2 = l.scale * kLog2e;
     a.err = current_error_word();
+    a.hnd = l.hnd ? 1 : 0;
     cudaError_t err = cudaFuncSetAttribute(paged_append_int8_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));

@@ -86,6 +86,7 @@ struct Args {
     float *k_scales_w, *v_scales_w;
     int num_slots;
     uint32_t *err;   // the caller's device error word, or null (this file's own word)
+    int hnd;         // HND codes: page boxes addressed by (offset, page * kv_heads + kv head)
 };
 
 // Quantises one vector held as four bf16 values per lane (lane l: elements 4 l .. 4 l + 3)
@@ -251,9 +252,10 @@ __global__ void __launch_bounds__(kThreads, 3)
                 const int off_new = (ctx - 1) % P;
                 const long long slot = static_cast<long long>(new_page) * P + off_new;
                 if (new_page >= 0 && slot < a.num_slots) {
-                    const size_t row = (static_cast<size_t>(slot) * a.kv_heads + kvh) * D;
                     const size_t sidx =
                         (static_cast<size_t>(new_page) * a.kv_heads + kvh) * P + off_new;
+                    const size_t row =
+                        (a.hnd ? sidx : static_cast<size_t>(slot) * a.kv_heads + kvh) * D;
                     quantise_store_row(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx, lane);
                     quantise_store_row(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx, lane);
                 } else if (lane == 0) {
@@ -266,10 +268,11 @@ __global__ void __launch_bounds__(kThreads, 3)
             }
             if (i < np) {
                 if (op == 0) {
-                    tma_load_3d(stage + i * P * D, &tmap_k, 0, kvh, page * P, &full[st], policy);
+                    tma_load_3d(stage + i * P * D, &tmap_k, 0, a.hnd ? 0 : kvh,
+                                a.hnd ? page * a.kv_heads + kvh : page * P, &full[st], policy);
                 } else if (op == 1) {
-                    tma_load_3d(stage + kOffV + i * P * D, &tmap_v, 0, kvh, page * P, &full[st],
-                                policy);
+                    tma_load_3d(stage + kOffV + i * P * D, &tmap_v, 0, a.hnd ? 0 : kvh,
+                                a.hnd ? page * a.kv_heads + kvh : page * P, &full[st], policy);
                 } else {
                     const float *src = (op == 2 ? a.k_scales : a.v_scales) +
                                        (static_cast<size_t>(page) * a.kv_heads + kvh) * P;
@@ -534,6 +537,7 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.v_scales_w = l.v_scales_w;
     a.num_slots = l.num_slots;
     a.err = current_error_word();
+    a.hnd = l.hnd ? 1 : 0;
     auto kernel = paged_decode_int8_kernel<SPLIT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));

@@ -75,6 +75,7 @@ struct DecodeInt8Launch {
     void *k_codes_w = nullptr, *v_codes_w = nullptr;
     float *k_scales_w = nullptr, *v_scales_w = nullptr;
     int num_slots = 0;
+    bool hnd = false;   // codes [pages][Hkv][P][D] (the tensor maps follow it too)
 };
 cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tmap_k,
                                const CUtensorMap &tmap_v, cudaStream_t stream);
@@ -127,6 +128,7 @@ struct AppendInt8Launch {
     const int32_t *context_lens;
     int num_seqs, num_tokens, max_q_len, q_heads, kv_heads, page_size;
     float scale;
+    bool hnd = false;   // codes [pages][Hkv][P][D] (the tensor maps follow it too)
 };
 
 // kvc_validate: the smallest offending index of each check (INT32_MAX when it passed), then two
@@ -152,7 +154,7 @@ cudaError_t launch_store(void *k_pool, void *v_pool, int kv_heads, int head_dim,
 cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
                               int kv_heads, int head_dim, int page_size, int num_slots,
                               const void *k_new, const void *v_new, const int32_t *slots,
-                              int num_tokens, cudaStream_t stream);
+                              int num_tokens, cudaStream_t stream, bool hnd = false);
 cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,
                               int kv_heads, int head_dim, const int32_t *src_pages,
                               const int32_t *dst_pages, int num_copies, cudaStream_t stream);

@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(256) store_boundary_kernel(
 // D = 32 * E values.  scale = max|x| / 127 and code = rint(x / scale) clamped to [-127, 127],
 // both in fp32 with round-to-nearest division, so the codes are the ones the quantiser's
 // definition gives; an all-zero vector stores scale 0 and codes 0.  Codes land in the pool
-// like bf16 values do ([slot][kv head][D]); scales at [page][kv head][offset].
+// like bf16 values do ([slot][kv head][D], or [page][kv head][offset][D] for HND pools);
+// scales at [page][kv head][offset].
 template <int E>
 __global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_codes,
                                                          int8_t *__restrict__ v_codes,
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_
                                                          const int32_t *__restrict__ slots,
                                                          int num_tokens, int kv_heads,
                                                          int page_size, int num_slots,
-                                                         uint32_t *word)
+                                                         uint32_t *word, bool hnd)
 {
     pdl_wait();
     pdl_trigger();
@@ -214,10 +215,11 @@ __global__ void __launch_bounds__(256) store_int8_kernel(int8_t *__restrict__ k_
             continue;
         }
         const size_t src = static_cast<size_t>(w) * D + lane * E;
-        const size_t dst = (static_cast<size_t>(slot) * kv_heads + g) * D + lane * E;
         const int page = slot / page_size;
         const size_t sidx = (static_cast<size_t>(page) * kv_heads + g) * page_size +
                             (slot - page * page_size);
+        // codes: NHD [slot][kv head][D]; HND [page][kv head][offset][D] (row sidx)
+        const size_t dst = (hnd ? sidx : static_cast<size_t>(slot) * kv_heads + g) * D + lane * E;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const __nv_bfloat16 *x = (which == 0 ? k_new : v_new) + src;
@@ -365,7 +367,7 @@ cudaError_t launch_store_boundary(void *k_pool, void *v_pool, int kv_heads, int 
 cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, float *v_scales,
                               int kv_heads, int head_dim, int page_size, int num_slots,
                               const void *k_new, const void *v_new, const int32_t *slots,
-                              int num_tokens, cudaStream_t stream)
+                              int num_tokens, cudaStream_t stream, bool hnd)
 {
     if (num_tokens == 0)
         return cudaSuccess;
@@ -381,11 +383,11 @@ cudaError_t launch_store_int8(void *k_codes, void *v_codes, float *k_scales, flo
     if (head_dim == 128)
         return launch_pdl(store_int8_kernel<4>, dim3(blocks), dim3(threads), 0, stream, kc, vc,
                           k_scales, v_scales, kn, vn, slots, num_tokens, kv_heads, page_size,
-                          num_slots, current_error_word());
+                          num_slots, current_error_word(), hnd);
     else
         return launch_pdl(store_int8_kernel<2>, dim3(blocks), dim3(threads), 0, stream, kc, vc,
                           k_scales, v_scales, kn, vn, slots, num_tokens, kv_heads, page_size,
-                          num_slots, current_error_word());
+                          num_slots, current_error_word(), hnd);
 }
 
 cudaError_t launch_copy_pages(void *k_pool, void *v_pool, int num_pages, int page_size,

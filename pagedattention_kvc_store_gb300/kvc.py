@@ -237,16 +237,20 @@ def kvc_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
         _ptr(slot_mapping), int(slot_mapping.shape[0]), _stream(stream)))
 
 
-def int8_pool_desc(k_codes: torch.Tensor) -> PoolDesc:
-    """Descriptor of a [num_pages, page_size, kv_heads, head_dim] int8 code pool."""
+def int8_pool_desc(k_codes: torch.Tensor, layout: str = "nhd") -> PoolDesc:
+    """Descriptor of an int8 code pool: [num_pages, page_size, kv_heads, head_dim] (layout
+    "nhd") or [num_pages, kv_heads, page_size, head_dim] (layout "hnd")."""
     if k_codes.dim() != 4 or k_codes.dtype != torch.int8:
-        raise ValueError("INT8 codes are an int8 [num_pages, page_size, kv_heads, head_dim]")
-    n, p, h, d = (int(x) for x in k_codes.shape)
-    return PoolDesc(n, p, h, d)
+        raise ValueError("INT8 codes are an int8 4-D tensor")
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout {layout!r}: 'nhd' or 'hnd'")
+    n, a, b, d = (int(x) for x in k_codes.shape)
+    p, h = (a, b) if layout == "nhd" else (b, a)
+    return PoolDesc(n, p, h, d, LAYOUTS[layout])
 
 
-def _int8_pools(k_codes, v_codes, k_scales, v_scales):
-    pool = int8_pool_desc(k_codes)
+def _int8_pools(k_codes, v_codes, k_scales, v_scales, layout="nhd"):
+    pool = int8_pool_desc(k_codes, layout)
     for name, t, dt in (("k_codes", k_codes, torch.int8), ("v_codes", v_codes, torch.int8),
                         ("k_scales", k_scales, torch.float32),
                         ("v_scales", v_scales, torch.float32)):
@@ -259,8 +263,8 @@ def _int8_pools(k_codes, v_codes, k_scales, v_scales):
 
 def kvc_store_int8(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch.Tensor,
                    v_scales: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
-                   slot_mapping: torch.Tensor, stream=None) -> None:
-    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+                   slot_mapping: torch.Tensor, stream=None, layout: str = "nhd") -> None:
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales, layout)
     _cuda("k_new", k_new, torch.bfloat16)
     _cuda("v_new", v_new, torch.bfloat16)
     _cuda("slot_mapping", slot_mapping, torch.int32)
@@ -283,8 +287,9 @@ def kvc_decode_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
                     v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
                     block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
                     scale: float = 0.0, num_splits: int = 0,
-                    workspace: Optional[torch.Tensor] = None, stream=None) -> None:
-    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+                    workspace: Optional[torch.Tensor] = None, stream=None,
+                    layout: str = "nhd") -> None:
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales, layout)
     _decode_out(out)
     _reachable("q", q, torch.bfloat16)
     _reachable("block_table", block_table, torch.int32)
@@ -302,10 +307,11 @@ def kvc_decode_int8_store(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tenso
                           k_scales: torch.Tensor, v_scales: torch.Tensor,
                           block_table: torch.Tensor, context_lens: torch.Tensor, max_ctx: int,
                           scale: float = 0.0, num_splits: int = 0,
-                          workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+                          workspace: Optional[torch.Tensor] = None, stream=None,
+                          layout: str = "nhd") -> None:
     """Quantise and store each sequence's new token (k_new / v_new bf16 [S, Hkv, D]) into the
     INT8 pools and decode over them, in one call."""
-    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales, layout)
     _decode_out(out)
     _reachable("q", q, torch.bfloat16)
     _reachable("k_new", k_new, torch.bfloat16)
@@ -327,9 +333,10 @@ def kvc_append_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor,
                     v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
                     block_table: torch.Tensor, q_indptr: torch.Tensor,
                     context_lens: torch.Tensor, max_q_len: int, max_ctx: int,
-                    scale: float = 0.0, stream=None) -> None:
-    """kvc_append over INT8 pages (codes int8 [pages, P, Hkv, D], scales fp32 [pages, Hkv, P])."""
-    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales)
+                    scale: float = 0.0, stream=None, layout: str = "nhd") -> None:
+    """kvc_append over INT8 pages (codes int8 [pages, P, Hkv, D], or [pages, Hkv, P, D] with
+    layout "hnd"; scales fp32 [pages, Hkv, P])."""
+    pool = _int8_pools(k_codes, v_codes, k_scales, v_scales, layout)
     _cuda("out", out)
     _cuda("q", q, torch.bfloat16)
     _cuda("block_table", block_table, torch.int32)

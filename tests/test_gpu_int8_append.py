@@ -162,7 +162,7 @@ def test_int8_append_single_position_is_its_stored_vector():
             np.testing.assert_allclose(got[s, h], want, rtol=2.0 ** -10, atol=1e-6)
 
 
-def test_int8_append_refuses_head_dim_64_and_hnd():
+def test_int8_append_refuses_head_dim_64():
     q = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(1, 2, 64, device="cuda")
     kc = torch.zeros(4, 16, 1, 64, dtype=torch.int8, device="cuda")
@@ -171,12 +171,6 @@ def test_int8_append_refuses_head_dim_64_and_hnd():
     ind = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
     with pytest.raises(kvc.KvcError, match="UNSUPPORTED"):
         kvc.kvc_append_int8(out, q, kc, kc, sc, sc, one, ind, one[0], 1, 1)
-    pool = kvc.PoolDesc(4, 16, 1, 128, kvc.KVC_HND)
-    q = torch.zeros(1, 2, 128, dtype=torch.bfloat16, device="cuda")
-    st = kvc.lib().kvc_append_int8(out.data_ptr(), 1, q.data_ptr(), kc.data_ptr(), kc.data_ptr(),
-                                   sc.data_ptr(), sc.data_ptr(), pool, one.data_ptr(), 1,
-                                   ind.data_ptr(), one.data_ptr(), 1, 1, 1, 1, 2, 0.0, None)
-    assert kvc.kvc.STATUS[st] == "KVC_ERR_UNSUPPORTED"
 
 
 def test_int8_append_flags_a_value_scale_beyond_fp16_range():
