@@ -471,7 +471,7 @@ kvc_status kvc_decode_int8_store(void *out, int32_t out_dtype, const void *q, co
  * softmax denominator sums the unrounded probabilities.  fp16's range limits value scales to
  * 4000 (|v| up to 5.08e5): a larger one sets a kvc_device_errors bit and its results are not
  * valid.  Positions past a sequence's context may hold any codes and NaN scales.  head_dim 128
- * only, NHD only (others: KVC_ERR_UNSUPPORTED).
+ * only (others: KVC_ERR_UNSUPPORTED); NHD or HND pools.
  */
 kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
                            const void *v_codes, const float *k_scales, const float *v_scales,
