@@ -425,8 +425,8 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
 /*
  * kvc_decode_int8 -- kvc_decode over INT8 pages (same arguments and outputs).  Its split-K
  * plan and workspace come from kvc_decode_int8_plan (the automatic split count differs from
- * kvc_decode's: the INT8 kernel keeps more CTAs resident per SM).  head_dim 128 only (others:
- * KVC_ERR_UNSUPPORTED).
+ * kvc_decode's: the INT8 kernel keeps more CTAs resident per SM).  head_dim 64 or 128
+ * (others: KVC_ERR_UNSUPPORTED); kvc_append_int8 takes head_dim 128 only.
  */
 kvc_status kvc_decode_int8_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
                                 int32_t max_ctx, int32_t num_splits, int32_t *splits_out,

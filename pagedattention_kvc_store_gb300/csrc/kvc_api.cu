@@ -162,12 +162,14 @@ struct MapKey {
     int device;
     int rank;
     bool int8 = false;   // uint8 elements (INT8 pages) instead of bf16
+    bool swizzle64 = false;   // 64-byte swizzle (rows of 64 bytes) instead of 128-byte
     cuuint64_t dims[4];
     cuuint64_t strides[3];
     cuuint32_t box[4];
     bool operator==(const MapKey &o) const
     {
-        if (ptr != o.ptr || device != o.device || rank != o.rank || int8 != o.int8)
+        if (ptr != o.ptr || device != o.device || rank != o.rank || int8 != o.int8 ||
+            swizzle64 != o.swizzle64)
             return false;
         for (int i = 0; i < rank; ++i)
             if (dims[i] != o.dims[i] || box[i] != o.box[i] ||
@@ -207,7 +209,8 @@ kvc_status tensor_map(MapKey key, CUtensorMap *out)
                     key.int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     static_cast<cuuint32_t>(key.rank),
                     const_cast<void *>(key.ptr), key.dims, key.strides, key.box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    key.swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(KVC_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)",
@@ -282,6 +285,7 @@ kvc_status pool_tensor_map_int8(const void *base, const kvc_pool_desc &pool, CUt
     k.ptr = base;
     k.rank = 3;
     k.int8 = true;
+    k.swizzle64 = pool.head_dim == 64;   // 64-byte code rows: the 64-byte swizzle
     if (pool.layout == KVC_HND) {
         k.dims[0] = static_cast<cuuint64_t>(pool.head_dim);
         k.dims[1] = static_cast<cuuint64_t>(pool.page_size);
@@ -600,8 +604,8 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
                                          bt_stride, context_lens, num_seqs, max_ctx, q_heads);
     if (st != KVC_OK)
         return st;
-    if (pool.head_dim != 128)
-        return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
+    if (pool.head_dim != 64 && pool.head_dim != 128)
+        return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 64, 128)",
                     pool.head_dim);
     if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
         return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
@@ -656,6 +660,7 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
     l.kv_heads = pool.kv_heads;
     l.page_size = pool.page_size;
     l.hnd = pool.layout == KVC_HND;
+    l.head_dim = pool.head_dim;
     l.chunk = p.chunk;
     l.n_split = p.splits;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));

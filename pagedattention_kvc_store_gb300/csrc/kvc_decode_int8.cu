@@ -45,7 +45,6 @@ namespace {
 
 __device__ uint32_t g_decode_int8_errors;
 
-constexpr int D = 128;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 4;
@@ -53,17 +52,21 @@ constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;   // 16
 constexpr int kMaxGroup = 8;
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int kCodeBytes = kStageKeys * D;                  // K (or V) codes of one stage
-constexpr int kScaleBytes = kStageKeys * 4;
-constexpr int kOffV = kCodeBytes;
-constexpr int kOffKs = 2 * kCodeBytes;
-constexpr int kOffVs = kOffKs + kScaleBytes;
-constexpr int kStageBytes = ((2 * kCodeBytes + 2 * kScaleBytes) + 1023) & ~1023;
-constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kCombineBytes =   // o rows, m, l per warp; weights per row
-    kConsumerWarps * kMaxGroup * (D + 4) * 4 + 3 * kConsumerWarps * kMaxGroup * 4;
-static_assert(kCombineBytes <= kRingBytes, "combine area aliases the ring");
-constexpr size_t kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8;
+// Stage layout for head_dim D (64 or 128): K codes [64 rows][D], V codes, K scales, V scales.
+template <int D>
+struct I8Geom {
+    static constexpr int kCodeBytes = kStageKeys * D;        // K (or V) codes of one stage
+    static constexpr int kScaleBytes = kStageKeys * 4;
+    static constexpr int kOffV = kCodeBytes;
+    static constexpr int kOffKs = 2 * kCodeBytes;
+    static constexpr int kOffVs = kOffKs + kScaleBytes;
+    static constexpr int kStageBytes = ((2 * kCodeBytes + 2 * kScaleBytes) + 1023) & ~1023;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kCombineBytes =   // o rows, m, l per warp; weights per row
+        kConsumerWarps * kMaxGroup * (D + 4) * 4 + 3 * kConsumerWarps * kMaxGroup * 4;
+    static_assert(kCombineBytes <= kRingBytes, "combine area aliases the ring");
+    static constexpr size_t kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8;
+};
 
 struct Args {
     const __nv_bfloat16 *q;
@@ -89,21 +92,24 @@ struct Args {
     int hnd;         // HND codes: page boxes addressed by (offset, page * kv_heads + kv head)
 };
 
-// Quantises one vector held as four bf16 values per lane (lane l: elements 4 l .. 4 l + 3)
-// and writes its codes and scale, with the arithmetic of kvc_store_int8 (TileInfer.jl "KV
-// cache", "INT8 cache": scale = max |x| / 127, codes rounded to nearest and clamped to +-127,
-// both quotients fp32 round-to-nearest), so both give the same bytes.
-__device__ __forceinline__ void quantise_store_row(uint2 x, int8_t *codes, float *scale_out,
-                                                   int lane)
+// Quantises one vector held as E bf16 values per lane (lane l: elements E l .. E l + E - 1;
+// E = head_dim / 32, packed two per word) and writes its codes and scale, with the arithmetic
+// of kvc_store_int8 (TileInfer.jl "KV cache", "INT8 cache": scale = max |x| / 127, codes
+// rounded to nearest and clamped to +-127, both quotients fp32 round-to-nearest), so both give
+// the same bytes.
+template <int E>
+__device__ __forceinline__ void quantise_store_row(const uint32_t (&x)[E / 2], int8_t *codes,
+                                                   float *scale_out, int lane)
 {
-    float f[4];
-    f[0] = __uint_as_float(x.x << 16);
-    f[1] = __uint_as_float(x.x & 0xFFFF0000u);
-    f[2] = __uint_as_float(x.y << 16);
-    f[3] = __uint_as_float(x.y & 0xFFFF0000u);
+    float f[E];
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+        f[2 * i] = __uint_as_float(x[i] << 16);
+        f[2 * i + 1] = __uint_as_float(x[i] & 0xFFFF0000u);
+    }
     float m = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int e = 0; e < E; ++e)
         m = fmaxf(m, fabsf(f[e]));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -111,13 +117,16 @@ __device__ __forceinline__ void quantise_store_row(uint2 x, int8_t *codes, float
     const float scale = __fdiv_rn(m, 127.0f);
     uint32_t packed = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < E; ++e) {
         int c = 0;
         if (scale != 0.0f)
             c = max(-127, min(127, __float2int_rn(__fdiv_rn(f[e], scale))));
         packed |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
     }
-    *reinterpret_cast<uint32_t *>(codes + lane * 4) = packed;
+    if (E == 4)
+        *reinterpret_cast<uint32_t *>(codes + lane * 4) = packed;
+    else
+        *reinterpret_cast<uint16_t *>(codes + lane * 2) = static_cast<uint16_t>(packed);
     if (lane == 0)
         *scale_out = scale;
 }
@@ -135,19 +144,27 @@ __device__ __forceinline__ uint32_t codes_f16x2(uint32_t a, uint32_t b)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Offset of byte `col` of stage row `row` in a 128-byte-swizzled [64][128] code tile.
+// Offset of byte `col` of stage row `row` in a [64][D] code tile: 128-byte rows with the
+// 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)), or 64-byte rows with the 64-byte
+// swizzle (chunk c of row r at c ^ ((r / 2) % 4)).
+template <int D>
 __device__ __forceinline__ uint32_t code_offset(int row, int col)
 {
-    return static_cast<uint32_t>(row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15));
+    const int phase = D == 128 ? (row & 7) : ((row >> 1) & 3);
+    return static_cast<uint32_t>(row * D + ((((col >> 4) ^ phase)) << 4) + (col & 15));
 }
 
-template <bool SPLIT>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 3)
     paged_decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const Args a)
 {
     pdl_wait();
     pdl_trigger();
+    using Geom = I8Geom<D>;
+    constexpr int kOffV = Geom::kOffV, kOffKs = Geom::kOffKs, kOffVs = Geom::kOffVs;
+    constexpr int kStageBytes = Geom::kStageBytes, kRingBytes = Geom::kRingBytes;
+    constexpr int E = D / 32;   // values of one vector per lane (the fused store)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -163,11 +180,16 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int P = a.page_size;
     // the new token's row, requested before anything else so that it is in registers by the
     // time the producer writes it
-    uint2 k_row_new = make_uint2(0u, 0u), v_row_new = k_row_new;
+    uint32_t k_row_new[E / 2] = {}, v_row_new[E / 2] = {};
     if (a.k_new != nullptr && warp == kConsumerWarps) {
-        const size_t src = (static_cast<size_t>(s) * a.kv_heads + kvh) * (D / 4) + lane;
-        k_row_new = __ldg(reinterpret_cast<const uint2 *>(a.k_new) + src);
-        v_row_new = __ldg(reinterpret_cast<const uint2 *>(a.v_new) + src);
+        const size_t src = ((static_cast<size_t>(s) * a.kv_heads + kvh) * 32 + lane) * (E / 2);
+        const uint32_t *kn = reinterpret_cast<const uint32_t *>(a.k_new) + src;
+        const uint32_t *vn = reinterpret_cast<const uint32_t *>(a.v_new) + src;
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) {
+            k_row_new[i] = __ldg(kn + i);
+            v_row_new[i] = __ldg(vn + i);
+        }
     }
     int ctx = a.context_lens[s];
     bool store_new = a.k_new != nullptr && ctx >= 1;
@@ -256,8 +278,10 @@ __global__ void __launch_bounds__(kThreads, 3)
                         (static_cast<size_t>(new_page) * a.kv_heads + kvh) * P + off_new;
                     const size_t row =
                         (a.hnd ? sidx : static_cast<size_t>(slot) * a.kv_heads + kvh) * D;
-                    quantise_store_row(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx, lane);
-                    quantise_store_row(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx, lane);
+                    quantise_store_row<E>(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx,
+                                          lane);
+                    quantise_store_row<E>(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx,
+                                          lane);
                 } else if (lane == 0) {
                     atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrSlotRange);   // skipped, as in the store
                 }
@@ -300,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint32_t qa[D / 16][2];
     float sl2 = a.scale_log2;
     {
-        const __nv_bfloat16 *qrow = a.q + (row0 + r) * D + 32 * t;
+        const __nv_bfloat16 *qrow = a.q + (row0 + r) * D + (D / 4) * t;
         float qv[D / 4];
         float qmax = 0.0f;
 #pragma unroll
@@ -335,17 +359,18 @@ __global__ void __launch_bounds__(kThreads, 3)
     // wrow + r and wrow + 8 + r.  V: the word of dims 4 r .. 4 r + 3 in each of the thread's
     // four positions; dims 32 q + 4 r lie at that offset xor (q << 5), since the swizzle only
     // permutes 16-byte chunks within a row and q moves the chunk index by 2 q.
-    uint32_t k_off[2][2];
+    constexpr int kKChunks = D / 64;   // 16-byte chunks of this thread's K bytes per row
+    uint32_t k_off[2][kKChunks];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        k_off[nt][0] = code_offset(wrow + 8 * nt + r, 32 * t);
-        k_off[nt][1] = code_offset(wrow + 8 * nt + r, 32 * t + 16);
-    }
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < kKChunks; ++h)
+            k_off[nt][h] = code_offset<D>(wrow + 8 * nt + r, (D / 4) * t + 16 * h);
     const int key[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
     uint32_t v_off[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        v_off[i] = kOffV + code_offset(wrow + key[i], 4 * r);
+        v_off[i] = kOffV + code_offset<D>(wrow + key[i], 4 * r);
     bool ok = true;
 
     for (int b = 0; b < n_blocks; ++b) {
@@ -363,11 +388,17 @@ __global__ void __launch_bounds__(kThreads, 3)
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const uint4 lo = *reinterpret_cast<const uint4 *>(stage + k_off[nt][0]);
-                const uint4 hi = *reinterpret_cast<const uint4 *>(stage + k_off[nt][1]);
-                const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                uint32_t w[D / 16];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int h = 0; h < kKChunks; ++h) {
+                    const uint4 c4 = *reinterpret_cast<const uint4 *>(stage + k_off[nt][h]);
+                    w[4 * h] = c4.x;
+                    w[4 * h + 1] = c4.y;
+                    w[4 * h + 2] = c4.z;
+                    w[4 * h + 3] = c4.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
                     uint32_t b0, b1;   // codes 0, 1 and codes 2, 3 of the word
                     codes_word_f16x2(w[kk], b0, b1);
                     mma_f16_16816(sc[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
@@ -411,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             // exactly this thread's (pa0, pa2); thread r reads one word (dims 32 q + 4 r .. + 3)
             // of each of its four positions per q
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < D / 32; ++q) {
                 uint32_t vw[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -507,10 +538,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
 }
 
-template <bool SPLIT>
+template <int D, bool SPLIT>
 cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUtensorMap &tv,
                      cudaStream_t stream)
 {
+    constexpr size_t kSmemBytes = I8Geom<D>::kSmemBytes;
     Args a;
     a.q = static_cast<const __nv_bfloat16 *>(l.q);
     a.k_scales = l.k_scales;
@@ -538,7 +570,7 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.num_slots = l.num_slots;
     a.err = current_error_word();
     a.hnd = l.hnd ? 1 : 0;
-    auto kernel = paged_decode_int8_kernel<SPLIT>;
+    auto kernel = paged_decode_int8_kernel<D, SPLIT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));
     if (err != cudaSuccess)
@@ -554,8 +586,11 @@ cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tma
 {
     if (l.num_seqs == 0)
         return cudaSuccess;
-    return l.n_split > 1 ? launch_t<true>(l, tmap_k, tmap_v, stream)
-                         : launch_t<false>(l, tmap_k, tmap_v, stream);
+    if (l.head_dim == 64)
+        return l.n_split > 1 ? launch_t<64, true>(l, tmap_k, tmap_v, stream)
+                             : launch_t<64, false>(l, tmap_k, tmap_v, stream);
+    return l.n_split > 1 ? launch_t<128, true>(l, tmap_k, tmap_v, stream)
+                         : launch_t<128, false>(l, tmap_k, tmap_v, stream);
 }
 
 cudaError_t read_and_clear_decode_int8_errors(uint32_t *flags)

@@ -56,7 +56,7 @@ struct DecodeLaunch {
     int num_slots = 0;
 };
 
-// Decode over INT8 pages (head_dim 128): codes like a bf16 pool, scales [pages][Hkv][P].
+// Decode over INT8 pages (head_dim 64 or 128): codes like a bf16 pool, scales [pages][Hkv][P].
 struct DecodeInt8Launch {
     const void *q;
     const float *k_scales, *v_scales;
@@ -75,6 +75,7 @@ struct DecodeInt8Launch {
     void *k_codes_w = nullptr, *v_codes_w = nullptr;
     float *k_scales_w = nullptr, *v_scales_w = nullptr;
     int num_slots = 0;
+    int head_dim = 128;
     bool hnd = false;   // codes [pages][Hkv][P][D] (the tensor maps follow it too)
 };
 cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tmap_k,

@@ -68,12 +68,13 @@ def test_batched_decode_int8_store(num_splits, out_dtype):
 
 @pytest.mark.parametrize("P", [16, 32, 64])
 @pytest.mark.parametrize("G", [1, 4, 8])
-def test_edges(P, G):
+@pytest.mark.parametrize("D", [128, 64])
+def test_edges(P, G, D):
     """One-position contexts and newest positions at the first / last offset of a page, with
-    one, three and the planned number of splits."""
+    one, three and the planned number of splits, at head_dim 128 and 64."""
     ctx = np.array([1, 2, P - 1, P, P + 1, 2 * P, 3 * P - 1, 5 * P + 7, 64, 65, 700])
-    case = build_case(900 + P + G, name="int8-decode-store-edges", page_size=P, q_heads=2 * G,
-                      kv_heads=2, head_dim=128, context_lens=lambda rng: ctx,
+    case = build_case(900 + P + G + D, name="int8-decode-store-edges", page_size=P,
+                      q_heads=2 * G, kv_heads=2, head_dim=D, context_lens=lambda rng: ctx,
                       q_lens=lambda c: np.minimum(c, 1))
     for splits in (1, 3, 0):
         out, pools = fused_int8(case, num_splits=splits)

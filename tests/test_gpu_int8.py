@@ -90,16 +90,31 @@ def test_int8_decode_batched_workload_f32_every_sequence():
                            "INT8 batched decode, fp32 output, every sequence")
 
 
-def test_int8_head_dim_64_is_refused():
-    case = config_case(1)   # head_dim 64
-    kc = torch.zeros(case.num_pages, case.page_size, case.kv_heads, 64, dtype=torch.int8,
-                     device="cuda")
-    sc = torch.zeros(case.num_pages, case.kv_heads, case.page_size, device="cuda")
-    out = torch.empty(case.num_seqs, case.q_heads, 64, device="cuda")
-    with pytest.raises(kvc.KvcError, match="UNSUPPORTED"):
-        kvc.kvc_decode_int8(out, bf16_tensor(case.q, "cuda"), kc, kc, sc, sc,
-                            i32_tensor(case.block_table, "cuda"),
-                            i32_tensor(case.context_lens, "cuda"), case.max_ctx)
+@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_int8_decode_head_dim_64(P, G):
+    """head_dim 64 (64-byte code rows, 64-byte swizzle): the store's codes and scales bit-exact
+    and the decode within tolerance, split and whole, fp32 and bf16 output."""
+    case = build_case(720 + P + G, name="int8-d64", page_size=P, q_heads=2 * G, kv_heads=2,
+                      head_dim=64, context_lens=lambda rng: rng.integers(1, 700, size=20),
+                      q_lens=lambda ctx: np.ones_like(ctx))
+    for splits in (1, 3, 0):
+        out, pools = run_int8(case, num_splits=splits)
+        assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
+                               f"INT8 decode D=64 P={P} G={G} splits={splits}")
+    # bf16 output: the attention tolerance plus the output's own rounding (half an ulp),
+    # since scale * code is seldom a bf16 number
+    out, pools = run_int8(case, out_dtype=torch.bfloat16)
+    ref = oracle_int8(case, pools)
+    err = np.abs(out_to_f64(out) - ref)
+    assert (err - 2.0 ** -8 * np.abs(ref)).max() <= 1e-2 and err.mean() <= 1e-3
+
+
+def test_int8_tiny_decode_head_dim_64():
+    """The tiny workload (head_dim 64, contexts 1, 17, 33, 100) on INT8 pages, every sequence."""
+    case = config_case(1)
+    out, pools = run_int8(case, num_splits=2)
+    assert_attention_close(out_to_f64(out), oracle_int8(case, pools), "INT8 tiny decode")
 
 
 def test_int8_single_position_is_its_stored_vector():
