@@ -426,7 +426,7 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
  * kvc_decode_int8 -- kvc_decode over INT8 pages (same arguments and outputs).  Its split-K
  * plan and workspace come from kvc_decode_int8_plan (the automatic split count differs from
  * kvc_decode's: the INT8 kernel keeps more CTAs resident per SM).  head_dim 64 or 128
- * (others: KVC_ERR_UNSUPPORTED); kvc_append_int8 takes head_dim 128 only.
+ * (others: KVC_ERR_UNSUPPORTED).
  */
 kvc_status kvc_decode_int8_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
                                 int32_t max_ctx, int32_t num_splits, int32_t *splits_out,
@@ -470,8 +470,8 @@ kvc_status kvc_decode_int8_store(void *out, int32_t out_dtype, const void *q, co
  * as fp16); the probability times the value scale enters the PV product as fp16 and the
  * softmax denominator sums the unrounded probabilities.  fp16's range limits value scales to
  * 4000 (|v| up to 5.08e5): a larger one sets a kvc_device_errors bit and its results are not
- * valid.  Positions past a sequence's context may hold any codes and NaN scales.  head_dim 128
- * only (others: KVC_ERR_UNSUPPORTED); NHD or HND pools.
+ * valid.  Positions past a sequence's context may hold any codes and NaN scales.  head_dim 64 or
+ * 128 (others: KVC_ERR_UNSUPPORTED); NHD or HND pools.
  */
 kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const void *k_codes,
                            const void *v_codes, const float *k_scales, const float *v_scales,

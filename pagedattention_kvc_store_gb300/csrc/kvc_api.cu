@@ -1184,8 +1184,8 @@ kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const vo
                                          bt_stride, context_lens, num_seqs, max_ctx, q_heads);
     if (st != KVC_OK)
         return st;
-    if (pool.head_dim != 128)
-        return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 128)",
+    if (pool.head_dim != 64 && pool.head_dim != 128)
+        return fail(KVC_ERR_UNSUPPORTED, "INT8 pages: head_dim %d (supported: 64, 128)",
                     pool.head_dim);
     if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
         return fail(KVC_ERR_INVALID_ARG, "scales missing or not 16-byte aligned");
@@ -1220,6 +1220,7 @@ kvc_status kvc_append_int8(void *out, int32_t out_dtype, const void *q, const vo
     l.q_heads = q_heads;
     l.kv_heads = pool.kv_heads;
     l.page_size = pool.page_size;
+    l.head_dim = pool.head_dim;
     l.hnd = pool.layout == KVC_HND;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     cudaError_t err = kvc::launch_append_int8(l, tq, tk, tv, static_cast<cudaStream_t>(stream));

@@ -53,8 +53,6 @@ using append::kM;
 using append::seq_of;
 using append::Walker;
 
-constexpr int D = 128;
-constexpr int kHalves = 2;                 // 64-dim halves of a bf16 row
 constexpr int kThreads = 14 * 32;
 constexpr int kConverters = 4;
 constexpr int kCodeSlots = 7;              // 64-position code half-slots
@@ -64,16 +62,22 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 4.0f;
 constexpr float kMaxValueScale = 4000.0f;   // 2^4 * 4000 < 65504, fp16's largest value
 
-constexpr int kQBytes = kHalves * kM * 128;       // one bf16 query tile
-constexpr int kOpBytes = kHalves * kBN * 128;     // K or V of 128 positions, bf16
-constexpr int kCodeBytes = kHalfRows * D;         // codes of 64 positions
 constexpr int kScaleBytes = 2 * kBN * 4;          // K scales, then V scales, of one block
-constexpr int kOffOp = 2 * kQBytes;               // operand slots: K0, K1, V
-constexpr int kOffCode = kOffOp + 3 * kOpBytes;
-constexpr int kOffScale = kOffCode + kCodeSlots * kCodeBytes;
-constexpr int kOffBar = kOffScale + kScaleSlots * kScaleBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = D;
+
+// Shared memory for head_dim D (64 or 128): query tiles, operand slots, code slots, scales.
+template <int D>
+struct A8Geom {
+    static constexpr int kHalves = D / 64;                 // 64-dim halves of a 16-bit row
+    static constexpr int kQBytes = kHalves * kM * 128;     // one bf16 query tile
+    static constexpr int kOpBytes = kHalves * kBN * 128;   // K or V of 128 positions, 16-bit
+    static constexpr int kCodeBytes = kHalfRows * D;       // codes of 64 positions
+    static constexpr int kOffOp = 2 * kQBytes;             // operand slots: K0, K1, V
+    static constexpr int kOffCode = kOffOp + 3 * kOpBytes;
+    static constexpr int kOffScale = kOffCode + kCodeSlots * kCodeBytes;
+    static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleBytes;
+    static constexpr uint32_t kColS = D;   // TMEM per tile w at 256 w: O [0, D), S [D, D + 128)
+};
 
 enum BarIndex : int {
     kBarCodeFull = 0,
@@ -93,8 +97,12 @@ enum BarIndex : int {
     kBarDrain = kBarPvDone + 2,
     kBarCount
 };
-constexpr size_t kSmemBytes = kOffBar + kBarCount * 8 + 16;
-static_assert(kSmemBytes <= 232448, "shared memory");
+template <int D>
+constexpr size_t a8_smem_bytes()
+{
+    return A8Geom<D>::kOffBar + kBarCount * 8 + 16;
+}
+static_assert(a8_smem_bytes<128>() <= 232448 && a8_smem_bytes<64>() <= 232448, "shared memory");
 
 struct Args {
     void *out;
@@ -124,8 +132,13 @@ __device__ __forceinline__ void block_of_fill(int j, int nb, bool &is_k, int &b)
 // bf16, V codes fp16.  One warp; lane (r0, c) = (lane / 8, lane % 8) converts dims
 // 16 c .. 16 c + 15 of rows 4 k + r0; a row's swizzle phase (row mod 8) is r0 for even k and
 // r0 + 4 for odd k, so each lane's offsets are two constants.
+template <int D>
 __device__ __forceinline__ void convert_rows(const uint8_t *src, uint8_t *dst, int rows,
-                                             bool to_bf16, int lane)
+                                             bool to_bf16, int lane);
+
+template <>
+__device__ __forceinline__ void convert_rows<128>(const uint8_t *src, uint8_t *dst, int rows,
+                                                  bool to_bf16, int lane)
 {
     const int r0 = lane >> 3;
     const int c = lane & 7;
@@ -169,6 +182,52 @@ __device__ __forceinline__ void convert_rows(const uint8_t *src, uint8_t *dst, i
     }
 }
 
+// The same for head_dim 64: code rows of 64 bytes under the 64-byte swizzle (16-byte chunk c
+// of row r at c ^ ((r / 2) % 4)) -> rows of a one-half operand slot [128 rows][64 dims].  Lane
+// (r0, c) = (lane / 4, lane % 4) converts dims 16 c .. 16 c + 15 of rows 8 k + r0 (output
+// chunks 2 c and 2 c + 1 of the row, 128-byte swizzle); both loads of a step issue before the
+// stores.
+template <>
+__device__ __forceinline__ void convert_rows<64>(const uint8_t *src, uint8_t *dst, int rows,
+                                                 bool to_bf16, int lane)
+{
+    const int r0 = lane >> 2;
+    const int c = lane & 3;
+#pragma unroll 1
+    for (int s4 = 0; s4 < rows; s4 += 16) {
+        uint4 cw[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int row = s4 + 8 * k + r0;
+            cw[k] = *reinterpret_cast<const uint4 *>(src + row * 64 +
+                                                     ((c ^ ((row >> 1) & 3)) << 4));
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int row = s4 + 8 * k + r0;
+            uint32_t f[8];
+            if (to_bf16) {
+                codes_word_bf16x2(cw[k].x, f[0], f[1]);
+                codes_word_bf16x2(cw[k].y, f[2], f[3]);
+                codes_word_bf16x2(cw[k].z, f[4], f[5]);
+                codes_word_bf16x2(cw[k].w, f[6], f[7]);
+            } else {
+                codes_word_f16x2(cw[k].x, f[0], f[1]);
+                codes_word_f16x2(cw[k].y, f[2], f[3]);
+                codes_word_f16x2(cw[k].z, f[4], f[5]);
+                codes_word_f16x2(cw[k].w, f[6], f[7]);
+            }
+            uint8_t *out = dst + row * 128;
+            const int sw = row & 7;
+            *reinterpret_cast<uint4 *>(out + (((2 * c) ^ sw) << 4)) =
+                make_uint4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<uint4 *>(out + (((2 * c + 1) ^ sw) << 4)) =
+                make_uint4(f[4], f[5], f[6], f[7]);
+        }
+    }
+}
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_append_int8_kernel(const __grid_constant__ CUtensorMap tmap_q,
                              const __grid_constant__ CUtensorMap tmap_k,
@@ -176,6 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     pdl_wait();
     pdl_trigger();
+    using Geom = A8Geom<D>;
+    constexpr int kHalves = Geom::kHalves, kQBytes = Geom::kQBytes, kOpBytes = Geom::kOpBytes;
+    constexpr int kCodeBytes = Geom::kCodeBytes, kOffOp = Geom::kOffOp;
+    constexpr int kOffCode = Geom::kOffCode, kOffScale = Geom::kOffScale;
+    constexpr int kOffBar = Geom::kOffBar;
+    constexpr uint32_t kColS = Geom::kColS;
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_addr(smem) & 1023u) != 0) {
         if (threadIdx.x == 0)
@@ -406,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cols = (b + 1 == nb) ? last_cols : kBN;
                 const int r_lo = h * kHalfRows + sub * (kHalfRows / 2);
                 const int rows = min(max(cols - r_lo, 0), kHalfRows / 2);
-                convert_rows(code_slot(m) + sub * (kHalfRows / 2) * 128, dst + r_lo * 128, rows,
-                             is_k, lane);
+                convert_rows<D>(code_slot(m) + sub * (kHalfRows / 2) * D, dst + r_lo * 128,
+                                rows, is_k, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -820,13 +885,15 @@ cudaError_t launch_append_int8(const AppendInt8Launch &l, const CUtensorMap &tma
     a.scale_log2 = l.scale * kLog2e;
     a.err = current_error_word();
     a.hnd = l.hnd ? 1 : 0;
-    cudaError_t err = cudaFuncSetAttribute(paged_append_int8_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemBytes));
+    const bool d64 = l.head_dim == 64;
+    auto kernel = d64 ? paged_append_int8_kernel<64> : paged_append_int8_kernel<128>;
+    const size_t smem = d64 ? a8_smem_bytes<64>() : a8_smem_bytes<128>();
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
     if (err != cudaSuccess)
         return err;
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
-    return launch_pdl(paged_append_int8_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream,
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, stream,
                       tmap_q, tmap_k, tmap_v, a);
 }
 

@@ -118,7 +118,7 @@ struct AppendLaunch {
     void *k_pool_w = nullptr, *v_pool_w = nullptr;
 };
 
-// kvc_append_int8: AppendLaunch over INT8 pages (head_dim 128, NHD) plus the scale arrays.
+// kvc_append_int8: AppendLaunch over INT8 pages (head_dim 64 or 128) plus the scale arrays.
 struct AppendInt8Launch {
     void *out;
     int out_f32;
@@ -129,6 +129,7 @@ struct AppendInt8Launch {
     const int32_t *context_lens;
     int num_seqs, num_tokens, max_q_len, q_heads, kv_heads, page_size;
     float scale;
+    int head_dim = 128;
     bool hnd = false;   // codes [pages][Hkv][P][D] (the tensor maps follow it too)
 };
 

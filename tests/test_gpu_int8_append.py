@@ -85,11 +85,14 @@ class Int8AppendRun:
 
 @pytest.mark.parametrize("P", [16, 32, 64])
 @pytest.mark.parametrize("G", [1, 4, 8])
-def test_int8_append_ragged(P, G):
+@pytest.mark.parametrize("D", [128, 64])
+def test_int8_append_ragged(P, G, D):
     """Ragged contexts and chunk lengths: several 128-position blocks, several tile pairs
-    per (sequence, kv head), a ragged last block and a ragged last tile."""
-    case = build_case(500 + P + G, name="int8-append", page_size=P, q_heads=2 * G, kv_heads=2,
-                      head_dim=128, context_lens=lambda rng: rng.integers(1, 700, size=20),
+    per (sequence, kv head), a ragged last block and a ragged last tile; head_dim 128 and 64
+    (64-byte code rows, one-half operands)."""
+    case = build_case(500 + P + G + D, name="int8-append", page_size=P, q_heads=2 * G,
+                      kv_heads=2, head_dim=D,
+                      context_lens=lambda rng: rng.integers(1, 700, size=20),
                       q_lens=lambda ctx: np.minimum(ctx, 1 + (ctx * 7) % 181))
     run = Int8AppendRun(case)
     ref, rows = run.oracle()
@@ -162,15 +165,16 @@ def test_int8_append_single_position_is_its_stored_vector():
             np.testing.assert_allclose(got[s, h], want, rtol=2.0 ** -10, atol=1e-6)
 
 
-def test_int8_append_refuses_head_dim_64():
-    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
-    out = torch.empty(1, 2, 64, device="cuda")
-    kc = torch.zeros(4, 16, 1, 64, dtype=torch.int8, device="cuda")
-    sc = torch.zeros(4, 1, 16, device="cuda")
-    one = torch.ones(1, 1, dtype=torch.int32, device="cuda")
-    ind = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
-    with pytest.raises(kvc.KvcError, match="UNSUPPORTED"):
-        kvc.kvc_append_int8(out, q, kc, kc, sc, sc, one, ind, one[0], 1, 1)
+def test_int8_append_head_dim_64_edges():
+    """head_dim 64: no prefix, one-token chunks, chunks ending on block and tile boundaries,
+    a long chunk, and one-position contexts (the output is the stored vector's value)."""
+    ctx = np.array([1, 2, 17, 64, 65, 128, 129, 256, 300, 5, 640, 1000, 1])
+    qlen = np.array([1, 2, 17, 64, 1, 128, 1, 64, 300, 5, 1, 512, 1])
+    case = build_case(82, name="int8-edges-d64", page_size=16, q_heads=8, kv_heads=2,
+                      head_dim=64, context_lens=lambda rng: ctx, q_lens=lambda c: qlen)
+    run = Int8AppendRun(case)
+    ref, rows = run.oracle()
+    assert_attention_close(run.attend()[rows], ref, "INT8 append edges D=64")
 
 
 def test_int8_append_flags_a_value_scale_beyond_fp16_range():
