@@ -501,7 +501,7 @@ def run_decode_legs(torch, kvc, args, dev, stream, flush, peaks, rank):
             "us": round(t8 * 1e3, 1), "bytes": b8, "gbs": round(b8 / (t8 / 1e3) / 1e9, 1),
             "frac_of_hbm": round(b8 / (t8 / 1e3) / 1e9 / peaks["hbm"], 4),
             "bf16_us": round(t16 * 1e3, 1), "bf16_bytes": b16,
-            "speedup_vs_bf16": round(t16 / t8, 3), "splits": splits,
+            "speedup_vs_bf16": round(t16 / t8, 3), "ctas": splits,
             "gpu_launches_per_step": 2 if splits > 1 else 1,
             "traffic_decode_int8_kernel": traffic_from_profile("decode_int8_batched"),
             "step_store_decode_us": {"fused": round(t8_fused * 1e3, 1),

@@ -423,10 +423,18 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
                           const int32_t *slot_mapping, int32_t num_tokens, void *stream);
 
 /*
- * kvc_decode_int8 -- kvc_decode over INT8 pages (same arguments and outputs).  Its split-K
- * plan and workspace come from kvc_decode_int8_plan (the automatic split count differs from
- * kvc_decode's: the INT8 kernel keeps more CTAs resident per SM).  head_dim 64 or 128
- * (others: KVC_ERR_UNSUPPORTED).
+ * kvc_decode_int8 -- kvc_decode over INT8 pages (same arguments and outputs).  Its work plan
+ * differs from kvc_decode's split-K: for each kv head, the positions of all sequences (in
+ * 64-position blocks, sequence after sequence) are cut into equal runs, one CTA each, so that
+ * every CTA has the same work however the context lengths are spread; a sequence covered by
+ * several runs has its partial results merged (log-sum-exp) by a second launch.
+ * kvc_decode_int8_plan gives the plan for num_splits: 0 = one wave of resident CTAs (the
+ * default); 1 = one CTA per (sequence, kv head), no workspace and no merge; n > 1 = n runs
+ * per sequence (num_seqs * n per kv head).  A plan never has more runs per kv head than
+ * num_seqs * ceil(max_ctx / 64) (one per block), and at run time only as many runs as the
+ * actual blocks are used.  splits_out = the number of CTAs, chunk_out = 64 (the block);
+ * workspace_bytes_out = the workspace the call needs (0 for num_splits = 1).  head_dim 64 or
+ * 128 (others: KVC_ERR_UNSUPPORTED).
  */
 kvc_status kvc_decode_int8_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc pool,
                                 int32_t max_ctx, int32_t num_splits, int32_t *splits_out,

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdarg.h>
+#include <algorithm>
 #include <stdio.h>
 
 #include <mutex>
@@ -78,7 +79,7 @@ int device_sm_count()
     return 152;
 }
 
-constexpr int kInt8PlanTarget = 12;   // CTAs per SM the INT8 decode's automatic splits aim at
+constexpr int kInt8Resident = 3;   // INT8 decode CTAs resident per SM (its automatic CTA count)
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
@@ -132,6 +133,45 @@ Plan make_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool, int
         p.lse_offset = static_cast<size_t>(round_up(static_cast<int64_t>(o_bytes), 256));
         p.ws_bytes = p.lse_offset + rows * p.splits * sizeof(float);
     }
+    return p;
+}
+
+// INT8 decode plan.  num_splits = 1: one CTA per (sequence, kv head) unit, no workspace.
+// Otherwise each kv head's positions, in 64-position blocks over all sequences, are cut into
+// `runs` equal runs, one CTA per (run, kv head): one wave of resident CTAs (num_splits = 0) or
+// num_splits runs per sequence, at most one per block.  Workspace: partial rows and
+// log-sum-exps of kv_heads * (num_seqs + runs) slots, and (first slot, piece count) per unit.
+struct Int8Plan {
+    int ctas;
+    bool per_unit;
+    size_t ws_bytes, lse_offset, info_offset;
+};
+
+Int8Plan make_int8_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool,
+                        int32_t max_ctx, int32_t requested)
+{
+    Int8Plan p{};
+    const int64_t seqs = num_seqs > 0 ? num_seqs : 1;
+    const int64_t units = seqs * pool.kv_heads;
+    if (requested == 1) {
+        p.per_unit = true;
+        p.ctas = static_cast<int>(units);
+        return p;
+    }
+    const int64_t blocks = seqs * ceil_div(max_ctx > 0 ? max_ctx : 1, kvc::kStageKeys);
+    int64_t runs = requested <= 0
+                       ? kInt8Resident * static_cast<int64_t>(device_sm_count()) / pool.kv_heads
+                       : static_cast<int64_t>(requested) * seqs;
+    runs = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(runs, blocks),
+                                                  (int64_t(1) << 30) / pool.kv_heads));
+    p.ctas = static_cast<int>(runs * pool.kv_heads);
+    const int64_t group = q_heads / pool.kv_heads;
+    const int64_t slots = pool.kv_heads * (seqs + runs);
+    const int64_t o_bytes = slots * group * pool.head_dim * 4;
+    p.lse_offset = static_cast<size_t>(round_up(o_bytes, 256));
+    p.info_offset = static_cast<size_t>(
+        round_up(static_cast<int64_t>(p.lse_offset) + slots * group * 4, 256));
+    p.ws_bytes = p.info_offset + static_cast<size_t>(units) * 8;
     return p;
 }
 
@@ -554,11 +594,13 @@ kvc_status kvc_decode_int8_plan(int32_t num_seqs, int32_t q_heads, kvc_pool_desc
         return st;
     if (num_seqs < 0 || q_heads <= 0 || max_ctx < 0 || num_splits < 0)
         return fail(KVC_ERR_INVALID_ARG, "negative size or non-positive q_heads");
-    const Plan p = make_plan(num_seqs, q_heads, pool, max_ctx, num_splits, kInt8PlanTarget);
+    if ((st = check_group(pool, q_heads)) != KVC_OK)
+        return st;
+    const Int8Plan p = make_int8_plan(num_seqs, q_heads, pool, max_ctx, num_splits);
     if (splits_out)
-        *splits_out = p.splits;
+        *splits_out = p.ctas;
     if (chunk_out)
-        *chunk_out = p.chunk;
+        *chunk_out = kvc::kStageKeys;
     if (workspace_bytes_out)
         *workspace_bytes_out = p.ws_bytes;
     return ok();
@@ -613,8 +655,8 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
         return fail(KVC_ERR_INVALID_ARG, "num_splits %d", num_splits);
     if (num_seqs == 0)
         return ok();
-    const Plan p = make_plan(num_seqs, q_heads, pool, max_ctx, num_splits, kInt8PlanTarget);
-    if (p.splits > 1) {
+    const Int8Plan p = make_int8_plan(num_seqs, q_heads, pool, max_ctx, num_splits);
+    if (!p.per_unit) {
         if (workspace == nullptr || workspace_bytes < p.ws_bytes)
             return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given",
                         p.ws_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
@@ -648,10 +690,11 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
     l.v_scales = v_scales;
     l.out = out;
     l.out_f32 = out_dtype == KVC_F32;
-    l.part_o = static_cast<float *>(workspace);
-    l.part_lse = p.splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                          p.lse_offset)
-                              : nullptr;
+    if (!p.per_unit) {
+        l.part_o = static_cast<float *>(workspace);
+        l.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.lse_offset);
+        l.unit_info = static_cast<char *>(workspace) + p.info_offset;
+    }
     l.block_table = block_table;
     l.bt_stride = bt_stride;
     l.context_lens = context_lens;
@@ -661,8 +704,8 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
     l.page_size = pool.page_size;
     l.hnd = pool.layout == KVC_HND;
     l.head_dim = pool.head_dim;
-    l.chunk = p.chunk;
-    l.n_split = p.splits;
+    l.n_ctas = p.ctas;
+    l.per_unit = p.per_unit;
     l.scale = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     if (fused) {
         l.k_new = k_new;
@@ -677,12 +720,6 @@ kvc_status decode_int8_impl(void *out, int32_t out_dtype, const void *q, const v
     cudaError_t err = kvc::launch_decode_int8(l, tk, tv, s);
     if (err != cudaSuccess)
         return cuda_fail(err, "decode_int8 launch");
-    if (p.splits > 1) {
-        err = kvc::launch_merge(out, l.out_f32, l.part_o, l.part_lse, num_seqs * q_heads,
-                                p.splits, pool.head_dim, nullptr, s);
-        if (err != cudaSuccess)
-            return cuda_fail(err, "merge launch");
-    }
     return ok();
 }
 

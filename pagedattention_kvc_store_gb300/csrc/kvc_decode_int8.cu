@@ -8,32 +8,55 @@
 // |code| <= 127) for the tensor cores; the scales stay outside the products.  fp16 rather than
 // bf16 because two codes become an exact fp16 pair in three integer/half operations: bytes
 // b placed under the exponent 0x64 read as 1024 + b, and the code is b - 128; the query is
-// converted to fp16 once (scaled by a power of two when it would overflow fp16), and the
-// probabilities (at most 1) times the value scales enter the PV product as fp16.
+// converted to fp16 once per piece (scaled by a power of two when it would overflow fp16), and
+// the probabilities (at most 1) times the value scales enter the PV product as fp16.
 //
-// Layout: codes [num_pages * P][Hkv][128] int8 like the bf16 pools (128 bytes per vector);
-// scales [num_pages][Hkv][P] fp32, so the P scales of one (page, kv head) are one contiguous
-// run that a single bulk copy brings in.
+// Layout: codes [num_pages * P][Hkv][D] int8 like the bf16 pools (D bytes per vector), or
+// [num_pages][Hkv][P][D] (HND); scales [num_pages][Hkv][P] fp32, so the P scales of one (page,
+// kv head) are one contiguous run that a single bulk copy brings in.
 //
-// Kernel design (head_dim 128): one CTA per (split, kv head, sequence), 4 consumer warps and a
-// producer warp, three CTAs per SM.  The producer streams 64-position stages -- per page one TMA
-// box of K codes, one of V codes (128-byte swizzle) and one bulk copy each of the K and V
-// scales, issued by parallel lanes -- through a 4-deep ring.  Consumer warp w takes positions
-// 16 w .. 16 w + 15 of each stage:
-//   S = Q K^T on mma.sync m16n8k16 (fp16; the G query heads padded to 16 rows).  The order
-//   in which head_dim is contracted is free, so thread (., t) takes dims 32 t + 4 kk .. + 3
-//   for k-step kk: its K codes for a position are 32 contiguous bytes (two 16-byte loads) and
-//   its Q pairs two contiguous pairs;
-//   O^T += V^T (P * v_scale)^T with M = 16 dims and N = 8 query rows: the probabilities a
-//   thread holds from the S fragment are exactly its B fragment, half as many MMAs and
-//   accumulators as O = P V with rows padded to 16; the dims of tile dt are permuted so that
-//   thread row r reads dims 32 q + 4 r .. + 3 (q = 0..3), one 4-byte word per position and q,
-//   and the accumulators are put back in dim order when the warps combine.
+// Work partition.  The consumer warps convert every code they read, so a CTA is bound by its
+// own instruction stream, not by HBM: an SM runs at the pace of its three resident CTAs, and
+// every microsecond one of them spends starting up (page ids, first copies) or idle at the end
+// of a ragged grid is lost.  So for each kv head the positions of all sequences, in
+// 64-position blocks (sequence-major), are cut into R equal runs, one per CTA (CTA = run * Hkv
+// + kv head, R * Hkv = one wave of resident CTAs), and each CTA streams its run without a
+// break: the pieces of the sequences it covers follow one another through the same ring.  The
+// runs of all kv heads have the same bounds, so the CTAs that read one sequence's positions
+// for its kv heads start together and stay in step (the kv heads of a position share its NHD
+// rows: 8% faster than unaligned runs).  A piece that is a whole unit (sequence, kv head)
+// writes the output rows; the others write a partial (rows normalised by their own sum, and
+// the log-sum-exp) to slot h (S + R) + s + run of the workspace -- distinct for every piece,
+// consecutive for one unit's pieces -- and the unit's first piece records (first slot, piece
+// count) for the merge (merge_flat_kernel).  With num_splits = 1 the kernel instead runs one
+// CTA per unit (no workspace, no merge).  The producer alone walks the runs; it hands each
+// piece (its sequence, blocks and context) to the consumers in shared memory with the query
+// rows, so all warps of a CTA take the same path whatever the context lengths.
+//
+// CTA: 4 consumer warps and a producer warp, three CTAs per SM.  The producer loads each
+// piece's query rows into shared memory and streams 64-position stages -- per page one TMA box
+// of K codes, one of V codes (128-byte swizzle at D = 128, 64-byte at D = 64) and one bulk copy
+// each of the K and V scales, issued by parallel lanes -- through a 4-deep ring.  Consumer warp
+// w takes positions 16 w .. 16 w + 15 of each stage:
+//   S^T = K Q^T on mma.sync m16n8k16 (fp16): the warp's 16 positions are the M rows and the G
+//   query heads the N columns (padded to 8).  The order in which head_dim is contracted is
+//   free, so thread (r, t) takes dims (D / 4) t + 4 kk .. + 3 for k-step kk: its K codes of a
+//   position are D / 4 contiguous bytes, one word per k-step, and its Q pairs are two
+//   contiguous pairs;
+//   O^T += V^T (P * v_scale)^T with M = 16 dims and N = 8 query heads.  A thread's scores are
+//   positions r and r + 8 of heads 2t and 2t + 1; one 8x8 transpose (movmatrix) per half
+//   turns the fp16 probabilities into the B fragment of this product (positions 2t, 2t + 1 /
+//   8 + 2t, 9 + 2t of head r).  The dims of tile dt are permuted so that thread row r reads
+//   dims 32 q + 4 r .. + 3 (q = 0 .. D / 32 - 1), one 4-byte word per position and q, and the
+//   accumulators are put back in dim order when the warps combine.  The O^T rows a thread
+//   accumulates are its own score heads 2t, 2t + 1, so the rescale needs no exchange.
 // Online softmax in base 2, masked positions excluded before the exponential and their
-// probabilities set to 0 by selection (a scale left in an unused slot may be NaN).
-// Fused store (kvc_decode_int8_store): the producer of the CTA whose chunk ends at a
-// sequence's newest position quantises that token's K/V row with the INT8 store's arithmetic
-// and writes its codes and scale before the copies of that page.
+// probabilities set to 0 by selection (a scale left in an unused slot may be NaN).  At the end
+// of a piece the 4 warps combine in the buffer of the piece's last stage, which the consumers
+// release only afterwards, while the producer already streams the next piece.
+// Fused store (kvc_decode_int8_store): the producer of the CTA whose piece ends at a unit's
+// newest position quantises that token's K/V row with the INT8 store's arithmetic and writes
+// its codes and scale before the copies of that page.
 #include <math.h>
 
 #include "kvc_device.cuh"
@@ -51,8 +74,10 @@ constexpr int kStages = 4;
 constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;   // 16
 constexpr int kMaxGroup = 8;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Stage layout for head_dim D (64 or 128): K codes [64 rows][D], V codes, K scales, V scales.
+// The query rows of the current piece (bf16 [G][D]) and the barriers follow the ring.
 template <int D>
 struct I8Geom {
     static constexpr int kCodeBytes = kStageKeys * D;        // K (or V) codes of one stage
@@ -62,10 +87,14 @@ struct I8Geom {
     static constexpr int kOffVs = kOffKs + kScaleBytes;
     static constexpr int kStageBytes = ((2 * kCodeBytes + 2 * kScaleBytes) + 1023) & ~1023;
     static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kQBytes = kMaxGroup * D * 2;
     static constexpr int kCombineBytes =   // o rows, m, l per warp; weights per row
         kConsumerWarps * kMaxGroup * (D + 4) * 4 + 3 * kConsumerWarps * kMaxGroup * 4;
-    static_assert(kCombineBytes <= kRingBytes, "combine area aliases the ring");
-    static constexpr size_t kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8;
+    static_assert(kCombineBytes <= kStageBytes, "combine area is one stage buffer");
+    static constexpr int kBarBytes = (2 * kStages + 2) * 8;
+    static constexpr int kScratchBytes = 128;   // scan sums, run start, abort flag, piece
+    static constexpr size_t kSmemBytes =
+        1024 + kRingBytes + kQBytes + kBarBytes + kScratchBytes;
 };
 
 struct Args {
@@ -73,16 +102,17 @@ struct Args {
     const float *k_scales, *v_scales;
     void *out;
     int out_f32;
-    float *part_o;
-    float *part_lse;
+    float *part_o;       // [U + N][G][D] partials of the pieces that are not whole units
+    float *part_lse;     // [U + N][G]
+    int2 *unit_info;     // [U]: (first slot, piece count) of each non-empty unit
     const int32_t *block_table;
     int bt_stride;
     const int32_t *context_lens;
-    int q_heads, kv_heads, group, page_size;
-    int chunk, n_split;
+    int num_seqs, q_heads, kv_heads, group, page_size;
+    int per_unit;        // 1: one CTA per unit (blockIdx.x = unit), no partials
     float scale_log2;
     // kvc_decode_int8_store: sequence s's new key and value (bf16 [S][Hkv][D]), quantised and
-    // written to the code and scale pools (num_slots slots) by the CTA whose chunk ends at the
+    // written to the code and scale pools (num_slots slots) by the CTA whose piece ends at the
     // newest position, before that CTA's copies of the page; null otherwise.
     const __nv_bfloat16 *k_new, *v_new;
     int8_t *k_codes_w, *v_codes_w;
@@ -91,6 +121,94 @@ struct Args {
     uint32_t *err;   // the caller's device error word, or null (this file's own word)
     int hnd;         // HND codes: page boxes addressed by (offset, page * kv_heads + kv head)
 };
+
+__device__ __forceinline__ uint32_t *err_word(const Args &a)
+{
+    return a.err ? a.err : &g_decode_int8_errors;
+}
+
+// A sequence's context as the kernel reads it: clamped to [0, bt_stride * P] (a longer one is
+// flagged by CTA 0 and attends over the positions its block-table row holds, storing nothing).
+__device__ __forceinline__ int clamped_ctx(const Args &a, int s, bool *over = nullptr)
+{
+    const int raw = a.context_lens[s];
+    const int cap = a.bt_stride * a.page_size;
+    if (over)
+        *over = raw > cap;
+    return max(0, min(raw, cap));
+}
+
+__device__ __forceinline__ int blocks_of(int ctx) { return (ctx + kStageKeys - 1) / kStageKeys; }
+
+// A sequence's clamped context read by lane 0 of the calling warp and shared with its lanes
+// (the producer's walk takes every decision once for the whole warp).
+__device__ __forceinline__ int ctx_for_warp(const Args &a, int s, bool &over)
+{
+    int raw = 0;
+    if ((threadIdx.x & 31) == 0)
+        raw = a.context_lens[s];
+    raw = __shfl_sync(0xffffffffu, raw, 0);
+    const int cap = a.bt_stride * a.page_size;
+    over = raw > cap;
+    return max(0, min(raw, cap));
+}
+
+// Position of the producer's walk in its kv head's block order (sequence-major, then block).
+struct Cursor {
+    int s, blk;        // current sequence and its next block
+    int ctx, nb;       // the sequence's (clamped) context and block count
+    bool over;         // the context was past the block-table row
+    long long g;       // index of the next block in the kv head's order
+};
+
+// Loads the context of cursor sequence w.s, moving past sequences with no positions; false
+// when none is left (the contexts changed under the launch).
+__device__ __forceinline__ bool cursor_load(Cursor &w, const Args &a)
+{
+    for (; w.s < a.num_seqs; ++w.s) {
+        w.ctx = ctx_for_warp(a, w.s, w.over);
+        w.nb = blocks_of(w.ctx);
+        if (w.nb > 0)
+            return true;
+    }
+    return false;
+}
+
+// After a piece of n blocks: the next sequence when the piece ended this one; false when the
+// walk cannot go on.
+__device__ __forceinline__ bool cursor_advance(Cursor &w, const Args &a, int n, long long g1)
+{
+    w.g += n;
+    w.blk += n;
+    if (w.blk == w.nb) {
+        w.blk = 0;
+        ++w.s;
+        if (w.g < g1)
+            return cursor_load(w, a);
+    }
+    return true;
+}
+
+// One piece as the producer hands it to the consumers (with the query rows): sequence s of the
+// CTA's kv head, blocks blk0 .. blk0 + nblk - 1 of its nb, its context, and the index of its
+// last block in the kv head's order; nblk = 0 ends the CTA's work.
+struct PieceDesc {
+    int s, blk0, nblk, ctx, nb;
+    long long g_last;
+};
+
+// Run c of n: blocks [floor(c T / n), floor((c + 1) T / n)) of a kv head's T.
+__device__ __forceinline__ long long run_start(long long c, long long total, long long n)
+{
+    return static_cast<long long>((static_cast<unsigned __int128>(c) * total) / n);
+}
+
+// The run that holds block g: the largest c with run_start(c) <= g.
+__device__ __forceinline__ long long run_of(long long g, long long total, long long n)
+{
+    return static_cast<long long>(
+        (static_cast<unsigned __int128>(g + 1) * n - 1) / static_cast<unsigned __int128>(total));
+}
 
 // Quantises one vector held as E bf16 values per lane (lane l: elements E l .. E l + E - 1;
 // E = head_dim / 32, packed two per word) and writes its codes and scale, with the arithmetic
@@ -154,7 +272,8 @@ __device__ __forceinline__ uint32_t code_offset(int row, int col)
     return static_cast<uint32_t>(row * D + ((((col >> 4) ^ phase)) << 4) + (col & 15));
 }
 
-template <int D, bool SPLIT>
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 3)
     paged_decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const Args a)
@@ -168,194 +287,279 @@ __global__ void __launch_bounds__(kThreads, 3)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRingBytes);
+    __nv_bfloat16 *qbuf = reinterpret_cast<__nv_bfloat16 *>(smem + kRingBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRingBytes + Geom::kQBytes);
     uint64_t *empty = full + kStages;
+    uint64_t *q_full = empty + kStages;
+    uint64_t *q_empty = q_full + 1;
+    long long *scratch = reinterpret_cast<long long *>(q_empty + 1);   // [0] s0, [1] base, [2..] sums
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(scratch + 8);
 
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int s = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.group;
     const int P = a.page_size;
-    // the new token's row, requested before anything else so that it is in registers by the
-    // time the producer writes it
-    uint32_t k_row_new[E / 2] = {}, v_row_new[E / 2] = {};
-    if (a.k_new != nullptr && warp == kConsumerWarps) {
-        const size_t src = ((static_cast<size_t>(s) * a.kv_heads + kvh) * 32 + lane) * (E / 2);
-        const uint32_t *kn = reinterpret_cast<const uint32_t *>(a.k_new) + src;
-        const uint32_t *vn = reinterpret_cast<const uint32_t *>(a.v_new) + src;
-#pragma unroll
-        for (int i = 0; i < E / 2; ++i) {
-            k_row_new[i] = __ldg(kn + i);
-            v_row_new[i] = __ldg(vn + i);
-        }
-    }
-    int ctx = a.context_lens[s];
-    bool store_new = a.k_new != nullptr && ctx >= 1;
-    if (ctx > a.bt_stride * P) {
-        if (threadIdx.x == 0 && split == 0)
-            atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrContextRange);
-        ctx = a.bt_stride * P;
-        store_new = false;   // no slot for the new token: stored nowhere
-    }
-    const int k_begin = split * a.chunk;
-    const int k_end = min(ctx, k_begin + a.chunk);
-    const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
+    const int Hkv = a.kv_heads;
+    // CTA = run * Hkv + kv head: the runs of every kv head have the same bounds, so the CTAs
+    // reading one sequence's pages for its kv heads start together and stay in step (the kv
+    // heads of a position share its NHD rows)
+    const int kvh = static_cast<int>(blockIdx.x % Hkv);
+    const long long run = blockIdx.x / Hkv;
+    const long long n_run_ctas = gridDim.x / Hkv;
 
-    if (k_begin >= k_end) {
-        if (SPLIT) {
-            if (threadIdx.x < G)
-                a.part_lse[(row0 + threadIdx.x) * a.n_split + split] = -INFINITY;
-        } else {
-            for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-                store_out(a.out, a.out_f32, row0 * D + i, 0.0f);
-        }
-        return;
-    }
-
-    const int n_blocks = (k_end - k_begin + kStageKeys - 1) / kStageKeys;
-    const int first_page = k_begin / P;
-    const int n_pages = (k_end - k_begin + P - 1) / P;
-
+    volatile PieceDesc *desc = reinterpret_cast<volatile PieceDesc *>(scratch + 10);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
         }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, kConsumerWarps);
+        *abort_flag = 0;
+        scratch[0] = -1;
         fence_mbar_init();
     }
-    __syncthreads();
+
+    // ---- this CTA's run of blocks [g0, g1) and where it starts: sequence scratch[0], whose
+    // first block has global index scratch[1] (one unit: its context scratch[1] and blocks
+    // scratch[2]).  Every decision below reads shared memory, so the whole CTA takes it alike.
+    long long g0 = 0, g1 = 0, total = 0;   // per kv head
+    long long n_runs = n_run_ctas;          // runs of a kv head: at most one per block
+    if (a.per_unit) {
+        // one unit per CTA, numbered on its own: blocks [0, nb)
+        if (threadIdx.x == 0) {
+            const int s0 = static_cast<int>(run);
+            bool over;
+            const int ctx = clamped_ctx(a, s0, &over);
+            if (over && kvh == 0)
+                atomicOr(err_word(a), kErrContextRange);
+            scratch[0] = s0;
+            scratch[1] = ctx;
+            scratch[2] = blocks_of(ctx);
+            scratch[3] = over;
+        }
+        __syncthreads();
+        total = scratch[2];
+        g1 = total;
+        if (total == 0) {   // no positions: the rows are 0
+            const size_t row0 = static_cast<size_t>(blockIdx.x) * G;
+            for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+                store_out(a.out, a.out_f32, row0 * D + i, 0.0f);
+            return;
+        }
+    } else {
+        // block counts of all sequences, summed by a block-wide scan (every CTA computes the
+        // same total, a kv head's; CTA 0 flags contexts past their block-table rows)
+        const int S = a.num_seqs;
+        const int per = (S + kThreads - 1) / kThreads;
+        const int lo = min(S, static_cast<int>(threadIdx.x) * per);
+        const int hi = min(S, lo + per);
+        long long mine = 0;
+        for (int s = lo; s < hi; ++s) {
+            bool over;
+            mine += blocks_of(clamped_ctx(a, s, &over));
+            if (over && blockIdx.x == 0)
+                atomicOr(err_word(a), kErrContextRange);
+        }
+        long long incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off)
+                incl += v;
+        }
+        if (lane == 31)
+            scratch[2 + warp] = incl;
+        __syncthreads();
+        long long before = incl - mine, sum = 0;
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i) {
+            const long long t = scratch[2 + i];
+            if (i < warp)
+                before += t;
+            sum += t;
+        }
+        total = sum;
+        n_runs = min(n_run_ctas, total);
+        if (run < n_runs) {
+            g0 = run_start(run, total, n_runs);
+            g1 = run_start(run + 1, total, n_runs);
+        }
+        if (g0 < g1 && before <= g0 && g0 < before + mine) {
+            long long acc = before;
+            for (int s = lo; s < hi; ++s) {
+                const long long nb = blocks_of(clamped_ctx(a, s));
+                if (g0 < acc + nb) {
+                    scratch[0] = s;
+                    scratch[1] = acc;
+                    break;
+                }
+                acc += nb;
+            }
+        }
+        __syncthreads();
+        if (g0 >= g1 || scratch[0] < 0)
+            return;   // an empty run (fewer blocks than CTAs)
+    }
 
     if (warp == kConsumerWarps) {
         // ------------------------ producer (whole warp) -------------------------------------
-        const int32_t *bt_row =
-            a.block_table + static_cast<size_t>(s) * a.bt_stride + first_page;
         if (lane == 0) {
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
         }
         const uint64_t policy = l2_policy_evict_first();
-        int cached_base = -32;
-        int cached_page = 0;
-        int issued = 0;
+        int i = 0;   // stages issued
+        int p = 0;   // pieces handed over
         bool ok = true;
-        // this CTA writes the new token when its chunk ends at the newest position: before
-        // the last stage's copies read that page's codes and scales
-        const bool writes_new = store_new && k_end == ctx;
-        const int new_page = writes_new ? a.block_table[static_cast<size_t>(s) * a.bt_stride +
-                                                        (ctx - 1) / P]
-                                        : 0;
-        for (int b = 0; b < n_blocks; ++b) {
-            const int st = b % kStages;
-            if (b >= kStages &&
-                !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((b / kStages) - 1) & 1))) {
+        Cursor w;
+        w.s = static_cast<int>(scratch[0]);
+        w.g = g0;
+        if (a.per_unit) {
+            w.ctx = static_cast<int>(scratch[1]);
+            w.nb = static_cast<int>(total);
+            w.over = scratch[3] != 0;
+            w.blk = 0;
+        } else {
+            ok = cursor_load(w, a);
+            const long long off = g0 - scratch[1];
+            ok = ok && off < w.nb;
+            w.blk = ok ? static_cast<int>(off) : 0;
+        }
+        // hands piece p (nblk = 0: the end) over with its query rows, once the consumers have
+        // taken piece p - 1's
+        auto hand_over = [&](int s, int blk0, int nblk, int ctx, int nb) -> bool {
+            if (p > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty, (p - 1) & 1)))
+                return false;
+            if (nblk > 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    a.q + (static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G) * D);
+                uint4 *dst = reinterpret_cast<uint4 *>(qbuf);
+                for (int k = lane; k < G * D / 8; k += 32)
+                    dst[k] = src[k];
+            }
+            if (lane == 0) {
+                desc->s = s;
+                desc->blk0 = blk0;
+                desc->nblk = nblk;
+                desc->ctx = ctx;
+                desc->nb = nb;
+                desc->g_last = w.g - blk0 + nb - 1;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(q_full);
+            ++p;
+            return true;
+        };
+        while (ok && w.g < g1) {
+            const int blk0 = w.blk;
+            const int nblk = static_cast<int>(min(static_cast<long long>(w.nb - blk0), g1 - w.g));
+            const int s = w.s, ctx = w.ctx;
+            if (nblk <= 0 || !hand_over(s, blk0, nblk, ctx, w.nb)) {
                 ok = false;
                 break;
             }
-            const int rel0 = b * kStageKeys;
-            const int keys = min(kStageKeys, k_end - k_begin - rel0);
-            const int np = (keys + P - 1) / P;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[st],
-                                      static_cast<uint32_t>(np * P * (2 * D + 2 * 4)));
-            __syncwarp();
-            uint8_t *stage = smem + st * kStageBytes;
-            const int lp0 = rel0 / P;
-            if (lp0 + np > cached_base + 32) {
-                cached_base = lp0;
-                cached_page = (lp0 + lane < n_pages) ? bt_row[lp0 + lane] : 0;
-            }
-            // lane 4 i + op: page i's K codes, V codes, K scales, V scales
-            const int i = lane >> 2;
-            const int op = lane & 3;
-            const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + i) & 31);
-            if (writes_new && b + 1 == n_blocks) {
-                const int off_new = (ctx - 1) % P;
-                const long long slot = static_cast<long long>(new_page) * P + off_new;
-                if (new_page >= 0 && slot < a.num_slots) {
-                    const size_t sidx =
-                        (static_cast<size_t>(new_page) * a.kv_heads + kvh) * P + off_new;
-                    const size_t row =
-                        (a.hnd ? sidx : static_cast<size_t>(slot) * a.kv_heads + kvh) * D;
-                    quantise_store_row<E>(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx,
-                                          lane);
-                    quantise_store_row<E>(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx,
-                                          lane);
-                } else if (lane == 0) {
-                    atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrSlotRange);   // skipped, as in the store
+            const int32_t *bt_row = a.block_table + static_cast<size_t>(s) * a.bt_stride;
+            const int unit_pages = (ctx + P - 1) / P;
+            int cached_base = -32;
+            int cached_page = 0;
+            // this piece writes the new token when it ends at the unit's newest position:
+            // before the last stage's copies read that page's codes and scales
+            const bool writes_new = a.k_new != nullptr && !w.over && blk0 + nblk == w.nb;
+            uint32_t k_row_new[E / 2] = {}, v_row_new[E / 2] = {};
+            int new_page = 0;
+            if (writes_new) {
+                const size_t src = ((static_cast<size_t>(s) * Hkv + kvh) * 32 + lane) * (E / 2);
+                const uint32_t *kn = reinterpret_cast<const uint32_t *>(a.k_new) + src;
+                const uint32_t *vn = reinterpret_cast<const uint32_t *>(a.v_new) + src;
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) {
+                    k_row_new[e] = __ldg(kn + e);
+                    v_row_new[e] = __ldg(vn + e);
                 }
-                // the stores (generic proxy) before the copies (async proxy) that read them
-                fence_proxy_async_global();
+                new_page = bt_row[(ctx - 1) / P];
+            }
+            for (int b = 0; b < nblk; ++b) {
+                const int st = i % kStages;
+                if (i >= kStages &&
+                    !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / kStages) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int blk = blk0 + b;
+                const int keys = min(kStageKeys, ctx - blk * kStageKeys);
+                const int np = (keys + P - 1) / P;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[st],
+                                          static_cast<uint32_t>(np * P * (2 * D + 2 * 4)));
                 __syncwarp();
-                fence_proxy_async_global();
-            }
-            if (i < np) {
-                if (op == 0) {
-                    tma_load_3d(stage + i * P * D, &tmap_k, 0, a.hnd ? 0 : kvh,
-                                a.hnd ? page * a.kv_heads + kvh : page * P, &full[st], policy);
-                } else if (op == 1) {
-                    tma_load_3d(stage + kOffV + i * P * D, &tmap_v, 0, a.hnd ? 0 : kvh,
-                                a.hnd ? page * a.kv_heads + kvh : page * P, &full[st], policy);
-                } else {
-                    const float *src = (op == 2 ? a.k_scales : a.v_scales) +
-                                       (static_cast<size_t>(page) * a.kv_heads + kvh) * P;
-                    bulk_load(stage + (op == 2 ? kOffKs : kOffVs) + i * P * 4, src, P * 4,
-                              &full[st]);
+                uint8_t *stage = smem + st * kStageBytes;
+                const int lp0 = blk * kStageKeys / P;
+                if (lp0 + np > cached_base + 32) {
+                    cached_base = lp0;
+                    cached_page = (lp0 + lane < unit_pages) ? bt_row[lp0 + lane] : 0;
                 }
+                // lane 4 j + op: page j's K codes, V codes, K scales, V scales
+                const int j = lane >> 2;
+                const int op = lane & 3;
+                const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + j) & 31);
+                if (writes_new && b + 1 == nblk) {
+                    const int off_new = (ctx - 1) % P;
+                    const long long slot = static_cast<long long>(new_page) * P + off_new;
+                    if (new_page >= 0 && slot < a.num_slots) {
+                        const size_t sidx =
+                            (static_cast<size_t>(new_page) * Hkv + kvh) * P + off_new;
+                        const size_t row =
+                            (a.hnd ? sidx : static_cast<size_t>(slot) * Hkv + kvh) * D;
+                        quantise_store_row<E>(k_row_new, a.k_codes_w + row, a.k_scales_w + sidx,
+                                              lane);
+                        quantise_store_row<E>(v_row_new, a.v_codes_w + row, a.v_scales_w + sidx,
+                                              lane);
+                    } else if (lane == 0) {
+                        atomicOr(err_word(a), kErrSlotRange);   // skipped, as in the store
+                    }
+                    // the stores (generic proxy) before the copies (async proxy) that read them
+                    fence_proxy_async_global();
+                    __syncwarp();
+                    fence_proxy_async_global();
+                }
+                if (j < np) {
+                    if (op == 0) {
+                        tma_load_3d(stage + j * P * D, &tmap_k, 0, a.hnd ? 0 : kvh,
+                                    a.hnd ? page * Hkv + kvh : page * P, &full[st], policy);
+                    } else if (op == 1) {
+                        tma_load_3d(stage + kOffV + j * P * D, &tmap_v, 0, a.hnd ? 0 : kvh,
+                                    a.hnd ? page * Hkv + kvh : page * P, &full[st], policy);
+                    } else {
+                        const float *src = (op == 2 ? a.k_scales : a.v_scales) +
+                                           (static_cast<size_t>(page) * Hkv + kvh) * P;
+                        bulk_load(stage + (op == 2 ? kOffKs : kOffVs) + j * P * 4, src, P * 4,
+                                  &full[st]);
+                    }
+                }
+                ++i;
             }
-            issued = b + 1;
+            if (!ok)
+                break;
+            ok = cursor_advance(w, a, nblk, g1);
         }
+        if (ok)
+            ok = hand_over(0, 0, 0, 0, 0);   // the end
         if (!ok && lane == 0) {
-            atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrDecodeEmptyWait);
-            for (int b = max(0, issued - kStages); b < issued; ++b)
+            atomicOr(err_word(a), kErrDecodeEmptyWait);
+            for (int b = max(0, i - kStages); b < i; ++b)
                 if (!mbar_wait(&full[b % kStages], (b / kStages) & 1))
-                    atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrDrainWait);
+                    atomicOr(err_word(a), kErrDrainWait);
         }
         return;
     }
 
     // --------------------------------- consumers -----------------------------------------
-    const int r = lane >> 2;   // fragment row = q head of the group (rows >= G: padding)
+    const int r = lane >> 2;   // fragment group: positions r, r + 8; query head r of Q^T
     const int t = lane & 3;
-    // Q pairs in the contraction order (k-step kk uses dims 32 t + 4 kk + {0, 1} and {2, 3}),
-    // as fp16.  A power of two q_pow brings the largest |q| of the group below 2^14 when it
-    // is above, and is folded back into the score scale (exact either way).
-    uint32_t qa[D / 16][2];
-    float sl2 = a.scale_log2;
-    {
-        const __nv_bfloat16 *qrow = a.q + (row0 + r) * D + (D / 4) * t;
-        float qv[D / 4];
-        float qmax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i) {
-            qv[i] = r < G ? __bfloat162float(qrow[i]) : 0.0f;
-            qmax = fmaxf(qmax, fabsf(qv[i]));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
-        float q_pow = 1.0f;
-        while (qmax * q_pow > 16384.0f)
-            q_pow *= 0.5f;
-        sl2 = sl2 / q_pow;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qa[kk][0] = pack_f16x2(qv[4 * kk] * q_pow, qv[4 * kk + 1] * q_pow);
-            qa[kk][1] = pack_f16x2(qv[4 * kk + 2] * q_pow, qv[4 * kk + 3] * q_pow);
-        }
-    }
-    // O^T accumulators: tile dt holds dims pi(dt, m) x query rows n, this thread rows 2t,
-    // 2t + 1 of dims pi(dt, r) (c0, c1) and pi(dt, r + 8) (c2, c3), where
-    // pi(dt, r + 8 h) = 32 (dt >> 1) + 4 r + 2 (dt & 1) + h
-    float o[D / 16][4];
-#pragma unroll
-    for (int n = 0; n < D / 16; ++n)
-        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-    float m_run = -INFINITY;
-    float l_run = 0.0f;
     const int wrow = warp * kKeysPerWarp;   // first stage row of this warp
-    // Stage-independent offsets.  K: the two 16-byte halves of this thread's 32 bytes in rows
+    // Stage-independent offsets.  K: the 16-byte chunks of this thread's D / 4 bytes in rows
     // wrow + r and wrow + 8 + r.  V: the word of dims 4 r .. 4 r + 3 in each of the thread's
     // four positions; dims 32 q + 4 r lie at that offset xor (q << 5), since the swizzle only
     // permutes 16-byte chunks within a row and q moves the chunk index by 2 q.
@@ -371,174 +575,342 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         v_off[i] = kOffV + code_offset<D>(wrow + key[i], 4 * r);
+    constexpr int kRowStride = D + 4;
     bool ok = true;
+    int i = 0;   // stages consumed
+    int p = 0;   // pieces begun
 
-    for (int b = 0; b < n_blocks; ++b) {
-        const int st = b % kStages;
-        if (!mbar_wait(&full[st], (b / kStages) & 1)) {
-            ok = false;
-            break;
-        }
-        const uint8_t *stage = smem + st * kStageBytes;
-        const float *ks = reinterpret_cast<const float *>(stage + kOffKs) + wrow;
-        const float *vs = reinterpret_cast<const float *>(stage + kOffVs) + wrow;
-        const int n_valid = k_end - (k_begin + b * kStageKeys + wrow);
-        if (n_valid > 0) {
-            // S = Q K^T: B column r of n-tile nt is position 8 nt + r of this warp
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    while (true) {
+        // the next piece and its query rows.  Q^T pairs (the B fragment of S^T = K Q^T, column
+        // r = query head r, rows >= G padding) in the contraction order (k-step kk uses dims
+        // (D / 4) t + 4 kk + {0, 1} and {2, 3}), as fp16.  A power of two q_pow brings the
+        // largest |q| of the group below 2^14 when it is above, and is folded back into the
+        // score scale (exact either way).
+        const bool q_ok = __all_sync(0xffffffffu, mbar_wait(q_full, p & 1));
+        const int s = desc->s, blk0 = desc->blk0, nblk = desc->nblk;
+        const int ctx = desc->ctx, nb = desc->nb;
+        const long long g_last = desc->g_last;
+        uint32_t qa[D / 16][2];
+        float sl2 = a.scale_log2;
+        {
+            float qv[D / 4];
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(qbuf + r * D + (D / 4) * t);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t w[D / 16];
+            for (int k = 0; k < D / 32; ++k) {
+                uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+                if (r < G && q_ok)
+                    w4 = qrow[k];
+                const uint32_t wd[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qv[8 * k + 2 * e] = __uint_as_float(wd[e] << 16);
+                    qv[8 * k + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(q_empty);
+            if (!q_ok)
+                *abort_flag = 1;
+            // one decision for the 4 warps: stop on a wait that gave up, or at the end
+            named_barrier(1, kConsumerWarps * 32);
+            if (*abort_flag || nblk <= 0)
+                break;
+            float qmax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < D / 4; ++k)
+                qmax = fmaxf(qmax, fabsf(qv[k]));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+            float q_pow = 1.0f;
+            while (qmax * q_pow > 16384.0f)
+                q_pow *= 0.5f;
+            sl2 = sl2 / q_pow;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qa[kk][0] = pack_f16x2(qv[4 * kk] * q_pow, qv[4 * kk + 1] * q_pow);
+                qa[kk][1] = pack_f16x2(qv[4 * kk + 2] * q_pow, qv[4 * kk + 3] * q_pow);
+            }
+        }
+        const bool whole = blk0 == 0 && nblk == nb;
+        const int unit = s * Hkv + kvh;
+        const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
+        // O^T accumulators: tile dt holds dims pi(dt, m) x query heads n, this thread heads 2t,
+        // 2t + 1 of dims pi(dt, r) (c0, c1) and pi(dt, r + 8) (c2, c3), where
+        // pi(dt, r + 8 h) = 32 (dt >> 1) + 4 r + 2 (dt & 1) + h
+        float o[D / 16][4];
+#pragma unroll
+        for (int n = 0; n < D / 16; ++n)
+            o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+        // running max and row sum of query heads 2t and 2t + 1 (the heads of this thread's
+        // scores and of its O^T accumulators)
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.0f, 0.0f};
+        int last_st = -1;
+
+        for (int b = 0; ok && b < nblk; ++b) {
+            const int st = i % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (i / kStages) & 1))) {
+                ok = false;
+                break;
+            }
+            const uint8_t *stage = smem + st * kStageBytes;
+            const float *ks = reinterpret_cast<const float *>(stage + kOffKs) + wrow;
+            const float *vs = reinterpret_cast<const float *>(stage + kOffVs) + wrow;
+            const int n_valid = ctx - ((blk0 + b) * kStageKeys + wrow);
+            if (n_valid > 0) {
+                // S^T = K Q^T: A rows r and r + 8 are positions r and r + 8 of this warp (a0,
+                // a2 from one word of position r, a1, a3 from position r + 8), two chains
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int h = 0; h < kKChunks; ++h) {
-                    const uint4 c4 = *reinterpret_cast<const uint4 *>(stage + k_off[nt][h]);
-                    w[4 * h] = c4.x;
-                    w[4 * h + 1] = c4.y;
-                    w[4 * h + 2] = c4.z;
-                    w[4 * h + 3] = c4.w;
-                }
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(stage + k_off[0][h]);
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(stage + k_off[1][h]);
+                    const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w};
+                    const uint32_t w1[4] = {c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t b0, b1;   // codes 0, 1 and codes 2, 3 of the word
-                    codes_word_f16x2(w[kk], b0, b1);
-                    mma_f16_16816(sc[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0, a1, a2, a3;
+                        codes_word_f16x2(w0[j], a0, a2);
+                        codes_word_f16x2(w1[j], a1, a3);
+                        mma_f16_16816(sc[j & 1], a0, a1, a2, a3, qa[4 * h + j][0],
+                                      qa[4 * h + j][1]);
+                    }
+                }
+                // x[0], x[1]: position r, heads 2t, 2t + 1; x[2], x[3]: position r + 8;
+                // key-scaled
+                const bool v0 = r < n_valid, v1 = r + 8 < n_valid;
+                const float ks0 = v0 ? ks[r] * sl2 : 0.0f, ks1 = v1 ? ks[r + 8] * sl2 : 0.0f;
+                float x[4];
+                x[0] = v0 ? (sc[0][0] + sc[1][0]) * ks0 : -INFINITY;
+                x[1] = v0 ? (sc[0][1] + sc[1][1]) * ks0 : -INFINITY;
+                x[2] = v1 ? (sc[0][2] + sc[1][2]) * ks1 : -INFINITY;
+                x[3] = v1 ? (sc[0][3] + sc[1][3]) * ks1 : -INFINITY;
+                float mb0 = fmaxf(x[0], x[2]), mb1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mb0 = fmaxf(mb0, __shfl_xor_sync(0xffffffffu, mb0, off));
+                    mb1 = fmaxf(mb1, __shfl_xor_sync(0xffffffffu, mb1, off));
+                }
+                const float mn0 = fmaxf(m_run[0], mb0), mn1 = fmaxf(m_run[1], mb1);
+                if (__any_sync(0xffffffffu, mn0 > m_run[0] || mn1 > m_run[1])) {
+                    const float a0 = (m_run[0] == -INFINITY) ? 0.0f : fast_exp2(m_run[0] - mn0);
+                    const float a1 = (m_run[1] == -INFINITY) ? 0.0f : fast_exp2(m_run[1] - mn1);
+#pragma unroll
+                    for (int n = 0; n < D / 16; ++n) {
+                        o[n][0] *= a0;
+                        o[n][1] *= a1;
+                        o[n][2] *= a0;
+                        o[n][3] *= a1;
+                    }
+                    l_run[0] *= a0;
+                    l_run[1] *= a1;
+                    m_run[0] = mn0;
+                    m_run[1] = mn1;
+                }
+                const float mu0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
+                const float mu1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
+                const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
+                const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
+                l_run[0] += p0 + p2;
+                l_run[1] += p1 + p3;
+                const float vs0 = v0 ? vs[r] : 0.0f, vs1 = v1 ? vs[r + 8] : 0.0f;
+                // P' = P * v_scale as fp16 pairs (position r or r + 8; heads 2t, 2t + 1),
+                // turned by an 8x8 transpose into the B fragment of the PV product (positions
+                // 2t, 2t + 1 or 8 + 2t, 9 + 2t; head r)
+                const uint32_t pa0 =
+                    movmatrix_trans(pack_f16x2(v0 ? p0 * vs0 : 0.0f, v0 ? p1 * vs0 : 0.0f));
+                const uint32_t pa2 =
+                    movmatrix_trans(pack_f16x2(v1 ? p2 * vs1 : 0.0f, v1 ? p3 * vs1 : 0.0f));
+                // O^T += V^T P'^T: A = V^T (16 dims x 16 positions); thread r reads one word
+                // (dims 32 q + 4 r .. + 3) of each of its four positions per q
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t vw[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        vw[k] = *reinterpret_cast<const uint32_t *>(stage + (v_off[k] ^ (q << 5)));
+                    mma_f16_16816(o[2 * q], codes_f16x2<0>(vw[0], vw[1]),
+                                  codes_f16x2<1>(vw[0], vw[1]), codes_f16x2<0>(vw[2], vw[3]),
+                                  codes_f16x2<1>(vw[2], vw[3]), pa0, pa2);
+                    mma_f16_16816(o[2 * q + 1], codes_f16x2<2>(vw[0], vw[1]),
+                                  codes_f16x2<3>(vw[0], vw[1]), codes_f16x2<2>(vw[2], vw[3]),
+                                  codes_f16x2<3>(vw[2], vw[3]), pa0, pa2);
                 }
             }
-            // scores of positions 2t, 2t+1 (tile 0) and 8+2t, 9+2t (tile 1), key-scaled
-            float x[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
+            last_st = st;
+            ++i;
+            if (b + 1 < nblk) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[st]);
+            }
+        }
+
+        // --------------- combine the 4 warps' results in the last stage's buffer ----------
+        // Each warp leaves its unnormalised o rows (D + 4 floats apart: 16-byte aligned rows),
+        // running max and row sum; one thread per query head folds them into weights
+        // 2^(m_w - M) / L, and the rows are written as float4 (bf16x4) pieces: the output
+        // when the piece is the whole unit, else its partial slot.
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                x[i] = key[i] < n_valid ? x[i] * ks[key[i]] * sl2 : -INFINITY;
-            float mb = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-            const float m_new = fmaxf(m_run, mb);
-            if (__any_sync(0xffffffffu, m_new > m_run)) {
-                const float alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_new);
-                // this thread's accumulators are rows 2t and 2t + 1 (held by lanes 8t, 8t + 4)
-                const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-                const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+        for (int off = 4; off < 32; off <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+        }
+        const int cst = last_st >= 0 ? last_st : 0;
+        float *red_o = reinterpret_cast<float *>(smem + cst * kStageBytes);   // [W][8][D + 4]
+        float *red_m = red_o + kConsumerWarps * kMaxGroup * kRowStride;       // [W][8]
+        float *red_l = red_m + kConsumerWarps * kMaxGroup;                    // [W][8]
+        float *row_w = red_l + kConsumerWarps * kMaxGroup;                    // [8][W]
+        named_barrier(1, kConsumerWarps * 32);   // every warp is done reading that stage
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {   // query heads 2t and 2t + 1
+            const int row = 2 * t + e;
+            if (row < G) {
+                float *dst = red_o + (warp * kMaxGroup + row) * kRowStride;
 #pragma unroll
                 for (int n = 0; n < D / 16; ++n) {
-                    o[n][0] *= a0;
-                    o[n][1] *= a1;
-                    o[n][2] *= a0;
-                    o[n][3] *= a1;
+                    const int dim = 32 * (n >> 1) + 4 * r + 2 * (n & 1);
+                    *reinterpret_cast<float2 *>(dst + dim) = make_float2(o[n][e], o[n][2 + e]);
                 }
-                l_run *= alpha;
-                m_run = m_new;
-            }
-            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-            float p[4], pv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                p[i] = fast_exp2(x[i] - m_use);
-                pv[i] = key[i] < n_valid ? p[i] * vs[key[i]] : 0.0f;
-            }
-            l_run += (p[0] + p[1]) + (p[2] + p[3]);
-            const uint32_t pa0 = pack_f16x2(pv[0], pv[1]);   // positions 2t, 2t+1
-            const uint32_t pa2 = pack_f16x2(pv[2], pv[3]);   // positions 8+2t, 9+2t
-            // O^T += V^T P'^T: A = V^T (16 dims x 16 positions), B = P'^T, whose fragment is
-            // exactly this thread's (pa0, pa2); thread r reads one word (dims 32 q + 4 r .. + 3)
-            // of each of its four positions per q
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t vw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    vw[i] = *reinterpret_cast<const uint32_t *>(stage + (v_off[i] ^ (q << 5)));
-                mma_f16_16816(o[2 * q], codes_f16x2<0>(vw[0], vw[1]), codes_f16x2<1>(vw[0], vw[1]),
-                              codes_f16x2<0>(vw[2], vw[3]), codes_f16x2<1>(vw[2], vw[3]), pa0,
-                              pa2);
-                mma_f16_16816(o[2 * q + 1], codes_f16x2<2>(vw[0], vw[1]),
-                              codes_f16x2<3>(vw[0], vw[1]), codes_f16x2<2>(vw[2], vw[3]),
-                              codes_f16x2<3>(vw[2], vw[3]), pa0, pa2);
+                if (r == 0) {
+                    red_m[warp * kMaxGroup + row] = m_run[e];
+                    red_l[warp * kMaxGroup + row] = l_run[e];
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[st]);
+        // partial slots: kv head h owns [h (S + R), (h + 1) (S + R)), piece (s, run) is
+        // slot s + run there -- distinct for every piece, consecutive for one unit's pieces
+        const int slot = kvh * (a.num_seqs + static_cast<int>(n_run_ctas)) + s + static_cast<int>(run);
+        named_barrier(1, kConsumerWarps * 32);
+        if (threadIdx.x < G) {
+            const int row = threadIdx.x;
+            float M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kConsumerWarps; ++k)
+                M = fmaxf(M, red_m[k * kMaxGroup + row]);
+            float f[kConsumerWarps];
+            float L = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kConsumerWarps; ++k) {
+                const float mw = red_m[k * kMaxGroup + row];
+                f[k] = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
+                L += f[k] * red_l[k * kMaxGroup + row];
+            }
+            const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+#pragma unroll
+            for (int k = 0; k < kConsumerWarps; ++k)
+                row_w[row * kConsumerWarps + k] = f[k] * inv;
+            if (!whole)
+                a.part_lse[static_cast<size_t>(slot) * G + row] =
+                    (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+        named_barrier(1, kConsumerWarps * 32);
+        constexpr int kVec = D / 4;
+        for (int idx = threadIdx.x; idx < G * kVec; idx += kConsumerWarps * 32) {
+            const int row = idx / kVec;
+            const int col = (idx - row * kVec) * 4;
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int k = 0; k < kConsumerWarps; ++k) {
+                const float wt = row_w[row * kConsumerWarps + k];
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    red_o + (k * kMaxGroup + row) * kRowStride + col);
+                acc.x = fmaf(wt, v.x, acc.x);
+                acc.y = fmaf(wt, v.y, acc.y);
+                acc.z = fmaf(wt, v.z, acc.z);
+                acc.w = fmaf(wt, v.w, acc.w);
+            }
+            if (whole)
+                store_out4(a.out, a.out_f32, (row0 + row) * D + col, acc);
+            else
+                *reinterpret_cast<float4 *>(a.part_o + (static_cast<size_t>(slot) * G + row) * D +
+                                            col) = acc;
+        }
+        // the unit's first piece: where its pieces are and how many (the CTA runs holding
+        // its first and last blocks)
+        if (threadIdx.x == 0 && blk0 == 0 && !a.per_unit) {
+            const long long last = run_of(g_last, total, n_runs);
+            a.unit_info[unit] = make_int2(slot, static_cast<int>(last - run + 1));
+        }
+        if (!ok)
+            *abort_flag = 1;
+        named_barrier(1, kConsumerWarps * 32);   // the buffer is read: the stage goes back
+        if (ok && lane == 0 && last_st >= 0)
+            mbar_arrive(&empty[cst]);
+        if (*abort_flag)
+            break;
+        ++p;
     }
     if (!ok)
-        atomicOr(a.err ? a.err : &g_decode_int8_errors, kErrDecodeFullWait);
+        atomicOr(err_word(a), kErrDecodeFullWait);
+}
 
-    // ------------------------- combine the 4 warps' partial results -----------------------
-    // Each warp leaves its unnormalised o rows (D + 4 floats apart: 16-byte aligned rows),
-    // running max and row sum; one thread per query head folds them into weights
-    // 2^(m_w - M) / L, and the output is written as float4 (bf16x4) pieces.
-    constexpr int kRowStride = D + 4;
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    named_barrier(1, kConsumerWarps * 32);
-    float *red_o = reinterpret_cast<float *>(smem);                      // [W][8][D + 4]
-    float *red_m = red_o + kConsumerWarps * kMaxGroup * kRowStride;       // [W][8]
-    float *red_l = red_m + kConsumerWarps * kMaxGroup;                    // [W][8]
-    float *row_w = red_l + kConsumerWarps * kMaxGroup;                    // [8][W]
+// One warp per output row (sequence s, query head h of unit u = (s, h / G)): the log-sum-exp
+// combination of the unit's partial slots first .. first + count - 1, rows normalised by their
+// own sums.  Rows of a unit whose only piece wrote them are left alone; rows of a sequence
+// with no positions are 0.
+template <int D>
+__global__ void __launch_bounds__(128) merge_flat_kernel(const Args a)
+{
+    pdl_wait();
+    pdl_trigger();
+    constexpr int V = D / 32;
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= a.num_seqs * a.q_heads)
+        return;
+    const int s = row / a.q_heads;
+    const int h = row - s * a.q_heads;
+    const int G = a.group;
+    const int unit = s * a.kv_heads + h / G;
+    const int g = h - (h / G) * G;
+    float acc[V];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {   // query rows 2t and 2t + 1
-        const int row = 2 * t + e;
-        if (row < G) {
-            float *dst = red_o + (warp * kMaxGroup + row) * kRowStride;
+    for (int v = 0; v < V; ++v)
+        acc[v] = 0.0f;
+    float sum = 0.0f;
+    if (clamped_ctx(a, s) > 0) {
+        const int2 info = a.unit_info[unit];
+        if (info.y == 1)
+            return;
+        const float *lse = a.part_lse + static_cast<size_t>(info.x) * G + g;
+        const float *po = a.part_o + (static_cast<size_t>(info.x) * G + g) * D + lane * V;
+        float M = -INFINITY;
+        for (int j = lane; j < info.y; j += 32)
+            M = fmaxf(M, lse[static_cast<size_t>(j) * G]);
 #pragma unroll
-            for (int n = 0; n < D / 16; ++n) {
-                const int dim = 32 * (n >> 1) + 4 * r + 2 * (n & 1);
-                *reinterpret_cast<float2 *>(dst + dim) = make_float2(o[n][e], o[n][2 + e]);
+        for (int off = 16; off > 0; off >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M != -INFINITY) {
+#pragma unroll 4
+            for (int j = 0; j < info.y; ++j) {
+                const float lj = lse[static_cast<size_t>(j) * G];
+                if (lj == -INFINITY)
+                    continue;
+                const float wj = fast_exp2((lj - M) * kLog2e);
+                sum += wj;
+                const float *src = po + static_cast<size_t>(j) * G * D;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    acc[v] = fmaf(wj, src[v], acc[v]);
             }
         }
     }
-    if (r < G && t == 0) {
-        red_m[warp * kMaxGroup + r] = m_run;
-        red_l[warp * kMaxGroup + r] = l_run;
-    }
-    named_barrier(1, kConsumerWarps * 32);
-    if (threadIdx.x < G) {
-        const int row = threadIdx.x;
-        float M = -INFINITY;
+    const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
+    const size_t o = static_cast<size_t>(row) * D + lane * V;
+    if constexpr (V == 4) {
+        store_out4(a.out, a.out_f32, o,
+                   make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv));
+    } else {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-            M = fmaxf(M, red_m[w * kMaxGroup + row]);
-        float f[kConsumerWarps];
-        float L = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = red_m[w * kMaxGroup + row];
-            f[w] = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - M);
-            L += f[w] * red_l[w * kMaxGroup + row];
-        }
-        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-            row_w[row * kConsumerWarps + w] = f[w] * inv;
-        if (SPLIT)
-            a.part_lse[(row0 + row) * a.n_split + split] =
-                (L > 0.0f) ? (M + log2f(L)) * kLn2 : -INFINITY;
-    }
-    named_barrier(1, kConsumerWarps * 32);
-    constexpr int kVec = D / 4;
-    for (int idx = threadIdx.x; idx < G * kVec; idx += kConsumerWarps * 32) {
-        const int row = idx / kVec;
-        const int c = (idx - row * kVec) * 4;
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float wt = row_w[row * kConsumerWarps + w];
-            const float4 v = *reinterpret_cast<const float4 *>(
-                red_o + (w * kMaxGroup + row) * kRowStride + c);
-            acc.x = fmaf(wt, v.x, acc.x);
-            acc.y = fmaf(wt, v.y, acc.y);
-            acc.z = fmaf(wt, v.z, acc.z);
-            acc.w = fmaf(wt, v.w, acc.w);
-        }
-        if (SPLIT) {
-            const size_t prow = (row0 + row) * a.n_split + split;
-            *reinterpret_cast<float4 *>(a.part_o + prow * D + c) = acc;
-        } else {
-            store_out4(a.out, a.out_f32, (row0 + row) * D + c, acc);
-        }
+        for (int v = 0; v < V; ++v)
+            store_out(a.out, a.out_f32, o + v, acc[v] * inv);
     }
 }
 
-template <int D, bool SPLIT>
+template <int D>
 cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUtensorMap &tv,
                      cudaStream_t stream)
 {
@@ -551,16 +923,17 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.out_f32 = l.out_f32;
     a.part_o = l.part_o;
     a.part_lse = l.part_lse;
+    a.unit_info = static_cast<int2 *>(l.unit_info);
     a.block_table = l.block_table;
     a.bt_stride = l.bt_stride;
     a.context_lens = l.context_lens;
+    a.num_seqs = l.num_seqs;
     a.q_heads = l.q_heads;
     a.kv_heads = l.kv_heads;
     a.group = l.q_heads / l.kv_heads;
     a.page_size = l.page_size;
-    a.chunk = l.chunk;
-    a.n_split = l.n_split;
-    a.scale_log2 = l.scale * 1.4426950408889634f;
+    a.per_unit = l.per_unit ? 1 : 0;
+    a.scale_log2 = l.scale * kLog2e;
     a.k_new = static_cast<const __nv_bfloat16 *>(l.k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(l.v_new);
     a.k_codes_w = static_cast<int8_t *>(l.k_codes_w);
@@ -570,13 +943,18 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.num_slots = l.num_slots;
     a.err = current_error_word();
     a.hnd = l.hnd ? 1 : 0;
-    auto kernel = paged_decode_int8_kernel<D, SPLIT>;
+    auto kernel = paged_decode_int8_kernel<D>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));
     if (err != cudaSuccess)
         return err;
-    dim3 grid(l.n_split, l.kv_heads, l.num_seqs);
-    return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, tk, tv, a);
+    const unsigned grid = l.per_unit ? static_cast<unsigned>(l.num_seqs * l.kv_heads)
+                                     : static_cast<unsigned>(l.n_ctas);
+    err = launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, tk, tv, a);
+    if (err != cudaSuccess || l.per_unit)
+        return err;
+    const int rows = l.num_seqs * l.q_heads;
+    return launch_pdl(merge_flat_kernel<D>, dim3((rows + 3) / 4), dim3(128), 0, stream, a);
 }
 
 }  // namespace
@@ -587,10 +965,8 @@ cudaError_t launch_decode_int8(const DecodeInt8Launch &l, const CUtensorMap &tma
     if (l.num_seqs == 0)
         return cudaSuccess;
     if (l.head_dim == 64)
-        return l.n_split > 1 ? launch_t<64, true>(l, tmap_k, tmap_v, stream)
-                             : launch_t<64, false>(l, tmap_k, tmap_v, stream);
-    return l.n_split > 1 ? launch_t<128, true>(l, tmap_k, tmap_v, stream)
-                         : launch_t<128, false>(l, tmap_k, tmap_v, stream);
+        return launch_t<64>(l, tmap_k, tmap_v, stream);
+    return launch_t<128>(l, tmap_k, tmap_v, stream);
 }
 
 cudaError_t read_and_clear_decode_int8_errors(uint32_t *flags)

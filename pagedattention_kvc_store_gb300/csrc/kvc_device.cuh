@@ -490,6 +490,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return r;
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held as one register per lane (lane l: row
+// l / 4, columns 2 (l % 4) and 2 (l % 4) + 1): lane l receives row l / 4 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
     __half2 v = __floats2half2_rn(lo, hi);

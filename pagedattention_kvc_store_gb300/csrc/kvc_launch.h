@@ -57,18 +57,23 @@ struct DecodeLaunch {
 };
 
 // Decode over INT8 pages (head_dim 64 or 128): codes like a bf16 pool, scales [pages][Hkv][P].
+// The positions of all (sequence, kv head) units are cut into n_ctas equal runs of 64-position
+// blocks (one CTA each), whose pieces are merged by a second launch; per_unit runs one CTA per
+// unit instead and writes the output directly (no workspace, no merge).
 struct DecodeInt8Launch {
     const void *q;
     const float *k_scales, *v_scales;
     void *out;
     int out_f32;
-    float *part_o;            // [S][Hq][n_split][D] when n_split > 1
-    float *part_lse;          // [S][Hq][n_split]
+    float *part_o = nullptr;      // [units + n_ctas][G][D]
+    float *part_lse = nullptr;    // [units + n_ctas][G]
+    void *unit_info = nullptr;    // [units] int2: first partial slot, piece count
     const int32_t *block_table;
     int bt_stride;
     const int32_t *context_lens;
     int num_seqs, q_heads, kv_heads, page_size;
-    int chunk, n_split;
+    int n_ctas = 1;
+    bool per_unit = false;
     float scale;
     // fused store (kvc_decode_int8_store): new K/V [S][Hkv][D] bf16 and the pools to write
     const void *k_new = nullptr, *v_new = nullptr;

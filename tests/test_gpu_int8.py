@@ -130,3 +130,56 @@ def test_int8_single_position_is_its_stored_vector():
             want = vs[page, g, off] * vc[page, off, g].astype(np.float64)
             # the probability 1 times the value scale enters the PV product as bf16
             np.testing.assert_allclose(out_to_f64(out)[s, h], want, rtol=2.0 ** -8, atol=1e-6)
+
+
+def decode_int8_only(case, pools, ctx, num_splits):
+    """kvc_decode_int8 over given pools with the given context lengths (fp32 output)."""
+    kc, vc, ks, vs = (torch.from_numpy(a).cuda() for a in pools)
+    bt, ctx_t = i32_tensor(case.block_table, "cuda"), i32_tensor(ctx, "cuda")
+    out = torch.full((case.num_seqs, case.q_heads, case.head_dim), float("nan"),
+                     device="cuda")
+    pool = kvc.int8_pool_desc(kc)
+    _, _, ws = kvc.kvc_decode_int8_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
+                                        num_splits)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    kvc.kvc_decode_int8(out, bf16_tensor(case.q, "cuda"), kc, vc, ks, vs, bt, ctx_t,
+                        case.max_ctx, num_splits=num_splits, workspace=work)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_errors() == 0
+    return out_to_f64(out)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 7])
+def test_int8_partition_across_sequences(splits):
+    """The positions of all sequences are cut into equal runs per kv head: runs that cross
+    sequence boundaries, sequences much longer than a run (their rows merged from many
+    pieces), contexts of 1 .. 127 positions, and sequences with no positions between them
+    (their rows are 0)."""
+    ctx = np.array([1, 5000, 3, 1, 64, 65, 9000, 2, 127, 1, 3000, 17])
+    case = build_case(1300, name="int8-partition", page_size=16, q_heads=8, kv_heads=2,
+                      head_dim=128, context_lens=lambda rng: ctx,
+                      q_lens=lambda c: np.ones_like(c))
+    out, pools = run_int8(case, num_splits=splits)
+    assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
+                           f"INT8 partition splits={splits}")
+    ctx0 = ctx.copy()
+    ctx0[[0, 3, 9]] = 0
+    got = decode_int8_only(case, pools, ctx0, splits)
+    assert not got[[0, 3, 9]].any(), "a sequence with no positions has rows of 0"
+    keep = np.flatnonzero(ctx0 > 0)
+    kc, vc, ks, vs = pools
+    ref, _ = oracle.attention_int8(case.q[keep], kc, vc, ks, vs, case.block_table[keep],
+                                   ctx0[keep], np.arange(len(keep) + 1, dtype=np.int32),
+                                   num_threads=16)
+    assert_attention_close(got[keep], ref, f"INT8 partition with empty sequences {splits}")
+
+
+def test_int8_more_ctas_than_blocks():
+    """Fewer 64-position blocks than planned runs: only as many runs as blocks are used."""
+    case = build_case(1301, name="int8-few-blocks", page_size=16, q_heads=8, kv_heads=2,
+                      head_dim=128, context_lens=lambda rng: np.array([1, 2, 70]),
+                      q_lens=lambda c: np.ones_like(c))
+    for splits in (0, 9):
+        out, pools = run_int8(case, num_splits=splits)
+        assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
+                               f"INT8 few blocks splits={splits}")
