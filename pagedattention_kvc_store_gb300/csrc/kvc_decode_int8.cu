@@ -556,25 +556,33 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
 
     // --------------------------------- consumers -----------------------------------------
-    const int r = lane >> 2;   // fragment group: positions r, r + 8; query head r of Q^T
+    const int r = lane >> 2;   // fragment group: contraction rows r, r + 8; query head r
     const int t = lane & 3;
     const int wrow = warp * kKeysPerWarp;   // first stage row of this warp
+    // The PV product's contraction index k (0..15) runs over this warp's positions in the
+    // order in which a transposing ldmatrix hands V over: thread (g, t) gets, per dim, the
+    // bytes of positions 4t .. 4t + 3, whose pairs are its A fragment's k = 2t, 2t + 1 and
+    // 2t + 8, 2t + 9.  So k is position pk(k) = 4 ((k % 8) / 2) + 2 (k / 8) + k % 2, and the
+    // S^T rows r, r + 8 of this thread (k = r, r + 8, the movmatrix hands them over as k) are
+    // positions pos0 = pk(r) and pos1 = pos0 + 2.
+    const int pos0 = 4 * (r >> 1) + (r & 1);
+    const int pos1 = pos0 + 2;
     // Stage-independent offsets.  K: the 16-byte chunks of this thread's D / 4 bytes in rows
-    // wrow + r and wrow + 8 + r.  V: the word of dims 4 r .. 4 r + 3 in each of the thread's
-    // four positions; dims 32 q + 4 r lie at that offset xor (q << 5), since the swizzle only
-    // permutes 16-byte chunks within a row and q moves the chunk index by 2 q.
+    // wrow + pos0 and wrow + pos1.  V: lane l's row address of each ldmatrix.x2 (matrices of 16
+    // positions x 16 dims: row l % 16 of matrix 2 m + l / 16, 16-byte chunk 2 m + l / 16).
     constexpr int kKChunks = D / 64;   // 16-byte chunks of this thread's K bytes per row
+    constexpr int kVPairs = D / 32;    // ldmatrix.x2 loads per stage (two 16-dim tiles each)
     uint32_t k_off[2][kKChunks];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int h = 0; h < kKChunks; ++h) {
+        k_off[0][h] = code_offset<D>(wrow + pos0, (D / 4) * t + 16 * h);
+        k_off[1][h] = code_offset<D>(wrow + pos1, (D / 4) * t + 16 * h);
+    }
+    uint32_t v_ldm[kVPairs];
 #pragma unroll
-        for (int h = 0; h < kKChunks; ++h)
-            k_off[nt][h] = code_offset<D>(wrow + 8 * nt + r, (D / 4) * t + 16 * h);
-    const int key[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-    uint32_t v_off[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        v_off[i] = kOffV + code_offset<D>(wrow + key[i], 4 * r);
+    for (int m = 0; m < kVPairs; ++m)
+        v_ldm[m] = kOffV + code_offset<D>(wrow + (lane & 15), 16 * (2 * m + (lane >> 4)));
+    const uint32_t smem32 = smem_addr(smem);
     constexpr int kRowStride = D + 4;
     bool ok = true;
     int i = 0;   // stages consumed
@@ -636,9 +644,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         const bool whole = blk0 == 0 && nblk == nb;
         const int unit = s * Hkv + kvh;
         const size_t row0 = static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G;
-        // O^T accumulators: tile dt holds dims pi(dt, m) x query heads n, this thread heads 2t,
-        // 2t + 1 of dims pi(dt, r) (c0, c1) and pi(dt, r + 8) (c2, c3), where
-        // pi(dt, r + 8 h) = 32 (dt >> 1) + 4 r + 2 (dt & 1) + h
+        // O^T accumulators: tile n holds dims 16 n .. 16 n + 15 x query heads, this thread
+        // heads 2t, 2t + 1 of dims 16 n + r (c0, c1) and 16 n + r + 8 (c2, c3)
         float o[D / 16][4];
 #pragma unroll
         for (int n = 0; n < D / 16; ++n)
@@ -660,8 +667,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             const float *vs = reinterpret_cast<const float *>(stage + kOffVs) + wrow;
             const int n_valid = ctx - ((blk0 + b) * kStageKeys + wrow);
             if (n_valid > 0) {
-                // S^T = K Q^T: A rows r and r + 8 are positions r and r + 8 of this warp (a0,
-                // a2 from one word of position r, a1, a3 from position r + 8), two chains
+                // S^T = K Q^T: A rows r and r + 8 are positions pos0 and pos1 of this warp
+                // (a0, a2 from one word of position pos0, a1, a3 from pos1), two chains
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int h = 0; h < kKChunks; ++h) {
@@ -678,10 +685,10 @@ __global__ void __launch_bounds__(kThreads, 3)
                                       qa[4 * h + j][1]);
                     }
                 }
-                // x[0], x[1]: position r, heads 2t, 2t + 1; x[2], x[3]: position r + 8;
+                // x[0], x[1]: position pos0, heads 2t, 2t + 1; x[2], x[3]: position pos1;
                 // key-scaled
-                const bool v0 = r < n_valid, v1 = r + 8 < n_valid;
-                const float ks0 = v0 ? ks[r] * sl2 : 0.0f, ks1 = v1 ? ks[r + 8] * sl2 : 0.0f;
+                const bool v0 = pos0 < n_valid, v1 = pos1 < n_valid;
+                const float ks0 = v0 ? ks[pos0] * sl2 : 0.0f, ks1 = v1 ? ks[pos1] * sl2 : 0.0f;
                 float x[4];
                 x[0] = v0 ? (sc[0][0] + sc[1][0]) * ks0 : -INFINITY;
                 x[1] = v0 ? (sc[0][1] + sc[1][1]) * ks0 : -INFINITY;
@@ -715,28 +722,29 @@ __global__ void __launch_bounds__(kThreads, 3)
                 const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
                 l_run[0] += p0 + p2;
                 l_run[1] += p1 + p3;
-                const float vs0 = v0 ? vs[r] : 0.0f, vs1 = v1 ? vs[r + 8] : 0.0f;
-                // P' = P * v_scale as fp16 pairs (position r or r + 8; heads 2t, 2t + 1),
-                // turned by an 8x8 transpose into the B fragment of the PV product (positions
-                // 2t, 2t + 1 or 8 + 2t, 9 + 2t; head r)
+                const float vs0 = v0 ? vs[pos0] : 0.0f, vs1 = v1 ? vs[pos1] : 0.0f;
+                // P' = P * v_scale as fp16 pairs (k = r or r + 8; heads 2t, 2t + 1), turned by
+                // an 8x8 transpose into the B fragment of the PV product (k = 2t, 2t + 1 or
+                // 2t + 8, 2t + 9; head r)
                 const uint32_t pa0 =
                     movmatrix_trans(pack_f16x2(v0 ? p0 * vs0 : 0.0f, v0 ? p1 * vs0 : 0.0f));
                 const uint32_t pa2 =
                     movmatrix_trans(pack_f16x2(v1 ? p2 * vs1 : 0.0f, v1 ? p3 * vs1 : 0.0f));
-                // O^T += V^T P'^T: A = V^T (16 dims x 16 positions); thread r reads one word
-                // (dims 32 q + 4 r .. + 3) of each of its four positions per q
+                // O^T += V^T P'^T, A = V^T (16 dims x 16 positions): each transposed load gives
+                // two dim tiles; the bytes of positions 4t .. 4t + 3 of dim 16 n + r (and
+                // + 8) become a0, a2 (a1, a3) exactly as K's do
+                const uint32_t vbase = smem32 + st * kStageBytes;
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t vw[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        vw[k] = *reinterpret_cast<const uint32_t *>(stage + (v_off[k] ^ (q << 5)));
-                    mma_f16_16816(o[2 * q], codes_f16x2<0>(vw[0], vw[1]),
-                                  codes_f16x2<1>(vw[0], vw[1]), codes_f16x2<0>(vw[2], vw[3]),
-                                  codes_f16x2<1>(vw[2], vw[3]), pa0, pa2);
-                    mma_f16_16816(o[2 * q + 1], codes_f16x2<2>(vw[0], vw[1]),
-                                  codes_f16x2<3>(vw[0], vw[1]), codes_f16x2<2>(vw[2], vw[3]),
-                                  codes_f16x2<3>(vw[2], vw[3]), pa0, pa2);
+                for (int m = 0; m < kVPairs; ++m) {
+                    uint32_t e0, e1, e2, e3;
+                    ldsm_x2_trans_b8(vbase + v_ldm[m], e0, e1, e2, e3);
+                    uint32_t a0, a1, a2, a3;
+                    codes_word_f16x2(e0, a0, a2);
+                    codes_word_f16x2(e1, a1, a3);
+                    mma_f16_16816(o[2 * m], a0, a1, a2, a3, pa0, pa2);
+                    codes_word_f16x2(e2, a0, a2);
+                    codes_word_f16x2(e3, a1, a3);
+                    mma_f16_16816(o[2 * m + 1], a0, a1, a2, a3, pa0, pa2);
                 }
             }
             last_st = st;
@@ -771,8 +779,8 @@ __global__ void __launch_bounds__(kThreads, 3)
                 float *dst = red_o + (warp * kMaxGroup + row) * kRowStride;
 #pragma unroll
                 for (int n = 0; n < D / 16; ++n) {
-                    const int dim = 32 * (n >> 1) + 4 * r + 2 * (n & 1);
-                    *reinterpret_cast<float2 *>(dst + dim) = make_float2(o[n][e], o[n][2 + e]);
+                    dst[16 * n + r] = o[n][e];
+                    dst[16 * n + r + 8] = o[n][2 + e];
                 }
                 if (r == 0) {
                     red_m[warp * kMaxGroup + row] = m_run[e];

@@ -490,6 +490,18 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return r;
 }
 
+// Two 16x16 matrices of bytes from shared memory, transposed (ldmatrix .m16n16 .trans .b8):
+// lanes 0-15 give the 16-byte rows of matrix 0, lanes 16-31 those of matrix 1.  Lane l
+// (g = l / 4, t = l % 4) receives, per matrix, the bytes of rows 4t .. 4t + 3 in column g (d0)
+// and in column g + 8 (d1).  Ordered after earlier volatile asm (the mbarrier waits).
+__device__ __forceinline__ void ldsm_x2_trans_b8(uint32_t addr, uint32_t &d0, uint32_t &d1,
+                                                 uint32_t &d2, uint32_t &d3)
+{
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr));
+}
+
 // Transpose of an 8x8 matrix of 16-bit values held as one register per lane (lane l: row
 // l / 4, columns 2 (l % 4) and 2 (l % 4) + 1): lane l receives row l / 4 of the transpose.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
