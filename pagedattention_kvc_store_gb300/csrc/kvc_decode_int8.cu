@@ -452,6 +452,17 @@ __global__ void __launch_bounds__(kThreads, 3)
             ++p;
             return true;
         };
+        // per-lane constants of the copies: lane 4 j + op issues page j's K codes (op 0), V
+        // codes (1), K scales (2) or V scales (3); page sizes are powers of two
+        const int shP = __ffs(P) - 1;
+        const int j = lane >> 2;
+        const int op = lane & 3;
+        const uint32_t dst_off = op == 0   ? j * P * D
+                                 : op == 1 ? kOffV + j * P * D
+                                 : op == 2 ? kOffKs + j * P * 4
+                                           : kOffVs + j * P * 4;
+        const float *scale_base = op == 2 ? a.k_scales : a.v_scales;
+        const int c1 = a.hnd ? 0 : kvh;
         while (ok && w.g < g1) {
             const int blk0 = w.blk;
             const int nblk = static_cast<int>(min(static_cast<long long>(w.nb - blk0), g1 - w.g));
@@ -461,9 +472,13 @@ __global__ void __launch_bounds__(kThreads, 3)
                 break;
             }
             const int32_t *bt_row = a.block_table + static_cast<size_t>(s) * a.bt_stride;
-            const int unit_pages = (ctx + P - 1) / P;
-            int cached_base = -32;
-            int cached_page = 0;
+            const int unit_pages = (ctx + P - 1) >> shP;
+            // page ids in windows of 32 (one per lane), the next window requested one window
+            // ahead; a stage's pages never straddle two windows (64 / P divides 32)
+            int cached_base = blk0 << (6 - shP);
+            int cached_page = cached_base + lane < unit_pages ? bt_row[cached_base + lane] : 0;
+            int next_page =
+                cached_base + 32 + lane < unit_pages ? bt_row[cached_base + 32 + lane] : 0;
             // this piece writes the new token when it ends at the unit's newest position:
             // before the last stage's copies read that page's codes and scales
             const bool writes_new = a.k_new != nullptr && !w.over && blk0 + nblk == w.nb;
@@ -478,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                     k_row_new[e] = __ldg(kn + e);
                     v_row_new[e] = __ldg(vn + e);
                 }
-                new_page = bt_row[(ctx - 1) / P];
+                new_page = bt_row[(ctx - 1) >> shP];
             }
             for (int b = 0; b < nblk; ++b) {
                 const int st = i % kStages;
@@ -489,20 +504,20 @@ __global__ void __launch_bounds__(kThreads, 3)
                 }
                 const int blk = blk0 + b;
                 const int keys = min(kStageKeys, ctx - blk * kStageKeys);
-                const int np = (keys + P - 1) / P;
+                const int np = (keys + P - 1) >> shP;
                 if (lane == 0)
                     mbar_arrive_expect_tx(&full[st],
-                                          static_cast<uint32_t>(np * P * (2 * D + 2 * 4)));
+                                          static_cast<uint32_t>((np << shP) * (2 * D + 2 * 4)));
                 __syncwarp();
                 uint8_t *stage = smem + st * kStageBytes;
-                const int lp0 = blk * kStageKeys / P;
-                if (lp0 + np > cached_base + 32) {
-                    cached_base = lp0;
-                    cached_page = (lp0 + lane < unit_pages) ? bt_row[lp0 + lane] : 0;
+                const int lp0 = blk << (6 - shP);
+                if (lp0 >= cached_base + 32) {
+                    cached_base += 32;
+                    cached_page = next_page;
+                    next_page = cached_base + 32 + lane < unit_pages
+                                    ? bt_row[cached_base + 32 + lane]
+                                    : 0;
                 }
-                // lane 4 j + op: page j's K codes, V codes, K scales, V scales
-                const int j = lane >> 2;
-                const int op = lane & 3;
                 const int page = __shfl_sync(0xffffffffu, cached_page, (lp0 - cached_base + j) & 31);
                 if (writes_new && b + 1 == nblk) {
                     const int off_new = (ctx - 1) % P;
@@ -525,18 +540,13 @@ __global__ void __launch_bounds__(kThreads, 3)
                     fence_proxy_async_global();
                 }
                 if (j < np) {
-                    if (op == 0) {
-                        tma_load_3d(stage + j * P * D, &tmap_k, 0, a.hnd ? 0 : kvh,
-                                    a.hnd ? page * Hkv + kvh : page * P, &full[st], policy);
-                    } else if (op == 1) {
-                        tma_load_3d(stage + kOffV + j * P * D, &tmap_v, 0, a.hnd ? 0 : kvh,
-                                    a.hnd ? page * Hkv + kvh : page * P, &full[st], policy);
-                    } else {
-                        const float *src = (op == 2 ? a.k_scales : a.v_scales) +
-                                           (static_cast<size_t>(page) * Hkv + kvh) * P;
-                        bulk_load(stage + (op == 2 ? kOffKs : kOffVs) + j * P * 4, src, P * 4,
-                                  &full[st]);
-                    }
+                    const int pk = page * Hkv + kvh;   // (page, kv head): scales, HND boxes
+                    if (op < 2)
+                        tma_load_3d(stage + dst_off, op == 0 ? &tmap_k : &tmap_v, 0, c1,
+                                    a.hnd ? pk : page << shP, &full[st], policy);
+                    else
+                        bulk_load(stage + dst_off, scale_base + (static_cast<size_t>(pk) << shP),
+                                  P * 4, &full[st]);
                 }
                 ++i;
             }
