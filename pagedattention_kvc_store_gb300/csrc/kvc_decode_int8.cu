@@ -426,17 +426,29 @@ __global__ void __launch_bounds__(kThreads, 3)
             ok = ok && off < w.nb;
             w.blk = ok ? static_cast<int>(off) : 0;
         }
+        // a piece's query rows (bf16 [G][D], 16 bytes per lane and step), requested with its
+        // page ids so that both round trips overlap, and stored when the piece is handed over
+        constexpr int kQSteps = kMaxGroup * D / 8 / 32;
+        uint4 q_rows[kQSteps];
+        auto load_q = [&](int s) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                a.q + (static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G) * D);
+#pragma unroll
+            for (int k = 0; k < kQSteps; ++k)
+                if (lane + 32 * k < G * D / 8)
+                    q_rows[k] = src[lane + 32 * k];
+        };
         // hands piece p (nblk = 0: the end) over with its query rows, once the consumers have
         // taken piece p - 1's
         auto hand_over = [&](int s, int blk0, int nblk, int ctx, int nb) -> bool {
             if (p > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty, (p - 1) & 1)))
                 return false;
             if (nblk > 0) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    a.q + (static_cast<size_t>(s) * a.q_heads + static_cast<size_t>(kvh) * G) * D);
                 uint4 *dst = reinterpret_cast<uint4 *>(qbuf);
-                for (int k = lane; k < G * D / 8; k += 32)
-                    dst[k] = src[k];
+#pragma unroll
+                for (int k = 0; k < kQSteps; ++k)
+                    if (lane + 32 * k < G * D / 8)
+                        dst[lane + 32 * k] = q_rows[k];
             }
             if (lane == 0) {
                 desc->s = s;
@@ -467,10 +479,11 @@ __global__ void __launch_bounds__(kThreads, 3)
             const int blk0 = w.blk;
             const int nblk = static_cast<int>(min(static_cast<long long>(w.nb - blk0), g1 - w.g));
             const int s = w.s, ctx = w.ctx;
-            if (nblk <= 0 || !hand_over(s, blk0, nblk, ctx, w.nb)) {
+            if (nblk <= 0) {
                 ok = false;
                 break;
             }
+            load_q(s);
             const int32_t *bt_row = a.block_table + static_cast<size_t>(s) * a.bt_stride;
             const int unit_pages = (ctx + P - 1) >> shP;
             // page ids in windows of 32 (one per lane), the next window requested one window
@@ -549,6 +562,11 @@ __global__ void __launch_bounds__(kThreads, 3)
                                   P * 4, &full[st]);
                 }
                 ++i;
+                // the piece goes to the consumers once its first stage is on its way
+                if (b == 0 && !hand_over(s, blk0, nblk, ctx, w.nb)) {
+                    ok = false;
+                    break;
+                }
             }
             if (!ok)
                 break;
