@@ -893,6 +893,7 @@ __global__ void __launch_bounds__(128) merge_flat_kernel(const Args a)
     pdl_wait();
     pdl_trigger();
     constexpr int V = D / 32;
+    constexpr int kPre = 4;   // pieces whose rows are requested together with the lse values
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= a.num_seqs * a.q_heads)
@@ -902,35 +903,58 @@ __global__ void __launch_bounds__(128) merge_flat_kernel(const Args a)
     const int G = a.group;
     const int unit = s * a.kv_heads + h / G;
     const int g = h - (h / G) * G;
+    // both lookups in one round trip (a unit with no positions has no pieces, and its slot
+    // info is never written: only its context decides)
+    const int ctx = clamped_ctx(a, s);
+    const int2 info = a.unit_info[unit];
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v)
         acc[v] = 0.0f;
     float sum = 0.0f;
-    if (clamped_ctx(a, s) > 0) {
-        const int2 info = a.unit_info[unit];
+    if (ctx > 0) {
         if (info.y == 1)
-            return;
+            return;   // the unit's only piece wrote the rows
         const float *lse = a.part_lse + static_cast<size_t>(info.x) * G + g;
         const float *po = a.part_o + (static_cast<size_t>(info.x) * G + g) * D + lane * V;
+        // second round trip: every piece's lse (lane j holds piece j, j + 32, ...) and the
+        // first kPre pieces' rows
+        float pre[kPre][V];
+#pragma unroll
+        for (int j = 0; j < kPre; ++j)
+            if (j < info.y) {
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    pre[j][v] = __ldcg(po + static_cast<size_t>(j) * G * D + v);
+            }
         float M = -INFINITY;
-        for (int j = lane; j < info.y; j += 32)
-            M = fmaxf(M, lse[static_cast<size_t>(j) * G]);
+        const float mine = lane < info.y ? __ldcg(lse + static_cast<size_t>(lane) * G) : -INFINITY;
+        M = mine;
+        for (int j = lane + 32; j < info.y; j += 32)
+            M = fmaxf(M, __ldcg(lse + static_cast<size_t>(j) * G));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         if (M != -INFINITY) {
-#pragma unroll 4
-            for (int j = 0; j < info.y; ++j) {
-                const float lj = lse[static_cast<size_t>(j) * G];
-                if (lj == -INFINITY)
-                    continue;
+#pragma unroll
+            for (int j = 0; j < kPre; ++j) {
+                if (j < info.y) {
+                    const float wj = fast_exp2((__shfl_sync(0xffffffffu, mine, j) - M) * kLog2e);
+                    sum += wj;
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+                        acc[v] = fmaf(wj, pre[j][v], acc[v]);
+                }
+            }
+            for (int j = kPre; j < info.y; ++j) {
+                const float lj = j < 32 ? __shfl_sync(0xffffffffu, mine, j)
+                                        : __ldcg(lse + static_cast<size_t>(j) * G);
                 const float wj = fast_exp2((lj - M) * kLog2e);
                 sum += wj;
                 const float *src = po + static_cast<size_t>(j) * G * D;
 #pragma unroll
                 for (int v = 0; v < V; ++v)
-                    acc[v] = fmaf(wj, src[v], acc[v]);
+                    acc[v] = fmaf(wj, __ldcg(src + v), acc[v]);
             }
         }
     }
