@@ -175,6 +175,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap *tmap_k, const CUte
             prefetch_tensormap(tmap_v);
         }
         const uint64_t policy = l2_policy_evict_first();
+        const int shP = __ffs(P) - 1;   // page sizes are powers of two
         int cached_base = 0;
         int cached_page = pre_page;
         int issued = 0;
@@ -196,13 +197,13 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap *tmap_k, const CUte
             }
             const int rel0 = b * kStageKeys;
             const int keys = min(kStageKeys, k_end - k_begin - rel0);
-            const int np = (keys + P - 1) / P;
+            const int np = (keys + P - 1) >> shP;
             if (lane == 0)
-                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(np * P * D * 2 * 2));
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((np << shP) * D * 2 * 2));
             __syncwarp();
             uint8_t *kdst = smem + st * Geom::kStageBytes;
             uint8_t *vdst = kdst + Geom::kTileBytes;
-            const int lp0 = rel0 / P;   // first page of the stage inside this chunk
+            const int lp0 = rel0 >> shP;   // first page of the stage inside this chunk
             if (lp0 + np > cached_base + 32) {
                 cached_base = lp0;
                 cached_page = (lp0 + lane < n_pages) ? bt_row[lp0 + lane] : 0;
@@ -235,7 +236,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap *tmap_k, const CUte
             if (i < np) {
                 const int off = i * P * D * 2;
                 // NHD maps {64, slot, half, kv head}; HND maps {64, offset, half, block}
-                const int c1 = a.hnd ? 0 : page * P;
+                const int c1 = a.hnd ? 0 : page << shP;
                 const int c3 = a.hnd ? page * a.kv_heads + kvh : kvh;
                 if (lane & 1)
                     tma_load_4d_hint(vdst + off, tmap_v, 0, c1, 0, c3, &full[st], policy);
