@@ -1004,9 +1004,8 @@ kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
     const float sc = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(pool.head_dim));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    cudaError_t err = kvc::launch_grouped_setup(part_lse, key_start, group_indptr, group_seqs,
-                                                prefix_len, num_groups, num_seqs, q_heads,
-                                                g.n_prefix, g.stride, pool.page_size, bt_stride,
+    cudaError_t err = kvc::launch_grouped_setup(key_start, group_indptr, group_seqs, prefix_len,
+                                                num_groups, num_seqs, pool.page_size, bt_stride,
                                                 s);
     if (err != cudaSuccess)
         return cuda_fail(err, "grouped setup launch");

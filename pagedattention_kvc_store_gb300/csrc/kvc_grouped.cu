@@ -7,8 +7,8 @@
 // only the reading of the shared pages is done once per group instead of once per member.
 //
 // Decomposition (all partials are normalised fp32 pieces with their log-sum-exp):
-//   setup   grouped_setup_kernel: each sequence's key start (the end of its group's prefix,
-//           whole pages; 0 outside groups) and every prefix partial marked empty;
+//   setup   grouped_setup_kernel (one block): each sequence's key start (the end of its
+//           group's prefix, whole pages; 0 outside groups);
 //   prefix  one CTA per (prefix chunk, kv head, group): the chunk's pages, read once, against
 //           the query rows of every member of the group (members x G rows, at most 64), on
 //           mma.sync tiles of 16 rows;
@@ -16,7 +16,12 @@
 //           member's positions from its key start;
 //   merge   log-sum-exp over prefix and suffix partials (merge_kernel).
 // Prefix and suffix CTAs are one grid (grouped_decode_kernel), prefix CTAs first: the suffix
-// CTAs take the SMs as the prefix CTAs drain.  A TMA producer warp streams the prefix pages
+// CTAs take the SMs as the prefix CTAs drain.  A prefix split that holds no position of its
+// group marks the split empty (lse -inf) for the group's rows, and the first suffix CTA of a
+// sequence that starts at position 0 (no shared prefix) marks all of its rows' prefix splits
+// empty, so every prefix partial the merge reads is written in this grid.  Prefix CTAs read
+// nothing the setup kernel writes, so they start without waiting for it (the setup kernel
+// itself waits for all earlier work before it lets them launch); suffix CTAs wait for it.  A TMA producer warp streams the prefix pages
 // (one box per page) into a 3-deep swizzled ring; four consumer warps cover 1, 2 or 4 row
 // tiles, the warps of one tile splitting each 64-position stage between them and combining
 // through shared memory at the end.
@@ -67,39 +72,25 @@ struct Args {
     uint32_t *err;   // the caller's device error word, or null (this file's own word)
 };
 
-// Block 0 sets every sequence's key start: 0, then, for each group member, the end of the
-// group's prefix in whole pages (the two phases separated by the block barrier).  The other
-// blocks mark every prefix split of every row empty (lse -inf): prefix CTAs overwrite the
-// splits that hold positions of a member.
-__global__ void grouped_setup_kernel(float *__restrict__ part_lse, int32_t *__restrict__ key_start,
+// Every sequence's key start: 0, then, for each group member, the end of the group's prefix in
+// whole pages (the two phases separated by the block barrier).  One block.
+__global__ void grouped_setup_kernel(int32_t *__restrict__ key_start,
                                      const int32_t *__restrict__ group_indptr,
                                      const int32_t *__restrict__ group_seqs,
                                      const int32_t *__restrict__ prefix_len, int num_groups,
-                                     int num_seqs, int q_heads, int n_prefix, int split_stride,
-                                     int page_size, int bt_stride)
+                                     int num_seqs, int page_size, int bt_stride)
 {
     pdl_wait();
     pdl_trigger();
-    if (blockIdx.x == 0) {
-        for (int s = threadIdx.x; s < num_seqs; s += blockDim.x)
-            key_start[s] = 0;
-        __syncthreads();
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int g = warp; g < num_groups; g += blockDim.x >> 5) {
-            int pre = (prefix_len[g] / page_size) * page_size;   // whole pages only
-            pre = min(max(pre, 0), bt_stride * page_size);
-            for (int i = group_indptr[g] + lane; i < group_indptr[g + 1]; i += 32)
-                key_start[group_seqs[i]] = pre;
-        }
-        return;
-    }
-    const size_t total = static_cast<size_t>(num_seqs) * q_heads * n_prefix;
-    const size_t step = static_cast<size_t>(gridDim.x - 1) * blockDim.x;
-    for (size_t i = static_cast<size_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < total;
-         i += step) {
-        const size_t row = i / n_prefix;
-        const size_t j = i - row * n_prefix;
-        part_lse[row * split_stride + j] = -INFINITY;
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x)
+        key_start[s] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int g = warp; g < num_groups; g += blockDim.x >> 5) {
+        int pre = (prefix_len[g] / page_size) * page_size;   // whole pages only
+        pre = min(max(pre, 0), bt_stride * page_size);
+        for (int i = group_indptr[g] + lane; i < group_indptr[g + 1]; i += 32)
+            key_start[group_seqs[i]] = pre;
     }
 }
 
@@ -298,8 +289,16 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUte
     prefix = min(max(prefix, 0), a.bt_stride * P);
     const int k_begin = split * a.chunk;
     const int k_end = min(prefix, k_begin + a.chunk);
-    if (k_begin >= k_end || rows <= 0)
-        return;   // the setup kernel already marked this split empty for every row
+    if (k_begin >= k_end || rows <= 0) {
+        // no position of the group's prefix in this split: empty for each member row
+        for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+            const int seq = a.group_seqs[m0 + r / G];
+            const size_t row = static_cast<size_t>(seq) * a.q_heads +
+                               static_cast<size_t>(kvh) * G + (r - (r / G) * G);
+            a.part_lse[row * a.split_stride + split] = -INFINITY;
+        }
+        return;
+    }
     const int leader = a.group_seqs[m0];
     const int n_blocks = (k_end - k_begin + kStageKeys - 1) / kStageKeys;
     const int first_page = k_begin / P;
@@ -637,23 +636,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                           const __grid_constant__ CUtensorMap tmap_v, const Args a,
                           const dec::Args da, const int n_prefix_ctas)
 {
-    pdl_wait();
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int idx = blockIdx.x;
     if (idx < n_prefix_ctas) {
+        // reads only inputs older than the setup kernel (queries, tables, groups), which has
+        // itself waited for all earlier work before letting this grid launch
         const int split = idx % a.n_split;
         const int rest = idx / a.n_split;
         prefix_cta<D, NMT>(&tmap_k, &tmap_v, a, split, rest % a.kv_heads, rest / a.kv_heads,
                            smem);
     } else {
+        pdl_wait();   // the key starts
         const int j = idx - n_prefix_ctas;
         const int split = j % da.n_split;
         const int rest = j / da.n_split;
-        dec::decode_cta<D, true>(&tmap_k, &tmap_v, da, split, rest % da.kv_heads,
-                                 rest / da.kv_heads, smem,
+        const int kvh = rest % da.kv_heads;
+        const int s = rest / da.kv_heads;
+        if (split == 0 && da.key_start[s] == 0) {
+            // a sequence without a shared prefix: its rows' prefix splits are empty
+            const int G = da.group;
+            for (int t = threadIdx.x; t < G * a.n_split; t += blockDim.x) {
+                const size_t row = static_cast<size_t>(s) * da.q_heads +
+                                   static_cast<size_t>(kvh) * G + t / a.n_split;
+                a.part_lse[row * a.split_stride + (t - (t / a.n_split) * a.n_split)] = -INFINITY;
+            }
+        }
+        dec::decode_cta<D, true>(&tmap_k, &tmap_v, da, split, kvh, s, smem,
                                  da.err ? da.err : &g_grouped_errors);
     }
 }
@@ -716,18 +727,14 @@ cudaError_t launch_d(const GroupedPrefixLaunch &p, const DecodeLaunch &l, const 
 
 }  // namespace
 
-cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int32_t *group_indptr,
+cudaError_t launch_grouped_setup(int32_t *key_start, const int32_t *group_indptr,
                                  const int32_t *group_seqs, const int32_t *prefix_len,
-                                 int num_groups, int num_seqs, int q_heads, int n_prefix_splits,
-                                 int split_stride, int page_size, int bt_stride,
+                                 int num_groups, int num_seqs, int page_size, int bt_stride,
                                  cudaStream_t stream)
 {
-    const size_t total = static_cast<size_t>(num_seqs) * q_heads * n_prefix_splits;
-    const size_t want = (total + 255) / 256;
-    const int blocks = 1 + static_cast<int>(want < 1024 ? want : 1024);
-    return launch_pdl(grouped_setup_kernel, dim3(blocks), dim3(256), 0, stream, part_lse,
-                      key_start, group_indptr, group_seqs, prefix_len, num_groups, num_seqs,
-                      q_heads, n_prefix_splits, split_stride, page_size, bt_stride);
+    return launch_pdl(grouped_setup_kernel, dim3(1), dim3(256), 0, stream, key_start,
+                      group_indptr, group_seqs, prefix_len, num_groups, num_seqs, page_size,
+                      bt_stride);
 }
 
 cudaError_t launch_group_detect(const int32_t *block_table, int bt_stride,

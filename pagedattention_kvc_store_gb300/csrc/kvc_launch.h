@@ -170,12 +170,11 @@ cudaError_t launch_decode(const DecodeLaunch &a, const CUtensorMap &tmap_k,
 cudaError_t launch_merge(void *out, int out_f32, const float *part_o, const float *part_lse,
                          int rows, int n_split, int head_dim, float *lse_out,
                          cudaStream_t stream);
-// Grouped decode: sets every row's prefix partials to empty and key_start to 0, then each
-// group's members' key_start to the group's prefix length.
-cudaError_t launch_grouped_setup(float *part_lse, int32_t *key_start, const int32_t *group_indptr,
+// Grouped decode: sets key_start to 0, then each group's members' key_start to the group's
+// prefix length (one block; the grouped grid marks the empty prefix partials itself).
+cudaError_t launch_grouped_setup(int32_t *key_start, const int32_t *group_indptr,
                                  const int32_t *group_seqs, const int32_t *prefix_len,
-                                 int num_groups, int num_seqs, int q_heads, int n_prefix_splits,
-                                 int split_stride, int page_size, int bt_stride,
+                                 int num_groups, int num_seqs, int page_size, int bt_stride,
                                  cudaStream_t stream);
 // Groups from block tables (adjacent sequences agreeing on leading shareable pages), one CTA:
 // group_indptr[num_seqs / 2 + 1], group_seqs[num_seqs], prefix_len[num_seqs / 2], num_groups[1].
