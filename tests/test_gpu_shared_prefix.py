@@ -30,7 +30,8 @@ def _run_shared(case, g):
     pool = kvc.pool_desc(g.d.k_pool)
     ws = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
                                            len(case.groups), max_prefix)
-    work = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    # every byte 0xFF: a partial slot the grid failed to write (or to mark empty) reads as NaN
+    work = torch.full((ws,), 0xFF, dtype=torch.uint8, device="cuda")
     out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.float32,
                       device="cuda")
     kvc.kvc_decode_shared_prefix(out, g.d.q, g.d.k_pool, g.d.v_pool, g.d.block_table,
