@@ -6,10 +6,11 @@
 // says, the cache is not dequantised: a key's scale multiplies its score, and a value's scale
 // its probability before the PV product.  Codes are converted to fp16 in registers (exact:
 // |code| <= 127) for the tensor cores; the scales stay outside the products.  fp16 rather than
-// bf16 because two codes become an exact fp16 pair in three integer/half operations: bytes
-// b placed under the exponent 0x64 read as 1024 + b, and the code is b - 128; the query is
-// converted to fp16 once per piece (scaled by a power of two when it would overflow fp16), and
-// the probabilities (at most 1) times the value scales enter the PV product as fp16.
+// bf16 because four codes become two exact fp16 pairs in five integer/half operations: the
+// sign bits flipped (b = code + 128), the bytes placed under the exponent 0x64 (1024 + b), and
+// 1152 subtracted; the query is converted to fp16 once per piece (scaled by a power of two
+// when it would overflow fp16), and the probabilities (at most 1) times the value scales enter
+// the PV product as fp16.
 //
 // Layout: codes [num_pages * P][Hkv][D] int8 like the bf16 pools (D bytes per vector), or
 // [num_pages][Hkv][P][D] (HND); scales [num_pages][Hkv][P] fp32, so the P scales of one (page,
@@ -24,7 +25,7 @@
 // break: the pieces of the sequences it covers follow one another through the same ring.  The
 // runs of all kv heads have the same bounds, so the CTAs that read one sequence's positions
 // for its kv heads start together and stay in step (the kv heads of a position share its NHD
-// rows: 8% faster than unaligned runs).  A piece that is a whole unit (sequence, kv head)
+// rows; on 64 sequences of 512-4,096 positions 76.9 against 91.3 us for unaligned runs).  A piece that is a whole unit (sequence, kv head)
 // writes the output rows; the others write a partial (rows normalised by their own sum, and
 // the log-sum-exp) to slot h (S + R) + s + run of the workspace -- distinct for every piece,
 // consecutive for one unit's pieces -- and the unit's first piece records (first slot, piece
@@ -43,12 +44,14 @@
 //   free, so thread (r, t) takes dims (D / 4) t + 4 kk .. + 3 for k-step kk: its K codes of a
 //   position are D / 4 contiguous bytes, one word per k-step, and its Q pairs are two
 //   contiguous pairs;
-//   O^T += V^T (P * v_scale)^T with M = 16 dims and N = 8 query heads.  A thread's scores are
-//   positions r and r + 8 of heads 2t and 2t + 1; one 8x8 transpose (movmatrix) per half
-//   turns the fp16 probabilities into the B fragment of this product (positions 2t, 2t + 1 /
-//   8 + 2t, 9 + 2t of head r).  The dims of tile dt are permuted so that thread row r reads
-//   dims 32 q + 4 r .. + 3 (q = 0 .. D / 32 - 1), one 4-byte word per position and q, and the
-//   accumulators are put back in dim order when the warps combine.  The O^T rows a thread
+//   O^T += V^T (P * v_scale)^T with M = 16 dims and N = 8 query heads, V^T from a transposing
+//   8-bit ldmatrix (m16n16, x2: two dim tiles per load), which gives each thread the bytes of
+//   positions 4t .. 4t + 3 of one dim per register, converted like K's.  The contraction over
+//   the warp's 16 positions runs in that order, so contraction index k is position
+//   4 ((k % 8) / 2) + 2 (k / 8) + k % 2; a thread's score rows r, r + 8 (its S^T rows, and so
+//   the K rows it reads) are the positions of k = r and r + 8, and one 8x8 transpose
+//   (movmatrix) per half turns its fp16 probabilities (heads 2t, 2t + 1) into the B fragment
+//   of the PV product (k = 2t, 2t + 1 / 2t + 8, 2t + 9; head r).  The O^T rows a thread
 //   accumulates are its own score heads 2t, 2t + 1, so the rescale needs no exchange.
 // Online softmax in base 2, masked positions excluded before the exponential and their
 // probabilities set to 0 by selection (a scale left in an unused slot may be NaN).  At the end
@@ -249,19 +252,6 @@ __device__ __forceinline__ void quantise_store_row(const uint32_t (&x)[E / 2], i
         *scale_out = scale;
 }
 
-// fp16 pair (low: byte c of a, high: byte c of b) of two words of int8 codes, exact.  The
-// bytes are moved under exponent bits 0x64 (fp16 1024 + m for m in 0..255) with the sign bit
-// of the code flipped (m = code + 128), and 1152 is subtracted from both halves.
-template <int c>
-__device__ __forceinline__ uint32_t codes_f16x2(uint32_t a, uint32_t b)
-{
-    const uint32_t bytes = __byte_perm(a, b, c | ((4 + c) << 8));   // [a.c, a.0, b.c, a.0]
-    const uint32_t biased = (bytes & 0x00FF00FFu) ^ 0x64806480u;
-    const __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&biased),
-                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
 // Offset of byte `col` of stage row `row` in a [64][D] code tile: 128-byte rows with the
 // 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)), or 64-byte rows with the 64-byte
 // swizzle (chunk c of row r at c ^ ((r / 2) % 4)).
@@ -271,7 +261,6 @@ __device__ __forceinline__ uint32_t code_offset(int row, int col)
     const int phase = D == 128 ? (row & 7) : ((row >> 1) & 3);
     return static_cast<uint32_t>(row * D + ((((col >> 4) ^ phase)) << 4) + (col & 15));
 }
-
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 3)
