@@ -47,7 +47,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
-    p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer (MB)")
+    p.add_argument("--flush-mb", type=int, default=512,
+                   help="L2 flush: MB written, then half as many read")
     p.add_argument("--append-steps", type=int, default=60)
     p.add_argument("--append-docs", type=int, default=1000,
                    help="documents in the rewind-append leg (smaller for profiler captures)")
@@ -263,6 +264,24 @@ def traffic_from_profile(kernel_tag: str):
 # the CUDA path
 # ---------------------------------------------------------------------------------------
 
+class L2Flush:
+    """The L2 flush run before every timed GPU step, outside its events: a write of a buffer
+    larger than L2 (evicting every input), then a read of another one (256 MB) so that the
+    write's own dirty lines go back to HBM here rather than during the timed step, whose
+    reads would otherwise evict them and pay for their write-back (up to an L2's worth of
+    DRAM writes that are not the step's work)."""
+
+    def __init__(self, torch, mb, dev):
+        self.write_buf = torch.empty(mb << 20, dtype=torch.uint8, device=dev)
+        self.read_buf = torch.ones(max(mb // 2, 1) << 18, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.write_buf.zero_()
+        self.torch.sum(self.read_buf, dim=0, out=self.sink)
+
+
 def time_graph(torch, fn, stream, flush, steps):
     """Capture fn in a CUDA graph; median device time (ms) over `steps` replays, L2 flushed
     between replays outside the timed events."""
@@ -276,7 +295,7 @@ def time_graph(torch, fn, stream, flush, steps):
     torch.cuda.synchronize()
     ts = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         g.replay()
@@ -568,7 +587,8 @@ def headline_config(case, args, world):
     return {"workload": WORKLOAD, "num_seqs": case.num_seqs, "q_heads": case.q_heads,
             "kv_heads": case.kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
             "sum_ctx": int(case.context_lens.sum()),
-            "l2": f"flushed between GPU steps ({args.flush_mb} MB write)",
+            "l2": (f"flushed between GPU steps ({args.flush_mb} MB write, then a "
+                   f"{max(args.flush_mb // 2, 1)} MB read that drains its dirty lines)"),
             "parallelism": f"replicas x{world} (sequences sharded, no collective)"}
 
 
@@ -635,7 +655,7 @@ def run_kvc(args):
     args.cpu_on = rank == 0 and world == 1 and not args.no_cpu_baseline
     if args.no_headline:
         # the legs alone (for profiler captures of one leg's kernels); not a bench line
-        flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+        flush = L2Flush(torch, args.flush_mb, dev)
         stream = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(stream):
             legs = {}
@@ -657,7 +677,7 @@ def run_kvc(args):
     pool = kvc.pool_desc(d.k_pool)
     splits, chunk, ws = kvc.kvc_decode_plan(S, Hq, pool, case.max_ctx, 0)
     work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, args.flush_mb, dev)
 
     def store_part():
         kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, None, case.page_size)
@@ -701,7 +721,7 @@ def run_kvc(args):
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(n)]
             for e0, e1 in evs:
-                flush.zero_()                   # L2 flush, outside the timed events
+                flush()                         # L2 flush, outside the timed events
                 e0.record(stream)
                 graph.replay()
                 e1.record(stream)
@@ -709,7 +729,7 @@ def run_kvc(args):
             return [a.elapsed_time(b) for a, b in evs]
 
         for _ in range(W):
-            flush.zero_()
+            flush()
             g_step.replay()
         torch.cuda.synchronize()
         barrier(world)
@@ -823,7 +843,7 @@ def run_e2e(torch, kvc, case, d, dev, stream, flush, splits, work, steps):
     def timed(fn):
         times = []
         for _ in range(steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -890,7 +910,7 @@ def run_append(torch, kvc, args, dev, stream, flush, peaks, rank):
         torch.cuda.synchronize()
         st_ms, ap_ms = [], []
         for _ in range(args.append_steps):
-            flush.zero_()
+            flush()
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
             g1.replay()
