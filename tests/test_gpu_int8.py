@@ -183,3 +183,27 @@ def test_int8_more_ctas_than_blocks():
         out, pools = run_int8(case, num_splits=splits)
         assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
                                f"INT8 few blocks splits={splits}")
+
+
+@pytest.mark.parametrize("num_seqs", [256, 300])
+def test_int8_large_batch_merge(num_seqs):
+    """Many short sequences (each run of the cut crosses many of them, most units are whole
+    and the rest are merged), with empty sequences among them, the default cut and an
+    explicit one."""
+    case = build_case(1302 + num_seqs, name="int8-many", page_size=16, q_heads=8, kv_heads=2,
+                      head_dim=128, context_lens=lambda rng: rng.integers(1, 400, size=num_seqs),
+                      q_lens=lambda c: np.ones_like(c))
+    for splits in (0, 2):
+        out, pools = run_int8(case, num_splits=splits)
+        assert_attention_close(out_to_f64(out), oracle_int8(case, pools),
+                               f"INT8 {num_seqs} sequences splits={splits}")
+    ctx0 = case.context_lens.copy()
+    ctx0[::7] = 0
+    got = decode_int8_only(case, pools, ctx0, 0)
+    assert not got[ctx0 == 0].any(), "a sequence with no positions has rows of 0"
+    keep = np.flatnonzero(ctx0 > 0)
+    kc, vc, ks, vs = pools
+    ref, _ = oracle.attention_int8(case.q[keep], kc, vc, ks, vs, case.block_table[keep],
+                                   ctx0[keep], np.arange(len(keep) + 1, dtype=np.int32),
+                                   num_threads=16)
+    assert_attention_close(got[keep], ref, f"INT8 {num_seqs} sequences with empty ones")
