@@ -109,21 +109,45 @@ constexpr int kDetectThreads = 1024;
 constexpr int kDetectTile = kDetectThreads;
 constexpr int kDetectMaxMembers = 64;
 
+// The first kAgreeSpan entries of both rows are requested together with the two context
+// lengths (entries below bt_stride are always in the rows), so a pair whose agreement ends
+// within them costs one memory round trip; longer agreements go on kAgreeSpan at a time.
+constexpr int kAgreeSpan = 128;
+
 __device__ int pair_agreement(const int32_t *__restrict__ bt, int bt_stride,
                               const int32_t *__restrict__ ctx, int page_size, int s, int lane)
 {
     if (s == 0)
         return 0;
+    constexpr int kPer = kAgreeSpan / 32;
+    const int32_t *a = bt + static_cast<size_t>(s - 1) * bt_stride;
+    const int32_t *b = bt + static_cast<size_t>(s) * bt_stride;
+    int av[kPer], bv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int k = 32 * u + lane;
+        av[u] = k < bt_stride ? a[k] : 0;
+        bv[u] = k < bt_stride ? b[k] : 0;
+    }
     const int sh0 = min(max(ctx[s - 1] - 1, 0) / page_size, bt_stride);
     const int sh1 = min(max(ctx[s] - 1, 0) / page_size, bt_stride);
     const int lim = min(sh0, sh1);
-    const int32_t *a = bt + static_cast<size_t>(s - 1) * bt_stride;
-    const int32_t *b = bt + static_cast<size_t>(s) * bt_stride;
-    for (int k0 = 0; k0 < lim; k0 += 32) {
-        const int k = k0 + lane;
-        const unsigned diff = __ballot_sync(0xffffffffu, k < lim && a[k] != b[k]);
-        if (diff != 0u)
-            return k0 + __ffs(diff) - 1;
+    for (int k0 = 0; k0 < lim; k0 += kAgreeSpan) {
+        if (k0 > 0) {
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int k = k0 + 32 * u + lane;
+                av[u] = k < lim ? a[k] : 0;
+                bv[u] = k < lim ? b[k] : 0;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = k0 + 32 * u + lane;
+            const unsigned diff = __ballot_sync(0xffffffffu, k < lim && av[u] != bv[u]);
+            if (diff != 0u)
+                return k0 + 32 * u + __ffs(diff) - 1;
+        }
     }
     return lim;
 }
