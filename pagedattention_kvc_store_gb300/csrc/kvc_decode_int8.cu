@@ -200,17 +200,30 @@ struct PieceDesc {
     long long g_last;
 };
 
+// floor((x y + add) / d) for x y + add below 2^64 + 2^63 (d > 0): in 64-bit arithmetic when the
+// product fits (every practical size; a 128-bit quotient is a long software routine), else in
+// 128-bit.
+__device__ __forceinline__ unsigned long long mul_div(unsigned long long x, unsigned long long y,
+                                                      long long add, unsigned long long d)
+{
+    const unsigned long long lo = x * y;
+    if (__umul64hi(x, y) == 0 && (add >= 0 ? lo <= ~0ull - static_cast<unsigned long long>(add)
+                                           : lo >= static_cast<unsigned long long>(-add)))
+        return (lo + static_cast<unsigned long long>(add)) / d;
+    const __int128 num = static_cast<__int128>(static_cast<unsigned __int128>(x) * y) + add;
+    return static_cast<unsigned long long>(static_cast<unsigned __int128>(num) / d);
+}
+
 // Run c of n: blocks [floor(c T / n), floor((c + 1) T / n)) of a kv head's T.
 __device__ __forceinline__ long long run_start(long long c, long long total, long long n)
 {
-    return static_cast<long long>((static_cast<unsigned __int128>(c) * total) / n);
+    return static_cast<long long>(mul_div(c, total, 0, n));
 }
 
 // The run that holds block g: the largest c with run_start(c) <= g.
 __device__ __forceinline__ long long run_of(long long g, long long total, long long n)
 {
-    return static_cast<long long>(
-        (static_cast<unsigned __int128>(g + 1) * n - 1) / static_cast<unsigned __int128>(total));
+    return static_cast<long long>(mul_div(g + 1, n, -1, total));
 }
 
 // Quantises one vector held as E bf16 values per lane (lane l: elements E l .. E l + E - 1;
