@@ -424,10 +424,13 @@ GroupPlan make_group_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc
     const int64_t unit = kvc::kStageKeys;
     if (max_prefix_len > 0 && num_groups > 0) {
         const int64_t units = static_cast<int64_t>(num_groups) * pool.kv_heads;
-        // about 2 CTAs per SM over the prefix (one wave of the grid's resident CTAs): measured
-        // on 32 groups x 8 members with 2,048 shared positions, 2 prefix splits 111.7 us,
-        // 3 splits 113.8, 4 118.0, 5 117.9, 8 130.2
-        const int64_t want = ceil_div(2 * static_cast<int64_t>(device_sm_count()), units);
+        // as many prefix splits as keep the prefix CTAs within one wave of the grid's resident
+        // CTAs (2 per SM), at least one: the rest of that wave takes suffix CTAs from the start
+        // and no second wave of long prefix CTAs sets the tail (measured on 32 groups x 8
+        // members with 2,048 shared positions, 256 (group, kv head) units: 1 split 102.9 us
+        // against 105.0-107.0 for 2; 3, 4, 5 and 8 splits were slower still)
+        const int64_t want =
+            std::max<int64_t>(1, 2 * static_cast<int64_t>(device_sm_count()) / units);
         int64_t chunk = round_up(ceil_div(max_prefix_len, want), unit);
         if (chunk < 256)
             chunk = 256;
