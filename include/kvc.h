@@ -251,9 +251,11 @@ kvc_status kvc_shared_prefix_groups(const int32_t *block_table, int32_t bt_strid
  *   max_group_size  host bound on members per group; max_group_size * G must be <= 64
  *   max_prefix_len  host bound on prefix_len
  *   workspace       kvc_decode_shared_prefix_plan(...) bytes (required), 16-byte aligned
- * The other arguments are kvc_decode's.  Five kernels are enqueued: a set-up pass, the prefix
- * partials (one CTA per prefix chunk, kv head and group), the suffix partials (the decode
- * kernel started at each member's prefix end) and the log-sum-exp merge.
+ * The other arguments are kvc_decode's.  Three kernels are enqueued: a set-up pass (each
+ * sequence's prefix end), one grid of the prefix partials (one CTA per prefix chunk, kv head
+ * and group) followed by the suffix partials (a decode CTA per kv head and sequence, from its
+ * prefix end), and the log-sum-exp merge.  Empty group slots cost a CTA that exits after
+ * reading its group's bounds.
  */
 kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
                                     const void *k_pool, const void *v_pool, kvc_pool_desc pool,
