@@ -200,6 +200,11 @@ struct PieceDesc {
     long long g_last;
 };
 
+// The cost of a piece's start against its blocks' (16 per 64-position block) when the runs are
+// cut: a CTA pays about 0.9 of a block's streaming time for each further sequence its run
+// holds (the combine and write-out of the piece before it, the next piece's query rows).
+constexpr long long kPieceCost = 14;
+
 // floor((x y + add) / d) for x y + add below 2^64 + 2^63 (d > 0): in 64-bit arithmetic when the
 // product fits (every practical size; a 128-bit quotient is a long software routine), else in
 // 128-bit.
@@ -214,16 +219,25 @@ __device__ __forceinline__ unsigned long long mul_div(unsigned long long x, unsi
     return static_cast<unsigned long long>(static_cast<unsigned __int128>(num) / d);
 }
 
-// Run c of n: blocks [floor(c T / n), floor((c + 1) T / n)) of a kv head's T.
-__device__ __forceinline__ long long run_start(long long c, long long total, long long n)
+// Runs are cut in cost units: block g of sequence s sits at cost 16 g + kPieceCost (s + 1)
+// (strictly increasing along a kv head's block order; a kv head's T blocks over S sequences
+// span C = 16 T + kPieceCost S), and run c of n holds the blocks at costs
+// [floor(c C / n), floor((c + 1) C / n)).
+__device__ __forceinline__ long long block_cost(long long g, int s)
 {
-    return static_cast<long long>(mul_div(c, total, 0, n));
+    return 16 * g + kPieceCost * (s + 1);
 }
 
-// The run that holds block g: the largest c with run_start(c) <= g.
-__device__ __forceinline__ long long run_of(long long g, long long total, long long n)
+// Start of run c of n in cost units: floor(c C / n).
+__device__ __forceinline__ long long run_start(long long c, long long cost, long long n)
 {
-    return static_cast<long long>(mul_div(g + 1, n, -1, total));
+    return static_cast<long long>(mul_div(c, cost, 0, n));
+}
+
+// The run that holds cost position x: the largest c with run_start(c) <= x.
+__device__ __forceinline__ long long run_of(long long x, long long cost, long long n)
+{
+    return static_cast<long long>(mul_div(x + 1, n, -1, cost));
 }
 
 // Quantises one vector held as E bf16 values per lane (lane l: elements E l .. E l + E - 1;
@@ -319,13 +333,17 @@ __global__ void __launch_bounds__(kThreads, 3)
         mbar_init(q_empty, kConsumerWarps);
         *abort_flag = 0;
         scratch[0] = -1;
+        scratch[7] = -1;
+        scratch[9] = -1;
         fence_mbar_init();
     }
 
     // ---- this CTA's run of blocks [g0, g1) and where it starts: sequence scratch[0], whose
     // first block has global index scratch[1] (one unit: its context scratch[1] and blocks
-    // scratch[2]).  Every decision below reads shared memory, so the whole CTA takes it alike.
+    // scratch[2]); g0 and g1 in scratch[9] and scratch[7].  Every decision below reads shared
+    // memory, so the whole CTA takes it alike.
     long long g0 = 0, g1 = 0, total = 0;   // per kv head
+    long long cost = 0;                     // the kv head's blocks and pieces in cost units
     long long n_runs = n_run_ctas;          // runs of a kv head: at most one per block
     if (a.per_unit) {
         // one unit per CTA, numbered on its own: blocks [0, nb)
@@ -383,25 +401,36 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
         total = sum;
         n_runs = min(n_run_ctas, total);
+        cost = 16 * total + kPieceCost * S;
         if (run < n_runs) {
-            g0 = run_start(run, total, n_runs);
-            g1 = run_start(run + 1, total, n_runs);
-        }
-        if (g0 < g1 && before <= g0 && g0 < before + mine) {
+            // the run's bounds in cost units; sequence s covers costs [kPieceCost s + 16 B_s,
+            // kPieceCost (s + 1) + 16 (B_s + nb_s)) (B_s: blocks before it), which tile
+            // [0, cost), so exactly one thread finds each bound below the end: the first block
+            // at or past it (B_s + nb_s when it falls after s's last block)
+            const long long c0 = run_start(run, cost, n_runs);
+            const long long c1 = run_start(run + 1, cost, n_runs);
             long long acc = before;
             for (int s = lo; s < hi; ++s) {
                 const long long nb = blocks_of(clamped_ctx(a, s));
-                if (g0 < acc + nb) {
-                    scratch[0] = s;
-                    scratch[1] = acc;
-                    break;
+                const long long lo_cost = kPieceCost * s + 16 * acc;
+                const long long first = block_cost(acc, s);
+                const long long hi_cost = first + 16 * nb;
+                if (c0 >= lo_cost && c0 < hi_cost) {
+                    const long long off = min(nb, max(0LL, (c0 - first + 15) / 16));
+                    scratch[9] = acc + off;
+                    scratch[0] = off < nb ? s : s + 1;   // empty ones are skipped by the walk
+                    scratch[1] = off < nb ? acc : acc + nb;
                 }
+                if (c1 >= lo_cost && c1 < hi_cost)
+                    scratch[7] = acc + min(nb, max(0LL, (c1 - first + 15) / 16));
                 acc += nb;
             }
         }
         __syncthreads();
-        if (g0 >= g1 || scratch[0] < 0)
-            return;   // an empty run (fewer blocks than CTAs)
+        g0 = scratch[9] >= 0 ? scratch[9] : total;
+        g1 = scratch[7] >= 0 ? scratch[7] : total;   // the last run ends with the blocks
+        if (run >= n_runs || g0 >= g1 || scratch[0] < 0 || scratch[0] >= S)
+            return;   // an empty run
     }
 
     if (warp == kConsumerWarps) {
@@ -869,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         // the unit's first piece: where its pieces are and how many (the CTA runs holding
         // its first and last blocks)
         if (threadIdx.x == 0 && blk0 == 0 && !a.per_unit) {
-            const long long last = run_of(g_last, total, n_runs);
+            const long long last = run_of(block_cost(g_last, s), cost, n_runs);
             a.unit_info[unit] = make_int2(slot, static_cast<int>(last - run + 1));
         }
         if (!ok)
