@@ -427,9 +427,10 @@ kvc_status kvc_store_int8(void *k_codes, void *v_codes, float *k_scales, float *
 /*
  * kvc_decode_int8 -- kvc_decode over INT8 pages (same arguments and outputs).  Its work plan
  * differs from kvc_decode's split-K: for each kv head, the positions of all sequences (in
- * 64-position blocks, sequence after sequence) are cut into equal runs, one CTA each, so that
- * every CTA has the same work however the context lengths are spread; a sequence covered by
- * several runs has its partial results merged (log-sum-exp) by a second launch.
+ * 64-position blocks, sequence after sequence) are cut into runs of equal cost (a block, plus
+ * most of a block for each sequence a run starts), one CTA each, so that every CTA has the
+ * same work however the context lengths are spread; a sequence covered by several runs has its
+ * partial results merged (log-sum-exp) by a second launch.
  * kvc_decode_int8_plan gives the plan for num_splits: 0 = one wave of resident CTAs (the
  * default); 1 = one CTA per (sequence, kv head), no workspace and no merge; n > 1 = n runs
  * per sequence (num_seqs * n per kv head).  A plan never has more runs per kv head than

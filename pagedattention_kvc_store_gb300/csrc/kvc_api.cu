@@ -138,7 +138,8 @@ Plan make_plan(int32_t num_seqs, int32_t q_heads, const kvc_pool_desc &pool, int
 
 // INT8 decode plan.  num_splits = 1: one CTA per (sequence, kv head) unit, no workspace.
 // Otherwise each kv head's positions, in 64-position blocks over all sequences, are cut into
-// `runs` equal runs, one CTA per (run, kv head): one wave of resident CTAs (num_splits = 0) or
+// `runs` runs of equal cost (the kernel weighs each sequence start against its blocks), one CTA
+// per (run, kv head): one wave of resident CTAs (num_splits = 0) or
 // num_splits runs per sequence, at most one per block.  Workspace: partial rows and
 // log-sum-exps of kv_heads * (num_seqs + runs) slots, and (first slot, piece count) per unit.
 struct Int8Plan {

@@ -16,23 +16,24 @@
 // [num_pages][Hkv][P][D] (HND); scales [num_pages][Hkv][P] fp32, so the P scales of one (page,
 // kv head) are one contiguous run that a single bulk copy brings in.
 //
-// Work partition.  The consumer warps convert every code they read, so a CTA is bound by its
-// own instruction stream, not by HBM: an SM runs at the pace of its three resident CTAs, and
-// every microsecond one of them spends starting up (page ids, first copies) or idle at the end
-// of a ragged grid is lost.  So for each kv head the positions of all sequences, in
-// 64-position blocks (sequence-major), are cut into R equal runs, one per CTA (CTA = run * Hkv
-// + kv head, R * Hkv = one wave of resident CTAs), and each CTA streams its run without a
-// break: the pieces of the sequences it covers follow one another through the same ring.  The
-// runs of all kv heads have the same bounds, so the CTAs that read one sequence's positions
-// for its kv heads start together and stay in step (the kv heads of a position share its NHD
-// rows; on 64 sequences of 512-4,096 positions 76.9 against 91.3 us for unaligned runs).  A piece that is a whole unit (sequence, kv head)
-// writes the output rows; the others write a partial (rows normalised by their own sum, and
-// the log-sum-exp) to slot h (S + R) + s + run of the workspace -- distinct for every piece,
-// consecutive for one unit's pieces -- and the unit's first piece records (first slot, piece
-// count) for the merge (merge_flat_kernel).  With num_splits = 1 the kernel instead runs one
-// CTA per unit (no workspace, no merge).  The producer alone walks the runs; it hands each
-// piece (its sequence, blocks and context) to the consumers in shared memory with the query
-// rows, so all warps of a CTA take the same path whatever the context lengths.
+// Work partition.  The consumer warps convert every code they read, so a CTA is bound by its own
+// instruction stream, not by HBM: an SM runs at the pace of its three resident CTAs, and every
+// microsecond one of them spends starting up (page ids, first copies) or idle at the end of a
+// ragged grid is lost.  So for each kv head the positions of all sequences, in 64-position blocks
+// (sequence-major), are cut into R runs of equal cost, one per CTA (CTA = run * Hkv + kv head, R *
+// Hkv = one wave of resident CTAs), a block costing 16 and each sequence start kPieceCost (a
+// further piece costs its CTA about 0.9 of a block), and each CTA streams its run without a break:
+// the pieces of the sequences it covers follow one another through the same ring.  The runs of all
+// kv heads have the same bounds, so the CTAs that read one sequence's positions for its kv heads
+// start together and stay in step (the kv heads of a position share its NHD rows; on 64 sequences
+// of 512-4,096 positions 76.9 against 91.3 us for unaligned runs).  A piece that is a whole unit
+// (sequence, kv head) writes the output rows; the others write a partial (rows normalised by their
+// own sum, and the log-sum-exp) to slot h (S + R) + s + run of the workspace -- distinct for every
+// piece, consecutive for one unit's pieces -- and the unit's first piece records (first slot,
+// piece count) for the merge (merge_flat_kernel).  With num_splits = 1 the kernel instead runs one
+// CTA per unit (no workspace, no merge).  The producer alone walks the runs; it hands each piece
+// (its sequence, blocks and context) to the consumers in shared memory with the query rows, so all
+// warps of a CTA take the same path whatever the context lengths.
 //
 // CTA: 4 consumer warps and a producer warp, three CTAs per SM.  The producer loads each
 // piece's query rows into shared memory and streams 64-position stages -- per page one TMA box
@@ -308,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint64_t *empty = full + kStages;
     uint64_t *q_full = empty + kStages;
     uint64_t *q_empty = q_full + 1;
-    long long *scratch = reinterpret_cast<long long *>(q_empty + 1);   // [0] s0, [1] base, [2..] sums
+    // [0] first sequence, [1] its first block, [2..6] scan sums, [7] g1, [9] g0
+    long long *scratch = reinterpret_cast<long long *>(q_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(scratch + 8);
 
     const int warp = threadIdx.x >> 5;

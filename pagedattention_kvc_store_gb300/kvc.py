@@ -276,8 +276,9 @@ def kvc_store_int8(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch
 def kvc_decode_int8_plan(num_seqs: int, q_heads: int, pool: PoolDesc, max_ctx: int,
                          num_splits: int = 0) -> Tuple[int, int, int]:
     """(CTAs, block, workspace_bytes) of kvc_decode_int8's plan: per kv head, the positions of
-    all sequences in 64-position blocks are cut into equal runs (num_splits 0: one wave of
-    resident CTAs; 1: one CTA per (sequence, kv head), no workspace; n: n runs per sequence)."""
+    all sequences in 64-position blocks are cut into runs of equal cost (num_splits 0: one
+    wave of resident CTAs; 1: one CTA per (sequence, kv head), no workspace; n: n runs per
+    sequence)."""
     splits, chunk, ws = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
     _check("kvc_decode_int8_plan", lib().kvc_decode_int8_plan(
         int(num_seqs), int(q_heads), pool, int(max_ctx), int(num_splits), ctypes.byref(splits),
