@@ -29,11 +29,12 @@
 // of 512-4,096 positions 76.9 against 91.3 us for unaligned runs).  A piece that is a whole unit
 // (sequence, kv head) writes the output rows; the others write a partial (rows normalised by their
 // own sum, and the log-sum-exp) to slot h (S + R) + s + run of the workspace -- distinct for every
-// piece, consecutive for one unit's pieces -- and the unit's first piece records (first slot,
-// piece count) for the merge (merge_flat_kernel).  With num_splits = 1 the kernel instead runs one
-// CTA per unit (no workspace, no merge).  The producer alone walks the runs; it hands each piece
-// (its sequence, blocks and context) to the consumers in shared memory with the query rows, so all
-// warps of a CTA take the same path whatever the context lengths.
+// piece, consecutive for one unit's pieces.  The merge (merge_flat_kernel) finds a unit's slots
+// from the context lengths with the same cut; in batches of over kMergeScanSeqs sequences the
+// unit's first piece records them (first slot, piece count) instead.  With num_splits = 1 the
+// kernel instead runs one CTA per unit (no workspace, no merge).  The producer alone walks the
+// runs; it hands each piece (its sequence, blocks and context) to the consumers in shared memory
+// with the query rows, so all warps of a CTA take the same path whatever the context lengths.
 //
 // CTA: 4 consumer warps and a producer warp, three CTAs per SM.  The producer loads each
 // piece's query rows into shared memory and streams 64-position stages -- per page one TMA box
@@ -101,6 +102,11 @@ struct I8Geom {
         1024 + kRingBytes + kQBytes + kBarBytes + kScratchBytes;
 };
 
+// Batches of up to this many sequences: the merge finds each unit's partial slots from the
+// context lengths itself, before it waits for the decode; larger ones read the slot info the
+// decode wrote (a scan of every context per merge warp would grow with the square of the batch).
+constexpr int kMergeScanSeqs = 256;
+
 struct Args {
     const __nv_bfloat16 *q;
     const float *k_scales, *v_scales;
@@ -108,7 +114,9 @@ struct Args {
     int out_f32;
     float *part_o;       // [U + N][G][D] partials of the pieces that are not whole units
     float *part_lse;     // [U + N][G]
-    int2 *unit_info;     // [U]: (first slot, piece count) of each non-empty unit
+    int2 *unit_info;     // [U]: (first slot, piece count) of each non-empty unit, written
+                         // for batches over kMergeScanSeqs sequences
+    int runs;            // runs per kv head (the grid is runs * kv_heads CTAs)
     const int32_t *block_table;
     int bt_stride;
     const int32_t *context_lens;
@@ -898,8 +906,8 @@ __global__ void __launch_bounds__(kThreads, 3)
                                             col) = acc;
         }
         // the unit's first piece: where its pieces are and how many (the CTA runs holding
-        // its first and last blocks)
-        if (threadIdx.x == 0 && blk0 == 0 && !a.per_unit) {
+        // its first and last blocks), for the merge of a batch too large to find them itself
+        if (threadIdx.x == 0 && blk0 == 0 && !a.per_unit && a.num_seqs > kMergeScanSeqs) {
             const long long last = run_of(block_cost(g_last, s), cost, n_runs);
             a.unit_info[unit] = make_int2(slot, static_cast<int>(last - run + 1));
         }
@@ -923,47 +931,83 @@ __global__ void __launch_bounds__(kThreads, 3)
 template <int D>
 __global__ void __launch_bounds__(128) merge_flat_kernel(const Args a)
 {
-    pdl_wait();
-    pdl_trigger();
     constexpr int V = D / 32;
     constexpr int kPre = 4;   // pieces whose rows are requested together with the lse values
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    if (row >= a.num_seqs * a.q_heads)
-        return;
-    const int s = row / a.q_heads;
-    const int h = row - s * a.q_heads;
+    const int n_rows = a.num_seqs * a.q_heads;
+    const int row = blockIdx.x * 4 + warp;
+    const int s = min(row, n_rows - 1) / a.q_heads;
+    const int h = min(row, n_rows - 1) - s * a.q_heads;
     const int G = a.group;
-    const int unit = s * a.kv_heads + h / G;
-    const int g = h - (h / G) * G;
-    // both lookups in one round trip (a unit with no positions has no pieces, and its slot
-    // info is never written: only its context decides)
+    const int kvh = h / G;
+    const int unit = s * a.kv_heads + kvh;
+    const int g = h - kvh * G;
+    // Launched as a dependent of the decode, the merge's CTAs reach the wait below while the
+    // decode's last CTAs still run: a small batch's slot ranges (from the context lengths,
+    // which the decode does not write) are found before it.
     const int ctx = clamped_ctx(a, s);
-    const int2 info = a.unit_info[unit];
+    int first = 0, count = 0;   // the unit's partial slots
+    const bool scan = a.num_seqs <= kMergeScanSeqs;
+    if (scan) {
+        // blocks before sequence s and all of them (the same for every kv head), summed by the
+        // warp; then the runs holding s's first and last blocks, cut as the decode cut them
+        long long total = 0, before = 0;
+        for (int t = lane; t < a.num_seqs; t += 32) {
+            const long long nb = blocks_of(clamped_ctx(a, t));
+            total += nb;
+            before += t < s ? nb : 0;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            total += __shfl_xor_sync(0xffffffffu, total, off);
+            before += __shfl_xor_sync(0xffffffffu, before, off);
+        }
+        const int nb = blocks_of(ctx);
+        if (nb > 0) {
+            const long long R = a.runs;
+            const long long n_runs = min(R, total);
+            const long long cost = 16 * total + kPieceCost * a.num_seqs;
+            const long long r0 = run_of(block_cost(before, s), cost, n_runs);
+            const long long r1 = run_of(block_cost(before + nb - 1, s), cost, n_runs);
+            first = static_cast<int>(kvh * (a.num_seqs + R) + s + r0);
+            count = static_cast<int>(r1 - r0 + 1);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (row >= n_rows)
+        return;
+    if (!scan && ctx > 0) {
+        // a unit with no positions has no pieces, and its slot info is never written
+        const int2 info = a.unit_info[unit];
+        first = info.x;
+        count = info.y;
+    }
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v)
         acc[v] = 0.0f;
     float sum = 0.0f;
     if (ctx > 0) {
-        if (info.y == 1)
+        if (count == 1)
             return;   // the unit's only piece wrote the rows
-        const float *lse = a.part_lse + static_cast<size_t>(info.x) * G + g;
-        const float *po = a.part_o + (static_cast<size_t>(info.x) * G + g) * D + lane * V;
-        // second round trip: every piece's lse (lane j holds piece j, j + 32, ...) and the
-        // first kPre pieces' rows
+        const float *lse = a.part_lse + static_cast<size_t>(first) * G + g;
+        const float *po = a.part_o + (static_cast<size_t>(first) * G + g) * D + lane * V;
+        // one round trip after the wait: every piece's lse (lane j holds piece j, j + 32,
+        // ...) and the first kPre pieces' rows
         float pre[kPre][V];
 #pragma unroll
         for (int j = 0; j < kPre; ++j)
-            if (j < info.y) {
+            if (j < count) {
 #pragma unroll
                 for (int v = 0; v < V; ++v)
                     pre[j][v] = __ldcg(po + static_cast<size_t>(j) * G * D + v);
             }
         float M = -INFINITY;
-        const float mine = lane < info.y ? __ldcg(lse + static_cast<size_t>(lane) * G) : -INFINITY;
+        const float mine = lane < count ? __ldcg(lse + static_cast<size_t>(lane) * G) : -INFINITY;
         M = mine;
-        for (int j = lane + 32; j < info.y; j += 32)
+        for (int j = lane + 32; j < count; j += 32)
             M = fmaxf(M, __ldcg(lse + static_cast<size_t>(j) * G));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
@@ -971,7 +1015,7 @@ __global__ void __launch_bounds__(128) merge_flat_kernel(const Args a)
         if (M != -INFINITY) {
 #pragma unroll
             for (int j = 0; j < kPre; ++j) {
-                if (j < info.y) {
+                if (j < count) {
                     const float wj = fast_exp2((__shfl_sync(0xffffffffu, mine, j) - M) * kLog2e);
                     sum += wj;
 #pragma unroll
@@ -979,7 +1023,7 @@ __global__ void __launch_bounds__(128) merge_flat_kernel(const Args a)
                         acc[v] = fmaf(wj, pre[j][v], acc[v]);
                 }
             }
-            for (int j = kPre; j < info.y; ++j) {
+            for (int j = kPre; j < count; ++j) {
                 const float lj = j < 32 ? __shfl_sync(0xffffffffu, mine, j)
                                         : __ldcg(lse + static_cast<size_t>(j) * G);
                 const float wj = fast_exp2((lj - M) * kLog2e);
@@ -1017,6 +1061,7 @@ cudaError_t launch_t(const DecodeInt8Launch &l, const CUtensorMap &tk, const CUt
     a.part_o = l.part_o;
     a.part_lse = l.part_lse;
     a.unit_info = static_cast<int2 *>(l.unit_info);
+    a.runs = l.per_unit ? 0 : l.n_ctas / l.kv_heads;
     a.block_table = l.block_table;
     a.bt_stride = l.bt_stride;
     a.context_lens = l.context_lens;
