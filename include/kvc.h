@@ -358,7 +358,9 @@ kvc_status kvc_append(void *out, int32_t out_dtype, const void *q, const void *k
  * bt_stride * page_size) is an error the pools survive as they do kvc_slot_mapping +
  * kvc_store: the chunk's tokens the row covers are stored at their slots, the others are
  * skipped, and the device error word (kvc_device_errors) gets 1 << 7; that sequence's output
- * is undefined.  Two launches on `stream`.
+ * is undefined.  A block-table entry outside the pool (a page id < 0 or >= pool.num_pages) is
+ * likewise skipped for the tokens it would hold, as kvc_store skips a slot past the pool, with
+ * 1 << 6; that sequence's output is undefined.  Two launches on `stream`.
  */
 kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const void *k_new,
                             const void *v_new, void *k_pool, void *v_pool, kvc_pool_desc pool,

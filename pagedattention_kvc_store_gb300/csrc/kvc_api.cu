@@ -1211,6 +1211,7 @@ kvc_status kvc_append_store(void *out, int32_t out_dtype, const void *q, const v
         l.fused = true;
         l.k_pool_w = k_pool;
         l.v_pool_w = v_pool;
+        l.num_pages = pool.num_pages;
         err = kvc::launch_append_tc(l, tq, tk, tv, s, &tkn, &tvn);
     }
     return err == cudaSuccess ? ok() : cuda_fail(err, "append launch");

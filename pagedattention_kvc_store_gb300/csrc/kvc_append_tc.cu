@@ -94,6 +94,7 @@ struct Args {
     // (stored before the launch).
     int fused;
     uint8_t *k_pool_w, *v_pool_w;   // the pools, for rows of a partly filled last page
+    int num_pages;                  // their pages (a page id outside them is skipped)
     uint32_t *err;                  // the caller's device error word, or null (this file's own)
 };
 
@@ -321,6 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint8_t *pool = is_k ? a.k_pool_w : a.v_pool_w;
                         for (int lp = s_lo; lp < s_hi; ++lp) {
                             const int page = __shfl_sync(0xffffffffu, my_page, lp - s_lo);
+                            if (page < 0 || page >= a.num_pages) {   // outside the pool: skip, flag
+                                if (lane == 0)
+                                    atomicOr(err_word, kErrSlotRange);
+                                continue;
+                            }
                             const int i = lp - lp0;
                             const int r_lo = max(p_lo - lp * P, 0);
                             const int r_hi = min(p_hi - lp * P, P);
@@ -716,6 +722,7 @@ cudaError_t launch_t(const AppendLaunch &l, const CUtensorMap &tq, const CUtenso
     a.fused = l.fused ? 1 : 0;
     a.k_pool_w = static_cast<uint8_t *>(l.k_pool_w);
     a.v_pool_w = static_cast<uint8_t *>(l.v_pool_w);
+    a.num_pages = l.num_pages;
     a.err = current_error_word();
     const int tiles = (l.max_q_len * a.group + kM - 1) / kM;
     a.pairs_per_seq = (tiles + 1) / 2;

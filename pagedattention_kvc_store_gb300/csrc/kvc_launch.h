@@ -121,6 +121,7 @@ struct AppendLaunch {
     // launch_store_boundary wrote before.
     bool fused = false;
     void *k_pool_w = nullptr, *v_pool_w = nullptr;
+    int num_pages = 0;   // pages of the pools (fused: a page id outside them is skipped)
 };
 
 // kvc_append_int8: AppendLaunch over INT8 pages (head_dim 64 or 128) plus the scale arrays.

@@ -188,3 +188,55 @@ def test_append_store_context_past_the_row(P):
     # the other sequences' outputs are untouched by sequence 0's error
     rows = slice(int(case.q_indptr[1]), case.num_tokens)
     assert torch.equal(out_f[rows], out_s[rows])
+
+
+def test_append_store_page_outside_the_pool():
+    """A block-table entry past the pool (a caller error) on a page that holds only chunk
+    tokens: kvc_append_store must leave the pools exactly as kvc_slot_mapping + kvc_store do
+    (that page's tokens skipped, every other one stored) and both paths flag bit 1 << 6.
+    Sequence 0 has 200 positions, 50 of them new (positions 150 .. 199): its entry 10 (positions
+    160 .. 175) is set to the pool's page count on the device.  In the fused call the append
+    reads the chunk from k_new and writes its later pages itself; the separate append reads
+    that page through the pool's tensor map, past its end (zeros), so sequence 0's output
+    differs between the two and only the others are compared."""
+    P = 16
+    ctx = np.array([200, 211, 75, 90, 40])
+    qlen = np.array([50, 50, 9, 33, 40])
+    case = build_case(96, name="append-store-page-out", page_size=P, q_heads=16, kv_heads=4,
+                      head_dim=128, context_lens=lambda rng: ctx, q_lens=lambda c: qlen)
+    num_pages = case.k_pool.shape[0]
+    bad_table = case.block_table.copy()
+    bad_table[0, 10] = num_pages
+
+    def run(fused_call):
+        d = to_device(case)
+        d.block_table.copy_(torch.from_numpy(bad_table.astype(np.int32)))
+        out = torch.zeros(case.num_tokens, case.q_heads, case.head_dim, dtype=torch.float32,
+                          device="cuda")
+        kvc.kvc_device_errors()
+        if fused_call:
+            kvc.kvc_append_store(out, d.q, d.k_new, d.v_new, d.k_pool, d.v_pool, d.block_table,
+                                 d.q_indptr, d.context_lens, case.max_q_len, case.max_ctx)
+        else:
+            slots = torch.empty(case.num_tokens, dtype=torch.int32, device="cuda")
+            kvc.kvc_slot_mapping(slots, d.block_table, d.context_lens, d.q_indptr, P,
+                                 max_q_len=case.max_q_len)
+            kvc.kvc_store(d.k_pool, d.v_pool, d.k_new, d.v_new, slots)
+            kvc.kvc_append(out, d.q, d.k_pool, d.v_pool, d.block_table, d.q_indptr,
+                           d.context_lens, case.max_q_len, case.max_ctx)
+        torch.cuda.synchronize()
+        flags = kvc.kvc_device_errors()
+        return out, bf16_bits_of(d.k_pool), bf16_bits_of(d.v_pool), flags
+
+    out_f, kf, vf, flags_f = run(True)
+    out_s, ks, vs, flags_s = run(False)
+    assert flags_f & (1 << 6) and flags_s & (1 << 6)
+    assert np.array_equal(kf, ks), "K pools differ from slot mapping + store"
+    assert np.array_equal(vf, vs), "V pools differ from slot mapping + store"
+    # sequence 0's chunk tokens on its other new pages were stored
+    pos = np.arange(176, 200)
+    slots0 = case.block_table[0][pos // P].astype(np.int64) * P + pos % P
+    flat_k = kf.reshape(-1, case.kv_heads, case.head_dim)
+    assert np.array_equal(flat_k[slots0], case.k_new[26:50])
+    rows = slice(int(case.q_indptr[1]), case.num_tokens)
+    assert torch.equal(out_f[rows], out_s[rows])
