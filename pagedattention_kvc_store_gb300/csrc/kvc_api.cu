@@ -1058,6 +1058,9 @@ kvc_status kvc_decode_shared_prefix(void *out, int32_t out_dtype, const void *q,
     l.split_base = g.n_prefix;
     l.split_stride = g.stride;
     l.hnd = pool.layout == KVC_HND;
+    // one resident wave (2 per SM) of prefix CTAs at most: the empty slots of a group list
+    // found on the device then cost one load each instead of a CTA start
+    p.max_prefix_ctas = 2 * device_sm_count();
     if (g.n_prefix == 0)
         p.num_groups = 0;   // no prefix CTAs
     if ((err = kvc::launch_grouped_decode(p, l, tk, tv, s)) != cudaSuccess)

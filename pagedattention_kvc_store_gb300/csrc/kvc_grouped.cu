@@ -69,6 +69,7 @@ struct Args {
     int chunk, n_split, split_stride;
     float scale_log2;
     int hnd;   // HND pools: page boxes addressed by (page, kv head) block
+    int n_items;   // prefix work items: n_split * kv_heads * groups
     uint32_t *err;   // the caller's device error word, or null (this file's own word)
 };
 
@@ -289,9 +290,10 @@ __global__ void __launch_bounds__(kDetectThreads, 1)
         *num_groups = carry_groups;
 }
 
-// One prefix CTA: chunk `split` of the shared prefix of group `grp`, kv head `kvh`.
+// One prefix work item: chunk `split` of the shared prefix of group `grp`, kv head `kvh`.
+// Returns false in a thread whose bounded wait gave up (its error bit is set).
 template <int D, int NMT>
-__device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
+__device__ __forceinline__ bool prefix_cta(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                                            const Args &a, const int split, const int kvh,
                                            const int grp, uint8_t *smem)
 {
@@ -321,7 +323,7 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUte
                                static_cast<size_t>(kvh) * G + (r - (r / G) * G);
             a.part_lse[row * a.split_stride + split] = -INFINITY;
         }
-        return;
+        return true;
     }
     const int leader = a.group_seqs[m0];
     const int n_blocks = (k_end - k_begin + kStageKeys - 1) / kStageKeys;
@@ -394,7 +396,7 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUte
                 if (!mbar_wait(&full[b % kStages], (b / kStages) & 1))
                     atomicOr(a.err ? a.err : &g_grouped_errors, kErrDrainWait);
         }
-        return;
+        return ok;
     }
 
     // --------------------------------- consumers -----------------------------------------
@@ -648,6 +650,7 @@ __device__ __forceinline__ void prefix_cta(const CUtensorMap *tmap_k, const CUte
         }
         *reinterpret_cast<float4 *>(a.part_o + row_slot[r] * D + c) = acc;
     }
+    return ok;
 }
 
 // The whole shared-prefix decode in one grid: CTAs [0, n_prefix) are prefix CTAs ordered
@@ -667,11 +670,43 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int idx = blockIdx.x;
     if (idx < n_prefix_ctas) {
         // reads only inputs older than the setup kernel (queries, tables, groups), which has
-        // itself waited for all earlier work before letting this grid launch
-        const int split = idx % a.n_split;
-        const int rest = idx / a.n_split;
-        prefix_cta<D, NMT>(&tmap_k, &tmap_v, a, split, rest % a.kv_heads, rest / a.kv_heads,
-                           smem);
+        // itself waited for all earlier work before letting this grid launch.
+        // Work items idx, idx + n_prefix_ctas, ... (at most one resident wave of prefix CTAs):
+        // the first is taken as it comes; the others are checked for members 32 at a time in
+        // one read, so that a group list with empty slots (device-found groups fill a fixed
+        // capacity) costs a load per slot, not a CTA.  An item with members but no prefix
+        // position in its split still runs: it writes its rows' empty partials.
+        const int lane = threadIdx.x & 31;
+        int it = idx;
+        int batch = idx;                     // todo bit k: item batch + k * n_prefix_ctas
+        int next = idx + n_prefix_ctas;      // the first item not yet checked
+        uint32_t todo = 0u;
+        for (;;) {
+            const int split = it % a.n_split;
+            const int rest = it / a.n_split;
+            const bool ok = prefix_cta<D, NMT>(&tmap_k, &tmap_v, a, split, rest % a.kv_heads,
+                                               rest / a.kv_heads, smem);
+            while (todo == 0u && next < a.n_items) {
+                const long long c = next + static_cast<long long>(lane) * n_prefix_ctas;
+                bool live = false;
+                if (c < a.n_items) {
+                    const int grp = static_cast<int>(c / a.n_split) / a.kv_heads;
+                    live = a.group_indptr[grp + 1] > a.group_indptr[grp];
+                }
+                todo = __ballot_sync(0xffffffffu, live);
+                batch = next;
+                next += 32 * n_prefix_ctas;
+            }
+            if (todo == 0u)
+                break;
+            // the item is done with the ring, the barriers and the combine's shared memory
+            // before the next one's bulk copies write there; stop after a failed wait
+            fence_proxy_async_smem();
+            if (__syncthreads_or(!ok))
+                break;
+            it = batch + (__ffs(todo) - 1) * n_prefix_ctas;
+            todo &= todo - 1u;
+        }
     } else {
         pdl_wait();   // the key starts
         const int j = idx - n_prefix_ctas;
@@ -718,8 +753,13 @@ cudaError_t launch_t(const GroupedPrefixLaunch &p, const DecodeLaunch &l, const 
     a.split_stride = p.split_stride;
     a.scale_log2 = p.scale * kLog2e;
     const dec::Args da = dec::make_args(l);
-    const long long n_prefix =
+    const long long n_items =
         p.num_groups > 0 ? static_cast<long long>(p.n_split) * p.kv_heads * p.num_groups : 0;
+    if (n_items > 0x3FFFFFFFLL)
+        return cudaErrorInvalidConfiguration;
+    a.n_items = static_cast<int>(n_items);
+    const long long n_prefix =
+        p.max_prefix_ctas > 0 && n_items > p.max_prefix_ctas ? p.max_prefix_ctas : n_items;
     const long long n_ctas =
         n_prefix + static_cast<long long>(l.n_split) * l.kv_heads * l.num_seqs;
     if (n_ctas == 0)

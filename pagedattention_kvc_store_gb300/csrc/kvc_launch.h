@@ -103,6 +103,9 @@ struct GroupedPrefixLaunch {
     int chunk, n_split, split_stride;
     float scale;
     bool hnd = false;
+    // at most this many prefix CTAs, each taking every max_prefix_ctas-th work item after its
+    // first (0: one CTA per item)
+    int max_prefix_ctas = 0;
 };
 
 struct AppendLaunch {

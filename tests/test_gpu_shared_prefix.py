@@ -23,13 +23,13 @@ def _group_arrays(case):
     return indptr, seqs, np.asarray(prefix, np.int32)
 
 
-def _run_shared(case, g):
-    indptr, seqs, prefix = _group_arrays(case)
+def _run_shared(case, g, arrays=None):
+    indptr, seqs, prefix = _group_arrays(case) if arrays is None else arrays
     max_group = max((len(x) for x in case.groups), default=1)
     max_prefix = int(prefix.max()) if prefix.size else 0
     pool = kvc.pool_desc(g.d.k_pool)
     ws = kvc.kvc_decode_shared_prefix_plan(case.num_seqs, case.q_heads, pool, case.max_ctx,
-                                           len(case.groups), max_prefix)
+                                           len(prefix), max_prefix)
     # every byte 0xFF: a partial slot the grid failed to write (or to mark empty) reads as NaN
     work = torch.full((ws,), 0xFF, dtype=torch.uint8, device="cuda")
     out = torch.empty(case.num_seqs, case.q_heads, case.head_dim, dtype=torch.float32,
@@ -84,6 +84,37 @@ def test_random_groups(P, Hq, Hkv, D, members):
     got = _run_shared(case, g)
     ref, _ = OracleRun(case).attention()
     assert_attention_close(got, ref, f"groups {P},{Hq},{Hkv},{D},{members}")
+
+
+def test_more_work_items_than_one_wave_with_empty_slots():
+    """Groups x kv heads well above the prefix CTAs of one resident wave (2 per SM), so CTAs
+    take several items in turn, with empty group slots between and after the real ones (the
+    shape of a device-found list) and groups whose prefix is empty."""
+    P, Hkv = 16, 8
+    case = build_case(71, name="groups", page_size=P, q_heads=32, kv_heads=Hkv, head_dim=128,
+                      context_lens=lambda rng: rng.integers(1, 260, size=240),
+                      q_lens=np.ones_like, share_groups=_random_groups(P, 3))
+    indptr, seqs, prefix = _group_arrays(case)
+    sizes = np.diff(indptr)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert len(sizes) * Hkv > 2 * n_sm, "the case must exceed one wave of prefix CTAs"
+    # an empty slot after every third group and a tail of them, as a fixed-capacity list has
+    new_sizes, new_prefix = [], []
+    for i, (n, pre) in enumerate(zip(sizes, prefix)):
+        new_sizes.append(int(n))
+        new_prefix.append(int(pre))
+        if i % 3 == 2:
+            new_sizes.append(0)
+            new_prefix.append(0)
+    new_sizes += [0] * 40
+    new_prefix += [0] * 40
+    arrays = (np.concatenate([[0], np.cumsum(new_sizes)]).astype(np.int32), seqs,
+              np.asarray(new_prefix, np.int32))
+    g = GpuRun(case, decode=True)
+    g.store()
+    got = _run_shared(case, g, arrays)
+    ref, _ = OracleRun(case).attention()
+    assert_attention_close(got, ref, "groups over several prefix items per CTA")
 
 
 def test_rejects_groups_with_too_many_rows():
